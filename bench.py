@@ -1,0 +1,412 @@
+"""Benchmark: one decode step (KV append + paged decode attention) on GB300.
+
+Default workload: the Llama-3-8B-shaped GQA batch (B=64, 32 q / 8 kv heads,
+D=128, bf16, 16-token blocks, lengths log-uniform in [512, 32768], pool 1.1x
+the blocks in use), seeded synthetic data. One step = pa_append_kv of the new
+token of every sequence + pa_decode over all tokens. The pools (~2 GB) are
+larger than L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0). ``--impl reference`` times the fp64 CPU oracle
+on the host cores instead, on a bounded sample of the same workload.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention: achieved HBM GB/s (% of GB300 peak), queries·heads/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 126 * 2**20
+
+# DRAM traffic of the split-attention kernel from an ncu capture (per launch,
+# scaled to the full workload), valid only for the kernel sources it was
+# measured on (sha256 of the split kernel's source files).
+TRAFFIC = {"source_sha": None, "workload": "llama3_8b_gqa", "bytes_per_launch": None}
+
+
+def split_source_sha() -> str:
+    h = hashlib.sha256()
+    for name in ("pa_split.cuh", "pa_split.cu", "pa_ptx.cuh"):
+        with open(os.path.join(ROOT, "paged_kv_cache_202_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def measured_peak_gbs():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBs", "hbm_gb_s"):
+            if key in d:
+                v = d[key]
+                if isinstance(v, dict):
+                    v = v.get("burst", v.get("value"))
+                return float(v), "measured"
+    except (OSError, ValueError, TypeError):
+        pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples in the background (timestamps in ms)."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                self.samples.append((time.time(), parts))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        inside = [p for (t, p) in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not inside:
+            inside = [p for (_, p) in self.samples]
+            window = "run"
+        if not inside:
+            return None
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4)
+                          if p[5 + i].lower() in ("active", "1")})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside), "window": window}
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)),
+            int(os.environ.get("LOCAL_RANK", 0)))
+
+
+def oracle_sample_gbs(wl, budget_s: float, min_pairs: int = 1):
+    """Time the fp64 oracle on (b, h) pairs of the workload for about budget_s.
+
+    Returns (GB/s of algorithmic bytes, seconds, pairs, threads). The bytes of
+    one (b, h) pair are sequence b's decode bytes divided by Hq.
+    """
+    import oracle
+    import paged_kv_cache_202_gb300 as pa
+    kp, vp = wl.pools_after_append()
+    threads = os.cpu_count() or 1
+    eb = wl.elem_bytes
+    per_seq = [pa.decode_bytes([int(L)], wl.Hq, wl.Hkv, wl.D, wl.block_size, eb, eb) / wl.Hq
+               for L in wl.seq_lens]
+    order = np.random.default_rng(0).permutation(wl.B * wl.Hq)
+    # calibrate on a few pairs
+    pairs, done_bytes, elapsed, i = 0, 0.0, 0.0, 0
+    chunk = max(min_pairs, threads)
+    while (elapsed < budget_s or pairs < min_pairs) and i < order.size:
+        sel = order[i:i + chunk]
+        i += chunk
+        pr = np.stack([sel // wl.Hq, sel % wl.Hq], axis=1).astype(np.int32)
+        t = time.perf_counter()
+        oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale, pairs=pr,
+                      nthreads=threads)
+        elapsed += time.perf_counter() - t
+        pairs += len(sel)
+        done_bytes += sum(per_seq[int(b)] for b in sel // wl.Hq)
+        chunk = min(chunk * 2, 4096)
+    return done_bytes / elapsed / 1e9, elapsed, pairs, threads
+
+
+def run_reference(args, rank):
+    if rank != 0:
+        return
+    from paged_kv_cache_202_gb300.workloads import make_workload
+    import oracle
+    oracle.build()
+    wl = make_workload(args.workload)
+    total = args.steps + args.warmup
+    per_step = max(0.05, min(20.0, 120.0 / max(total, 1)))
+    vals = []
+    t_all = 0.0
+    pairs_all = 0
+    threads = 1
+    for step in range(total):
+        gbs, el, pairs, threads = oracle_sample_gbs(wl, per_step)
+        if step >= args.warmup:
+            vals.append(gbs)
+            t_all += el
+            pairs_all += pairs
+    value = statistics.median(vals) if vals else 0.0
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * t_all / max(len(vals), 1), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
+                   "block_size": wl.block_size, "kv_dtype": wl.dtype,
+                   "l2": "inputs larger than L2"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{pairs_all} random (sequence, q-head) rows over "
+                                   f"{len(vals)} steps, ~{per_step:.2f} s each"},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, rank, world, local_rank):
+    import __graft_entry__
+    import paged_kv_cache_202_gb300 as pa
+    from paged_kv_cache_202_gb300.workloads import make_workload
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    wl = make_workload(args.workload, seed=args.seed + rank if args.seed is not None else None)
+    t_gen = time.time()
+    bf = wl.dtype == "bf16"
+
+    def to_dev(a):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16 if bf else np.float32))
+        return (t.view(torch.bfloat16) if bf else t).to(dev)
+
+    q, k_new, v_new = to_dev(wl.q), to_dev(wl.k_new), to_dev(wl.v_new)
+    k_pool, v_pool = to_dev(wl.k_pool), to_dev(wl.v_pool)
+    tables = torch.from_numpy(wl.block_tables).to(dev)
+    seq_lens = torch.from_numpy(wl.seq_lens).to(dev)
+    cache_lens = torch.from_numpy(wl.cache_lens).to(dev)
+    out_dtype = torch.bfloat16 if bf else torch.float32
+    out = torch.empty(wl.B, wl.Hq, wl.D, dtype=out_dtype, device=dev)
+    plan = pa.Plan()
+    stream = torch.cuda.current_stream()
+    max_len = wl.max_seq_len
+
+    def step():
+        pa.pa_append_kv(k_new, v_new, k_pool, v_pool, tables, cache_lens, stream)
+        pa.pa_decode(q, k_pool, v_pool, tables, seq_lens, wl.scale, out, max_len, plan, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert pa.pa_last_device_error(plan) == 0 and pa.pa_last_device_error(None) == 0
+
+    eb = wl.elem_bytes
+    dec_bytes = pa.decode_bytes(wl.seq_lens, wl.Hq, wl.Hkv, wl.D, wl.block_size, eb, eb)
+    app_bytes = pa.append_bytes(wl.B, wl.Hkv, wl.D, eb)
+    step_bytes = dec_bytes + app_bytes
+
+    # Timed region: K steps, split-kernel events per step.
+    ev_split = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+    for a_, b_ in ev_split:       # create the underlying events before the timed region
+        a_.record(stream)
+        b_.record(stream)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    w0 = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        plan.set_split_events(*ev_split[i])
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    barrier()
+    plan.set_split_events(None, None)
+    time.sleep(0.25)
+    sampler.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_step = ms_total / args.steps
+    split_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ev_split)
+    err = pa.pa_last_device_error(plan)
+
+    # Parity of the timed output against the oracle on sampled rows (rank 0).
+    parity = None
+    if rank == 0 and not args.no_parity:
+        import oracle
+        kp, vp = wl.pools_after_append()
+        rng = np.random.default_rng(1)
+        idx = rng.choice(wl.B * wl.Hq, size=min(64, wl.B * wl.Hq), replace=False)
+        pr = np.stack([idx // wl.Hq, idx % wl.Hq], axis=1).astype(np.int32)
+        ref = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale, pairs=pr)
+        got = out.float().cpu().numpy()[pr[:, 0], pr[:, 1]].astype(np.float64)
+        parity = {"rows": int(len(pr)), "max_abs_err": float(np.abs(got - ref).max()),
+                  "tol": 1.5e-2 if bf else 2e-3}
+
+    # End to end through the public API: inputs from pinned host memory each step,
+    # result read back each step.
+    h_q = torch.empty_like(q, device="cpu").pin_memory()
+    h_q.copy_(q)
+    h_kn = torch.empty_like(k_new, device="cpu").pin_memory()
+    h_kn.copy_(k_new)
+    h_vn = torch.empty_like(v_new, device="cpu").pin_memory()
+    h_vn.copy_(v_new)
+    h_bt = torch.from_numpy(wl.block_tables).pin_memory()
+    h_sl = torch.from_numpy(wl.seq_lens).pin_memory()
+    h_cl = torch.from_numpy(wl.cache_lens).pin_memory()
+    h_out = torch.empty_like(out, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_kn, h_vn, h_bt, h_sl, h_cl))
+    d2h = h_out.numel() * h_out.element_size()
+    e2e_steps = max(1, min(args.steps, 200))
+
+    def e2e_step():
+        q.copy_(h_q, non_blocking=True)
+        k_new.copy_(h_kn, non_blocking=True)
+        v_new.copy_(h_vn, non_blocking=True)
+        tables.copy_(h_bt, non_blocking=True)
+        seq_lens.copy_(h_sl, non_blocking=True)
+        cache_lens.copy_(h_cl, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    barrier()
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, el, pairs, threads = oracle_sample_gbs(wl, args.cpu_budget)
+        cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+               "sample": f"{pairs} random (sequence, q-head) rows of the workload, "
+                         f"{el:.1f} s, bytes per row = its sequence's decode bytes / Hq"}
+
+    peak, peak_kind = measured_peak_gbs()
+    achieved = dec_bytes / (split_ms * 1e-3) / 1e9
+    sha = split_source_sha()
+    traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["source_sha"] == sha and \
+        TRAFFIC["workload"] == wl.name else None
+    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    clocks = sampler.summary(w0, w1)
+    path, blocks, warps = plan.info()
+    plan.free()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
+            if bf else "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
+                       "block_size": wl.block_size, "num_blocks": wl.num_blocks,
+                       "tokens": int(wl.seq_lens.sum()), "kv_dtype": wl.dtype,
+                       "l2": f"inputs larger than L2 ({2 * wl.k_pool.nbytes / 2**30:.2f} GiB "
+                             f"of pools vs {L2_BYTES / 2**20:.0f} MiB L2), no flush",
+                       "step": "pa_append_kv + pa_decode", "parallelism": f"replicas x{world}"},
+            "pct_of_peak": 100.0 * value / world / peak,
+            "qheads_per_s": world * wl.B * wl.Hq / (ms_step * 1e-3),
+            "roofline": {"bound": "hbm", "kernel": "split attention", "achieved": achieved,
+                         "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": traffic,
+                         "algorithmic_bytes": dec_bytes, "ms_per_launch": split_ms},
+            "e2e": {"value": world * step_bytes / e2e_s / 1e9, "unit": "GB/s",
+                    "ms_per_step": e2e_s * 1e3, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": 3 * args.steps,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "parity": parity,
+            "device_error": err,
+            "kernel": {"path": {1: "simple", 2: "fma", 3: "mma"}.get(path, path),
+                       "blocks": blocks, "warps": warps},
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="llama3_8b_gqa")
+    ap.add_argument("--seed", type=int, default=None)
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-parity", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local_rank = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank)
+    else:
+        run_ours(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

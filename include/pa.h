@@ -1,0 +1,183 @@
+/*
+ * pa.h -- C ABI of the paged decode attention library (libpa.so).
+ *
+ * One decode step of a transformer layer whose KV cache is paged: each
+ * sequence's keys and values live in fixed-size blocks of 16 or 32 tokens
+ * scattered through two global pools (one for K, one for V), and a
+ * per-sequence block table maps logical block i to its physical block.
+ * ("PagedAttention: The Cache Was Storing Nothing" §2.2; "Paged Attention
+ * Meets FlexAttention" review, "What carries the argument": two global page
+ * buffers and one block table per sequence.)
+ *
+ * Layouts (all row-major, contiguous, device memory unless stated):
+ *   K pool, V pool   [num_blocks][Hkv][block_size][D]   kv_dtype elements
+ *   block_tables     int32 [B][max_blocks]; entry i of row b is the physical
+ *                    block of logical block i; entries at or past
+ *                    ceil(len_b / block_size) are never read
+ *   q                [B][Hq][D]  kv_dtype elements
+ *   k_new, v_new     [B][Hkv][D] kv_dtype elements
+ *   out              [B][Hq][D]  out_dtype elements
+ * Query head h reads kv head h / (Hq / Hkv) (consecutive groups;
+ * "PagedAttention: The Cache Was Storing Nothing" §3.1).
+ *
+ * Ownership: the caller owns every tensor. The library owns only the plan
+ * object returned through pa_decode's plan_inout and the device workspace
+ * inside it, both released by pa_free.
+ *
+ * Streams and errors: every call is asynchronous on the given stream (NULL =
+ * the legacy default stream); no call synchronises the host. Argument errors
+ * are detected on the host before anything is launched and return a status
+ * other than PA_OK. A CUDA launch or allocation failure returns PA_ERR_CUDA.
+ * Data errors that only the device can see (a length outside its range, a
+ * table entry outside the pool) never fault: the kernels skip the access,
+ * write zeros for the affected outputs and raise a bit in a device error word
+ * that pa_last_device_error reads back.
+ *
+ * Supported shapes: kv_dtype PA_BF16 or PA_F32, D in {64, 128}, block_size in
+ * {16, 32}, Hq a multiple of Hkv. Pools, q, k_new, v_new and out must be
+ * 16-byte aligned.
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t is struct CUstream_st* */
+struct CUevent_st;  /* cudaEvent_t is struct CUevent_st* */
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_NULL = 1,        /* a required pointer is NULL */
+    PA_ERR_SHAPE = 2,       /* sizes out of range or inconsistent */
+    PA_ERR_DTYPE = 3,       /* unsupported element type */
+    PA_ERR_BLOCK_SIZE = 4,  /* block_size not 16 or 32 */
+    PA_ERR_WORKSPACE = 5,   /* workspace too small for the request */
+    PA_ERR_CUDA = 6,        /* a CUDA call failed */
+    PA_ERR_BOUNDS = 7,      /* the device saw a length or table entry out of range */
+    PA_ERR_ALIGN = 8        /* a tensor is not 16-byte aligned */
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Bits of the device error word (pa_last_device_error). */
+enum {
+    PA_DEVERR_SEQ_LEN = 1,      /* decode: seq_len < 1 or > min(max_seq_len, max_blocks*bs) */
+    PA_DEVERR_TABLE = 2,        /* a table entry outside [0, num_blocks) */
+    PA_DEVERR_TIMEOUT = 4,      /* a pipeline wait gave up (the kernel returned early) */
+    PA_DEVERR_CACHE_LEN = 8     /* append: cache_len < 0 or >= max_blocks*bs */
+};
+
+/* Kernel selection for pa_decode (pa_plan_set_path). */
+enum {
+    PA_PATH_AUTO = 0,    /* bf16 with g = 1: FMA path; bf16 with g >= 2: tensor-core path; f32: simple */
+    PA_PATH_SIMPLE = 1,  /* one warp per (sequence, q head), plain loads, no split */
+    PA_PATH_FMA = 2,     /* bf16 only: bulk-staged pages, CUDA-core dot products */
+    PA_PATH_MMA = 3      /* bf16 only: bulk-staged pages, GQA group through bf16 mma tiles */
+};
+
+/* Opaque: split plan, device workspace and device error word. */
+typedef struct pa_plan pa_plan;
+
+/*
+ * pa_append_kv -- write one new token per sequence into its tail block.
+ *
+ * The cache grows by one token per generated token and only the last block
+ * of a sequence is partly full ("PagedAttention: The Cache Was Storing
+ * Nothing" §1 and §2.2). For every sequence b and kv head j, with
+ * pos = cache_lens[b]:
+ *     K[block_tables[b][pos / block_size]][j][pos % block_size][:] = k_new[b][j][:]
+ * and the same for V. The copy is bit-exact (NaN payloads included).
+ *
+ *   k_new, v_new   device, [B][Hkv][D] kv_dtype, read only
+ *   k_pool, v_pool device, [num_blocks][Hkv][block_size][D], written in place
+ *   block_tables   device, int32 [B][max_blocks]
+ *   cache_lens     device, int32 [B]: tokens already cached = write position
+ *
+ * Precondition: the written block is private to its sequence (reference
+ * count 1). Shared blocks must be copied by the caller before a sequence
+ * writes into them (copy on write, same page §2.3). A cache_len outside
+ * [0, max_blocks*block_size) or a table entry outside [0, num_blocks) skips
+ * that sequence and raises PA_DEVERR_CACHE_LEN / PA_DEVERR_TABLE in the
+ * library-wide append error word (pa_last_device_error with plan = NULL).
+ * B = 0 is a no-op.
+ */
+pa_status pa_append_kv(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                       const int32_t* block_tables, int max_blocks, const int32_t* cache_lens,
+                       int B, int Hkv, int D, int block_size, int num_blocks, pa_dtype kv_dtype,
+                       struct CUstream_st* stream);
+
+/*
+ * pa_decode -- paged decode attention for one new query per (sequence, head).
+ *
+ * out[b][h][:] = sum_t w_t v_t with w = softmax_t(scale * q[b][h] . k_t) over
+ * the logical tokens t < seq_lens[b] of sequence b, k_t and v_t read through
+ * the block table: exactly ordinary attention with one indirection per block
+ * ("39 · PagedAttention" §1-§2; scale = 1/sqrt(D) in "FlashAttention vs
+ * PagedAttention"). The sequence is split across warps; partial results
+ * (m, l, acc) are merged with m = max(m1, m2), l = l1 e^(m1-m) + l2 e^(m2-m)
+ * ("39 · PagedAttention" §3), by a second small kernel where a sequence
+ * spans more than one warp.
+ *
+ *   q             device, [B][Hq][D] kv_dtype
+ *   k_pool/v_pool device, [num_blocks][Hkv][block_size][D] kv_dtype, read only
+ *   block_tables  device, int32 [B][max_blocks]
+ *   seq_lens      device, int32 [B]: tokens attended, >= 1 (includes the token
+ *                 appended this step); must be <= max_seq_len
+ *   max_seq_len   host bound on every seq_lens[b]; sizes the launch
+ *   scale         score scale (normally 1/sqrt(D))
+ *   out           device, [B][Hq][D] out_dtype (bf16 rounded to nearest even)
+ *   plan_inout    in/out: *plan_inout == NULL makes the library create a plan
+ *                 (device workspace allocation, the only allocation); a plan
+ *                 is reused by later calls and grows its workspace only when
+ *                 a call needs more. Release it with pa_free.
+ *
+ * Device-side violations (seq_len out of range, table entry outside the pool)
+ * write zeros for the affected (b, h) rows and raise bits in the plan's error
+ * word. B = 0 is a no-op (no plan is created).
+ */
+pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
+                    const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int B,
+                    int Hq, int Hkv, int D, int block_size, int num_blocks, int max_seq_len,
+                    float scale, pa_dtype kv_dtype, void* out, pa_dtype out_dtype,
+                    pa_plan** plan_inout, struct CUstream_st* stream);
+
+/* Release a plan and its device workspace. NULL is a no-op. The caller must
+ * make sure no work using the plan is still running (e.g. sync its stream). */
+pa_status pa_free(pa_plan* plan);
+
+/* Static English text for a status code. Never NULL. */
+const char* pa_status_str(pa_status status);
+
+/*
+ * pa_last_device_error -- read and clear a device error word (synchronous:
+ * waits for the device). plan != NULL reads the plan's decode word;
+ * plan == NULL reads the library-wide append word of the current device.
+ * *err receives a bit set of PA_DEVERR_*; 0 means no error seen.
+ */
+pa_status pa_last_device_error(pa_plan* plan, int* err);
+
+/* Force a kernel path for later pa_decode calls on this plan (PA_PATH_*).
+ * A forced path that does not support a call's shape makes that call return
+ * PA_ERR_DTYPE. */
+pa_status pa_plan_set_path(pa_plan* plan, int path);
+
+/* The path the last pa_decode call on this plan launched (PA_PATH_*), the
+ * number of thread blocks and warps of its split kernel. Any output pointer
+ * may be NULL. */
+pa_status pa_plan_info(const pa_plan* plan, int* path, int* blocks, int* warps);
+
+/* Timing hook: when both events are non-NULL, later pa_decode calls on this
+ * plan record `start` right before the split-attention kernel and `stop`
+ * right after it, on the call's stream. Pass NULLs to stop recording. */
+pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
+                                   struct CUevent_st* stop);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

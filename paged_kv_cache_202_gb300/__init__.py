@@ -1,0 +1,199 @@
+"""Paged decode attention on GB300 (sm_103a): Python binding of libpa.so.
+
+The functions here carry the C-ABI names of ``include/pa.h`` and only
+marshal arguments: torch tensors give device pointers, shapes and the current
+CUDA stream; every step of the computation runs in the library's kernels.
+There is no fallback: if ``libpa.so`` is missing, every call raises.
+
+Layouts (contiguous, on one CUDA device):
+    q            [B, Hq, D]               bf16 or float32 (the pool dtype)
+    k_pool/v_pool [num_blocks, Hkv, block_size, D]
+    block_tables int32 [B, max_blocks]
+    seq_lens     int32 [B]   decode lengths (include the token appended this step)
+    cache_lens   int32 [B]   append positions
+    out          [B, Hq, D]               bf16 or float32
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libpa.so")
+HEADER = os.path.join(os.path.dirname(_PKG), "include", "pa.h")
+
+PA_OK, PA_ERR_NULL, PA_ERR_SHAPE, PA_ERR_DTYPE, PA_ERR_BLOCK_SIZE = 0, 1, 2, 3, 4
+PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_BOUNDS, PA_ERR_ALIGN = 5, 6, 7, 8
+PA_F32, PA_BF16 = 0, 1
+PA_DEVERR_SEQ_LEN, PA_DEVERR_TABLE, PA_DEVERR_TIMEOUT, PA_DEVERR_CACHE_LEN = 1, 2, 4, 8
+PA_PATH_AUTO, PA_PATH_SIMPLE, PA_PATH_FMA, PA_PATH_MMA = 0, 1, 2, 3
+
+_lib = None
+
+
+class PagedAttentionError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {pa_status_str(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded ``libpa.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                           "`python -c 'import __graft_entry__ as g; g.build()'`")
+    L = ctypes.CDLL(LIB_PATH)
+    vp, ci, cf = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    L.pa_append_kv.argtypes = [vp, vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, vp]
+    L.pa_append_kv.restype = ci
+    L.pa_decode.argtypes = [vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci, vp, ci,
+                            ctypes.POINTER(vp), vp]
+    L.pa_decode.restype = ci
+    L.pa_free.argtypes = [vp]
+    L.pa_free.restype = ci
+    L.pa_status_str.argtypes = [ci]
+    L.pa_status_str.restype = ctypes.c_char_p
+    L.pa_last_device_error.argtypes = [vp, ctypes.POINTER(ci)]
+    L.pa_last_device_error.restype = ci
+    L.pa_plan_set_path.argtypes = [vp, ci]
+    L.pa_plan_set_path.restype = ci
+    L.pa_plan_info.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci), ctypes.POINTER(ci)]
+    L.pa_plan_info.restype = ci
+    L.pa_plan_set_split_events.argtypes = [vp, vp, vp]
+    L.pa_plan_set_split_events.restype = ci
+    _lib = L
+    return L
+
+
+def declared_functions() -> list[str]:
+    """Names of the functions that ``include/pa.h`` declares."""
+    with open(HEADER) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_[a-z0-9_]+)\s*\(", text)))
+
+
+def pa_status_str(status: int) -> str:
+    return lib().pa_status_str(int(status)).decode()
+
+
+def _check(status: int, what: str) -> None:
+    if status != PA_OK:
+        raise PagedAttentionError(status, what)
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    if t.dtype == torch.float32:
+        return PA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t: torch.Tensor) -> int:
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return t.data_ptr()
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+class Plan:
+    """Owner of a ``pa_plan*`` (split plan + device workspace)."""
+
+    def __init__(self):
+        self.handle = ctypes.c_void_p(None)
+
+    def free(self) -> None:
+        if self.handle.value:
+            _check(lib().pa_free(self.handle), "pa_free")
+            self.handle = ctypes.c_void_p(None)
+
+    def set_path(self, path: int) -> None:
+        _check(lib().pa_plan_set_path(self.handle, int(path)), "pa_plan_set_path")
+
+    def info(self) -> tuple[int, int, int]:
+        p, b, w = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
+        _check(lib().pa_plan_info(self.handle, ctypes.byref(p), ctypes.byref(b), ctypes.byref(w)),
+               "pa_plan_info")
+        return p.value, b.value, w.value
+
+    def set_split_events(self, start, stop) -> None:
+        s = ctypes.c_void_p(start.cuda_event if start is not None else None)
+        e = ctypes.c_void_p(stop.cuda_event if stop is not None else None)
+        _check(lib().pa_plan_set_split_events(self.handle, s, e), "pa_plan_set_split_events")
+
+    def last_device_error(self) -> int:
+        return pa_last_device_error(self)
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.free()
+
+
+def pa_append_kv(k_new: torch.Tensor, v_new: torch.Tensor, k_pool: torch.Tensor,
+                 v_pool: torch.Tensor, block_tables: torch.Tensor, cache_lens: torch.Tensor,
+                 stream=None) -> None:
+    """Write each sequence's new K/V token into its tail block (in place)."""
+    NB, Hkv, bs, D = k_pool.shape
+    B = cache_lens.shape[0]
+    st = lib().pa_append_kv(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+                            _ptr(block_tables), block_tables.shape[1], _ptr(cache_lens), B, Hkv,
+                            D, bs, NB, _dtype(k_pool), _stream(stream))
+    _check(st, "pa_append_kv")
+
+
+def pa_decode(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+              block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+              out: torch.Tensor, max_seq_len: int, plan: Plan, stream=None) -> torch.Tensor:
+    """Paged decode attention into ``out``; returns ``out``."""
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_pool.shape
+    st = lib().pa_decode(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                         block_tables.shape[1], _ptr(seq_lens), B, Hq, Hkv, D, bs, NB,
+                         int(max_seq_len), float(scale), _dtype(k_pool), _ptr(out), _dtype(out),
+                         ctypes.byref(plan.handle), _stream(stream))
+    _check(st, "pa_decode")
+    return out
+
+
+def pa_free(plan: Plan) -> None:
+    plan.free()
+
+
+def pa_last_device_error(plan: Plan | None) -> int:
+    err = ctypes.c_int(0)
+    h = plan.handle if plan is not None else ctypes.c_void_p(None)
+    _check(lib().pa_last_device_error(h, ctypes.byref(err)), "pa_last_device_error")
+    return err.value
+
+
+def decode_bytes(seq_lens, Hq: int, Hkv: int, D: int, block_size: int, kv_elem_bytes: int,
+                 out_elem_bytes: int) -> int:
+    """Algorithmic HBM bytes of one decode call (the roofline numerator).
+
+    Every attended K and V element once, one 4-byte table entry per attended
+    block, the queries, the lengths and the output.
+    """
+    total = 0
+    for L in (int(x) for x in seq_lens):
+        total += 2 * Hkv * D * L * kv_elem_bytes + 4 * (-(-L // block_size))
+    B = len(seq_lens)
+    return total + B * Hq * D * kv_elem_bytes + 4 * B + B * Hq * D * out_elem_bytes
+
+
+def append_bytes(B: int, Hkv: int, D: int, kv_elem_bytes: int) -> int:
+    """Algorithmic bytes of one append: new K/V rows read and written, lengths, table entries."""
+    return 2 * (2 * B * Hkv * D * kv_elem_bytes) + 4 * B + 4 * B

@@ -1,0 +1,378 @@
+// Host side of the C ABI declared in include/pa.h: argument validation, kernel
+// selection, split planning, workspace ownership and launches.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <algorithm>
+#include <cstring>
+#include <mutex>
+#include <vector>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+using pa::SplitLaunch;
+
+constexpr size_t kSmemLimit = 232448;     // opt-in dynamic shared memory per block on sm_10x
+constexpr size_t kRingBudget = 200 * 1024; // bytes of stages per block
+constexpr int kMinPagesPerWarp = 4;
+constexpr int kHeadSlice = 16;             // query heads per kv unit on the tensor-core path
+constexpr int kMaxBatch = 8192;            // per-sequence arrays live in shared memory
+
+struct MapKey {
+    const void* ptr = nullptr;
+    int rows = 0, D = 0, BS = 0;
+    bool operator==(const MapKey& o) const {
+        return ptr == o.ptr && rows == o.rows && D == o.D && BS == o.BS;
+    }
+};
+
+struct OccKey {
+    int kind, D, BS, NT, warps;
+    size_t smem;
+    int blocks_per_sm;
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// View a [NB][Hkv][BS][D] bf16 pool as a 3-D tensor (D, BS, NB*Hkv) whose
+// boxes are [64 columns][BS rows][1 page] with the 128-byte swizzle.
+bool encode_pool_map(CUtensorMap* map, const void* pool, int rows, int D, int BS) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(BS),
+                          static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(BS) * D * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BS), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Optional override "warps,stages" of the split kernel's block shape.
+void tuning_override(int* warps, int* stages) {
+    const char* s = std::getenv("PA_SPLIT_TUNING");
+    if (!s) return;
+    int w = 0, st = 0;
+    if (std::sscanf(s, "%d,%d", &w, &st) == 2 && w >= 1 && w <= 8 && st >= 1 && st <= 16) {
+        *warps = w;
+        *stages = st;
+    }
+}
+
+struct DeviceGuard {
+    int prev = -1;
+    explicit DeviceGuard(int dev) {
+        if (dev >= 0 && cudaGetDevice(&prev) == cudaSuccess && prev != dev) cudaSetDevice(dev);
+        else prev = -1;
+    }
+    ~DeviceGuard() {
+        if (prev >= 0) cudaSetDevice(prev);
+    }
+};
+
+}  // namespace
+
+struct pa_plan {
+    int device = -1;
+    int num_sms = 0;
+    void* ws = nullptr;
+    size_t ws_bytes = 0;
+    int* err = nullptr;
+    int forced_path = PA_PATH_AUTO;
+    int last_path = 0, last_blocks = 0, last_warps = 0;
+    cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
+    MapKey kkey, vkey;
+    CUtensorMap kmap, vmap;
+    std::vector<OccKey> occ;
+};
+
+extern "C" {
+
+const char* pa_status_str(pa_status s) {
+    switch (s) {
+        case PA_OK: return "ok";
+        case PA_ERR_NULL: return "a required pointer is NULL";
+        case PA_ERR_SHAPE: return "sizes out of range or inconsistent";
+        case PA_ERR_DTYPE: return "unsupported element type or path";
+        case PA_ERR_BLOCK_SIZE: return "block_size must be 16 or 32";
+        case PA_ERR_WORKSPACE: return "workspace too small";
+        case PA_ERR_CUDA: return "a CUDA call failed";
+        case PA_ERR_BOUNDS: return "a length or table entry was out of range on the device";
+        case PA_ERR_ALIGN: return "a tensor is not 16-byte aligned";
+    }
+    return "unknown status";
+}
+
+pa_status pa_append_kv(const void* k_new, const void* v_new, void* k_pool, void* v_pool,
+                       const int32_t* block_tables, int max_blocks, const int32_t* cache_lens,
+                       int B, int Hkv, int D, int block_size, int num_blocks, pa_dtype kv_dtype,
+                       struct CUstream_st* stream) {
+    if (!k_new || !v_new || !k_pool || !v_pool || !block_tables || !cache_lens) return PA_ERR_NULL;
+    if (kv_dtype != PA_F32 && kv_dtype != PA_BF16) return PA_ERR_DTYPE;
+    if (block_size != 16 && block_size != 32) return PA_ERR_BLOCK_SIZE;
+    if (B < 0 || Hkv < 1 || (D != 64 && D != 128) || num_blocks < 1 || max_blocks < 1)
+        return PA_ERR_SHAPE;
+    if (static_cast<int64_t>(max_blocks) * block_size > INT32_MAX) return PA_ERR_SHAPE;
+    if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_pool) || !aligned16(v_pool))
+        return PA_ERR_ALIGN;
+    if (B == 0) return PA_OK;
+    pa::AppendArgs a{k_new, v_new, k_pool, v_pool, block_tables, cache_lens,
+                     B, Hkv, D, block_size, max_blocks, num_blocks,
+                     kv_dtype == PA_F32 ? 4 : 2};
+    return pa::launch_append(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
+pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
+                    const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int B,
+                    int Hq, int Hkv, int D, int block_size, int num_blocks, int max_seq_len,
+                    float scale, pa_dtype kv_dtype, void* out, pa_dtype out_dtype,
+                    pa_plan** plan_inout, struct CUstream_st* stream_) {
+    if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out || !plan_inout)
+        return PA_ERR_NULL;
+    if ((kv_dtype != PA_F32 && kv_dtype != PA_BF16) || (out_dtype != PA_F32 && out_dtype != PA_BF16))
+        return PA_ERR_DTYPE;
+    if (block_size != 16 && block_size != 32) return PA_ERR_BLOCK_SIZE;
+    if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (D != 64 && D != 128) || num_blocks < 1 ||
+        max_blocks < 1 || max_seq_len < 1 || !std::isfinite(scale) || B > kMaxBatch)
+        return PA_ERR_SHAPE;
+    if (static_cast<int64_t>(num_blocks) * Hkv > INT32_MAX ||
+        static_cast<int64_t>(max_blocks) * block_size > INT32_MAX)
+        return PA_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return PA_ERR_ALIGN;
+    if (B == 0) return PA_OK;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
+    pa_plan* plan = *plan_inout;
+    if (!plan) {
+        plan = new pa_plan();
+        plan->device = dev;
+        if (cudaDeviceGetAttribute(&plan->num_sms, cudaDevAttrMultiProcessorCount, dev) !=
+                cudaSuccess ||
+            cudaMalloc(reinterpret_cast<void**>(&plan->err), 256) != cudaSuccess ||
+            cudaMemset(plan->err, 0, 256) != cudaSuccess) {
+            if (plan->err) cudaFree(plan->err);
+            delete plan;
+            return PA_ERR_CUDA;
+        }
+        *plan_inout = plan;
+    }
+    if (plan->device != dev) return PA_ERR_CUDA;  // a plan belongs to one device
+
+    const int g = Hq / Hkv;
+    int path = plan->forced_path;
+    if (path == PA_PATH_AUTO) {
+        path = kv_dtype == PA_F32 ? PA_PATH_SIMPLE : (g == 1 ? PA_PATH_FMA : PA_PATH_MMA);
+    }
+    if (kv_dtype == PA_F32 && path != PA_PATH_SIMPLE) return PA_ERR_DTYPE;
+    const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+
+    if (path == PA_PATH_SIMPLE) {
+        pa::SimpleArgs a{q, k_pool, v_pool, block_tables, seq_lens, out, plan->err,
+                         B, Hq, Hkv, D, block_size, max_blocks, num_blocks, max_seq_len,
+                         scale_log2, kv_dtype == PA_BF16, out_dtype == PA_BF16};
+        if (plan->ev_start) cudaEventRecord(plan->ev_start, stream);
+        const cudaError_t e = pa::launch_simple(a, stream);
+        if (plan->ev_stop) cudaEventRecord(plan->ev_stop, stream);
+        plan->last_path = PA_PATH_SIMPLE;
+        plan->last_blocks = (B * Hq + 3) / 4;
+        plan->last_warps = B * Hq;
+        return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
+
+    // Split paths (bf16 pools).
+    int nslices, GS, NT = 0, kind;
+    if (path == PA_PATH_FMA) {
+        kind = pa::kSplitFma;
+        nslices = g;  // one query head per kv unit
+        GS = 1;
+    } else {
+        kind = pa::kSplitMma;
+        nslices = (g + kHeadSlice - 1) / kHeadSlice;
+        GS = (g + nslices - 1) / nslices;
+        NT = (GS + 7) / 8;
+    }
+    const int U = Hkv * nslices;
+    const int64_t max_pages = (static_cast<int64_t>(std::min(max_seq_len, max_blocks * block_size)) +
+                               block_size - 1) / block_size;
+    const int64_t P_max = static_cast<int64_t>(B) * U * max_pages;
+    if (P_max > INT32_MAX) return PA_ERR_SHAPE;
+
+    const size_t stage_bytes = round_up(2u * block_size * D * 2u + static_cast<size_t>(GS) * D * 2u, 1024);
+    const size_t lens_bytes = round_up(static_cast<size_t>(2 * B + 1) * 4u, 1024);
+    int warps = 4;
+    int stages = static_cast<int>(std::min<size_t>(6, kRingBudget / (warps * stage_bytes)));
+    tuning_override(&warps, &stages);
+    if (stages < 1) stages = 1;
+    const size_t smem = 1024 + lens_bytes + static_cast<size_t>(warps) * stages * stage_bytes +
+                        static_cast<size_t>(warps) * stages * 8;
+    if (smem > kSmemLimit) return PA_ERR_SHAPE;
+
+    SplitLaunch L{kind, D, block_size, NT, warps, 0, smem};
+    int per_sm = 0;
+    for (const OccKey& o : plan->occ) {
+        if (o.kind == kind && o.D == D && o.BS == block_size && o.NT == NT && o.warps == warps &&
+            o.smem == smem)
+            per_sm = o.blocks_per_sm;
+    }
+    if (per_sm == 0) {
+        cudaError_t e;
+        per_sm = pa::split_blocks_per_sm(L, &e);
+        if (e != cudaSuccess || per_sm < 1) return PA_ERR_CUDA;
+        plan->occ.push_back(OccKey{kind, D, block_size, NT, warps, smem, per_sm});
+    }
+    const int64_t need = (P_max + static_cast<int64_t>(warps) * kMinPagesPerWarp - 1) /
+                         (static_cast<int64_t>(warps) * kMinPagesPerWarp);
+    L.blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(need, static_cast<int64_t>(plan->num_sms) * per_sm)));
+    const int NW = L.blocks * warps;
+
+    // Workspace: metadata, partial (m, l), partial value sums.
+    const size_t meta_bytes = round_up(static_cast<size_t>(pa::kMetaHeader + B + 1) * 4u, 256);
+    const size_t ml_bytes = round_up(static_cast<size_t>(2) * NW * GS * 2 * 4u, 256);
+    const size_t acc_bytes = round_up(static_cast<size_t>(2) * NW * GS * D * 4u, 256);
+    const size_t need_ws = meta_bytes + ml_bytes + acc_bytes;
+    if (plan->ws_bytes < need_ws) {
+        if (plan->ws) cudaFree(plan->ws);
+        plan->ws = nullptr;
+        plan->ws_bytes = 0;
+        if (cudaMalloc(&plan->ws, need_ws) != cudaSuccess) return PA_ERR_CUDA;
+        plan->ws_bytes = need_ws;
+    }
+    char* ws = static_cast<char*>(plan->ws);
+    int* meta = reinterpret_cast<int*>(ws);
+    float* ml = reinterpret_cast<float*>(ws + meta_bytes);
+    float* acc = reinterpret_cast<float*>(ws + meta_bytes + ml_bytes);
+
+    const int rows = num_blocks * Hkv;
+    MapKey kk{k_pool, rows, D, block_size}, vk{v_pool, rows, D, block_size};
+    if (!(plan->kkey == kk)) {
+        if (!encode_pool_map(&plan->kmap, k_pool, rows, D, block_size)) {
+            plan->kkey = MapKey{};
+            return PA_ERR_CUDA;
+        }
+        plan->kkey = kk;
+    }
+    if (!(plan->vkey == vk)) {
+        if (!encode_pool_map(&plan->vmap, v_pool, rows, D, block_size)) {
+            plan->vkey = MapKey{};
+            return PA_ERR_CUDA;
+        }
+        plan->vkey = vk;
+    }
+
+    pa::SplitArgs a{};
+    a.q = static_cast<const uint16_t*>(q);
+    a.tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.ws_acc = acc;
+    a.ws_ml = ml;
+    a.ws_meta = meta;
+    a.err = plan->err;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.g = g;
+    a.GS = GS;
+    a.nslices = nslices;
+    a.U = U;
+    a.max_blocks = max_blocks;
+    a.num_blocks = num_blocks;
+    a.max_seq_len = max_seq_len;
+    a.scale_log2 = scale_log2;
+    a.out_bf16 = out_dtype == PA_BF16;
+    a.stages = stages;
+    a.stage_bytes = static_cast<int>(stage_bytes);
+    a.lens_bytes = static_cast<int>(lens_bytes);
+
+    if (plan->ev_start) cudaEventRecord(plan->ev_start, stream);
+    cudaError_t e = pa::launch_split(L, plan->kmap, plan->vmap, a, stream);
+    if (plan->ev_stop) cudaEventRecord(plan->ev_stop, stream);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
+    pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, GS, nslices, U, D, out_dtype == PA_BF16};
+    e = pa::launch_merge(m, stream);
+    plan->last_path = path;
+    plan->last_blocks = L.blocks;
+    plan->last_warps = NW;
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_free(pa_plan* plan) {
+    if (!plan) return PA_OK;
+    DeviceGuard guard(plan->device);
+    pa_status st = PA_OK;
+    if (plan->ws && cudaFree(plan->ws) != cudaSuccess) st = PA_ERR_CUDA;
+    if (plan->err && cudaFree(plan->err) != cudaSuccess) st = PA_ERR_CUDA;
+    delete plan;
+    return st;
+}
+
+pa_status pa_last_device_error(pa_plan* plan, int* err) {
+    if (!err) return PA_ERR_NULL;
+    *err = 0;
+    if (!plan) {
+        if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+        return pa::read_append_error(err) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
+    DeviceGuard guard(plan->device);
+    if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpy(&v, plan->err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemset(plan->err, 0, sizeof(int)) != cudaSuccess)
+        return PA_ERR_CUDA;
+    *err = v;
+    return PA_OK;
+}
+
+pa_status pa_plan_set_path(pa_plan* plan, int path) {
+    if (!plan) return PA_ERR_NULL;
+    if (path < PA_PATH_AUTO || path > PA_PATH_MMA) return PA_ERR_SHAPE;
+    plan->forced_path = path;
+    return PA_OK;
+}
+
+pa_status pa_plan_info(const pa_plan* plan, int* path, int* blocks, int* warps) {
+    if (!plan) return PA_ERR_NULL;
+    if (path) *path = plan->last_path;
+    if (blocks) *blocks = plan->last_blocks;
+    if (warps) *warps = plan->last_warps;
+    return PA_OK;
+}
+
+pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
+                                   struct CUevent_st* stop) {
+    if (!plan) return PA_ERR_NULL;
+    if ((start == nullptr) != (stop == nullptr)) return PA_ERR_NULL;
+    plan->ev_start = reinterpret_cast<cudaEvent_t>(start);
+    plan->ev_stop = reinterpret_cast<cudaEvent_t>(stop);
+    return PA_OK;
+}
+
+}  // extern "C"

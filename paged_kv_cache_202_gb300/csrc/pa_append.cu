@@ -1,0 +1,60 @@
+// KV append: the step's new key/value rows go to slot cache_len % BS of the
+// physical block that the table names for logical block cache_len / BS -- the
+// only partly filled block of the sequence ("PagedAttention: The Cache Was
+// Storing Nothing" §1 and §2.2). A raw 16-byte-vector copy, bit-exact.
+#include "pa_internal.h"
+
+namespace pa {
+namespace {
+
+__device__ int g_append_error;  // library-wide append error word (per device)
+
+__global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
+    const int b = blockIdx.x;
+    const int pos = a.cache_lens[b];
+    if (pos < 0 || pos >= a.max_blocks * a.BS) {
+        if (threadIdx.x == 0) atomicOr(&g_append_error, kErrCacheLen);
+        return;
+    }
+    const int phys = a.tables[static_cast<size_t>(b) * a.max_blocks + pos / a.BS];
+    if (phys < 0 || phys >= a.num_blocks) {
+        if (threadIdx.x == 0) atomicOr(&g_append_error, kErrTable);
+        return;
+    }
+    const int row_bytes = a.D * a.elem_bytes;
+    const int chunks = row_bytes / 16;        // 16-byte vectors per head row
+    const int per_pool = a.Hkv * chunks;
+    const int slot = pos % a.BS;
+    for (int i = threadIdx.x; i < 2 * per_pool; i += blockDim.x) {
+        const int which = i / per_pool;       // 0 = K, 1 = V
+        const int r = i - which * per_pool;
+        const int h = r / chunks, c = r - h * chunks;
+        const char* src = static_cast<const char*>(which ? a.v_new : a.k_new) +
+                          (static_cast<size_t>(b) * a.Hkv + h) * row_bytes + c * 16;
+        char* dst = static_cast<char*>(which ? a.vpool : a.kpool) +
+                    ((static_cast<size_t>(phys) * a.Hkv + h) * a.BS + slot) * row_bytes + c * 16;
+        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
+    if (a.B == 0) return cudaSuccess;
+    const int per_seq = 2 * a.Hkv * (a.D * a.elem_bytes / 16);
+    const int threads = per_seq >= 256 ? 256 : ((per_seq + 31) / 32) * 32;
+    append_kernel<<<a.B, threads, 0, stream>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t read_append_error(int* err) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_append_error, sizeof(int));
+    if (e != cudaSuccess) return e;
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_append_error, &zero, sizeof(int));
+    *err = v;
+    return e;
+}
+
+}  // namespace pa

@@ -1,0 +1,97 @@
+// Internal declarations shared by the host entry points and the kernel files.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+// Workspace metadata written by block 0 of the split kernel and read by the
+// merge kernel: [0] total pages P, [1] pages per warp, [2] warps, [3] unused,
+// then the page prefix sums pre[0..B] (pre[b] = pages of sequences < b).
+constexpr int kMetaHeader = 4;
+
+// Bits of the device error word (mirrors PA_DEVERR_* in pa.h).
+constexpr int kErrSeqLen = 1;
+constexpr int kErrTable = 2;
+constexpr int kErrTimeout = 4;
+constexpr int kErrCacheLen = 8;
+
+// Wall-clock limit of any single pipeline wait inside a kernel.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+enum SplitKind { kSplitFma = 0, kSplitMma = 1 };
+
+// Arguments of the split-attention kernels (bf16 KV).
+struct SplitArgs {
+    const uint16_t* q;         // [B][Hq][D] bf16 bits
+    const int32_t* tables;     // [B][max_blocks]
+    const int32_t* seq_lens;   // [B]
+    void* out;                 // [B][Hq][D], bf16 or f32
+    float* ws_acc;             // [2 * warps][GS][D]  partial value sums
+    float* ws_ml;              // [2 * warps][GS][2]  partial (max, sum)
+    int* ws_meta;              // kMetaHeader + B + 1 ints
+    int* err;                  // device error word
+    int B, Hq, Hkv, g;         // g = Hq / Hkv
+    int GS, nslices, U;        // q heads per slice, slices per kv head, U = Hkv * nslices
+    int max_blocks, num_blocks, max_seq_len;
+    float scale_log2;          // scale * log2(e)
+    int out_bf16;
+    int stages;                // pipeline stages per warp
+    int stage_bytes;           // bytes per stage (multiple of 1024)
+    int lens_bytes;            // bytes of the per-sequence arrays at the front of shared memory
+};
+
+struct SplitLaunch {
+    int kind;      // SplitKind
+    int D, BS, NT; // head dim, block size, n-tiles of 8 q heads (MMA)
+    int warps;     // warps per block
+    int blocks;    // grid size
+    size_t smem;   // dynamic shared memory bytes
+};
+
+// Returns the resident blocks per SM of a split-kernel variant at the given
+// block size and dynamic shared memory, or 0 (and sets *status) on error.
+int split_blocks_per_sm(const SplitLaunch& L, cudaError_t* status);
+cudaError_t launch_split(const SplitLaunch& L, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                         const SplitArgs& a, cudaStream_t stream);
+
+struct MergeArgs {
+    const int* ws_meta;
+    const float* ws_acc;
+    const float* ws_ml;
+    void* out;
+    int B, Hq, g, GS, nslices, U, D;
+    int out_bf16;
+};
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
+
+struct SimpleArgs {
+    const void* q;
+    const void* kpool;
+    const void* vpool;
+    const int32_t* tables;
+    const int32_t* seq_lens;
+    void* out;
+    int* err;
+    int B, Hq, Hkv, D, BS, max_blocks, num_blocks, max_seq_len;
+    float scale_log2;
+    int kv_bf16, out_bf16;
+};
+cudaError_t launch_simple(const SimpleArgs& a, cudaStream_t stream);
+
+struct AppendArgs {
+    const void* k_new;
+    const void* v_new;
+    void* kpool;
+    void* vpool;
+    const int32_t* tables;
+    const int32_t* cache_lens;
+    int B, Hkv, D, BS, max_blocks, num_blocks, elem_bytes;
+};
+cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+// Read and clear the append error word of the current device (synchronous).
+cudaError_t read_append_error(int* err);
+
+}  // namespace pa

@@ -1,0 +1,68 @@
+// Instantiations and launch of the split paged decode kernels.
+#include "pa_split.cuh"
+
+namespace pa {
+namespace split {
+
+template <int D, int BS>
+__global__ void __launch_bounds__(256, 1)
+    fma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+               const SplitArgs a) {
+    split_body<D, BS, FmaState<D, BS>>(&kmap, &vmap, a);
+}
+
+template <int D, int BS, int NT>
+__global__ void __launch_bounds__(256, 1)
+    mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+               const SplitArgs a) {
+    split_body<D, BS, MmaState<D, BS, NT>>(&kmap, &vmap, a);
+}
+
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, SplitArgs);
+
+KernelFn select(const SplitLaunch& L) {
+#define PA_CASE(D_, BS_)                                                        \
+    if (L.D == D_ && L.BS == BS_) {                                             \
+        if (L.kind == kSplitFma) return fma_kernel<D_, BS_>;                    \
+        if (L.kind == kSplitMma && L.NT == 1) return mma_kernel<D_, BS_, 1>;    \
+        if (L.kind == kSplitMma && L.NT == 2) return mma_kernel<D_, BS_, 2>;    \
+    }
+    PA_CASE(128, 16)
+    PA_CASE(128, 32)
+    PA_CASE(64, 16)
+    PA_CASE(64, 32)
+#undef PA_CASE
+    return nullptr;
+}
+
+}  // namespace split
+
+int split_blocks_per_sm(const SplitLaunch& L, cudaError_t* status) {
+    split::KernelFn fn = split::select(L);
+    if (!fn) {
+        *status = cudaErrorInvalidValue;
+        return 0;
+    }
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(fn),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(L.smem));
+    if (e != cudaSuccess) {
+        *status = e;
+        return 0;
+    }
+    int n = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, reinterpret_cast<const void*>(fn),
+                                                      L.warps * 32, L.smem);
+    *status = e;
+    return e == cudaSuccess ? n : 0;
+}
+
+cudaError_t launch_split(const SplitLaunch& L, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                         const SplitArgs& a, cudaStream_t stream) {
+    split::KernelFn fn = split::select(L);
+    if (!fn) return cudaErrorInvalidValue;
+    fn<<<L.blocks, L.warps * 32, L.smem, stream>>>(kmap, vmap, a);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,613 @@
+// Split paged decode attention for bf16 KV pools.
+//
+// Work decomposition. Every (sequence b, kv unit u) pair is a "segment": the
+// ordered list of the nb_b = ceil(L_b / BS) logical blocks ("pages") the
+// query heads of unit u attend over ("39 · PagedAttention" §2: walk the
+// logical blocks in order through the block table). A kv unit is one kv head
+// and one slice of at most 16 of the query heads that share it
+// ("PagedAttention: The Cache Was Storing Nothing" §3.1). All segments are
+// concatenated into one stream of P pages and cut into equal contiguous
+// ranges, one per resident warp of a persistent grid. A warp therefore
+// processes a balanced number of pages whatever the length mix; it produces a
+// finished output row for every segment it covers completely, and a partial
+// (m, l, acc) for at most two segments cut by its range boundaries. The merge
+// kernel combines those with the two-partial rule of "39 · PagedAttention" §3.
+// Splitting along the sequence is what keeps the chip busy when a decode has
+// only one query row ("PagedAttention: The Cache Was Storing Nothing", "Where
+// this goes next").
+//
+// Data movement. Each warp runs its own pipeline of `stages` shared-memory
+// stages. One page of one kv head is a contiguous [BS][D] bf16 block in the
+// pool; lane 0 reads its physical id from the block table (one indirection
+// per page) and moves the K and V pages into a stage with tiled bulk tensor
+// copies in 64-column boxes with the 128-byte swizzle, completing on the
+// stage's mbarrier. The first page of a segment also brings the segment's
+// query rows. Consumers read the stage with ldmatrix / 128-bit loads that the
+// swizzle keeps free of bank conflicts.
+//
+// Arithmetic. Scores are kept in the log2 domain (s * scale * log2 e) so the
+// exponentials are single ex2 instructions. Slots past a sequence's length
+// are excluded by predicate, never multiplied by zero: their scores become
+// -inf and, on the tensor-core path, their V elements are replaced by zero
+// before the product so that NaN or garbage there cannot leak into a sum.
+//   * FMA path (one query head per kv head): lane = (d-half, token); each
+//     lane dots half a key with half the query, a shuffle joins the halves.
+//   * MMA path (a GQA group of g >= 2 query heads): S^T[16 tok x 8 heads] =
+//     K[16 x D] Q^T via bf16 m16n8k16 tiles with fp32 accumulation; the
+//     probabilities are split into a bf16 pair hi + lo (about 16 significant
+//     bits together), transposed in registers (movmatrix) and fed to
+//     O^T[D x 8 heads] += V^T[D x 16 tok] (P_hi^T + P_lo^T).
+#pragma once
+
+#include "pa_internal.h"
+#include "pa_ptx.cuh"
+
+namespace pa {
+namespace split {
+
+struct Cursor {
+    int b, u, p, nb;  // sequence, kv unit, logical page, pages of sequence b
+};
+
+__device__ __forceinline__ int seq_pages(const int* pre, int b) { return pre[b + 1] - pre[b]; }
+
+__device__ __forceinline__ void advance(Cursor& c, const int* pre, int U, int B) {
+    if (++c.p == c.nb) {
+        c.p = 0;
+        if (++c.u == U) {
+            c.u = 0;
+            do {
+                ++c.b;
+            } while (c.b < B && seq_pages(pre, c.b) == 0);
+            c.nb = (c.b < B) ? seq_pages(pre, c.b) : 0;
+        }
+    }
+}
+
+// Block-wide: validate the lengths and build the page prefix sums pre[0..B]
+// and the attended lengths len[0..B) in shared memory. Invalid lengths count
+// as zero pages (their rows are written as zeros by the merge kernel).
+template <int BS>
+__device__ void scan_lengths(const int32_t* __restrict__ seq_lens, int B, int limit, int* pre,
+                             int* len, int* err) {
+    __shared__ int warp_tot[32];
+    const int T = blockDim.x, tid = threadIdx.x;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = T >> 5;
+    const int chunk = (B + T - 1) / T;
+    const int lo = min(tid * chunk, B), hi = min(lo + chunk, B);
+    int sum = 0;
+    bool bad = false;
+    for (int b = lo; b < hi; ++b) {
+        const int L = seq_lens[b];
+        const bool ok = L >= 1 && L <= limit;
+        bad |= !ok;
+        len[b] = ok ? L : 0;
+        sum += ok ? (L + BS - 1) / BS : 0;
+    }
+    if (bad && blockIdx.x == 0) atomicOr(err, kErrSeqLen);
+    int x = sum;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) warp_tot[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        int t = lane < nwarps ? warp_tot[lane] : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, t, off);
+            if (lane >= off) t += y;
+        }
+        if (lane < nwarps) warp_tot[lane] = t;
+    }
+    __syncthreads();
+    int run = x - sum + (warp > 0 ? warp_tot[warp - 1] : 0);
+    for (int b = lo; b < hi; ++b) {
+        pre[b] = run;
+        run += (len[b] + BS - 1) / BS;
+    }
+    if (tid == T - 1) pre[B] = run;
+    __syncthreads();
+}
+
+__device__ __forceinline__ uint32_t swz(uint32_t region, int chunk, int tok, int BS) {
+    // 16-byte chunk `chunk` of row `tok` in a [BS][D] page stored as D/64 boxes
+    // of [BS][64] with the 128-byte swizzle.
+    return region + (chunk >> 3) * (BS * 128) + tok * 128 + ((((chunk & 7) ^ (tok & 7))) << 4);
+}
+
+// ------------------------------------------------------------------ FMA path
+template <int D, int BS>
+struct FmaState {
+    static constexpr int HALF = D / 2;   // query elements per lane
+    static constexpr int DPL = D / 32;   // output elements per lane
+    static constexpr int TPL = BS / 16;  // tokens per lane
+    float qf[HALF];
+    float acc[DPL];
+    float m, l;
+
+    __device__ __forceinline__ void start(uint32_t qst, int /*nh*/, int lane) {
+        const int hh = lane >> 4;
+#pragma unroll
+        for (int c = 0; c < HALF / 8; ++c) {
+            const uint4 w = lds_u128(qst + hh * D + c * 16);
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                qf[c * 8 + 2 * e] = bf16_lo(ws[e]);
+                qf[c * 8 + 2 * e + 1] = bf16_hi(ws[e]);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+        m = -INFINITY;
+        l = 0.f;
+    }
+
+    __device__ __forceinline__ void page(uint32_t kst, uint32_t vst, int nv, float scale_log2,
+                                         int lane) {
+        const int hh = lane >> 4, tl = lane & 15;
+        float sc[TPL];
+#pragma unroll
+        for (int j = 0; j < TPL; ++j) {
+            const int tok = tl + 16 * j;
+            float dot = 0.f;
+#pragma unroll
+            for (int c = 0; c < HALF / 8; ++c) {
+                const uint4 w = lds_u128(swz(kst, hh * (HALF / 8) + c, tok, BS));
+                const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    dot = fmaf(qf[c * 8 + 2 * e], bf16_lo(ws[e]), dot);
+                    dot = fmaf(qf[c * 8 + 2 * e + 1], bf16_hi(ws[e]), dot);
+                }
+            }
+            dot += __shfl_xor_sync(0xffffffffu, dot, 16);
+            sc[j] = tok < nv ? dot * scale_log2 : -INFINITY;
+        }
+        float mx = sc[0];
+#pragma unroll
+        for (int j = 1; j < TPL; ++j) mx = fmaxf(mx, sc[j]);
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m_new = fmaxf(m, mx);
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float alpha = fast_exp2(m - m_use);
+        float p[TPL];
+        float psum = 0.f;
+#pragma unroll
+        for (int j = 0; j < TPL; ++j) {
+            p[j] = fast_exp2(sc[j] - m_use);
+            psum += p[j];
+        }
+        l = l * alpha + (hh == 0 ? psum : 0.f);
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] *= alpha;
+        m = m_new;
+        // Weighted values: lane owns DPL consecutive dims, token by token.
+        const int d0 = lane * DPL;
+        const int chunk = d0 >> 3;
+        const uint32_t within = (d0 & 7) * 2;
+#pragma unroll
+        for (int j = 0; j < TPL; ++j) {
+          const int nt_j = min(16, nv - 16 * j);
+          for (int tt = 0; tt < nt_j; ++tt) {
+            const int t = 16 * j + tt;
+            const float pt = __shfl_sync(0xffffffffu, p[j], tt);
+            const uint32_t addr = swz(vst, chunk, t, BS) + within;
+            if constexpr (DPL == 4) {
+                const uint2 w = lds_u64(addr);
+                acc[0] = fmaf(pt, bf16_lo(w.x), acc[0]);
+                acc[1] = fmaf(pt, bf16_hi(w.x), acc[1]);
+                acc[2] = fmaf(pt, bf16_lo(w.y), acc[2]);
+                acc[3] = fmaf(pt, bf16_hi(w.y), acc[3]);
+            } else {
+                const uint32_t w = lds_u32(addr);
+                acc[0] = fmaf(pt, bf16_lo(w), acc[0]);
+                acc[1] = fmaf(pt, bf16_hi(w), acc[1]);
+            }
+          }
+        }
+    }
+
+    __device__ __forceinline__ void finish(const SplitArgs& a, int b, int hq0, int nh, bool full,
+                                           bool poison, int slot, int lane) {
+        (void)nh;
+        float lt = l;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+        const int d0 = lane * DPL;
+        if (full) {
+            const float inv = poison ? 0.f : 1.f / lt;
+            const size_t row = (static_cast<size_t>(b) * a.Hq + hq0) * D;
+            if (a.out_bf16) {
+                uint16_t* o = static_cast<uint16_t*>(a.out) + row + d0;
+                if constexpr (DPL == 4) {
+                    uint2 w;
+                    w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+                    w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+                    *reinterpret_cast<uint2*>(o) = w;
+                } else {
+                    *reinterpret_cast<uint32_t*>(o) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+                }
+            } else {
+                float* o = static_cast<float*>(a.out) + row + d0;
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) o[i] = acc[i] * inv;
+            }
+        } else {
+            float* o = a.ws_acc + static_cast<size_t>(slot) * a.GS * D + d0;
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) o[i] = poison ? 0.f : acc[i];
+            if (lane == 0) {
+                a.ws_ml[static_cast<size_t>(slot) * a.GS * 2 + 0] = poison ? __int_as_float(0x7fc00000) : m;
+                a.ws_ml[static_cast<size_t>(slot) * a.GS * 2 + 1] = poison ? 0.f : lt;
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------------ MMA path
+template <int D, int BS, int NT>
+struct MmaState {
+    static constexpr int KS = D / 16;     // k-steps of the score product, m-tiles of the value product
+    static constexpr int TILES = BS / 16; // 16-token tiles per page
+    uint32_t qb[KS][NT][2];               // Q^T fragments (B operand)
+    float o[KS][NT][4];                   // O^T accumulators
+    float m[NT][2], l[NT][2];
+
+    __device__ __forceinline__ void start(uint32_t qst, int nh, int lane) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int row = nt * 8 + (lane >> 2);
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                const uint32_t addr = qst + row * (D * 2) + (16 * kk + 2 * (lane & 3)) * 2;
+                qb[kk][nt][0] = row < nh ? lds_u32(addr) : 0u;
+                qb[kk][nt][1] = row < nh ? lds_u32(addr + 16) : 0u;
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                m[nt][j] = -INFINITY;
+                l[nt][j] = 0.f;
+            }
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[mt][nt][i] = 0.f;
+        }
+    }
+
+    __device__ __forceinline__ void page(uint32_t kst, uint32_t vst, int nv, float scale_log2,
+                                         int lane) {
+        float s[TILES][NT][4];
+#pragma unroll
+        for (int t = 0; t < TILES; ++t)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) s[t][nt][i] = 0.f;
+        // Scores S^T = K Q^T.
+#pragma unroll
+        for (int t = 0; t < TILES; ++t) {
+            const int tok = t * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(swz(kst, 2 * kk + (lane >> 4), tok, BS), a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_bf16_16816(s[t][nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+            }
+        }
+        // Scale to the log2 domain, mask the tail, column maxima over the tokens.
+        float mx[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            mx[nt][0] = -INFINITY;
+            mx[nt][1] = -INFINITY;
+        }
+#pragma unroll
+        for (int t = 0; t < TILES; ++t) {
+            const int tok = t * 16 + (lane >> 2);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int tk = tok + (i >= 2 ? 8 : 0);
+                    const float v = tk < nv ? s[t][nt][i] * scale_log2 : -INFINITY;
+                    s[t][nt][i] = v;
+                    mx[nt][i & 1] = fmaxf(mx[nt][i & 1], v);
+                }
+            }
+        }
+        float alpha[NT][2], m_use[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float x = mx[nt][j];
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 4));
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 8));
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, 16));
+                const float m_new = fmaxf(m[nt][j], x);
+                m_use[nt][j] = m_new == -INFINITY ? 0.f : m_new;
+                alpha[nt][j] = fast_exp2(m[nt][j] - m_use[nt][j]);
+                m[nt][j] = m_new;
+            }
+        }
+        // Probabilities as a bf16 pair hi + lo (hi = bf16(p), lo = bf16(p - hi)),
+        // transposed in registers into the B operand of P V.
+        uint32_t pb[TILES][NT][2][2];  // [tile][n-tile][hi/lo][token half]
+        float ps[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            ps[nt][0] = 0.f;
+            ps[nt][1] = 0.f;
+        }
+#pragma unroll
+        for (int t = 0; t < TILES; ++t) {
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float p[4];
+#pragma unroll
+                for (int i = 0; i < 4; ++i) p[i] = fast_exp2(s[t][nt][i] - m_use[nt][i & 1]);
+                ps[nt][0] += p[0] + p[2];
+                ps[nt][1] += p[1] + p[3];
+                const uint32_t top = pack_bf16x2(p[0], p[1]);
+                const uint32_t bot = pack_bf16x2(p[2], p[3]);
+                const uint32_t top_lo = pack_bf16x2(p[0] - bf16_lo(top), p[1] - bf16_hi(top));
+                const uint32_t bot_lo = pack_bf16x2(p[2] - bf16_lo(bot), p[3] - bf16_hi(bot));
+                pb[t][nt][0][0] = movmatrix_trans(top);
+                pb[t][nt][0][1] = movmatrix_trans(bot);
+                pb[t][nt][1][0] = movmatrix_trans(top_lo);
+                pb[t][nt][1][1] = movmatrix_trans(bot_lo);
+            }
+        }
+        // Values O^T += V^T P^T.
+        const bool tail = nv < BS;
+        const int t0 = 2 * (lane & 3);
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+#pragma unroll
+            for (int t = 0; t < TILES; ++t) {
+                const int tok = t * 16 + (lane >> 4) * 8 + (lane & 7);
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4_trans(swz(vst, 2 * mt + ((lane >> 3) & 1), tok, BS), a0, a1, a2, a3);
+                if (tail) {
+                    const int tb = t * 16 + t0;
+                    const uint32_t keep01 = (tb < nv ? 0x0000ffffu : 0u) | (tb + 1 < nv ? 0xffff0000u : 0u);
+                    const uint32_t keep89 = (tb + 8 < nv ? 0x0000ffffu : 0u) | (tb + 9 < nv ? 0xffff0000u : 0u);
+                    a0 &= keep01;
+                    a1 &= keep01;
+                    a2 &= keep89;
+                    a3 &= keep89;
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, pb[t][nt][0][0], pb[t][nt][0][1]);
+                    mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, pb[t][nt][1][0], pb[t][nt][1][1]);
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ void finish(const SplitArgs& a, int b, int hq0, int nh, bool full,
+                                           bool poison, int slot, int lane) {
+        float lt[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                float x = l[nt][j];
+                x += __shfl_xor_sync(0xffffffffu, x, 4);
+                x += __shfl_xor_sync(0xffffffffu, x, 8);
+                x += __shfl_xor_sync(0xffffffffu, x, 16);
+                lt[nt][j] = x;
+            }
+        const int dr = lane >> 2;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int head = nt * 8 + 2 * (lane & 3) + j;
+                if (head >= nh) continue;
+                if (full) {
+                    const float inv = poison ? 0.f : 1.f / lt[nt][j];
+                    const size_t row = (static_cast<size_t>(b) * a.Hq + hq0 + head) * D;
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt) {
+#pragma unroll
+                        for (int r = 0; r < 2; ++r) {
+                            const int d = mt * 16 + dr + 8 * r;
+                            const float v = o[mt][nt][2 * r + j] * inv;
+                            if (a.out_bf16)
+                                static_cast<uint16_t*>(a.out)[row + d] = f32_to_bf16_bits(v);
+                            else
+                                static_cast<float*>(a.out)[row + d] = v;
+                        }
+                    }
+                } else {
+                    float* acc = a.ws_acc + (static_cast<size_t>(slot) * a.GS + head) * D;
+#pragma unroll
+                    for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                        for (int r = 0; r < 2; ++r)
+                            acc[mt * 16 + dr + 8 * r] = poison ? 0.f : o[mt][nt][2 * r + j];
+                    if (dr == 0) {
+                        float* ml = a.ws_ml + (static_cast<size_t>(slot) * a.GS + head) * 2;
+                        ml[0] = poison ? __int_as_float(0x7fc00000) : m[nt][j];
+                        ml[1] = poison ? 0.f : lt[nt][j];
+                    }
+                }
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------------ kernel
+template <int D, int BS, typename State>
+__device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtensorMap* vmap,
+                                           const SplitArgs& a) {
+    extern __shared__ uint8_t smem_raw[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    int* pre = reinterpret_cast<int*>(smem_raw + (base - raw));
+    int* len = pre + (a.B + 1);
+    const uint32_t ring0 = base + a.lens_bytes;
+    const uint32_t bars0 = ring0 + static_cast<uint32_t>(W * a.stages * a.stage_bytes);
+
+    if (threadIdx.x == 0) {
+        prefetch_tensormap(kmap);
+        prefetch_tensormap(vmap);
+    }
+    const int limit = min(a.max_seq_len, a.max_blocks * BS);
+    scan_lengths<BS>(a.seq_lens, a.B, limit, pre, len, a.err);
+
+    const int P = a.U * pre[a.B];
+    const int NW = gridDim.x * W;
+    const int per = (P + NW - 1) / NW;
+    if (blockIdx.x == 0) {
+        for (int i = threadIdx.x; i <= a.B; i += blockDim.x) a.ws_meta[kMetaHeader + i] = pre[i];
+        if (threadIdx.x == 0) {
+            a.ws_meta[0] = P;
+            a.ws_meta[1] = per;
+            a.ws_meta[2] = NW;
+            a.ws_meta[3] = 0;
+        }
+    }
+    const int gw = blockIdx.x * W + warp;
+    const int x0 = gw * per;
+    const int x1 = min(x0 + per, P);
+    if (per == 0 || x0 >= x1) return;
+    const int npages = x1 - x0;
+    const int S = a.stages;
+    const uint32_t my_bars = bars0 + warp * S * 8;
+    const uint32_t my_ring = ring0 + static_cast<uint32_t>(warp * S * a.stage_bytes);
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(my_bars + 8 * s, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+
+    // Locate the first page of this warp's range.
+    Cursor cc;
+    {
+        int lo = 0, hi = a.B - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (a.U * pre[mid] <= x0) lo = mid; else hi = mid - 1;
+        }
+        const int nb = seq_pages(pre, lo);
+        const int off = x0 - a.U * pre[lo];
+        cc = Cursor{lo, off / nb, off % nb, nb};
+    }
+    Cursor ci = cc;
+    const uint32_t kv_bytes = 2u * BS * D * 2u;
+    const uint64_t policy = policy_evict_first();
+    int tb_row = -1, tb_base = -1, tbl = -1;  // table batch: entries [tb_base, tb_base+32) of row tb_row
+    uint32_t badmask = 0, phase = 0;
+
+    // Issue page `k` of the range (cursor ci) into stage s; warp-collective.
+    auto issue = [&](int s, bool qstart) {
+        const int pbase = ci.p & ~31;
+        if (ci.b != tb_row || pbase != tb_base) {
+            tb_row = ci.b;
+            tb_base = pbase;
+            tbl = (pbase + lane < ci.nb)
+                      ? __ldg(a.tables + static_cast<size_t>(ci.b) * a.max_blocks + pbase + lane)
+                      : -1;
+        }
+        const int phys = __shfl_sync(0xffffffffu, tbl, ci.p - pbase);
+        const bool bad = phys < 0 || phys >= a.num_blocks;
+        badmask = bad ? (badmask | (1u << s)) : (badmask & ~(1u << s));
+        if (lane == 0) {
+            const uint32_t bar = my_bars + 8 * s;
+            const uint32_t stg = my_ring + static_cast<uint32_t>(s * a.stage_bytes);
+            const int kvh = ci.u / a.nslices, slice = ci.u - kvh * a.nslices;
+            const int nh = min(a.GS, a.g - slice * a.GS);
+            const uint32_t qbytes = qstart ? static_cast<uint32_t>(nh * D * 2) : 0u;
+            if (bad) {
+                atomicOr(a.err, kErrTable);
+                if (qstart) {
+                    mbar_arrive_expect_tx(bar, qbytes);
+                } else {
+                    mbar_arrive(bar);
+                }
+            } else {
+                mbar_arrive_expect_tx(bar, kv_bytes + qbytes);
+                const int row = phys * a.Hkv + kvh;
+#pragma unroll
+                for (int h = 0; h < D / 64; ++h) {
+                    tma_load_3d(stg + h * (BS * 128), kmap, h * 64, 0, row, bar, policy);
+                    tma_load_3d(stg + BS * D * 2 + h * (BS * 128), vmap, h * 64, 0, row, bar, policy);
+                }
+            }
+            if (qstart) {
+                const uint16_t* src =
+                    a.q + (static_cast<size_t>(ci.b) * a.Hq + kvh * a.g + slice * a.GS) * D;
+                bulk_load(stg + 2 * BS * D * 2, src, qbytes, bar);
+            }
+        }
+    };
+
+    int k_issue = 0;
+    for (int s = 0; k_issue < min(S, npages); ++s, ++k_issue) {
+        issue(s, k_issue == 0 || ci.p == 0);
+        advance(ci, pre, a.U, a.B);
+    }
+
+    State st;
+    int p_first = 0, hq0 = 0, nh = 0;
+    bool poison = false;
+    int s = 0;
+    for (int k = 0; k < npages; ++k) {
+        const uint32_t bar = my_bars + 8 * s;
+        const uint32_t stg = my_ring + static_cast<uint32_t>(s * a.stage_bytes);
+        const bool ready = mbar_wait_bounded(bar, (phase >> s) & 1u, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, ready)) {
+            // Give up: report, wait (bounded) for this warp's copies in flight, return.
+            if (lane == 0) atomicOr(a.err, kErrTimeout);
+            for (int j = k; j < k_issue; ++j) {
+                const int sj = j % S;
+                mbar_wait_bounded(my_bars + 8 * sj, (phase >> sj) & 1u, kWaitLimitNs);
+            }
+            return;
+        }
+        phase ^= 1u << s;
+        if (k == 0 || cc.p == 0) {
+            const int kvh = cc.u / a.nslices, slice = cc.u - kvh * a.nslices;
+            nh = min(a.GS, a.g - slice * a.GS);
+            hq0 = kvh * a.g + slice * a.GS;
+            st.start(stg + 2 * BS * D * 2, nh, lane);
+            p_first = cc.p;
+            poison = false;
+        }
+        if ((badmask >> s) & 1u) {
+            poison = true;
+        } else {
+            const int nv = (cc.p == cc.nb - 1) ? len[cc.b] - cc.p * BS : BS;
+            st.page(stg, stg + BS * D * 2, nv, a.scale_log2, lane);
+        }
+        __syncwarp();
+        if (k_issue < npages) {
+            fence_proxy_async_smem();
+            issue(s, ci.p == 0);
+            advance(ci, pre, a.U, a.B);
+            ++k_issue;
+        }
+        if (cc.p == cc.nb - 1 || k == npages - 1) {
+            const bool full = p_first == 0 && cc.p == cc.nb - 1;
+            const int slot = gw * 2 + (p_first > 0 ? 0 : 1);
+            st.finish(a, cc.b, hq0, nh, full, poison, slot, lane);
+        }
+        advance(cc, pre, a.U, a.B);
+        if (++s == S) s = 0;
+    }
+}
+
+}  // namespace split
+}  // namespace pa

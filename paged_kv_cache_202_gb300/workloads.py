@@ -155,6 +155,11 @@ def _draw_lengths(spec, B: int, rng: np.random.Generator) -> np.ndarray:
     kind = spec[0]
     if kind == "fixed":
         return np.full(B, spec[1], dtype=np.int64)
+    if kind == "list":             # explicit lengths, one per sequence
+        out = np.asarray(spec[1], dtype=np.int64)
+        if out.shape != (B,):
+            raise ValueError("length list does not match B")
+        return out
     if kind == "uniform":          # integers, both ends included
         return rng.integers(spec[1], spec[2] + 1, size=B)
     if kind == "loguniform":       # floor(exp(U(ln lo, ln hi))), clipped

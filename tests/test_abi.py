@@ -1,0 +1,132 @@
+"""The C-ABI library builds for sm_103a, loads, exports every declared symbol,
+and rejects bad arguments on the host before touching a GPU (no GPU needed)."""
+
+import ctypes
+
+import pytest
+
+import paged_kv_cache_202_gb300 as pa
+from paged_kv_cache_202_gb300 import _build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return pa.lib()
+
+
+def test_exports_every_declared_function(lib):
+    names = pa.declared_functions()
+    assert {"pa_append_kv", "pa_decode", "pa_free", "pa_status_str",
+            "pa_last_device_error"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"libpa.so does not export {n}"
+
+
+def test_status_strings(lib):
+    for s in range(0, 9):
+        assert pa.pa_status_str(s) and pa.pa_status_str(s) != "unknown status"
+    assert pa.pa_status_str(99) == "unknown status"
+
+
+ALIGNED = 0x10000  # a fake, 16-byte aligned device address: never dereferenced
+
+
+def _decode(lib, **kw):
+    args = dict(q=ALIGNED, k=ALIGNED, v=ALIGNED, bt=ALIGNED, mb=4, sl=ALIGNED, B=2, Hq=8, Hkv=2,
+                D=128, bs=16, NB=64, maxlen=64, scale=0.1, kvdt=pa.PA_BF16, out=ALIGNED,
+                odt=pa.PA_BF16, plan=True)
+    args.update(kw)
+    plan = ctypes.c_void_p(None)
+    pp = ctypes.byref(plan) if args["plan"] else None
+    st = lib.pa_decode(args["q"], args["k"], args["v"], args["bt"], args["mb"], args["sl"],
+                       args["B"], args["Hq"], args["Hkv"], args["D"], args["bs"], args["NB"],
+                       args["maxlen"], args["scale"], args["kvdt"], args["out"], args["odt"], pp,
+                       None)
+    assert plan.value is None, "an argument error must not create a plan"
+    return st
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), pa.PA_ERR_NULL),
+    (dict(k=None), pa.PA_ERR_NULL),
+    (dict(bt=None), pa.PA_ERR_NULL),
+    (dict(sl=None), pa.PA_ERR_NULL),
+    (dict(out=None), pa.PA_ERR_NULL),
+    (dict(plan=False), pa.PA_ERR_NULL),
+    (dict(kvdt=7), pa.PA_ERR_DTYPE),
+    (dict(odt=-1), pa.PA_ERR_DTYPE),
+    (dict(bs=8), pa.PA_ERR_BLOCK_SIZE),
+    (dict(bs=64), pa.PA_ERR_BLOCK_SIZE),
+    (dict(D=96), pa.PA_ERR_SHAPE),
+    (dict(Hq=6, Hkv=4), pa.PA_ERR_SHAPE),
+    (dict(Hkv=0), pa.PA_ERR_SHAPE),
+    (dict(B=-1), pa.PA_ERR_SHAPE),
+    (dict(NB=0), pa.PA_ERR_SHAPE),
+    (dict(mb=0), pa.PA_ERR_SHAPE),
+    (dict(maxlen=0), pa.PA_ERR_SHAPE),
+    (dict(scale=float("nan")), pa.PA_ERR_SHAPE),
+    (dict(B=100000), pa.PA_ERR_SHAPE),
+    (dict(q=ALIGNED + 8), pa.PA_ERR_ALIGN),
+    (dict(out=ALIGNED + 2), pa.PA_ERR_ALIGN),
+    (dict(v=ALIGNED + 4), pa.PA_ERR_ALIGN),
+])
+def test_decode_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _decode(lib, **kw) == status
+
+
+def test_decode_empty_batch_is_a_no_op(lib):
+    assert _decode(lib, B=0) == pa.PA_OK
+
+
+def _append(lib, **kw):
+    args = dict(kn=ALIGNED, vn=ALIGNED, k=ALIGNED, v=ALIGNED, bt=ALIGNED, mb=4, cl=ALIGNED, B=2,
+                Hkv=2, D=128, bs=16, NB=64, dt=pa.PA_BF16)
+    args.update(kw)
+    return lib.pa_append_kv(args["kn"], args["vn"], args["k"], args["v"], args["bt"], args["mb"],
+                            args["cl"], args["B"], args["Hkv"], args["D"], args["bs"], args["NB"],
+                            args["dt"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(kn=None), pa.PA_ERR_NULL),
+    (dict(cl=None), pa.PA_ERR_NULL),
+    (dict(dt=3), pa.PA_ERR_DTYPE),
+    (dict(bs=48), pa.PA_ERR_BLOCK_SIZE),
+    (dict(D=32), pa.PA_ERR_SHAPE),
+    (dict(Hkv=0), pa.PA_ERR_SHAPE),
+    (dict(NB=0), pa.PA_ERR_SHAPE),
+    (dict(k=ALIGNED + 2), pa.PA_ERR_ALIGN),
+])
+def test_append_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _append(lib, **kw) == status
+
+
+def test_append_empty_batch_is_a_no_op(lib):
+    assert _append(lib, B=0) == pa.PA_OK
+
+
+def test_plan_calls_reject_null(lib):
+    assert lib.pa_free(None) == pa.PA_OK
+    assert lib.pa_plan_set_path(None, 0) == pa.PA_ERR_NULL
+    assert lib.pa_plan_info(None, None, None, None) == pa.PA_ERR_NULL
+    assert lib.pa_plan_set_split_events(None, None, None) == pa.PA_ERR_NULL
+    assert lib.pa_last_device_error(None, None) == pa.PA_ERR_NULL
+
+
+def test_binding_byte_counter_matches_oracle():
+    import numpy as np
+    import oracle
+    rng = np.random.default_rng(0)
+    for bs in (16, 32):
+        lens = rng.integers(1, 5000, size=17)
+        for Hq, Hkv, D, e, eo in ((32, 8, 128, 2, 2), (4, 4, 64, 4, 4), (64, 8, 128, 2, 4)):
+            assert pa.decode_bytes(lens, Hq, Hkv, D, bs, e, eo) == \
+                oracle.decode_bytes(lens, Hq, Hkv, D, bs, e, eo)
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(pa, "_lib", None)
+    monkeypatch.setattr(pa, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="missing"):
+        pa.lib()
