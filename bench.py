@@ -135,7 +135,13 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
-def oracle_sample_gbs(wl, budget_s: float, min_pairs: int = 1):
+def _copy_appended(wl):
+    import dataclasses
+    kp, vp = wl.pools_after_append()
+    return dataclasses.replace(wl, k_pool=kp, v_pool=vp)
+
+
+def oracle_sample_gbs(wl, budget_s: float, min_pairs: int = 1, appended: bool = False):
     """Time the fp64 oracle on (b, h) pairs of the workload for about budget_s.
 
     Returns (GB/s of algorithmic bytes, seconds, pairs, threads). The bytes of
@@ -143,7 +149,9 @@ def oracle_sample_gbs(wl, budget_s: float, min_pairs: int = 1):
     """
     import oracle
     import paged_kv_cache_202_gb300 as pa
-    kp, vp = wl.pools_after_append()
+    if not appended:
+        wl = _copy_appended(wl)
+    kp, vp = wl.k_pool, wl.v_pool
     threads = os.cpu_count() or 1
     eb = wl.elem_bytes
     per_seq = [pa.decode_bytes([int(L)], wl.Hq, wl.Hkv, wl.D, wl.block_size, eb, eb) / wl.Hq
@@ -173,6 +181,7 @@ def run_reference(args, rank):
     import oracle
     oracle.build()
     wl = make_workload(args.workload)
+    wl.append_in_place()
     total = args.steps + args.warmup
     per_step = max(0.05, min(20.0, 120.0 / max(total, 1)))
     vals = []
@@ -180,7 +189,7 @@ def run_reference(args, rank):
     pairs_all = 0
     threads = 1
     for step in range(total):
-        gbs, el, pairs, threads = oracle_sample_gbs(wl, per_step)
+        gbs, el, pairs, threads = oracle_sample_gbs(wl, per_step, appended=True)
         if step >= args.warmup:
             vals.append(gbs)
             t_all += el
@@ -220,7 +229,6 @@ def run_ours(args, rank, world, local_rank):
             torch.distributed.barrier()
 
     wl = make_workload(args.workload, seed=args.seed + rank if args.seed is not None else None)
-    t_gen = time.time()
     bf = wl.dtype == "bf16"
 
     def to_dev(a):
@@ -232,6 +240,8 @@ def run_ours(args, rank, world, local_rank):
     tables = torch.from_numpy(wl.block_tables).to(dev)
     seq_lens = torch.from_numpy(wl.seq_lens).to(dev)
     cache_lens = torch.from_numpy(wl.cache_lens).to(dev)
+    torch.cuda.synchronize()
+    wl.append_in_place()   # host copy now holds the post-append state the oracle reads
     out_dtype = torch.bfloat16 if bf else torch.float32
     out = torch.empty(wl.B, wl.Hq, wl.D, dtype=out_dtype, device=dev)
     plan = pa.Plan()
@@ -290,7 +300,7 @@ def run_ours(args, rank, world, local_rank):
     parity = None
     if rank == 0 and not args.no_parity:
         import oracle
-        kp, vp = wl.pools_after_append()
+        kp, vp = wl.k_pool, wl.v_pool
         rng = np.random.default_rng(1)
         idx = rng.choice(wl.B * wl.Hq, size=min(64, wl.B * wl.Hq), replace=False)
         pr = np.stack([idx // wl.Hq, idx % wl.Hq], axis=1).astype(np.int32)
@@ -339,7 +349,7 @@ def run_ours(args, rank, world, local_rank):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, el, pairs, threads = oracle_sample_gbs(wl, args.cpu_budget)
+        gbs, el, pairs, threads = oracle_sample_gbs(wl, args.cpu_budget, appended=True)
         cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{pairs} random (sequence, q-head) rows of the workload, "
                          f"{el:.1f} s, bytes per row = its sequence's decode bytes / Hq"}

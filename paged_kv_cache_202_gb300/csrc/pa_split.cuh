@@ -366,6 +366,15 @@ struct MmaState {
                 pb[t][nt][1][1] = movmatrix_trans(bot_lo);
             }
         }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) l[nt][j] = l[nt][j] * alpha[nt][j] + ps[nt][j];
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[mt][nt][i] *= alpha[nt][i & 1];
+        }
         // Values O^T += V^T P^T.
         const bool tail = nv < BS;
         const int t0 = 2 * (lane & 3);

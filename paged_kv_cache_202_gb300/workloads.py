@@ -35,8 +35,10 @@ step appends it at position ``cache_len`` and then attends over ``L`` tokens.
 
 from __future__ import annotations
 
+import concurrent.futures
 import dataclasses
 import math
+import os
 
 import numpy as np
 import torch
@@ -139,6 +141,15 @@ class Workload:
     def max_seq_len(self) -> int:
         return int(self.seq_lens.max()) if self.B else 1
 
+    def append_in_place(self) -> None:
+        """Write the step's new token into this workload's own pools (numpy index write)."""
+        bs = self.block_size
+        for b in range(self.B):
+            pos = int(self.cache_lens[b])
+            phys = int(self.block_tables[b, pos // bs])
+            self.k_pool[phys, :, pos % bs, :] = self.k_new[b]
+            self.v_pool[phys, :, pos % bs, :] = self.v_new[b]
+
     def pools_after_append(self):
         """Copies of the pools with the step's new token written in (numpy index write)."""
         kp, vp = self.k_pool.copy(), self.v_pool.copy()
@@ -172,19 +183,32 @@ def _draw_lengths(spec, B: int, rng: np.random.Generator) -> np.ndarray:
     raise ValueError(kind)
 
 
-def _normal_f32(rng: np.random.Generator, shape, chunk: int = 1 << 25) -> np.ndarray:
-    out = np.empty(int(np.prod(shape)), dtype=np.float32)
-    for i in range(0, out.size, chunk):
-        n = min(chunk, out.size - i)
-        out[i:i + n] = rng.standard_normal(n, dtype=np.float32)
-    return out.reshape(shape)
+_CHUNK = 1 << 24
 
 
-def _normal_bf16(rng: np.random.Generator, shape, chunk: int = 1 << 25) -> np.ndarray:
-    out = np.empty(int(np.prod(shape)), dtype=np.uint16)
-    for i in range(0, out.size, chunk):
-        n = min(chunk, out.size - i)
-        out[i:i + n] = bf16_bits(rng.standard_normal(n, dtype=np.float32))
+def _normal(seq: np.random.SeedSequence, shape, dtype: str) -> np.ndarray:
+    """Standard normal values, float32 or rounded to bfloat16 bits.
+
+    The array is filled in fixed chunks of 2^24 elements; chunk c draws from
+    its own PCG64 stream spawned from ``seq``, so the values do not depend on
+    how many threads fill them.
+    """
+    n = int(np.prod(shape))
+    out = np.empty(n, dtype=np.float32 if dtype == "f32" else np.uint16)
+    nchunks = max(1, -(-n // _CHUNK))
+    streams = seq.spawn(nchunks)
+
+    def fill(c):
+        lo, hi = c * _CHUNK, min(n, (c + 1) * _CHUNK)
+        x = np.random.Generator(np.random.PCG64(streams[c])).standard_normal(hi - lo,
+                                                                            dtype=np.float32)
+        out[lo:hi] = x if dtype == "f32" else bf16_bits(x)
+
+    if nchunks == 1:
+        fill(0)
+    else:
+        with concurrent.futures.ThreadPoolExecutor(min(nchunks, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, range(nchunks)))
     return out.reshape(shape)
 
 
@@ -195,7 +219,9 @@ def make_workload(name: str, seed: int | None = None, **overrides) -> Workload:
     ``B`` or ``lengths`` for a case the oracle finishes in seconds).
 
     Draw order from ``numpy.random.default_rng(seed)``: lengths, the free-list
-    permutation, K pool, V pool, q, k_new, v_new, then the K outlier mask.
+    permutation, then the K outlier mask. The K pool, V pool, q, k_new and
+    v_new values come from five PCG64 streams spawned from
+    ``SeedSequence(seed)`` (see ``_normal``).
     """
     cfg = dict(CONFIGS[name])
     cfg.update(overrides)
@@ -241,20 +267,13 @@ def make_workload(name: str, seed: int | None = None, **overrides) -> Workload:
             alloc.refcount[prefix] -= 1  # the prefix itself was counted once at alloc
 
     pool_shape = (NB, Hkv, bs, D)
-    if dtype == "f32":
-        kpool = _normal_f32(rng, pool_shape)
-        vpool = _normal_f32(rng, pool_shape)
-        q = _normal_f32(rng, (B, Hq, D))
-        k_new = _normal_f32(rng, (B, Hkv, D))
-        v_new = _normal_f32(rng, (B, Hkv, D))
-        nan = np.float32(np.nan)
-    else:
-        kpool = _normal_bf16(rng, pool_shape)
-        vpool = _normal_bf16(rng, pool_shape)
-        q = _normal_bf16(rng, (B, Hq, D))
-        k_new = _normal_bf16(rng, (B, Hkv, D))
-        v_new = _normal_bf16(rng, (B, Hkv, D))
-        nan = np.uint16(0x7FC0)
+    seqs = np.random.SeedSequence(seed).spawn(5)
+    kpool = _normal(seqs[0], pool_shape, dtype)
+    vpool = _normal(seqs[1], pool_shape, dtype)
+    q = _normal(seqs[2], (B, Hq, D), dtype)
+    k_new = _normal(seqs[3], (B, Hkv, D), dtype)
+    v_new = _normal(seqs[4], (B, Hkv, D), dtype)
+    nan = np.float32(np.nan) if dtype == "f32" else np.uint16(0x7FC0)
 
     if "k_outliers" in cfg:
         # A Bernoulli(frac) mask per (sequence, token) scales that token's keys
