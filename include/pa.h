@@ -176,6 +176,43 @@ pa_status pa_plan_info(const pa_plan* plan, int* path, int* blocks, int* warps);
 pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
                                    struct CUevent_st* stop);
 
+/*
+ * pa_decode_noalloc -- pa_decode for callers that cannot let a library
+ * allocate device memory. The pages have no counterpart of this call; it is
+ * a deployment variant of the same computation.
+ *
+ * Who needs it: callers that own all device memory themselves, such as a
+ * serving engine that has reserved the free HBM as its KV block pool and
+ * budgets it exactly, or a plugin host that hands a kernel only its tensors.
+ * A cudaMalloc inside their call would take memory outside that budget, and
+ * cudaMalloc / cudaFree synchronise the device, stalling other streams.
+ *
+ * Arguments and result are those of pa_decode for bf16 pools (kv_dtype must
+ * be PA_BF16; the kernel choice is pa_decode's automatic one), without a plan:
+ * the split partials live in one 8 MiB device array inside the library, which
+ * every GPU that loads the library holds until the process exits. No
+ * cudaMalloc, cudaFree or other allocating call is made.
+ *
+ *   device_error  device pointer to an int that receives PA_DEVERR_* bits
+ *                 (the caller clears it); NULL = errors are not reported.
+ *
+ * Limits and rules:
+ *   - a call whose partials need more than 8 MiB (about 2 x warps x query
+ *     heads per kv unit x D x 4 bytes; e.g. 16 query heads per kv head with
+ *     D = 128 on a 152-SM GPU) returns PA_ERR_WORKSPACE and launches nothing;
+ *   - every call shares the array and it keeps the last call's contents;
+ *     calls whose work overlaps on the GPU (unordered streams) race on it and
+ *     must be serialised by the caller;
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ */
+pa_status pa_decode_noalloc(const void* q, const void* k_pool, const void* v_pool,
+                            const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,
+                            int B, int Hq, int Hkv, int D, int block_size, int num_blocks,
+                            int max_seq_len, float scale, pa_dtype kv_dtype, void* out,
+                            pa_dtype out_dtype, int* device_error, struct CUstream_st* stream);
+
 #ifdef __cplusplus
 }
 #endif

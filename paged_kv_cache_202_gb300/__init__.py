@@ -68,6 +68,9 @@ def lib() -> ctypes.CDLL:
     L.pa_plan_info.restype = ci
     L.pa_plan_set_split_events.argtypes = [vp, vp, vp]
     L.pa_plan_set_split_events.restype = ci
+    L.pa_decode_noalloc.argtypes = [vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci, vp,
+                                    ci, vp, vp]
+    L.pa_decode_noalloc.restype = ci
     _lib = L
     return L
 
@@ -166,6 +169,26 @@ def pa_decode(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                          int(max_seq_len), float(scale), _dtype(k_pool), _ptr(out), _dtype(out),
                          ctypes.byref(plan.handle), _stream(stream))
     _check(st, "pa_decode")
+    return out
+
+
+def pa_decode_noalloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
+                      block_tables: torch.Tensor, seq_lens: torch.Tensor, scale: float,
+                      out: torch.Tensor, max_seq_len: int, device_error: torch.Tensor | None = None,
+                      stream=None) -> torch.Tensor:
+    """``pa_decode`` without a plan: the library allocates nothing (bf16 pools).
+
+    For callers that manage all device memory themselves. ``device_error``, if
+    given, is an int32 device tensor of one element that receives error bits.
+    """
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_pool.shape
+    err = _ptr(device_error) if device_error is not None else None
+    st = lib().pa_decode_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                                 block_tables.shape[1], _ptr(seq_lens), B, Hq, Hkv, D, bs, NB,
+                                 int(max_seq_len), float(scale), _dtype(k_pool), _ptr(out),
+                                 _dtype(out), err, _stream(stream))
+    _check(st, "pa_decode_noalloc")
     return out
 
 

@@ -1,0 +1,250 @@
+// pa_decode_noalloc: the split paged decode with a fixed, library-owned
+// scratch area instead of a plan workspace, for callers that must not have a
+// library allocate device memory.
+//
+// Some callers own every byte of device memory themselves: a serving engine
+// that has reserved the HBM it does not need for weights as its KV block pool
+// and budgets it exactly, or a plugin host that hands a kernel only its input
+// and output tensors. A cudaMalloc inside such a call takes memory outside
+// that budget, and cudaMalloc / cudaFree also synchronise the device, which
+// stalls the caller's other streams. This entry point therefore allocates
+// nothing: the split partials and metadata live in one file-scope device
+// array of kNoAllocScratchBytes that every GPU loading this library holds
+// until the process exits.
+//
+// Scratch rules. All calls share the one array and it keeps the last call's
+// contents; everything a call reads from it is written earlier in the same
+// call (the only word that must start at zero, the fallback error word, is
+// cleared by each call). Calls whose kernels overlap on the GPU (different
+// streams without ordering) race on the array: serialise them. A call whose
+// partials would not fit in the array returns PA_ERR_WORKSPACE before any
+// launch.
+//
+// Set-up. The device address of the array is looked up once per device with
+// cudaGetSymbolAddress, on the first call made while that device is current;
+// host code never passes the array's host-side name to a kernel. That first
+// call should come before any stream capture.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+#include <vector>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+constexpr int kMaxDevices = 64;
+constexpr size_t kRingBudget = 200 * 1024;
+constexpr size_t kSmemLimit = 232448;
+constexpr int kMinPagesPerWarp = 4;
+constexpr int kHeadSlice = 16;
+constexpr int kMaxBatch = 8192;
+
+}  // namespace
+
+// The shared scratch array (8 MiB on every device that loads the library).
+static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
+
+namespace {
+
+struct DeviceScratch {
+    std::once_flag once;
+    void* ptr = nullptr;
+    cudaError_t status = cudaSuccess;
+};
+DeviceScratch g_scratch[kMaxDevices];
+
+// Device address of the scratch array on device `dev` (the current device).
+void* scratch_address(int dev, cudaError_t* status) {
+    if (dev < 0 || dev >= kMaxDevices) {
+        *status = cudaErrorInvalidDevice;
+        return nullptr;
+    }
+    DeviceScratch& d = g_scratch[dev];
+    std::call_once(d.once, [&d] {
+        d.status = cudaGetSymbolAddress(&d.ptr, g_decode_scratch);
+        if (d.status != cudaSuccess) d.ptr = nullptr;
+    });
+    *status = d.status;
+    return d.ptr;
+}
+
+struct OccEntry {
+    int dev, kind, D, BS, NT, warps;
+    size_t smem;
+    int blocks_per_sm;
+};
+std::mutex g_occ_mutex;
+std::vector<OccEntry> g_occ;
+
+int blocks_per_sm(int dev, const pa::SplitLaunch& L, cudaError_t* status) {
+    {
+        std::lock_guard<std::mutex> lk(g_occ_mutex);
+        for (const OccEntry& o : g_occ)
+            if (o.dev == dev && o.kind == L.kind && o.D == L.D && o.BS == L.BS && o.NT == L.NT &&
+                o.warps == L.warps && o.smem == L.smem) {
+                *status = cudaSuccess;
+                return o.blocks_per_sm;
+            }
+    }
+    const int n = pa::split_blocks_per_sm(L, status);
+    if (*status == cudaSuccess && n > 0) {
+        std::lock_guard<std::mutex> lk(g_occ_mutex);
+        g_occ.push_back(OccEntry{dev, L.kind, L.D, L.BS, L.NT, L.warps, L.smem, n});
+    }
+    return n;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool encode_pool(CUtensorMap* map, const void* pool, int rows, int D, int BS) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(BS),
+                          static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(BS) * D * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BS), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides,
+              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const void* v_pool,
+                                       const int32_t* block_tables, int max_blocks,
+                                       const int32_t* seq_lens, int B, int Hq, int Hkv, int D,
+                                       int block_size, int num_blocks, int max_seq_len,
+                                       float scale, pa_dtype kv_dtype, void* out,
+                                       pa_dtype out_dtype, int* device_error,
+                                       struct CUstream_st* stream_) {
+    if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out) return PA_ERR_NULL;
+    if (kv_dtype != PA_BF16 || (out_dtype != PA_F32 && out_dtype != PA_BF16)) return PA_ERR_DTYPE;
+    if (block_size != 16 && block_size != 32) return PA_ERR_BLOCK_SIZE;
+    if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (D != 64 && D != 128) || num_blocks < 1 ||
+        max_blocks < 1 || max_seq_len < 1 || !std::isfinite(scale) || B > kMaxBatch)
+        return PA_ERR_SHAPE;
+    if (static_cast<int64_t>(num_blocks) * Hkv > INT32_MAX ||
+        static_cast<int64_t>(max_blocks) * block_size > INT32_MAX)
+        return PA_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return PA_ERR_ALIGN;
+    if (B == 0) return PA_OK;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+
+    int dev = 0, num_sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return PA_ERR_CUDA;
+    cudaError_t st;
+    char* scratch = static_cast<char*>(scratch_address(dev, &st));
+    if (!scratch) return PA_ERR_CUDA;
+
+    // Same planning as pa_decode's automatic choice: one query head per kv
+    // unit when the group has one head, tensor-core tiles otherwise.
+    const int g = Hq / Hkv;
+    int kind, nslices, GS, NT = 0;
+    if (g == 1) {
+        kind = pa::kSplitFma;
+        nslices = 1;
+        GS = 1;
+    } else {
+        kind = pa::kSplitMma;
+        nslices = (g + kHeadSlice - 1) / kHeadSlice;
+        GS = (g + nslices - 1) / nslices;
+        NT = (GS + 7) / 8;
+    }
+    const int U = Hkv * nslices;
+    const int64_t max_pages =
+        (static_cast<int64_t>(std::min(max_seq_len, max_blocks * block_size)) + block_size - 1) /
+        block_size;
+    const int64_t P_max = static_cast<int64_t>(B) * U * max_pages;
+    if (P_max > INT32_MAX) return PA_ERR_SHAPE;
+    const size_t stage_bytes =
+        round_up(2u * block_size * D * 2u + static_cast<size_t>(GS) * D * 2u, 1024);
+    const size_t lens_bytes = round_up(static_cast<size_t>(2 * B + 1) * 4u, 1024);
+    const int warps = 4;
+    const int stages = static_cast<int>(std::min<size_t>(6, kRingBudget / (warps * stage_bytes)));
+    if (stages < 1) return PA_ERR_SHAPE;
+    const size_t smem = 1024 + lens_bytes + static_cast<size_t>(warps) * stages * stage_bytes +
+                        static_cast<size_t>(warps) * stages * 8;
+    if (smem > kSmemLimit) return PA_ERR_SHAPE;
+    pa::SplitLaunch L{kind, D, block_size, NT, warps, 0, smem};
+    const int per_sm = blocks_per_sm(dev, L, &st);
+    if (st != cudaSuccess || per_sm < 1) return PA_ERR_CUDA;
+    const int64_t need = (P_max + static_cast<int64_t>(warps) * kMinPagesPerWarp - 1) /
+                         (static_cast<int64_t>(warps) * kMinPagesPerWarp);
+    L.blocks = static_cast<int>(
+        std::max<int64_t>(1, std::min<int64_t>(need, static_cast<int64_t>(num_sms) * per_sm)));
+    const int NW = L.blocks * warps;
+
+    // Scratch layout: fallback error word, metadata, partial (m, l), partial sums.
+    const size_t err_bytes = 256;
+    const size_t meta_bytes = round_up(static_cast<size_t>(pa::kMetaHeader + B + 1) * 4u, 256);
+    const size_t ml_bytes = round_up(static_cast<size_t>(2) * NW * GS * 2 * 4u, 256);
+    const size_t acc_bytes = round_up(static_cast<size_t>(2) * NW * GS * D * 4u, 256);
+    if (err_bytes + meta_bytes + ml_bytes + acc_bytes > kNoAllocScratchBytes)
+        return PA_ERR_WORKSPACE;
+    int* err = reinterpret_cast<int*>(scratch);
+    int* meta = reinterpret_cast<int*>(scratch + err_bytes);
+    float* ml = reinterpret_cast<float*>(scratch + err_bytes + meta_bytes);
+    float* acc = reinterpret_cast<float*>(scratch + err_bytes + meta_bytes + ml_bytes);
+    if (!device_error) {
+        if (cudaMemsetAsync(err, 0, sizeof(int), stream) != cudaSuccess) return PA_ERR_CUDA;
+        device_error = err;
+    }
+
+    CUtensorMap kmap, vmap;
+    const int rows = num_blocks * Hkv;
+    if (!encode_pool(&kmap, k_pool, rows, D, block_size) ||
+        !encode_pool(&vmap, v_pool, rows, D, block_size))
+        return PA_ERR_CUDA;
+
+    pa::SplitArgs a{};
+    a.q = static_cast<const uint16_t*>(q);
+    a.tables = block_tables;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.ws_acc = acc;
+    a.ws_ml = ml;
+    a.ws_meta = meta;
+    a.err = device_error;
+    a.B = B;
+    a.Hq = Hq;
+    a.Hkv = Hkv;
+    a.g = g;
+    a.GS = GS;
+    a.nslices = nslices;
+    a.U = U;
+    a.max_blocks = max_blocks;
+    a.num_blocks = num_blocks;
+    a.max_seq_len = max_seq_len;
+    a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    a.out_bf16 = out_dtype == PA_BF16;
+    a.stages = stages;
+    a.stage_bytes = static_cast<int>(stage_bytes);
+    a.lens_bytes = static_cast<int>(lens_bytes);
+    if (pa::launch_split(L, kmap, vmap, a, stream) != cudaSuccess) return PA_ERR_CUDA;
+    pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, GS, nslices, U, D, out_dtype == PA_BF16};
+    return pa::launch_merge(m, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}

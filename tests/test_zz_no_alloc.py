@@ -1,0 +1,63 @@
+"""pa_decode_noalloc: the decode entry point for callers that cannot let a
+library allocate device memory (an engine that budgets all HBM itself, or a
+plugin host that hands a kernel only its tensors).
+
+Its output must match pa_decode's on the same inputs, on two calls in a row
+with different shapes, so that the shared scratch array's leftover contents
+from the first call cannot leak into the second. The file is named to be
+collected last.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import paged_kv_cache_202_gb300 as pa
+from paged_kv_cache_202_gb300.workloads import make_workload
+
+from gpu_helpers import DeviceStep, out_f64, tol
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _both(wl):
+    ds = DeviceStep(wl)
+    ds.append()
+    with pa.Plan() as plan:
+        ref = out_f64(ds.decode(plan))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full_like(ds.out, float("nan"))
+    pa.pa_decode_noalloc(ds.q, ds.k_pool, ds.v_pool, ds.tables, ds.seq_lens, wl.scale, out,
+                         wl.max_seq_len, device_error=err)
+    torch.cuda.synchronize()
+    return ref, out_f64(out), int(err.item())
+
+
+def test_noalloc_matches_decode_on_two_calls_in_a_row():
+    first = make_workload("llama3_8b_gqa", seed=21, B=12, lengths=("loguniform", 1, 6000),
+                          max_len=6144)
+    second = make_workload("llama7b_mha", seed=22, B=5, Hq=8, Hkv=8,
+                           lengths=("uniform", 1, 1500), max_len=1536, pool=("fixed", 1024))
+    for wl in (first, second):
+        ref, got, err = _both(wl)
+        assert err == 0
+        assert np.isfinite(got).all()
+        assert np.abs(got - ref).max() <= tol(wl)
+
+
+def test_noalloc_rejects_calls_beyond_its_scratch():
+    # 16 query heads per kv head with D = 128 over a full-chip split needs more
+    # partial storage than the fixed scratch holds: rejected before any launch.
+    wl = make_workload("llama3_8b_gqa", seed=23, B=4, Hq=32, Hkv=2, lengths=("fixed", 100),
+                       max_len=8192)
+    ds = DeviceStep(wl)
+    with pytest.raises(pa.PagedAttentionError) as ei:
+        pa.pa_decode_noalloc(ds.q, ds.k_pool, ds.v_pool, ds.tables, ds.seq_lens, wl.scale,
+                             ds.out, 8192)
+    assert ei.value.status == pa.PA_ERR_WORKSPACE
