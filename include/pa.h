@@ -189,7 +189,7 @@ pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
  *
  * Arguments and result are those of pa_decode for bf16 pools (kv_dtype must
  * be PA_BF16; the kernel choice is pa_decode's automatic one), without a plan:
- * the split partials live in one 8 MiB device array inside the library, which
+ * the split partials live in one 16 MiB device array inside the library, which
  * every GPU that loads the library holds until the process exits. No
  * cudaMalloc, cudaFree or other allocating call is made.
  *
@@ -197,9 +197,10 @@ pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
  *                 (the caller clears it); NULL = errors are not reported.
  *
  * Limits and rules:
- *   - a call whose partials need more than 8 MiB (about 2 x warps x query
- *     heads per kv unit x D x 4 bytes; e.g. 16 query heads per kv head with
- *     D = 128 on a 152-SM GPU) returns PA_ERR_WORKSPACE and launches nothing;
+ *   - a call whose partials need more than 16 MiB (about 2 x warps x query
+ *     heads per kv unit x D x 4 bytes: with 16 query heads per kv head at
+ *     D = 128, a plan of more than about 1020 warps) returns
+ *     PA_ERR_WORKSPACE and launches nothing;
  *   - every call shares the array and it keeps the last call's contents;
  *     calls whose work overlaps on the GPU (unordered streams) race on it and
  *     must be serialised by the caller;

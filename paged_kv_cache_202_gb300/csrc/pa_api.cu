@@ -18,7 +18,8 @@ namespace {
 using pa::SplitLaunch;
 
 constexpr size_t kSmemLimit = 232448;     // opt-in dynamic shared memory per block on sm_10x
-constexpr size_t kRingBudget = 200 * 1024; // bytes of stages per block
+constexpr int kDefaultWarps = 3;           // warps per block of the split kernels
+constexpr int kDefaultStages = 1;          // pipeline stages per warp
 constexpr int kMinPagesPerWarp = 4;
 constexpr int kHeadSlice = 16;             // query heads per kv unit on the tensor-core path
 constexpr int kMaxBatch = 8192;            // per-sequence arrays live in shared memory
@@ -225,10 +226,13 @@ pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
     const int64_t P_max = static_cast<int64_t>(B) * U * max_pages;
     if (P_max > INT32_MAX) return PA_ERR_SHAPE;
 
-    const size_t stage_bytes = round_up(2u * block_size * D * 2u + static_cast<size_t>(GS) * D * 2u, 1024);
+    const size_t stage_bytes = round_up(2u * pa::kChunkTokens * D * 2u + static_cast<size_t>(GS) * D * 2u, 1024);
     const size_t lens_bytes = round_up(static_cast<size_t>(2 * B + 1) * 4u, 1024);
-    int warps = 4;
-    int stages = static_cast<int>(std::min<size_t>(6, kRingBudget / (warps * stage_bytes)));
+    // Many warps with one stage each: a warp waits for its chunk while the other
+    // warps of the SM compute, so bytes in flight scale with the warp count
+    // (3 warps per block, up to 4 blocks per SM at 32-token stages).
+    int warps = kDefaultWarps;
+    int stages = kDefaultStages;
     tuning_override(&warps, &stages);
     if (stages < 1) stages = 1;
     const size_t smem = 1024 + lens_bytes + static_cast<size_t>(warps) * stages * stage_bytes +

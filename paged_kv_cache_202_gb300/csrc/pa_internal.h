@@ -23,6 +23,10 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 enum SplitKind { kSplitFma = 0, kSplitMma = 1 };
 
+// Tokens per pipeline stage of the split kernels: two 16-token pages or one
+// 32-token page of the same (sequence, kv unit) segment.
+constexpr int kChunkTokens = 32;
+
 // Arguments of the split-attention kernels (bf16 KV).
 struct SplitArgs {
     const uint16_t* q;         // [B][Hq][D] bf16 bits

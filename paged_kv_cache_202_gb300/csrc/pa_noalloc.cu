@@ -36,9 +36,10 @@
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
 constexpr int kMaxDevices = 64;
-constexpr size_t kRingBudget = 200 * 1024;
+constexpr int kDefaultWarps = 3;
+constexpr int kDefaultStages = 1;
 constexpr size_t kSmemLimit = 232448;
 constexpr int kMinPagesPerWarp = 4;
 constexpr int kHeadSlice = 16;
@@ -46,7 +47,7 @@ constexpr int kMaxBatch = 8192;
 
 }  // namespace
 
-// The shared scratch array (8 MiB on every device that loads the library).
+// The shared scratch array (16 MiB on every device that loads the library).
 static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchBytes];
 
 namespace {
@@ -181,11 +182,10 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     const int64_t P_max = static_cast<int64_t>(B) * U * max_pages;
     if (P_max > INT32_MAX) return PA_ERR_SHAPE;
     const size_t stage_bytes =
-        round_up(2u * block_size * D * 2u + static_cast<size_t>(GS) * D * 2u, 1024);
+        round_up(2u * pa::kChunkTokens * D * 2u + static_cast<size_t>(GS) * D * 2u, 1024);
     const size_t lens_bytes = round_up(static_cast<size_t>(2 * B + 1) * 4u, 1024);
-    const int warps = 4;
-    const int stages = static_cast<int>(std::min<size_t>(6, kRingBudget / (warps * stage_bytes)));
-    if (stages < 1) return PA_ERR_SHAPE;
+    const int warps = kDefaultWarps;
+    const int stages = kDefaultStages;
     const size_t smem = 1024 + lens_bytes + static_cast<size_t>(warps) * stages * stage_bytes +
                         static_cast<size_t>(warps) * stages * 8;
     if (smem > kSmemLimit) return PA_ERR_SHAPE;

@@ -8,14 +8,14 @@ template <int D, int BS>
 __global__ void __launch_bounds__(256, 1)
     fma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                const SplitArgs a) {
-    split_body<D, BS, FmaState<D, BS>>(&kmap, &vmap, a);
+    split_body<D, BS, FmaState<D, kChunkTokens>>(&kmap, &vmap, a);
 }
 
 template <int D, int BS, int NT>
 __global__ void __launch_bounds__(256, 1)
     mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                const SplitArgs a) {
-    split_body<D, BS, MmaState<D, BS, NT>>(&kmap, &vmap, a);
+    split_body<D, BS, MmaState<D, kChunkTokens, NT>>(&kmap, &vmap, a);
 }
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, SplitArgs);

@@ -366,14 +366,22 @@ struct MmaState {
                 pb[t][nt][1][1] = movmatrix_trans(bot_lo);
             }
         }
+        bool rescale = false;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-            for (int j = 0; j < 2; ++j) l[nt][j] = l[nt][j] * alpha[nt][j] + ps[nt][j];
+            for (int j = 0; j < 2; ++j) {
+                l[nt][j] = l[nt][j] * alpha[nt][j] + ps[nt][j];
+                rescale |= alpha[nt][j] != 1.f;
+            }
+        }
+        if (__any_sync(0xffffffffu, rescale)) {  // skipped while no running max moves
 #pragma unroll
-            for (int mt = 0; mt < KS; ++mt)
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) o[mt][nt][i] *= alpha[nt][i & 1];
+                for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) o[mt][nt][i] *= alpha[nt][i & 1];
         }
         // Values O^T += V^T P^T.
         const bool tail = nv < BS;
@@ -457,9 +465,15 @@ struct MmaState {
 };
 
 // ------------------------------------------------------------------ kernel
+// One pipeline stage holds a chunk of CT = kChunkTokens consecutive tokens of
+// one segment: two 16-token pages stacked (block size 16) or one 32-token
+// page. Both give the same shared-memory image, [D/64 boxes][32 rows][128 B]
+// with the 128-byte swizzle, so the arithmetic sees one 32-token tile pair.
 template <int D, int BS, typename State>
 __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtensorMap* vmap,
                                            const SplitArgs& a) {
+    constexpr int CT = kChunkTokens;
+    constexpr int CP = CT / BS;  // pages per chunk
     extern __shared__ uint8_t smem_raw[];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, W = blockDim.x >> 5;
     const uint32_t raw = smem_addr(smem_raw);
@@ -492,7 +506,6 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
     const int x0 = gw * per;
     const int x1 = min(x0 + per, P);
     if (per == 0 || x0 >= x1) return;
-    const int npages = x1 - x0;
     const int S = a.stages;
     const uint32_t my_bars = bars0 + warp * S * 8;
     const uint32_t my_ring = ring0 + static_cast<uint32_t>(warp * S * a.stage_bytes);
@@ -515,23 +528,36 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
         cc = Cursor{lo, off / nb, off % nb, nb};
     }
     Cursor ci = cc;
-    const uint32_t kv_bytes = 2u * BS * D * 2u;
+    int xc = x0, xi = x0;  // global page index of the consume and issue cursors
+    const uint32_t page_bytes = 2u * BS * D * 2u;  // K + V of one page
     const uint64_t policy = policy_evict_first();
     int tb_row = -1, tb_base = -1, tbl = -1;  // table batch: entries [tb_base, tb_base+32) of row tb_row
     uint32_t badmask = 0, phase = 0;
 
-    // Issue page `k` of the range (cursor ci) into stage s; warp-collective.
-    auto issue = [&](int s, bool qstart) {
-        const int pbase = ci.p & ~31;
-        if (ci.b != tb_row || pbase != tb_base) {
-            tb_row = ci.b;
+    auto chunk_pages = [&](const Cursor& c, int x) { return min(min(CP, c.nb - c.p), x1 - x); };
+    auto table_entry = [&](int b, int p, int nb) {
+        const int pbase = p & ~31;
+        if (b != tb_row || pbase != tb_base) {
+            tb_row = b;
             tb_base = pbase;
-            tbl = (pbase + lane < ci.nb)
-                      ? __ldg(a.tables + static_cast<size_t>(ci.b) * a.max_blocks + pbase + lane)
+            tbl = (pbase + lane < nb)
+                      ? __ldg(a.tables + static_cast<size_t>(b) * a.max_blocks + pbase + lane)
                       : -1;
         }
-        const int phys = __shfl_sync(0xffffffffu, tbl, ci.p - pbase);
-        const bool bad = phys < 0 || phys >= a.num_blocks;
+        return __shfl_sync(0xffffffffu, tbl, p - pbase);
+    };
+
+    // Issue the chunk at the issue cursor into stage s; warp-collective.
+    auto issue = [&](int s) {
+        const int n = chunk_pages(ci, xi);
+        const bool qstart = xi == x0 || ci.p == 0;
+        int phys[CP];
+        bool bad = false;
+#pragma unroll
+        for (int j = 0; j < CP; ++j) {
+            phys[j] = j < n ? table_entry(ci.b, ci.p + j, ci.nb) : 0;
+            bad |= j < n && (phys[j] < 0 || phys[j] >= a.num_blocks);
+        }
         badmask = bad ? (badmask | (1u << s)) : (badmask & ~(1u << s));
         if (lane == 0) {
             const uint32_t bar = my_bars + 8 * s;
@@ -547,73 +573,78 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
                     mbar_arrive(bar);
                 }
             } else {
-                mbar_arrive_expect_tx(bar, kv_bytes + qbytes);
-                const int row = phys * a.Hkv + kvh;
+                mbar_arrive_expect_tx(bar, n * page_bytes + qbytes);
+                for (int j = 0; j < n; ++j) {
+                    const int row = phys[j] * a.Hkv + kvh;
 #pragma unroll
-                for (int h = 0; h < D / 64; ++h) {
-                    tma_load_3d(stg + h * (BS * 128), kmap, h * 64, 0, row, bar, policy);
-                    tma_load_3d(stg + BS * D * 2 + h * (BS * 128), vmap, h * 64, 0, row, bar, policy);
+                    for (int h = 0; h < D / 64; ++h) {
+                        const uint32_t off = h * (CT * 128) + j * (BS * 128);
+                        tma_load_3d(stg + off, kmap, h * 64, 0, row, bar, policy);
+                        tma_load_3d(stg + CT * D * 2 + off, vmap, h * 64, 0, row, bar, policy);
+                    }
                 }
             }
             if (qstart) {
                 const uint16_t* src =
                     a.q + (static_cast<size_t>(ci.b) * a.Hq + kvh * a.g + slice * a.GS) * D;
-                bulk_load(stg + 2 * BS * D * 2, src, qbytes, bar);
+                bulk_load(stg + 2 * CT * D * 2, src, qbytes, bar);
             }
         }
+        for (int j = 0; j < n; ++j) advance(ci, pre, a.U, a.B);
+        xi += n;
     };
 
-    int k_issue = 0;
-    for (int s = 0; k_issue < min(S, npages); ++s, ++k_issue) {
-        issue(s, k_issue == 0 || ci.p == 0);
-        advance(ci, pre, a.U, a.B);
-    }
+    int n_issued = 0;
+    for (int s = 0; s < S && xi < x1; ++s, ++n_issued) issue(s);
 
     State st;
     int p_first = 0, hq0 = 0, nh = 0;
     bool poison = false;
-    int s = 0;
-    for (int k = 0; k < npages; ++k) {
+    int s = 0, n_done = 0;
+    while (xc < x1) {
         const uint32_t bar = my_bars + 8 * s;
         const uint32_t stg = my_ring + static_cast<uint32_t>(s * a.stage_bytes);
         const bool ready = mbar_wait_bounded(bar, (phase >> s) & 1u, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ready)) {
             // Give up: report, wait (bounded) for this warp's copies in flight, return.
             if (lane == 0) atomicOr(a.err, kErrTimeout);
-            for (int j = k; j < k_issue; ++j) {
+            for (int j = n_done; j < n_issued; ++j) {
                 const int sj = j % S;
                 mbar_wait_bounded(my_bars + 8 * sj, (phase >> sj) & 1u, kWaitLimitNs);
             }
             return;
         }
         phase ^= 1u << s;
-        if (k == 0 || cc.p == 0) {
+        const int n = chunk_pages(cc, xc);
+        if (xc == x0 || cc.p == 0) {
             const int kvh = cc.u / a.nslices, slice = cc.u - kvh * a.nslices;
             nh = min(a.GS, a.g - slice * a.GS);
             hq0 = kvh * a.g + slice * a.GS;
-            st.start(stg + 2 * BS * D * 2, nh, lane);
+            st.start(stg + 2 * CT * D * 2, nh, lane);
             p_first = cc.p;
             poison = false;
         }
         if ((badmask >> s) & 1u) {
             poison = true;
         } else {
-            const int nv = (cc.p == cc.nb - 1) ? len[cc.b] - cc.p * BS : BS;
-            st.page(stg, stg + BS * D * 2, nv, a.scale_log2, lane);
+            const int nv = min(n * BS, len[cc.b] - cc.p * BS);
+            st.page(stg, stg + CT * D * 2, nv, a.scale_log2, lane);
         }
         __syncwarp();
-        if (k_issue < npages) {
+        if (xi < x1) {
             fence_proxy_async_smem();
-            issue(s, ci.p == 0);
-            advance(ci, pre, a.U, a.B);
-            ++k_issue;
+            issue(s);
+            ++n_issued;
         }
-        if (cc.p == cc.nb - 1 || k == npages - 1) {
-            const bool full = p_first == 0 && cc.p == cc.nb - 1;
+        const int p_last = cc.p + n - 1;
+        if (p_last == cc.nb - 1 || xc + n == x1) {
+            const bool full = p_first == 0 && p_last == cc.nb - 1;
             const int slot = gw * 2 + (p_first > 0 ? 0 : 1);
             st.finish(a, cc.b, hq0, nh, full, poison, slot, lane);
         }
-        advance(cc, pre, a.U, a.B);
+        for (int j = 0; j < n; ++j) advance(cc, pre, a.U, a.B);
+        xc += n;
+        ++n_done;
         if (++s == S) s = 0;
     }
 }
