@@ -398,6 +398,80 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.destroy_process_group()
 
 
+def run_row(args, local_rank):
+    """Measure one of the other hot-path kernels on the workload: whole-pool
+    block copies (copy on write) or PagedEviction page scores."""
+    import __graft_entry__
+    import paged_kv_cache_202_gb300 as pa
+    from paged_kv_cache_202_gb300.workloads import make_workload
+
+    __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = make_workload(args.workload)
+    bf = wl.dtype == "bf16"
+
+    def to_dev(a):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16 if bf else np.float32))
+        return (t.view(torch.bfloat16) if bf else t).to(dev)
+
+    k_pool, v_pool = to_dev(wl.k_pool), to_dev(wl.v_pool)
+    tables = torch.from_numpy(wl.block_tables).to(dev)
+    seq_lens = torch.from_numpy(wl.seq_lens).to(dev)
+    eb = wl.elem_bytes
+    if args.row == "copy_blocks":
+        n = min(8192, wl.num_blocks // 2)
+        perm = np.random.default_rng(0).permutation(wl.num_blocks)
+        src = torch.from_numpy(perm[:n].astype(np.int32)).to(dev)
+        dst = torch.from_numpy(perm[n:2 * n].astype(np.int32)).to(dev)
+        block_bytes = wl.Hkv * wl.block_size * wl.D * eb
+        nbytes = 2 * n * block_bytes * 2 + 8 * n  # both pools, read + write; the id lists
+
+        def call():
+            pa.pa_copy_blocks(k_pool, v_pool, src, dst)
+        what = f"{n} random block pairs of {block_bytes} bytes per pool"
+    else:
+        B, MB = wl.block_tables.shape
+        scores = torch.empty(B, MB, dtype=torch.float32, device=dev)
+        victims = torch.empty(B, dtype=torch.int32, device=dev)
+        nblk = sum(-(-int(L) // wl.block_size) for L in wl.seq_lens)
+        nbytes = 2 * wl.Hkv * wl.D * eb * int(wl.seq_lens.sum()) + 4 * nblk + 4 * B + \
+            4 * nblk + 4 * B  # K and V once, table entries, lengths, scores, victims
+
+        def call():
+            pa.pa_page_scores(k_pool, v_pool, tables, seq_lens, wl.max_seq_len, scores, victims)
+        what = "every attended page of every sequence"
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    stream = torch.cuda.current_stream()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for a_, b_ in ev:
+        a_.record(stream)
+        call()
+        b_.record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ev)
+    peak, peak_kind = measured_peak_gbs()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "row": args.row, "metric": f"{args.row}: achieved HBM GB/s", "value": gbs, "unit": "GB/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "what": what,
+                   "l2": "inputs larger than L2, no flush"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": gbs / peak, "algorithmic_bytes": nbytes},
+        "gpu_launches": (1 if args.row == "copy_blocks" else 2) * args.steps,
+    }), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -409,12 +483,15 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
+    ap.add_argument("--row", default="decode", choices=["decode", "copy_blocks", "page_scores"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         run_reference(args, rank)
+    elif args.row != "decode":
+        run_row(args, local_rank)
     else:
         run_ours(args, rank, world, local_rank)
 

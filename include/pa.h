@@ -58,7 +58,8 @@ typedef enum {
     PA_ERR_WORKSPACE = 5,   /* workspace too small for the request */
     PA_ERR_CUDA = 6,        /* a CUDA call failed */
     PA_ERR_BOUNDS = 7,      /* the device saw a length or table entry out of range */
-    PA_ERR_ALIGN = 8        /* a tensor is not 16-byte aligned */
+    PA_ERR_ALIGN = 8,       /* a tensor is not 16-byte aligned */
+    PA_ERR_NO_BLOCKS = 9    /* the block pool has too few free blocks */
 } pa_status;
 
 typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
@@ -68,7 +69,8 @@ enum {
     PA_DEVERR_SEQ_LEN = 1,      /* decode: seq_len < 1 or > min(max_seq_len, max_blocks*bs) */
     PA_DEVERR_TABLE = 2,        /* a table entry outside [0, num_blocks) */
     PA_DEVERR_TIMEOUT = 4,      /* a pipeline wait gave up (the kernel returned early) */
-    PA_DEVERR_CACHE_LEN = 8     /* append: cache_len < 0 or >= max_blocks*bs */
+    PA_DEVERR_CACHE_LEN = 8,    /* append: cache_len < 0 or >= max_blocks*bs */
+    PA_DEVERR_COPY = 16         /* block copy: an id outside [0, num_blocks) */
 };
 
 /* Kernel selection for pa_decode (pa_plan_set_path). */
@@ -155,7 +157,8 @@ const char* pa_status_str(pa_status status);
 /*
  * pa_last_device_error -- read and clear a device error word (synchronous:
  * waits for the device). plan != NULL reads the plan's decode word;
- * plan == NULL reads the library-wide append word of the current device.
+ * plan == NULL reads the library-wide word of pa_append_kv and
+ * pa_copy_blocks on the current device.
  * *err receives a bit set of PA_DEVERR_*; 0 means no error seen.
  */
 pa_status pa_last_device_error(pa_plan* plan, int* err);
@@ -175,6 +178,92 @@ pa_status pa_plan_info(const pa_plan* plan, int* path, int* blocks, int* warps);
  * right after it, on the call's stream. Pass NULLs to stop recording. */
 pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
                                    struct CUevent_st* stop);
+
+/* ------------------------------------------------------------------------
+ * Block management: free list, sharing and copy on write.
+ *
+ * "PagedAttention: The Cache Was Storing Nothing" §2.2-§2.3: every free block
+ * fits any request; tables of several sequences may name the same physical
+ * block (shared prefixes, beam candidates); a shared block is copied only when
+ * a sequence diverges and writes into it. The manager lives on the host: an
+ * O(1) free list (a stack of block ids) and one reference count per block
+ * (the number of tables naming it). All pa_bm_* calls are thread-safe (one
+ * mutex per manager) and take host pointers.
+ * ---------------------------------------------------------------------- */
+typedef struct pa_block_manager pa_block_manager;
+
+/* A manager of num_blocks blocks, all free; freed with pa_bm_destroy. */
+pa_status pa_bm_create(int num_blocks, pa_block_manager** out);
+pa_status pa_bm_destroy(pa_block_manager* bm);
+/* Take n free blocks (reference count 1 each) into ids[0..n); PA_ERR_NO_BLOCKS
+ * (and no change) when fewer than n are free. */
+pa_status pa_bm_alloc(pa_block_manager* bm, int n, int32_t* ids);
+/* Add one reference to each of ids[0..n) (a forked table now names them too);
+ * PA_ERR_BOUNDS (no change) if an id is outside the pool or not allocated. */
+pa_status pa_bm_fork(pa_block_manager* bm, const int32_t* ids, int n);
+/* Drop one reference from each of ids[0..n); a block whose count reaches 0
+ * returns to the free list. PA_ERR_BOUNDS (no change) on an id that is not
+ * held that many times. */
+pa_status pa_bm_release(pa_block_manager* bm, const int32_t* ids, int n);
+pa_status pa_bm_refcount(const pa_block_manager* bm, int32_t id, int* count);
+pa_status pa_bm_num_free(const pa_block_manager* bm, int* n);
+
+/*
+ * pa_bm_prepare_append -- make every sequence's append target writable.
+ *
+ * For each b, the block of logical index cache_lens[b] / block_size in host
+ * table row b (tables: host int32 [B][max_blocks]) becomes private: a missing
+ * entry (< 0) gets a fresh block; a block with reference count > 1 is
+ * replaced in the table by a fresh block and the pair (old, fresh) is
+ * appended to copy_src / copy_dst (host arrays of capacity B), the old block
+ * losing this table's reference. *n_copies receives the number of pairs; run
+ * pa_copy_blocks on them (and upload the changed table rows) before
+ * pa_append_kv. On any error nothing changes: PA_ERR_BOUNDS for a position
+ * or id out of range, PA_ERR_NO_BLOCKS when the free list is too short.
+ */
+pa_status pa_bm_prepare_append(pa_block_manager* bm, int32_t* tables, int B, int max_blocks,
+                               const int32_t* cache_lens, int block_size, int32_t* copy_src,
+                               int32_t* copy_dst, int* n_copies);
+
+/*
+ * pa_copy_blocks -- batched whole-block copies on the device (copy on write).
+ *
+ * For i < n: block copy_dst[i] of both pools becomes a bit-exact copy of block
+ * copy_src[i] (every kv head and slot). copy_src / copy_dst are device int32
+ * arrays. The copies run in parallel: the destinations must be distinct and
+ * no destination may be a source. An id outside [0, num_blocks) skips that
+ * pair and raises PA_DEVERR_COPY in the library-wide word that
+ * pa_last_device_error(NULL, ...) reads. n = 0 is a no-op.
+ */
+pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* copy_src,
+                         const int32_t* copy_dst, int n, int Hkv, int D, int block_size,
+                         int num_blocks, pa_dtype kv_dtype, struct CUstream_st* stream);
+
+/*
+ * pa_page_scores -- PagedEviction page scores and the page to evict.
+ *
+ * Pith review of arXiv 2509.04377 (PagedEviction), "Core claim": a token's
+ * importance is ||V||_2 / ||K||_2 of its cached value and key, a page's is the
+ * mean over its tokens, and when a sequence's newest page has just filled
+ * (seq_len % block_size == 0) its lowest-scoring page is evicted. K and V of a
+ * token are taken over all kv heads together; ||K|| = 0 scores +inf; every
+ * full page is a candidate; ties go to the lowest logical page.
+ *
+ *   k_pool, v_pool, block_tables, seq_lens  as for pa_decode (device, read only)
+ *   scores    device float [B][max_blocks]: entry p < ceil(L_b / block_size)
+ *             receives page p's mean (over its valid tokens); others untouched
+ *   victims   device int32 [B]: the logical page to evict, or -1 (no full
+ *             newest page this step, or a bad table entry in the sequence)
+ *   device_error  device int or NULL: receives PA_DEVERR_SEQ_LEN /
+ *             PA_DEVERR_TABLE bits (the caller clears it)
+ *
+ * Reads every attended K and V element once (HBM-bound). fp32 arithmetic.
+ */
+pa_status pa_page_scores(const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                         int max_blocks, const int32_t* seq_lens, int B, int Hkv, int D,
+                         int block_size, int num_blocks, int max_seq_len, pa_dtype kv_dtype,
+                         float* scores, int32_t* victims, int* device_error,
+                         struct CUstream_st* stream);
 
 /*
  * pa_decode_noalloc -- pa_decode for callers that cannot let a library

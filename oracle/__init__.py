@@ -17,6 +17,12 @@ Every function states the passage it follows (page title and section):
 * ``num_blocks`` / ``kv_elems_per_token`` / ``decode_bytes`` -- "PagedAttention:
   The Cache Was Storing Nothing" §2.1 (ceil(L / block_size) blocks per request)
   and §3 (2 x heads x head_dim x layers cached numbers per token).
+* ``copy_blocks`` -- the same page, §2.3: a block shared by several tables is
+  copied when one sequence diverges and writes into it (copy on write).
+* ``page_scores`` -- Pith review of arXiv 2509.04377 (PagedEviction), "Core
+  claim" and "What carries the argument": token importance ||V||_2 / ||K||_2,
+  page importance = mean over the page's tokens, and when the newest page has
+  just filled (L % block_size == 0) the lowest-scoring page is evicted.
 * ``append`` -- the same page, §1-§2.2: the cache grows by one token per step
   and only the last block is partly full, so the new token goes to slot
   ``cache_len % bs`` of the block the table names for ``cache_len // bs``.
@@ -83,6 +89,10 @@ def _load():
     lib.oracle_merge.restype = ci
     lib.oracle_append.argtypes = [vp, vp, vp, vp, i32p, ci, i32p, ci, ci, ci, ci, ci, ci]
     lib.oracle_append.restype = ci
+    lib.oracle_copy_blocks.argtypes = [vp, vp, i32p, i32p, ci, ci, ci64]
+    lib.oracle_copy_blocks.restype = ci
+    lib.oracle_page_scores.argtypes = [vp, vp, i32p, ci, i32p, ci, ci, ci, ci, ci, ci, f64p, i32p]
+    lib.oracle_page_scores.restype = ci
     _lib = lib
     return lib
 
@@ -227,3 +237,40 @@ def append(k_new, v_new, kpool: np.ndarray, vpool: np.ndarray, block_tables, cac
                                vpool.ctypes.data, _ptr_i32(bt), bt.shape[1], _ptr_i32(cl), B, Hkv,
                                D, bs, NB, kpool.dtype.itemsize)
     _check(rc)
+
+
+def copy_blocks(kpool: np.ndarray, vpool: np.ndarray, src, dst) -> None:
+    """Copy whole blocks src[i] -> dst[i] of both pools in place, in order."""
+    if kpool.dtype != vpool.dtype or kpool.shape != vpool.shape:
+        raise TypeError("oracle: pools must match")
+    if not (kpool.flags.c_contiguous and vpool.flags.c_contiguous):
+        raise ValueError("oracle: pools must be contiguous")
+    s, d = _i32(src), _i32(dst)
+    if s.shape != d.shape:
+        raise ValueError("oracle: src and dst differ in length")
+    NB = kpool.shape[0]
+    block_bytes = kpool.nbytes // NB
+    _check(_load().oracle_copy_blocks(kpool.ctypes.data, vpool.ctypes.data, _ptr_i32(s),
+                                      _ptr_i32(d), s.size, NB, block_bytes))
+
+
+def page_scores(kpool, vpool, block_tables, seq_lens):
+    """Per-page mean of ||V||/||K|| and the page to evict (or -1) per sequence.
+
+    Returns (scores float64 [B, max_blocks] with NaN past each sequence's
+    pages, victims int32 [B]).
+    """
+    kpool, dk = _storage(kpool)
+    vpool, dv = _storage(vpool)
+    if dk != dv or kpool.shape != vpool.shape:
+        raise TypeError("oracle: pools must match")
+    bt = _i32(block_tables)
+    sl = _i32(seq_lens)
+    NB, Hkv, bs, D = kpool.shape
+    B, MB = bt.shape
+    scores = np.full((B, MB), np.nan, dtype=np.float64)
+    victims = np.empty(B, dtype=np.int32)
+    _check(_load().oracle_page_scores(kpool.ctypes.data, vpool.ctypes.data, _ptr_i32(bt), MB,
+                                      _ptr_i32(sl), B, Hkv, D, bs, NB, dk, _ptr_f64(scores),
+                                      _ptr_i32(victims)))
+    return scores, victims

@@ -36,6 +36,7 @@
 // (the upper 16 bits of a float32). Every stored value is widened exactly to
 // double before any arithmetic.
 
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <cstring>
@@ -316,6 +317,79 @@ int oracle_append(const void* k_new, const void* v_new, void* kpool, void* vpool
                         static_cast<const char*>(v_new) + src * elem_bytes,
                         static_cast<size_t>(D) * elem_bytes);
         }
+    }
+    return 0;
+}
+
+// Block copies for copy-on-write ("PagedAttention: The Cache Was Storing
+// Nothing" §2.3: a shared block is copied only when a sequence diverges and
+// writes into it). Copies whole blocks (every kv head, every slot) of both
+// pools, pair i copying block src[i] to block dst[i], in order. block_bytes is
+// the size of one block of one pool. Returns -3 on an id outside the pool.
+int oracle_copy_blocks(void* kpool, void* vpool, const int32_t* src, const int32_t* dst, int n,
+                       int num_blocks, int64_t block_bytes) {
+    if (n < 0 || num_blocks < 1 || block_bytes < 1) return -1;
+    for (int i = 0; i < n; ++i) {
+        if (src[i] < 0 || src[i] >= num_blocks || dst[i] < 0 || dst[i] >= num_blocks) return -3;
+        char* k = static_cast<char*>(kpool);
+        char* v = static_cast<char*>(vpool);
+        std::memmove(k + dst[i] * block_bytes, k + src[i] * block_bytes, static_cast<size_t>(block_bytes));
+        std::memmove(v + dst[i] * block_bytes, v + src[i] * block_bytes, static_cast<size_t>(block_bytes));
+    }
+    return 0;
+}
+
+// PagedEviction page scores (Pith review of arXiv 2509.04377, "Core claim" and
+// "What carries the argument"): a token's importance is S = ||V||_2 / ||K||_2
+// of its cached value and key, a page's importance is the mean of S over its
+// tokens, and when the most recent page has just filled (L % bs == 0) the page
+// with the lowest mean is the one to evict. Readings: K and V of a token are
+// its vectors over all kv heads together (one block table serves every head,
+// so a page is evicted for all heads at once); ||K|| = 0 gives S = +inf; every
+// full page is a candidate; ties go to the lowest logical page.
+// scores[b * max_blocks + p] receives the mean over the valid tokens of
+// logical page p < ceil(L_b / bs) (other entries untouched); victims[b] the
+// page to evict, or -1 when L_b % bs != 0. Returns -2 / -3 on a bad length /
+// table entry.
+int oracle_page_scores(const void* kpool, const void* vpool, const int32_t* table, int max_blocks,
+                       const int32_t* seq_lens, int B, int Hkv, int D, int bs, int num_blocks,
+                       int dtype, double* scores, int32_t* victims) {
+    if (B < 0 || Hkv < 1 || D < 1 || bs < 1 || num_blocks < 1 || max_blocks < 1) return -1;
+    if (dtype != 0 && dtype != 1) return -1;
+    for (int b = 0; b < B; ++b) {
+        const int64_t L = seq_lens[b];
+        if (L < 1 || L > static_cast<int64_t>(max_blocks) * bs) return -2;
+        const int64_t nb = (L + bs - 1) / bs;
+        for (int64_t p = 0; p < nb; ++p) {
+            const int32_t phys = table[static_cast<int64_t>(b) * max_blocks + p];
+            if (phys < 0 || phys >= num_blocks) return -3;
+            const int64_t n = std::min<int64_t>(bs, L - p * bs);
+            double sum = 0.0;
+            for (int64_t slot = 0; slot < n; ++slot) {
+                double kk = 0.0, vv = 0.0;
+                for (int j = 0; j < Hkv; ++j) {
+                    const int64_t off = ((static_cast<int64_t>(phys) * Hkv + j) * bs + slot) * D;
+                    for (int d = 0; d < D; ++d) {
+                        const double k = load_elem(kpool, off + d, dtype);
+                        const double v = load_elem(vpool, off + d, dtype);
+                        kk += k * k;
+                        vv += v * v;
+                    }
+                }
+                sum += kk > 0.0 ? std::sqrt(vv) / std::sqrt(kk)
+                                : std::numeric_limits<double>::infinity();
+            }
+            scores[static_cast<int64_t>(b) * max_blocks + p] = sum / static_cast<double>(n);
+        }
+        int32_t victim = -1;
+        if (L % bs == 0) {
+            for (int64_t p = 0; p < nb; ++p) {
+                const double sp = scores[static_cast<int64_t>(b) * max_blocks + p];
+                if (victim < 0 || sp < scores[static_cast<int64_t>(b) * max_blocks + victim])
+                    victim = static_cast<int32_t>(p);
+            }
+        }
+        victims[b] = victim;
     }
     return 0;
 }

@@ -27,9 +27,10 @@ LIB_PATH = os.path.join(_PKG, "libpa.so")
 HEADER = os.path.join(os.path.dirname(_PKG), "include", "pa.h")
 
 PA_OK, PA_ERR_NULL, PA_ERR_SHAPE, PA_ERR_DTYPE, PA_ERR_BLOCK_SIZE = 0, 1, 2, 3, 4
-PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_BOUNDS, PA_ERR_ALIGN = 5, 6, 7, 8
+PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_BOUNDS, PA_ERR_ALIGN, PA_ERR_NO_BLOCKS = 5, 6, 7, 8, 9
 PA_F32, PA_BF16 = 0, 1
 PA_DEVERR_SEQ_LEN, PA_DEVERR_TABLE, PA_DEVERR_TIMEOUT, PA_DEVERR_CACHE_LEN = 1, 2, 4, 8
+PA_DEVERR_COPY = 16
 PA_PATH_AUTO, PA_PATH_SIMPLE, PA_PATH_FMA, PA_PATH_MMA = 0, 1, 2, 3
 
 _lib = None
@@ -71,6 +72,23 @@ def lib() -> ctypes.CDLL:
     L.pa_decode_noalloc.argtypes = [vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci, vp,
                                     ci, vp, vp]
     L.pa_decode_noalloc.restype = ci
+    i32p = ctypes.POINTER(ctypes.c_int32)
+    L.pa_copy_blocks.argtypes = [vp, vp, vp, vp, ci, ci, ci, ci, ci, ci, vp]
+    L.pa_copy_blocks.restype = ci
+    L.pa_bm_create.argtypes = [ci, ctypes.POINTER(vp)]
+    L.pa_bm_destroy.argtypes = [vp]
+    L.pa_bm_alloc.argtypes = [vp, ci, i32p]
+    L.pa_bm_fork.argtypes = [vp, i32p, ci]
+    L.pa_bm_release.argtypes = [vp, i32p, ci]
+    L.pa_bm_refcount.argtypes = [vp, ctypes.c_int32, ctypes.POINTER(ci)]
+    L.pa_bm_num_free.argtypes = [vp, ctypes.POINTER(ci)]
+    L.pa_bm_prepare_append.argtypes = [vp, i32p, ci, ci, i32p, ci, i32p, i32p,
+                                       ctypes.POINTER(ci)]
+    L.pa_page_scores.argtypes = [vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp]
+    L.pa_page_scores.restype = ci
+    for name in ("pa_bm_create", "pa_bm_destroy", "pa_bm_alloc", "pa_bm_fork", "pa_bm_release",
+                 "pa_bm_refcount", "pa_bm_num_free", "pa_bm_prepare_append"):
+        getattr(L, name).restype = ci
     _lib = L
     return L
 
@@ -190,6 +208,105 @@ def pa_decode_noalloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
                                  _dtype(out), err, _stream(stream))
     _check(st, "pa_decode_noalloc")
     return out
+
+
+def pa_copy_blocks(k_pool: torch.Tensor, v_pool: torch.Tensor, copy_src: torch.Tensor,
+                   copy_dst: torch.Tensor, stream=None) -> None:
+    """Copy whole blocks copy_src[i] -> copy_dst[i] of both pools (int32 device tensors)."""
+    NB, Hkv, bs, D = k_pool.shape
+    n = copy_src.numel()
+    if copy_dst.numel() != n:
+        raise ValueError("copy_src and copy_dst differ in length")
+    st = lib().pa_copy_blocks(_ptr(k_pool), _ptr(v_pool), _ptr(copy_src) if n else None,
+                              _ptr(copy_dst) if n else None, n, Hkv, D, bs, NB, _dtype(k_pool),
+                              _stream(stream))
+    _check(st, "pa_copy_blocks")
+
+
+def pa_page_scores(k_pool: torch.Tensor, v_pool: torch.Tensor, block_tables: torch.Tensor,
+                   seq_lens: torch.Tensor, max_seq_len: int, scores: torch.Tensor,
+                   victims: torch.Tensor, device_error: torch.Tensor | None = None,
+                   stream=None) -> None:
+    """PagedEviction page scores (float32 [B, max_blocks]) and victims (int32 [B])."""
+    NB, Hkv, bs, D = k_pool.shape
+    B, MB = block_tables.shape
+    err = _ptr(device_error) if device_error is not None else None
+    st = lib().pa_page_scores(_ptr(k_pool), _ptr(v_pool), _ptr(block_tables), MB, _ptr(seq_lens),
+                              B, Hkv, D, bs, NB, int(max_seq_len), _dtype(k_pool), _ptr(scores),
+                              _ptr(victims), err, _stream(stream))
+    _check(st, "pa_page_scores")
+
+
+class BlockManager:
+    """Host block manager (``pa_bm_*``): O(1) free list, reference counts, copy on write.
+
+    Arrays are numpy int32 (host memory).
+    """
+
+    def __init__(self, num_blocks: int):
+        import numpy as np  # noqa: F401  (arrays below)
+        self.handle = ctypes.c_void_p(None)
+        _check(lib().pa_bm_create(int(num_blocks), ctypes.byref(self.handle)), "pa_bm_create")
+
+    @staticmethod
+    def _i32p(a):
+        return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+    def close(self) -> None:
+        if self.handle.value:
+            lib().pa_bm_destroy(self.handle)
+            self.handle = ctypes.c_void_p(None)
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def alloc(self, n: int):
+        import numpy as np
+        ids = np.empty(max(n, 1), dtype=np.int32)
+        _check(lib().pa_bm_alloc(self.handle, int(n), self._i32p(ids)), "pa_bm_alloc")
+        return ids[:n]
+
+    def fork(self, ids) -> None:
+        import numpy as np
+        a = np.ascontiguousarray(ids, dtype=np.int32)
+        _check(lib().pa_bm_fork(self.handle, self._i32p(a), a.size), "pa_bm_fork")
+
+    def release(self, ids) -> None:
+        import numpy as np
+        a = np.ascontiguousarray(ids, dtype=np.int32)
+        _check(lib().pa_bm_release(self.handle, self._i32p(a), a.size), "pa_bm_release")
+
+    def refcount(self, block: int) -> int:
+        c = ctypes.c_int()
+        _check(lib().pa_bm_refcount(self.handle, int(block), ctypes.byref(c)), "pa_bm_refcount")
+        return c.value
+
+    @property
+    def num_free(self) -> int:
+        c = ctypes.c_int()
+        _check(lib().pa_bm_num_free(self.handle, ctypes.byref(c)), "pa_bm_num_free")
+        return c.value
+
+    def prepare_append(self, tables, cache_lens, block_size: int):
+        """Make each append target private; tables (host int32 [B, MB]) change in place.
+
+        Returns (copy_src, copy_dst) int32 arrays of the copy-on-write pairs.
+        """
+        import numpy as np
+        if not (tables.dtype == np.int32 and tables.flags.c_contiguous):
+            raise ValueError("tables must be a contiguous int32 array")
+        cl = np.ascontiguousarray(cache_lens, dtype=np.int32)
+        B, MB = tables.shape
+        src = np.empty(max(B, 1), dtype=np.int32)
+        dst = np.empty(max(B, 1), dtype=np.int32)
+        n = ctypes.c_int(0)
+        _check(lib().pa_bm_prepare_append(self.handle, self._i32p(tables), B, MB, self._i32p(cl),
+                                          int(block_size), self._i32p(src), self._i32p(dst),
+                                          ctypes.byref(n)), "pa_bm_prepare_append")
+        return src[:n.value].copy(), dst[:n.value].copy()
 
 
 def pa_free(plan: Plan) -> None:

@@ -123,6 +123,7 @@ const char* pa_status_str(pa_status s) {
         case PA_ERR_CUDA: return "a CUDA call failed";
         case PA_ERR_BOUNDS: return "a length or table entry was out of range on the device";
         case PA_ERR_ALIGN: return "a tensor is not 16-byte aligned";
+        case PA_ERR_NO_BLOCKS: return "the block pool has too few free blocks";
     }
     return "unknown status";
 }
@@ -326,6 +327,23 @@ pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
     plan->last_blocks = L.blocks;
     plan->last_warps = NW;
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* copy_src,
+                         const int32_t* copy_dst, int n, int Hkv, int D, int block_size,
+                         int num_blocks, pa_dtype kv_dtype, struct CUstream_st* stream) {
+    if (!k_pool || !v_pool || (n > 0 && (!copy_src || !copy_dst))) return PA_ERR_NULL;
+    if (kv_dtype != PA_F32 && kv_dtype != PA_BF16) return PA_ERR_DTYPE;
+    if (block_size != 16 && block_size != 32) return PA_ERR_BLOCK_SIZE;
+    if (n < 0 || n > 65535 || Hkv < 1 || (D != 64 && D != 128) || num_blocks < 1)
+        return PA_ERR_SHAPE;
+    if (!aligned16(k_pool) || !aligned16(v_pool)) return PA_ERR_ALIGN;
+    if (n == 0) return PA_OK;
+    pa::CopyArgs a{k_pool, v_pool, copy_src, copy_dst, n, num_blocks,
+                   static_cast<int64_t>(Hkv) * block_size * D * (kv_dtype == PA_F32 ? 4 : 2)};
+    return pa::launch_copy_blocks(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
 }
 
 pa_status pa_free(pa_plan* plan) {

@@ -2,12 +2,14 @@
 // physical block that the table names for logical block cache_len / BS -- the
 // only partly filled block of the sequence ("PagedAttention: The Cache Was
 // Storing Nothing" §1 and §2.2). A raw 16-byte-vector copy, bit-exact.
+#include <algorithm>
+
 #include "pa_internal.h"
 
 namespace pa {
 namespace {
 
-__device__ int g_append_error;  // library-wide append error word (per device)
+__device__ int g_append_error;  // library-wide word of append and block copies (per device)
 
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
     const int b = blockIdx.x;
@@ -37,7 +39,34 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
     }
 }
 
+// Block copies: blockIdx.y = copy pair, blockIdx.z = pool (0 = K, 1 = V);
+// the x blocks stride over the block's 16-byte vectors.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const CopyArgs a) {
+    const int i = blockIdx.y;
+    const int32_t s = a.src[i], d = a.dst[i];
+    if (s < 0 || s >= a.num_blocks || d < 0 || d >= a.num_blocks) {
+        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0) atomicOr(&g_append_error, kErrCopy);
+        return;
+    }
+    char* pool = static_cast<char*>(blockIdx.z ? a.vpool : a.kpool);
+    const uint4* src = reinterpret_cast<const uint4*>(pool + static_cast<int64_t>(s) * a.block_bytes);
+    uint4* dst = reinterpret_cast<uint4*>(pool + static_cast<int64_t>(d) * a.block_bytes);
+    const int64_t nvec = a.block_bytes / 16;
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec;
+         v += static_cast<int64_t>(gridDim.x) * blockDim.x)
+        dst[v] = src[v];
+}
+
 }  // namespace
+
+cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream) {
+    if (a.n == 0) return cudaSuccess;
+    const int64_t nvec = a.block_bytes / 16;
+    const int xblocks = static_cast<int>(std::min<int64_t>(8, (nvec + 255) / 256));
+    dim3 grid(xblocks, a.n, 2);
+    copy_blocks_kernel<<<grid, 256, 0, stream>>>(a);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     if (a.B == 0) return cudaSuccess;

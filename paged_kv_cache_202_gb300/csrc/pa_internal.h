@@ -17,6 +17,7 @@ constexpr int kErrSeqLen = 1;
 constexpr int kErrTable = 2;
 constexpr int kErrTimeout = 4;
 constexpr int kErrCacheLen = 8;
+constexpr int kErrCopy = 16;
 
 // Wall-clock limit of any single pipeline wait inside a kernel.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
@@ -95,6 +96,16 @@ struct AppendArgs {
     int B, Hkv, D, BS, max_blocks, num_blocks, elem_bytes;
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
+
+struct CopyArgs {
+    void* kpool;
+    void* vpool;
+    const int32_t* src;
+    const int32_t* dst;
+    int n, num_blocks;
+    int64_t block_bytes;  // bytes of one block of one pool (multiple of 16)
+};
+cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream);
 // Read and clear the append error word of the current device (synchronous).
 cudaError_t read_append_error(int* err);
 

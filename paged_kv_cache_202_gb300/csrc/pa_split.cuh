@@ -84,7 +84,7 @@ __device__ void scan_lengths(const int32_t* __restrict__ seq_lens, int B, int li
         len[b] = ok ? L : 0;
         sum += ok ? (L + BS - 1) / BS : 0;
     }
-    if (bad && blockIdx.x == 0) atomicOr(err, kErrSeqLen);
+    if (bad && blockIdx.x == 0 && err) atomicOr(err, kErrSeqLen);
     int x = sum;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {

@@ -233,9 +233,11 @@ def make_workload(name: str, seed: int | None = None, **overrides) -> Workload:
     shared = int(cfg.get("shared_prefix_blocks", 0))
 
     L = _draw_lengths(cfg["lengths"], B, rng) if B else np.zeros(0, dtype=np.int64)
-    if shared:
+    if shared and cfg.get("clip_shared", True):
         # Sharing sequences (even b) keep their append position past the shared
-        # prefix so that the shared blocks are never written.
+        # prefix so that the shared blocks are never written. With
+        # clip_shared=False a sharing sequence may append inside the prefix;
+        # its step then needs copy on write first.
         L[0::2] = np.clip(L[0::2], shared * bs + 1, cfg["max_len"])
     nblk = (L + bs - 1) // bs
     max_blocks = int(cfg.get("max_blocks", -(-cfg["max_len"] // bs)))
@@ -243,7 +245,7 @@ def make_workload(name: str, seed: int | None = None, **overrides) -> Workload:
         raise ValueError("a sequence needs more blocks than the table holds")
 
     # Pool size.
-    private = int(nblk.sum()) - (shared * len(L[0::2]) if shared else 0)
+    private = int(nblk.sum()) - (int(np.minimum(nblk[0::2], shared).sum()) if shared else 0)
     in_use = private + shared
     pk = cfg["pool"]
     NB = int(pk[1]) if pk[0] == "fixed" else int(math.ceil(pk[1] * (in_use + (B if shared else 0))))
@@ -259,7 +261,8 @@ def make_workload(name: str, seed: int | None = None, **overrides) -> Workload:
         prefix = alloc.alloc(shared) if shared else []
         for b in range(B):
             if shared and b % 2 == 0:
-                blocks = alloc.share(prefix) + alloc.alloc(int(nblk[b]) - shared)
+                n_sh = min(shared, int(nblk[b]))
+                blocks = alloc.share(prefix[:n_sh]) + alloc.alloc(int(nblk[b]) - n_sh)
             else:
                 blocks = alloc.alloc(int(nblk[b]))
             tables[b, :len(blocks)] = blocks
@@ -299,6 +302,8 @@ def make_workload(name: str, seed: int | None = None, **overrides) -> Workload:
     for b in range(B):
         c = int(L[b]) - 1
         last = int(tables[b, c // bs])
+        if alloc.refcount[last] > 1:
+            continue  # a shared block holds tokens other sequences still read
         kpool[last, :, c % bs:, :] = nan
         vpool[last, :, c % bs:, :] = nan
 
