@@ -233,7 +233,7 @@ pa_status pa_bm_prepare_append(pa_block_manager* bm, int32_t* tables, int B, int
  * arrays. The copies run in parallel: the destinations must be distinct and
  * no destination may be a source. An id outside [0, num_blocks) skips that
  * pair and raises PA_DEVERR_COPY in the library-wide word that
- * pa_last_device_error(NULL, ...) reads. n = 0 is a no-op.
+ * pa_last_device_error(NULL, ...) reads. n = 0 is a no-op; n <= 2^24.
  */
 pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* copy_src,
                          const int32_t* copy_dst, int n, int Hkv, int D, int block_size,

@@ -335,7 +335,7 @@ pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* copy_src,
     if (!k_pool || !v_pool || (n > 0 && (!copy_src || !copy_dst))) return PA_ERR_NULL;
     if (kv_dtype != PA_F32 && kv_dtype != PA_BF16) return PA_ERR_DTYPE;
     if (block_size != 16 && block_size != 32) return PA_ERR_BLOCK_SIZE;
-    if (n < 0 || n > 65535 || Hkv < 1 || (D != 64 && D != 128) || num_blocks < 1)
+    if (n < 0 || n > (1 << 24) || Hkv < 1 || (D != 64 && D != 128) || num_blocks < 1)
         return PA_ERR_SHAPE;
     if (!aligned16(k_pool) || !aligned16(v_pool)) return PA_ERR_ALIGN;
     if (n == 0) return PA_OK;

@@ -39,31 +39,41 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
     }
 }
 
-// Block copies: blockIdx.y = copy pair, blockIdx.z = pool (0 = K, 1 = V);
-// the x blocks stride over the block's 16-byte vectors.
+// Block copies: blockIdx.x = copy pair, blockIdx.y = pool (0 = K, 1 = V).
+// Each thread issues kVec 16-byte loads before storing any of them, so a
+// block moves in about one memory round trip.
 __global__ void __launch_bounds__(256) copy_blocks_kernel(const CopyArgs a) {
-    const int i = blockIdx.y;
+    constexpr int kVec = 8;
+    const int i = blockIdx.x;
     const int32_t s = a.src[i], d = a.dst[i];
     if (s < 0 || s >= a.num_blocks || d < 0 || d >= a.num_blocks) {
-        if (threadIdx.x == 0 && blockIdx.x == 0 && blockIdx.z == 0) atomicOr(&g_append_error, kErrCopy);
+        if (threadIdx.x == 0 && blockIdx.y == 0) atomicOr(&g_append_error, kErrCopy);
         return;
     }
-    char* pool = static_cast<char*>(blockIdx.z ? a.vpool : a.kpool);
+    char* pool = static_cast<char*>(blockIdx.y ? a.vpool : a.kpool);
     const uint4* src = reinterpret_cast<const uint4*>(pool + static_cast<int64_t>(s) * a.block_bytes);
     uint4* dst = reinterpret_cast<uint4*>(pool + static_cast<int64_t>(d) * a.block_bytes);
     const int64_t nvec = a.block_bytes / 16;
-    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec;
-         v += static_cast<int64_t>(gridDim.x) * blockDim.x)
-        dst[v] = src[v];
+    for (int64_t base = 0; base < nvec; base += kVec * blockDim.x) {
+        uint4 w[kVec];
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) {
+            const int64_t v = base + k * blockDim.x + threadIdx.x;
+            if (v < nvec) w[k] = src[v];
+        }
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) {
+            const int64_t v = base + k * blockDim.x + threadIdx.x;
+            if (v < nvec) dst[v] = w[k];
+        }
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream) {
     if (a.n == 0) return cudaSuccess;
-    const int64_t nvec = a.block_bytes / 16;
-    const int xblocks = static_cast<int>(std::min<int64_t>(8, (nvec + 255) / 256));
-    dim3 grid(xblocks, a.n, 2);
+    dim3 grid(a.n, 2);
     copy_blocks_kernel<<<grid, 256, 0, stream>>>(a);
     return cudaGetLastError();
 }

@@ -10,12 +10,10 @@
 // a candidate and ties go to the lowest logical page.
 //
 // The scan reads every attended K and V element once: it is HBM-bound like
-// the decode. Blocks of a persistent grid walk the flattened (sequence, page)
-// list with a stride, so work is balanced whatever the length mix; each page
-// of each kv head is read with 16-byte vector loads, the squares of a token
-// row are reduced by shuffles, the per-token sums over heads are gathered in
-// shared memory, and one warp turns them into the page's mean. A second small
-// kernel picks each sequence's victim.
+// the decode, and is built the same way (balanced page ranges per warp of a
+// persistent grid, per-warp bulk-copy pipelines on mbarriers, no block-level
+// synchronisation after the prologue). A second small kernel picks each
+// sequence's victim.
 #include <algorithm>
 #include <cmath>
 
@@ -35,6 +33,7 @@ struct ScoreArgs {
     int32_t* victims;
     int* err;
     int B, Hkv, D, max_blocks, num_blocks, max_seq_len;
+    int stages, stage_bytes, lens_bytes;
 };
 
 __device__ __forceinline__ void report(int* err, int bit) {
@@ -46,14 +45,14 @@ __device__ __forceinline__ float sumsq16(const uint4 w);
 template <>
 __device__ __forceinline__ float sumsq16<uint16_t>(const uint4 w) {
     const uint32_t x[4] = {w.x, w.y, w.z, w.w};
-    float s = 0.f;
+    float s0 = 0.f, s1 = 0.f;  // two chains for instruction-level parallelism
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const float a = bf16_lo(x[i]), b = bf16_hi(x[i]);
-        s = fmaf(a, a, s);
-        s = fmaf(b, b, s);
+        s0 = fmaf(a, a, s0);
+        s1 = fmaf(b, b, s1);
     }
-    return s;
+    return s0 + s1;
 }
 template <>
 __device__ __forceinline__ float sumsq16<float>(const uint4 w) {
@@ -62,85 +61,161 @@ __device__ __forceinline__ float sumsq16<float>(const uint4 w) {
     return fmaf(a, a, fmaf(b, b, fmaf(c, c, d * d)));
 }
 
-__device__ __forceinline__ uint4 ld_stream(const void* p) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(p));
-    return v;
-}
+// Score kernel: persistent blocks of kWarps warps; the flattened page list is
+// cut into equal ranges, one per warp (as in the split decode). A warp streams
+// its pages head by head through a ring of shared-memory stages: one stage =
+// the K and V pages of one (block, kv head), each a contiguous run moved by a
+// 1-D bulk copy that completes on the stage's mbarrier. Lane (half, token)
+// sums the squares of its half row, rotating the 16-byte column order by the
+// token so that the eight rows a quarter-warp reads hit different banks; after
+// the last head of a page the halves are joined, the token ratios formed and
+// averaged, and lane 0 writes the page score.
+constexpr int kScoreWarps = 8;
 
 template <int BS, typename T>
-__global__ void __launch_bounds__(256) page_score_kernel(const ScoreArgs a) {
-    extern __shared__ int smem_i[];
-    __shared__ float tok_kk[32], tok_vv[32];
-    int* pre = smem_i;
+__global__ void __launch_bounds__(kScoreWarps * 32, 1) page_score_kernel(const ScoreArgs a) {
+    constexpr int TPL = BS / 16;  // tokens per lane
+    extern __shared__ uint8_t smem_raw[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t raw = smem_addr(smem_raw);
+    const uint32_t base = (raw + 127u) & ~127u;
+    int* pre = reinterpret_cast<int*>(smem_raw + (base - raw));
     int* len = pre + (a.B + 1);
-    const int tid = threadIdx.x, lane = tid & 31;
+    const uint32_t ring0 = base + a.lens_bytes;
+    const uint32_t bars0 = ring0 + kScoreWarps * a.stages * a.stage_bytes;
     const int limit = min(a.max_seq_len, a.max_blocks * BS);
     split::scan_lengths<BS>(a.seq_lens, a.B, limit, pre, len, a.err);
-    const int total = pre[a.B];
-    const int cpr = a.D * static_cast<int>(sizeof(T)) / 16;  // 16-byte chunks per token row
-    const int per_head = BS * cpr;
-    const int64_t row_bytes = static_cast<int64_t>(a.D) * sizeof(T);
-    for (int x = blockIdx.x; x < total; x += gridDim.x) {
+
+    const int P = pre[a.B];
+    const int NW = gridDim.x * kScoreWarps;
+    const int per = (P + NW - 1) / NW;
+    const int x0 = (blockIdx.x * kScoreWarps + warp) * per;
+    const int x1 = min(x0 + per, P);
+    if (per == 0 || x0 >= x1) return;
+    const int S = a.stages, H = a.Hkv;
+    const uint32_t my_bars = bars0 + warp * S * 8;
+    const uint32_t my_ring = ring0 + warp * S * a.stage_bytes;
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) mbar_init(my_bars + 8 * s, 1);
+        fence_barrier_init();
+    }
+    __syncwarp();
+    const uint32_t row_bytes = a.D * sizeof(T);
+    const uint32_t page_bytes = BS * row_bytes;  // one pool, one (block, head)
+
+    // Page cursors (sequence, logical page) for issue and consume.
+    auto locate = [&](int x, int& b, int& p) {
         int lo = 0, hi = a.B - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
             if (pre[mid] <= x) lo = mid; else hi = mid - 1;
         }
-        const int b = lo, p = x - pre[b];
-        const int phys = a.tables[static_cast<int64_t>(b) * a.max_blocks + p];
-        float* out = a.scores + static_cast<int64_t>(b) * a.max_blocks + p;
-        if (phys < 0 || phys >= a.num_blocks) {
-            if (tid == 0) {
-                report(a.err, kErrTable);
-                *out = __int_as_float(0x7fc00000);
-            }
-            continue;  // uniform across the block
-        }
-        const int n = min(BS, len[b] - p * BS);
-        if (tid < 32) {
-            tok_kk[tid] = 0.f;
-            tok_vv[tid] = 0.f;
-        }
-        __syncthreads();
-        const char* kbase = static_cast<const char*>(a.kpool) + static_cast<int64_t>(phys) * a.Hkv * BS * row_bytes;
-        const char* vbase = static_cast<const char*>(a.vpool) + static_cast<int64_t>(phys) * a.Hkv * BS * row_bytes;
-        const int nchunks = a.Hkv * per_head;
-#pragma unroll 4
-        for (int c = tid; c < nchunks; c += blockDim.x) {
-            const int h = c / per_head, r = c - h * per_head;
-            const int t = r / cpr;
-            float kk = 0.f, vv = 0.f;
-            if (t < n) {
-                const int64_t off = (static_cast<int64_t>(h) * BS) * row_bytes + static_cast<int64_t>(r) * 16;
-                kk = sumsq16<T>(ld_stream(kbase + off));
-                vv = sumsq16<T>(ld_stream(vbase + off));
-            }
-            // Lanes c .. c+cpr-1 hold one token row (cpr is a power of two <= 32
-            // and blockDim.x a multiple of 32, so a row never straddles warps).
-            for (int off = 1; off < cpr; off <<= 1) {
-                kk += __shfl_xor_sync(0xffffffffu, kk, off);
-                vv += __shfl_xor_sync(0xffffffffu, vv, off);
-            }
-            if ((lane & (cpr - 1)) == 0 && t < n) {
-                atomicAdd(&tok_kk[t], kk);
-                atomicAdd(&tok_vv[t], vv);
+        b = lo;
+        p = x - pre[lo];
+    };
+    int ib, ip, ih = 0, ix = x0;  // issue cursor: page x = (ib, ip), head ih
+    locate(x0, ib, ip);
+    int iphys = a.tables[static_cast<int64_t>(ib) * a.max_blocks + ip];
+    uint32_t badmask = 0, phase = 0;
+    const int nitems = (x1 - x0) * H;
+    int n_issued = 0;
+
+    auto issue = [&](int s) {
+        const bool bad = iphys < 0 || iphys >= a.num_blocks;
+        badmask = bad ? (badmask | (1u << s)) : (badmask & ~(1u << s));
+        if (lane == 0) {
+            const uint32_t bar = my_bars + 8 * s;
+            const uint32_t stg = my_ring + s * a.stage_bytes;
+            if (bad) {
+                mbar_arrive(bar);
+            } else {
+                const int64_t off = (static_cast<int64_t>(iphys) * H + ih) * page_bytes;
+                mbar_arrive_expect_tx(bar, 2 * page_bytes);
+                bulk_load(stg, static_cast<const char*>(a.kpool) + off, page_bytes, bar);
+                bulk_load(stg + page_bytes, static_cast<const char*>(a.vpool) + off, page_bytes, bar);
             }
         }
-        __syncthreads();
-        if (tid < 32) {
-            float s = 0.f;
-            if (tid < n) {
-                const float kk = tok_kk[tid], vv = tok_vv[tid];
-                s = kk > 0.f ? sqrtf(vv) / sqrtf(kk) : INFINITY;
+        if (++ih == H) {
+            ih = 0;
+            if (++ix < x1) {
+                if (++ip == pre[ib + 1] - pre[ib]) locate(ix, ib, ip);
+                iphys = a.tables[static_cast<int64_t>(ib) * a.max_blocks + ip];
+            }
+        }
+        ++n_issued;
+    };
+    for (int s = 0; s < S && n_issued < nitems; ++s) issue(s);
+
+    const int hh = lane >> 4, tl = lane & 15;
+    const int CH = row_bytes / 32;  // 16-byte columns in half a row
+    int cb, cp;
+    locate(x0, cb, cp);
+    float kk[TPL], vv[TPL];
+    bool poison = false;
+    int s = 0;
+    for (int k = 0; k < nitems; ++k) {
+        const int h = k % H;
+        if (h == 0) {
+#pragma unroll
+            for (int j = 0; j < TPL; ++j) kk[j] = vv[j] = 0.f;
+            poison = false;
+        }
+        const uint32_t bar = my_bars + 8 * s;
+        const uint32_t stg = my_ring + s * a.stage_bytes;
+        const bool ready = mbar_wait_bounded(bar, (phase >> s) & 1u, kWaitLimitNs);
+        if (!__all_sync(0xffffffffu, ready)) {
+            if (lane == 0) report(a.err, kErrTimeout);
+            for (int j = k; j < n_issued; ++j) {
+                const int sj = j % S;
+                mbar_wait_bounded(my_bars + 8 * sj, (phase >> sj) & 1u, kWaitLimitNs);
+            }
+            return;
+        }
+        phase ^= 1u << s;
+        const int n = min(BS, len[cb] - cp * BS);
+        if ((badmask >> s) & 1u) {
+            poison = true;
+        } else {
+#pragma unroll
+            for (int j = 0; j < TPL; ++j) {
+                const int t = tl + 16 * j;
+                if (t < n) {
+                    for (int c = 0; c < CH; ++c) {
+                        const int col = hh * CH + (c + t) % CH;
+                        kk[j] += sumsq16<T>(lds_u128(stg + t * row_bytes + col * 16));
+                        vv[j] += sumsq16<T>(lds_u128(stg + page_bytes + t * row_bytes + col * 16));
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (n_issued < nitems) {
+            fence_proxy_async_smem();
+            issue(s);
+        }
+        if (h == H - 1) {
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < TPL; ++j) {
+                const float k2 = kk[j] + __shfl_xor_sync(0xffffffffu, kk[j], 16);
+                const float v2 = vv[j] + __shfl_xor_sync(0xffffffffu, vv[j], 16);
+                const int t = tl + 16 * j;
+                if (hh == 0 && t < n) sum += k2 > 0.f ? sqrtf(v2) / sqrtf(k2) : INFINITY;
             }
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-            if (tid == 0) *out = s / static_cast<float>(n);
+            for (int off = 1; off < 32; off <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+            if (lane == 0) {
+                float* out = a.scores + static_cast<int64_t>(cb) * a.max_blocks + cp;
+                if (poison) {
+                    report(a.err, kErrTable);
+                    *out = __int_as_float(0x7fc00000);
+                } else {
+                    *out = sum / static_cast<float>(n);
+                }
+            }
+            if (k + 1 < nitems && ++cp == pre[cb + 1] - pre[cb]) locate(x0 + (k + 1) / H, cb, cp);
         }
-        __syncthreads();
+        if (++s == S) s = 0;
     }
 }
 
@@ -182,20 +257,29 @@ __global__ void __launch_bounds__(128) victim_kernel(const ScoreArgs a, int BS) 
 }
 
 template <int BS>
-cudaError_t launch_scores(const ScoreArgs& a, bool bf16, int num_sms, cudaStream_t stream) {
-    const size_t smem = static_cast<size_t>(2 * a.B + 1) * 4;
+cudaError_t launch_scores(ScoreArgs a, bool bf16, int num_sms, cudaStream_t stream) {
+    const int esize = bf16 ? 2 : 4;
+    a.stage_bytes = 2 * BS * a.D * esize;               // K and V page of one (block, head)
+    a.lens_bytes = static_cast<int>((static_cast<size_t>(2 * a.B + 1) * 4 + 127) / 128 * 128);
+    a.stages = std::max(1, std::min(8, (192 * 1024) / (kScoreWarps * a.stage_bytes)));
+    const size_t smem = 128 + a.lens_bytes + static_cast<size_t>(kScoreWarps) * a.stages * a.stage_bytes +
+                        static_cast<size_t>(kScoreWarps) * a.stages * 8;
     auto kern = bf16 ? page_score_kernel<BS, uint16_t> : page_score_kernel<BS, float>;
-    if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-    }
+    cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reinterpret_cast<const void*>(kern),
+                                                      kScoreWarps * 32, smem);
+    if (e != cudaSuccess) return e;
     const int64_t max_pages = static_cast<int64_t>(a.B) *
                               ((std::min(a.max_seq_len, a.max_blocks * BS) + BS - 1) / BS);
-    const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(max_pages, 8ll * num_sms)));
-    kern<<<blocks, 256, smem, stream>>>(a);
-    cudaError_t e = cudaGetLastError();
+    const int64_t need = (max_pages + kScoreWarps * 4 - 1) / (kScoreWarps * 4);
+    const int blocks = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>(need, static_cast<int64_t>(std::max(per_sm, 1)) * num_sms)));
+    kern<<<blocks, kScoreWarps * 32, smem, stream>>>(a);
+    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     victim_kernel<<<(a.B + 3) / 4, 128, 0, stream>>>(a, BS);
     return cudaGetLastError();
@@ -228,7 +312,7 @@ extern "C" pa_status pa_page_scores(const void* k_pool, const void* v_pool,
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return PA_ERR_CUDA;
     pa::ScoreArgs a{k_pool, v_pool, block_tables, seq_lens, scores, victims, device_error,
-                    B, Hkv, D, max_blocks, num_blocks, max_seq_len};
+                    B, Hkv, D, max_blocks, num_blocks, max_seq_len, 0, 0, 0};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool bf16 = kv_dtype == PA_BF16;
     const cudaError_t e = block_size == 16 ? pa::launch_scores<16>(a, bf16, sms, s)
