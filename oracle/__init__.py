@@ -19,6 +19,10 @@ Every function states the passage it follows (page title and section):
   and §3 (2 x heads x head_dim x layers cached numbers per token).
 * ``copy_blocks`` -- the same page, §2.3: a block shared by several tables is
   copied when one sequence diverges and writes into it (copy on write).
+* ``prefill`` -- "FlashAttention vs PagedAttention", "How prefill and decode
+  change the diagnosis": the newest n_b tokens of a sequence are queries at
+  once; query i (position L - n_b + i) attends causally to tokens <= its
+  position, each row computed as ``decode`` over that prefix.
 * ``page_scores`` -- Pith review of arXiv 2509.04377 (PagedEviction), "Core
   claim" and "What carries the argument": token importance ||V||_2 / ||K||_2,
   page importance = mean over the page's tokens, and when the newest page has
@@ -93,6 +97,9 @@ def _load():
     lib.oracle_copy_blocks.restype = ci
     lib.oracle_page_scores.argtypes = [vp, vp, i32p, ci, i32p, ci, ci, ci, ci, ci, ci, f64p, i32p]
     lib.oracle_page_scores.restype = ci
+    lib.oracle_prefill.argtypes = [vp, vp, vp, i32p, ci, i32p, i32p, ci, ci, ci, ci, ci, ci, cf,
+                                   ci, f64p, ci]
+    lib.oracle_prefill.restype = ci
     _lib = lib
     return lib
 
@@ -274,3 +281,27 @@ def page_scores(kpool, vpool, block_tables, seq_lens):
                                       _ptr_i32(sl), B, Hkv, D, bs, NB, dk, _ptr_f64(scores),
                                       _ptr_i32(victims)))
     return scores, victims
+
+
+def prefill(q, kpool, vpool, block_tables, seq_lens, q_start, scale: float,
+            nthreads: int | None = None) -> np.ndarray:
+    """Causal paged multi-query attention in float64; returns [q_start[-1], Hq, D]."""
+    q, dt = _storage(q)
+    kpool, dk = _storage(kpool)
+    vpool, dv = _storage(vpool)
+    if not (dt == dk == dv):
+        raise TypeError("oracle: q, K and V must share one storage type")
+    bt = _i32(block_tables)
+    sl = _i32(seq_lens)
+    qs = _i32(q_start)
+    T, Hq, D = q.shape
+    NB, Hkv, bs, D2 = kpool.shape
+    B, MB = bt.shape
+    if D2 != D or qs.shape != (B + 1,) or int(qs[-1]) != T or sl.shape != (B,):
+        raise ValueError("oracle: inconsistent shapes")
+    out = np.empty((T, Hq, D), dtype=np.float64)
+    nthreads = nthreads or os.cpu_count() or 1
+    _check(_load().oracle_prefill(q.ctypes.data, kpool.ctypes.data, vpool.ctypes.data,
+                                  _ptr_i32(bt), MB, _ptr_i32(sl), _ptr_i32(qs), B, Hq, Hkv, D, bs,
+                                  NB, float(scale), dt, _ptr_f64(out), int(nthreads)))
+    return out

@@ -394,4 +394,63 @@ int oracle_page_scores(const void* kpool, const void* vpool, const int32_t* tabl
     return 0;
 }
 
+// Paged multi-query attention (chunked prefill, speculative verification):
+// the n_b = q_start[b+1] - q_start[b] newest tokens of sequence b are queries;
+// query i sits at position pos = L_b - n_b + i and attends, causally, to the
+// tokens t <= pos through the block table ("FlashAttention vs PagedAttention",
+// "How prefill and decode change the diagnosis": prefill processes many prompt
+// positions at once; decode is the case n_b = 1). q and out are
+// [q_start[B]][Hq][D]; each row is the three-pass attention of decode over
+// L = pos + 1 tokens. Returns -2 on n_b < 1 or n_b > L_b.
+int oracle_prefill(const void* q, const void* kpool, const void* vpool, const int32_t* table,
+                   int max_blocks, const int32_t* seq_lens, const int32_t* q_start, int B, int Hq,
+                   int Hkv, int D, int bs, int num_blocks, float scale, int dtype, double* out,
+                   int nthreads) {
+    if (!valid_shape(B, Hq, Hkv, D, bs, num_blocks, max_blocks, dtype)) return -1;
+    for (int b = 0; b < B; ++b) {
+        const int32_t n = q_start[b + 1] - q_start[b];
+        if (n < 1 || n > seq_lens[b] || static_cast<int64_t>(seq_lens[b]) > static_cast<int64_t>(max_blocks) * bs)
+            return -2;
+    }
+    const int64_t rows = q_start[B];
+    // One "sequence" per query row: the same table row, length pos + 1.
+    std::vector<int32_t> row_seq(static_cast<size_t>(rows)), row_len(static_cast<size_t>(rows));
+    for (int b = 0; b < B; ++b) {
+        const int32_t n = q_start[b + 1] - q_start[b];
+        for (int32_t i = 0; i < n; ++i) {
+            row_seq[static_cast<size_t>(q_start[b] + i)] = b;
+            row_len[static_cast<size_t>(q_start[b] + i)] = seq_lens[b] - n + i + 1;
+        }
+    }
+    if (nthreads < 1) nthreads = 1;
+    std::vector<int> status(static_cast<size_t>(nthreads), 0);
+    auto work = [&](int tid) {
+        for (int64_t i = tid; i < rows * Hq; i += nthreads) {
+            const int64_t r = i / Hq;
+            const int h = static_cast<int>(i % Hq);
+            const int b = row_seq[static_cast<size_t>(r)];
+            const int32_t len = row_len[static_cast<size_t>(r)];
+            // The query row r becomes "sequence 0" of a one-sequence problem over
+            // sequence b's table with length len; q offsets index row r directly.
+            const Problem p{static_cast<const char*>(q) + (r * Hq) * D * (dtype == 0 ? 4 : 2),
+                            kpool, vpool, table + static_cast<int64_t>(b) * max_blocks, max_blocks,
+                            &len, 1, Hq, Hkv, D, bs, num_blocks, static_cast<double>(scale), dtype};
+            if (!attend_one(p, 0, h, out + i * D, nullptr)) {
+                status[static_cast<size_t>(tid)] = -3;
+                return;
+            }
+        }
+    };
+    if (nthreads == 1) {
+        work(0);
+    } else {
+        std::vector<std::thread> pool;
+        for (int tid = 0; tid < nthreads; ++tid) pool.emplace_back(work, tid);
+        for (auto& th : pool) th.join();
+    }
+    for (int st : status)
+        if (st != 0) return st;
+    return 0;
+}
+
 }  // extern "C"
