@@ -49,6 +49,30 @@ def split_source_sha() -> str:
     return h.hexdigest()
 
 
+def CONFIGS_NEW_TOKENS(name):
+    from paged_kv_cache_202_gb300.workloads import CONFIGS
+    return CONFIGS[name].get("new_tokens", 256)
+
+
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def measured_peak_tflops():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        for key in ("bf16_tflops", "bf16_TFLOPs"):
+            if key in d:
+                v = d[key]
+                if isinstance(v, dict):
+                    v = v.get("burst", v.get("value"))
+                return float(v), "measured"
+    except (OSError, ValueError, TypeError):
+        pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
 def measured_peak_gbs():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -419,7 +443,30 @@ def run_row(args, local_rank):
     tables = torch.from_numpy(wl.block_tables).to(dev)
     seq_lens = torch.from_numpy(wl.seq_lens).to(dev)
     eb = wl.elem_bytes
-    if args.row == "copy_blocks":
+    if args.row == "prefill":
+        n_new = int(CONFIGS_NEW_TOKENS(args.workload))
+        wl.append_in_place()
+        k_pool, v_pool = to_dev(wl.k_pool), to_dev(wl.v_pool)
+        ns = np.minimum(wl.seq_lens, n_new).astype(np.int64)
+        qs = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
+        T = int(qs[-1])
+        from paged_kv_cache_202_gb300.workloads import bf16_bits
+        qh = bf16_bits(np.random.default_rng(7).standard_normal((T, wl.Hq, wl.D))
+                       .astype(np.float32))
+        q = to_dev(qh)
+        q_start = torch.from_numpy(qs).to(dev)
+        out = torch.empty(T, wl.Hq, wl.D, dtype=torch.bfloat16, device=dev)
+        # causal: row i of sequence b sees L_b - n_b + i + 1 tokens; 4 D flops per token
+        toks = sum(int(((wl.seq_lens[b] - ns[b] + 1) * 2 + ns[b] - 1) * ns[b] // 2)
+                   for b in range(wl.B))
+        flops = 4 * wl.D * wl.Hq * toks
+        nbytes = 2 * wl.Hkv * wl.D * eb * int(wl.seq_lens.sum()) + 2 * T * wl.Hq * wl.D * 2
+
+        def call():
+            pa.pa_prefill(q, q_start, k_pool, v_pool, tables, seq_lens, wl.scale, out,
+                          int(ns.max()), wl.max_seq_len)
+        what = f"{T} query rows ({n_new} newest tokens per sequence), causal"
+    elif args.row == "copy_blocks":
         n = min(8192, wl.num_blocks // 2)
         perm = np.random.default_rng(0).permutation(wl.num_blocks)
         src = torch.from_numpy(perm[:n].astype(np.int32)).to(dev)
@@ -460,6 +507,34 @@ def run_row(args, local_rank):
     ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ev)
     peak, peak_kind = measured_peak_gbs()
     gbs = nbytes / (ms * 1e-3) / 1e9
+    if args.row == "prefill":
+        tpeak, tkind = measured_peak_tflops()
+        tfs = flops / (ms * 1e-3) / 1e12
+        parity = None
+        if not args.no_parity:
+            import oracle
+            rng = np.random.default_rng(3)
+            rows = rng.choice(T, size=min(24, T), replace=False)
+            seq_of = np.searchsorted(qs, rows, side="right") - 1
+            err = 0.0
+            for r, b in zip(rows, seq_of):
+                i = r - qs[b]
+                sub = oracle.prefill(qh[r:r + 1], wl.k_pool, wl.v_pool, wl.block_tables[b:b + 1],
+                                     [int(wl.seq_lens[b] - ns[b] + i + 1)], [0, 1], wl.scale)
+                got = out[r].float().cpu().numpy().astype(np.float64)
+                err = max(err, float(np.abs(got - sub[0]).max()))
+            parity = {"rows": int(len(rows)), "max_abs_err": err, "tol": 1.5e-2}
+        print(json.dumps({
+            "row": "prefill", "metric": "prefill: achieved bf16 TFLOP/s", "value": tfs,
+            "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "what": what},
+            "roofline": {"bound": "tensor", "achieved": tfs, "peak": tpeak, "peak_kind": tkind,
+                         "unit": "TFLOP/s", "frac": tfs / tpeak, "algorithmic_flops": flops,
+                         "hbm_gbs": gbs},
+            "parity": parity, "gpu_launches": args.steps,
+        }), flush=True)
+        return
     print(json.dumps({
         "row": args.row, "metric": f"{args.row}: achieved HBM GB/s", "value": gbs, "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -478,15 +553,19 @@ def main():
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="llama3_8b_gqa")
+    ap.add_argument("--workload", default=None,
+                    help="default: llama3_8b_gqa (prefill row: prefill_gqa)")
     ap.add_argument("--seed", type=int, default=None)
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
-    ap.add_argument("--row", default="decode", choices=["decode", "copy_blocks", "page_scores"])
+    ap.add_argument("--row", default="decode",
+                    choices=["decode", "copy_blocks", "page_scores", "prefill"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.workload is None:
+        args.workload = "prefill_gqa" if args.row == "prefill" else "llama3_8b_gqa"
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         run_reference(args, rank)

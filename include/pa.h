@@ -179,6 +179,36 @@ pa_status pa_plan_info(const pa_plan* plan, int* path, int* blocks, int* warps);
 pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
                                    struct CUevent_st* stop);
 
+/*
+ * pa_prefill -- causal paged multi-query attention (chunked prefill,
+ * speculative verification) on the tensor cores.
+ *
+ * The newest n_b = q_start[b+1] - q_start[b] tokens of sequence b are
+ * queries at once: query i sits at position L_b - n_b + i (L_b = seq_lens[b])
+ * and attends to the tokens t <= its position read through the block table
+ * ("FlashAttention vs PagedAttention", "How prefill and decode change the
+ * diagnosis"; each row is exactly the decode attention over its prefix). The
+ * K/V of the new tokens must already be in the pools.
+ *
+ *   q         device bf16 [q_start[B]][Hq][D], rows of sequence b at
+ *             q_start[b] .. q_start[b+1]-1
+ *   q_start   device int32 [B + 1], nondecreasing, q_start[0] = 0
+ *   max_q     host bound on every n_b (sizes the launch)
+ *   out       device [q_start[B]][Hq][D] out_dtype
+ *   device_error  device int or NULL (NULL = the library-wide word read by
+ *             pa_last_device_error(NULL, ...)): PA_DEVERR_* bits
+ *
+ * Supported: bf16 pools, D = 128, block_size 16 or 32, Hq / Hkv dividing 128,
+ * max_blocks <= 16384. n_b < 1, n_b > L_b or L_b out of range raise
+ * PA_DEVERR_SEQ_LEN and leave that sequence's rows untouched; a table entry
+ * outside the pool raises PA_DEVERR_TABLE and zeroes the affected rows.
+ */
+pa_status pa_prefill(const void* q, const int32_t* q_start, const void* k_pool, const void* v_pool,
+                     const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int B,
+                     int Hq, int Hkv, int D, int block_size, int num_blocks, int max_q,
+                     int max_seq_len, float scale, pa_dtype kv_dtype, void* out, pa_dtype out_dtype,
+                     int* device_error, struct CUstream_st* stream);
+
 /* ------------------------------------------------------------------------
  * Block management: free list, sharing and copy on write.
  *

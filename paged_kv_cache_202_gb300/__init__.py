@@ -84,6 +84,9 @@ def lib() -> ctypes.CDLL:
     L.pa_bm_num_free.argtypes = [vp, ctypes.POINTER(ci)]
     L.pa_bm_prepare_append.argtypes = [vp, i32p, ci, ci, i32p, ci, i32p, i32p,
                                        ctypes.POINTER(ci)]
+    L.pa_prefill.argtypes = [vp, vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf, ci, vp,
+                             ci, vp, vp]
+    L.pa_prefill.restype = ci
     L.pa_page_scores.argtypes = [vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp]
     L.pa_page_scores.restype = ci
     for name in ("pa_bm_create", "pa_bm_destroy", "pa_bm_alloc", "pa_bm_fork", "pa_bm_release",
@@ -221,6 +224,23 @@ def pa_copy_blocks(k_pool: torch.Tensor, v_pool: torch.Tensor, copy_src: torch.T
                               _ptr(copy_dst) if n else None, n, Hkv, D, bs, NB, _dtype(k_pool),
                               _stream(stream))
     _check(st, "pa_copy_blocks")
+
+
+def pa_prefill(q: torch.Tensor, q_start: torch.Tensor, k_pool: torch.Tensor,
+               v_pool: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+               scale: float, out: torch.Tensor, max_q: int, max_seq_len: int,
+               device_error: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Causal paged multi-query attention (bf16 pools, D = 128); returns ``out``."""
+    T, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_pool.shape
+    B, MB = block_tables.shape
+    err = _ptr(device_error) if device_error is not None else None
+    st = lib().pa_prefill(_ptr(q), _ptr(q_start), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+                          MB, _ptr(seq_lens), B, Hq, Hkv, D, bs, NB, int(max_q),
+                          int(max_seq_len), float(scale), _dtype(k_pool), _ptr(out), _dtype(out),
+                          err, _stream(stream))
+    _check(st, "pa_prefill")
+    return out
 
 
 def pa_page_scores(k_pool: torch.Tensor, v_pool: torch.Tensor, block_tables: torch.Tensor,

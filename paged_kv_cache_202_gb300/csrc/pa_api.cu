@@ -346,6 +346,43 @@ pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* copy_src,
                : PA_ERR_CUDA;
 }
 
+pa_status pa_prefill(const void* q, const int32_t* q_start, const void* k_pool,
+                     const void* v_pool, const int32_t* block_tables, int max_blocks,
+                     const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
+                     int num_blocks, int max_q, int max_seq_len, float scale, pa_dtype kv_dtype,
+                     void* out, pa_dtype out_dtype, int* device_error,
+                     struct CUstream_st* stream) {
+    if (!q || !q_start || !k_pool || !v_pool || !block_tables || !seq_lens || !out)
+        return PA_ERR_NULL;
+    if (kv_dtype != PA_BF16 || (out_dtype != PA_F32 && out_dtype != PA_BF16)) return PA_ERR_DTYPE;
+    if (block_size != 16 && block_size != 32) return PA_ERR_BLOCK_SIZE;
+    if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D != 128 || num_blocks < 1 ||
+        max_blocks < 1 || max_blocks > 16384 || max_q < 1 || max_seq_len < 1 ||
+        !std::isfinite(scale))
+        return PA_ERR_SHAPE;
+    const int g = Hq / Hkv;
+    if (g > 128 || 128 % g != 0) return PA_ERR_SHAPE;  // a block holds 128 / g whole queries
+    if (static_cast<int64_t>(num_blocks) * Hkv > INT32_MAX ||
+        static_cast<int64_t>(max_blocks) * block_size > INT32_MAX)
+        return PA_ERR_SHAPE;
+    if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
+        return PA_ERR_ALIGN;
+    if (B == 0) return PA_OK;
+    CUtensorMap kmap, vmap;
+    if (!encode_pool_map(&kmap, k_pool, num_blocks * Hkv, D, block_size) ||
+        !encode_pool_map(&vmap, v_pool, num_blocks * Hkv, D, block_size))
+        return PA_ERR_CUDA;
+    int* err = device_error;
+    if (!err && pa::append_error_address(&err) != cudaSuccess) return PA_ERR_CUDA;
+    const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    return pa::launch_prefill(kmap, vmap, q, q_start, block_tables, seq_lens, out, err, B, Hq, Hkv,
+                              max_blocks, num_blocks, max_seq_len, max_q, scale_log2,
+                              out_dtype == PA_BF16, block_size,
+                              reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PA_OK
+               : PA_ERR_CUDA;
+}
+
 pa_status pa_free(pa_plan* plan) {
     if (!plan) return PA_OK;
     DeviceGuard guard(plan->device);

@@ -97,3 +97,9 @@ cudaError_t read_append_error(int* err) {
 }
 
 }  // namespace pa
+
+namespace pa {
+cudaError_t append_error_address(int** p) {
+    return cudaGetSymbolAddress(reinterpret_cast<void**>(p), g_append_error);
+}
+}  // namespace pa

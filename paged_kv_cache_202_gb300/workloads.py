@@ -23,6 +23,9 @@ name                  shape
                       the blocks in use
 ``long_splitk``       B=8, 64 q / 8 kv heads, D=128, bf16, block 32, every
                       length 131072, 1% of tokens have K scaled by 8
+``prefill_gqa``       B=16, 32 q / 8 kv heads, D=128, bf16, block 16, lengths
+                      log-uniform in [1024, 16384]; the newest 256 tokens of
+                      each sequence are queries (chunked prefill)
 ``mixed_shared``      B=256, 32 q / 8 kv heads, D=128, bf16, block 16,
                       lengths geometric (mean 1024) clipped to [1, 8192];
                       even sequences share the same first 64 physical blocks
@@ -45,7 +48,7 @@ import torch
 
 # numpy PCG64 seeds: 1000 + the workload's ordinal.
 _ORDINAL = {"tiny_worked_60": 1, "llama7b_mha": 2, "llama3_8b_gqa": 3, "long_splitk": 4,
-            "mixed_shared": 5}
+            "mixed_shared": 5, "prefill_gqa": 6}
 
 CONFIGS = {
     "tiny_worked_60": dict(B=1, Hq=1, Hkv=1, D=64, block_size=16, dtype="f32",
@@ -59,6 +62,9 @@ CONFIGS = {
     "long_splitk": dict(B=8, Hq=64, Hkv=8, D=128, block_size=32, dtype="bf16",
                         lengths=("fixed", 131072), pool=("factor", 1.0), max_len=131072,
                         k_outliers=(0.01, 8.0)),
+    "prefill_gqa": dict(B=16, Hq=32, Hkv=8, D=128, block_size=16, dtype="bf16",
+                        lengths=("loguniform", 1024, 16384), pool=("factor", 1.1), max_len=16384,
+                        new_tokens=256),
     "mixed_shared": dict(B=256, Hq=32, Hkv=8, D=128, block_size=16, dtype="bf16",
                          lengths=("geometric", 1.0 / 1024.0, 1, 8192), pool=("factor", 1.1),
                          max_len=8192, shared_prefix_blocks=64),

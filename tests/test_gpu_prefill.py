@@ -1,0 +1,87 @@
+"""GPU: causal paged multi-query attention (tcgen05 tensor cores) against the
+fp64 oracle, within the bf16 tolerance. Query counts that do not fill a block,
+partial final chunks, NaN-poisoned slots past each sequence, GQA group sizes
+1..16 and both block sizes are covered."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_202_gb300 as pa
+from paged_kv_cache_202_gb300.workloads import bf16_bits, make_workload
+
+from gpu_helpers import BF16_TOL, DeviceStep, out_f64, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def _case(lens, ns, Hq=32, Hkv=8, bs=16, seed=0):
+    wl = make_workload("llama3_8b_gqa", seed=seed, B=len(lens), Hq=Hq, Hkv=Hkv, block_size=bs,
+                       lengths=("list", lens), max_len=max(lens) + bs)
+    wl.append_in_place()   # every token of the chunk is already in the pools
+    rng = np.random.default_rng(seed + 1)
+    T = int(sum(ns))
+    q = bf16_bits(rng.standard_normal((T, Hq, wl.D)).astype(np.float32))
+    qs = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
+    return wl, q, qs
+
+
+def _run(wl, q, qs, ns):
+    ds = DeviceStep(wl)
+    qd = to_dev(q, "bf16")
+    out = torch.full((q.shape[0], wl.Hq, wl.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_prefill(qd, torch.from_numpy(qs).cuda(), ds.k_pool, ds.v_pool, ds.tables, ds.seq_lens,
+                  wl.scale, out, max(ns), wl.max_seq_len, device_error=err)
+    torch.cuda.synchronize()
+    return out_f64(out), int(err.item())
+
+
+@pytest.mark.parametrize("Hq,Hkv,bs,lens,ns", [
+    (32, 8, 16, [200, 64, 1000], [37, 64, 130]),        # g = 4: 32 queries per block
+    (64, 8, 32, [513, 129], [129, 1]),                  # g = 8, block size 32
+    (8, 8, 16, [300, 1], [150, 1]),                     # g = 1: 128 queries per block
+    (16, 1, 16, [90, 640], [8, 40]),                    # g = 16 (MQA-like)
+    (4, 2, 32, [64, 65, 66], [64, 65, 2]),              # g = 2, ragged edges
+])
+def test_prefill_matches_oracle(Hq, Hkv, bs, lens, ns):
+    wl, q, qs = _case(lens, ns, Hq=Hq, Hkv=Hkv, bs=bs)
+    got, err = _run(wl, q, qs, ns)
+    assert err == 0
+    ref = oracle.prefill(q, wl.k_pool, wl.v_pool, wl.block_tables, wl.seq_lens, qs, wl.scale)
+    assert np.isfinite(got).all()
+    e = np.abs(got - ref).max()
+    assert e <= BF16_TOL, f"max abs error {e:.3e}"
+
+
+def test_single_query_prefill_matches_decode():
+    wl, q, qs = _case([77, 300, 16], [1, 1, 1])
+    got, err = _run(wl, q, qs, [1, 1, 1])
+    ref = oracle.prefill(q, wl.k_pool, wl.v_pool, wl.block_tables, wl.seq_lens, qs, wl.scale)
+    assert err == 0 and np.abs(got - ref).max() <= BF16_TOL
+
+
+def test_prefill_bad_lengths_and_table():
+    wl, q, qs = _case([100, 50], [10, 10])
+    ds = DeviceStep(wl)
+    qd = to_dev(q, "bf16")
+    out = torch.zeros((q.shape[0], wl.Hq, wl.D), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t = ds.tables.clone()
+    t[1, 0] = wl.num_blocks + 1
+    pa.pa_prefill(qd, torch.from_numpy(qs).cuda(), ds.k_pool, ds.v_pool, t, ds.seq_lens, wl.scale,
+                  out, 10, wl.max_seq_len, device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.PA_DEVERR_TABLE
+    got = out_f64(out)
+    assert (got[10:] == 0).all()
+    ref = oracle.prefill(q[:10], wl.k_pool, wl.v_pool, wl.block_tables[:1], wl.seq_lens[:1],
+                         qs[:2], wl.scale)
+    assert np.abs(got[:10] - ref).max() <= BF16_TOL
