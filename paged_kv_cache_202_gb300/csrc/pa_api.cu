@@ -20,6 +20,8 @@ using pa::SplitLaunch;
 constexpr size_t kSmemLimit = 232448;     // opt-in dynamic shared memory per block on sm_10x
 constexpr int kDefaultWarps = 3;           // warps per block of the split kernels
 constexpr int kDefaultStages = 1;          // pipeline stages per warp
+constexpr int kDynPermille = 150;          // share of the page stream scheduled dynamically
+constexpr int kDynMinPages = 1024;         // ... when a sequence may have this many pages
 constexpr int kMinPagesPerWarp = 4;
 constexpr int kHeadSlice = 16;             // query heads per kv unit on the tensor-core path
 constexpr int kMaxBatch = 8192;            // per-sequence arrays live in shared memory
@@ -81,6 +83,17 @@ void tuning_override(int* warps, int* stages) {
         *warps = w;
         *stages = st;
     }
+}
+
+// Optional override "permille[,pages]" of the dynamically scheduled share of
+// the page stream (0..500 per mille) and of the pages per dynamic piece.
+void dynamic_override(int* permille, int* pages) {
+    const char* s = std::getenv("PA_SPLIT_DYNAMIC");
+    if (!s) return;
+    int v = -1, p = -1;
+    const int n = std::sscanf(s, "%d,%d", &v, &p);
+    if (n >= 1 && v >= 0 && v <= 500) *permille = v;
+    if (n == 2 && p >= 1 && p <= 4096) *pages = p;
 }
 
 struct DeviceGuard {
@@ -236,8 +249,10 @@ pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
     int stages = kDefaultStages;
     tuning_override(&warps, &stages);
     if (stages < 1) stages = 1;
+    // ring, mbarriers (8 B each, padded to 16 B), per-stage range records (16 B each)
     const size_t smem = 1024 + lens_bytes + static_cast<size_t>(warps) * stages * stage_bytes +
-                        static_cast<size_t>(warps) * stages * 8;
+                        round_up(static_cast<size_t>(warps) * stages * 8, 16) +
+                        static_cast<size_t>(warps) * stages * 16;
     if (smem > kSmemLimit) return PA_ERR_SHAPE;
 
     SplitLaunch L{kind, D, block_size, NT, warps, 0, smem};
@@ -257,17 +272,27 @@ pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
                          (static_cast<int64_t>(warps) * kMinPagesPerWarp);
     L.blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(need, static_cast<int64_t>(plan->num_sms) * per_sm)));
     const int NW = L.blocks * warps;
+    // Dynamic tail: dyn_permille of the page stream in pieces of 256 tokens,
+    // only when sequences can be long (many pages per segment): there the
+    // static split leaves an uneven finish; short segments balance already
+    // and would only pay for the wider merge.
+    int dyn_permille = max_pages >= kDynMinPages ? kDynPermille : 0;
+    int dyn_pages = 256 / block_size;
+    dynamic_override(&dyn_permille, &dyn_pages);
+    const int64_t max_pieces = P_max * dyn_permille / 1000 / dyn_pages + 1;
+    const int64_t ranges = static_cast<int64_t>(NW) + max_pieces;
 
     // Workspace: metadata, partial (m, l), partial value sums.
     const size_t meta_bytes = round_up(static_cast<size_t>(pa::kMetaHeader + B + 1) * 4u, 256);
-    const size_t ml_bytes = round_up(static_cast<size_t>(2) * NW * GS * 2 * 4u, 256);
-    const size_t acc_bytes = round_up(static_cast<size_t>(2) * NW * GS * D * 4u, 256);
+    const size_t ml_bytes = round_up(static_cast<size_t>(2) * ranges * GS * 2 * 4u, 256);
+    const size_t acc_bytes = round_up(static_cast<size_t>(2) * ranges * GS * D * 4u, 256);
     const size_t need_ws = meta_bytes + ml_bytes + acc_bytes;
     if (plan->ws_bytes < need_ws) {
         if (plan->ws) cudaFree(plan->ws);
         plan->ws = nullptr;
         plan->ws_bytes = 0;
         if (cudaMalloc(&plan->ws, need_ws) != cudaSuccess) return PA_ERR_CUDA;
+        if (cudaMemset(plan->ws, 0, need_ws) != cudaSuccess) return PA_ERR_CUDA;  // piece counter = 0
         plan->ws_bytes = need_ws;
     }
     char* ws = static_cast<char*>(plan->ws);
@@ -316,12 +341,15 @@ pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
     a.stages = stages;
     a.stage_bytes = static_cast<int>(stage_bytes);
     a.lens_bytes = static_cast<int>(lens_bytes);
+    a.dyn_permille = dyn_permille;
+    a.dyn_pages = dyn_pages;
 
     if (plan->ev_start) cudaEventRecord(plan->ev_start, stream);
     cudaError_t e = pa::launch_split(L, plan->kmap, plan->vmap, a, stream);
     if (plan->ev_stop) cudaEventRecord(plan->ev_stop, stream);
     if (e != cudaSuccess) return PA_ERR_CUDA;
-    pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, GS, nslices, U, D, out_dtype == PA_BF16};
+    pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, GS, nslices, U, D, out_dtype == PA_BF16,
+                    dyn_permille > 0};
     e = pa::launch_merge(m, stream);
     plan->last_path = path;
     plan->last_blocks = L.blocks;

@@ -8,9 +8,12 @@
 namespace pa {
 
 // Workspace metadata written by block 0 of the split kernel and read by the
-// merge kernel: [0] total pages P, [1] pages per warp, [2] warps, [3] unused,
-// then the page prefix sums pre[0..B] (pre[b] = pages of sequences < b).
-constexpr int kMetaHeader = 4;
+// merge kernel: [0] total pages P, [1] pages per static range, [2] warps NW,
+// [3] dynamic-piece counter (zero between calls; the merge kernel resets it),
+// [4] end A of the static part of the page stream, [5] pages per dynamic
+// piece, [6] dynamic pieces, [7] unused, then the page prefix sums pre[0..B]
+// (pre[b] = pages of sequences < b).
+constexpr int kMetaHeader = 8;
 
 // Bits of the device error word (mirrors PA_DEVERR_* in pa.h).
 constexpr int kErrSeqLen = 1;
@@ -46,6 +49,8 @@ struct SplitArgs {
     int stages;                // pipeline stages per warp
     int stage_bytes;           // bytes per stage (multiple of 1024)
     int lens_bytes;            // bytes of the per-sequence arrays at the front of shared memory
+    int dyn_permille;          // fraction of the page stream handed out dynamically (1/1000)
+    int dyn_pages;             // pages per dynamic piece
 };
 
 struct SplitLaunch {
@@ -63,12 +68,13 @@ cudaError_t launch_split(const SplitLaunch& L, const CUtensorMap& kmap, const CU
                          const SplitArgs& a, cudaStream_t stream);
 
 struct MergeArgs {
-    const int* ws_meta;
+    int* ws_meta;
     const float* ws_acc;
     const float* ws_ml;
     void* out;
     int B, Hq, g, GS, nslices, U, D;
     int out_bf16;
+    int wide;  // 1: eight warps per row (many partials per row), 0: one warp per row
 };
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 

@@ -40,6 +40,8 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
 constexpr int kMaxDevices = 64;
 constexpr int kDefaultWarps = 3;
 constexpr int kDefaultStages = 1;
+constexpr int kDynPermille = 150;
+constexpr int kDynMinPages = 1024;
 constexpr size_t kSmemLimit = 232448;
 constexpr int kMinPagesPerWarp = 4;
 constexpr int kHeadSlice = 16;
@@ -128,6 +130,7 @@ bool encode_pool(CUtensorMap* map, const void* pool, int rows, int D, int BS) {
 }
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+void dynamic_override(int*, int*) {}  // the no-alloc entry point always uses the default
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -186,8 +189,10 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     const size_t lens_bytes = round_up(static_cast<size_t>(2 * B + 1) * 4u, 1024);
     const int warps = kDefaultWarps;
     const int stages = kDefaultStages;
+    // ring, mbarriers (8 B each, padded to 16 B), per-stage range records (16 B each)
     const size_t smem = 1024 + lens_bytes + static_cast<size_t>(warps) * stages * stage_bytes +
-                        static_cast<size_t>(warps) * stages * 8;
+                        round_up(static_cast<size_t>(warps) * stages * 8, 16) +
+                        static_cast<size_t>(warps) * stages * 16;
     if (smem > kSmemLimit) return PA_ERR_SHAPE;
     pa::SplitLaunch L{kind, D, block_size, NT, warps, 0, smem};
     const int per_sm = blocks_per_sm(dev, L, &st);
@@ -197,12 +202,21 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     L.blocks = static_cast<int>(
         std::max<int64_t>(1, std::min<int64_t>(need, static_cast<int64_t>(num_sms) * per_sm)));
     const int NW = L.blocks * warps;
+    // Dynamic tail: dyn_permille of the page stream in pieces of 256 tokens,
+    // only when sequences can be long (many pages per segment): there the
+    // static split leaves an uneven finish; short segments balance already
+    // and would only pay for the wider merge.
+    int dyn_permille = max_pages >= kDynMinPages ? kDynPermille : 0;
+    int dyn_pages = 256 / block_size;
+    dynamic_override(&dyn_permille, &dyn_pages);
+    const int64_t max_pieces = P_max * dyn_permille / 1000 / dyn_pages + 1;
+    const int64_t ranges = static_cast<int64_t>(NW) + max_pieces;
 
     // Scratch layout: fallback error word, metadata, partial (m, l), partial sums.
     const size_t err_bytes = 256;
     const size_t meta_bytes = round_up(static_cast<size_t>(pa::kMetaHeader + B + 1) * 4u, 256);
-    const size_t ml_bytes = round_up(static_cast<size_t>(2) * NW * GS * 2 * 4u, 256);
-    const size_t acc_bytes = round_up(static_cast<size_t>(2) * NW * GS * D * 4u, 256);
+    const size_t ml_bytes = round_up(static_cast<size_t>(2) * ranges * GS * 2 * 4u, 256);
+    const size_t acc_bytes = round_up(static_cast<size_t>(2) * ranges * GS * D * 4u, 256);
     if (err_bytes + meta_bytes + ml_bytes + acc_bytes > kNoAllocScratchBytes)
         return PA_ERR_WORKSPACE;
     int* err = reinterpret_cast<int*>(scratch);
@@ -213,6 +227,8 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
         if (cudaMemsetAsync(err, 0, sizeof(int), stream) != cudaSuccess) return PA_ERR_CUDA;
         device_error = err;
     }
+    // The split kernel's dynamic-piece counter must start at zero.
+    if (cudaMemsetAsync(meta + 3, 0, sizeof(int), stream) != cudaSuccess) return PA_ERR_CUDA;
 
     CUtensorMap kmap, vmap;
     const int rows = num_blocks * Hkv;
@@ -244,7 +260,10 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     a.stages = stages;
     a.stage_bytes = static_cast<int>(stage_bytes);
     a.lens_bytes = static_cast<int>(lens_bytes);
+    a.dyn_permille = dyn_permille;
+    a.dyn_pages = dyn_pages;
     if (pa::launch_split(L, kmap, vmap, a, stream) != cudaSuccess) return PA_ERR_CUDA;
-    pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, GS, nslices, U, D, out_dtype == PA_BF16};
+    pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, GS, nslices, U, D, out_dtype == PA_BF16,
+                    dyn_permille > 0};
     return pa::launch_merge(m, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

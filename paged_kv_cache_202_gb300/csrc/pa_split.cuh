@@ -6,12 +6,14 @@
 // logical blocks in order through the block table). A kv unit is one kv head
 // and one slice of at most 16 of the query heads that share it
 // ("PagedAttention: The Cache Was Storing Nothing" §3.1). All segments are
-// concatenated into one stream of P pages and cut into equal contiguous
-// ranges, one per resident warp of a persistent grid. A warp therefore
-// processes a balanced number of pages whatever the length mix; it produces a
-// finished output row for every segment it covers completely, and a partial
-// (m, l, acc) for at most two segments cut by its range boundaries. The merge
-// kernel combines those with the two-partial rule of "39 · PagedAttention" §3.
+// concatenated into one stream of P pages and cut into contiguous ranges: one
+// equal static range per resident warp of a persistent grid for most of the
+// stream, then small pieces claimed dynamically by whichever warp is free, so
+// the work is balanced whatever the length mix and whatever the speed of each
+// SM. A range produces a finished output row for every segment it covers
+// completely, and a partial (m, l, acc) for at most two segments cut by its
+// boundaries. The merge kernel combines those with the two-partial rule of
+// "39 · PagedAttention" §3.
 // Splitting along the sequence is what keeps the chip busy when a decode has
 // only one query row ("PagedAttention: The Cache Was Storing Nothing", "Where
 // this goes next").
@@ -469,6 +471,29 @@ struct MmaState {
 // one segment: two 16-token pages stacked (block size 16) or one 32-token
 // page. Both give the same shared-memory image, [D/64 boxes][32 rows][128 B]
 // with the 128-byte swizzle, so the arithmetic sees one 32-token tile pair.
+// Ranges of the page stream. The first (1 - f) of the stream is cut into equal
+// static ranges, one per warp; the last fraction f into small dynamic pieces of
+// dyn_pages pages that warps claim through an atomic counter once their static
+// range is done (guided self-scheduling: warps that run faster take more of the
+// tail). A range id r owns partial slots 2r (head) and 2r + 1 (tail): static
+// ranges have ids 0 .. NW-1, dynamic piece j has id NW + j.
+struct Range {
+    int x0, x1, id;
+};
+
+__device__ __forceinline__ void sts_v4i(uint32_t addr, int a0, int a1, int a2) {
+    asm volatile("st.shared.v4.s32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a0), "r"(a1), "r"(a2), "r"(0)
+                 : "memory");
+}
+
+__device__ __forceinline__ int4 lds_v4i(uint32_t addr) {
+    int4 v;
+    asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
 template <int D, int BS, typename State>
 __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtensorMap* vmap,
                                            const SplitArgs& a) {
@@ -480,8 +505,11 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
     const uint32_t base = (raw + 1023u) & ~1023u;
     int* pre = reinterpret_cast<int*>(smem_raw + (base - raw));
     int* len = pre + (a.B + 1);
+    const int S = a.stages;
     const uint32_t ring0 = base + a.lens_bytes;
-    const uint32_t bars0 = ring0 + static_cast<uint32_t>(W * a.stages * a.stage_bytes);
+    const uint32_t bars0 = ring0 + static_cast<uint32_t>(W * S * a.stage_bytes);
+    // Per stage: range x0, x1, id (16-byte records, so 16-byte aligned).
+    const uint32_t meta0 = bars0 + ((static_cast<uint32_t>(W * S * 8) + 15u) & ~15u);
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(kmap);
@@ -492,22 +520,28 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
 
     const int P = a.U * pre[a.B];
     const int NW = gridDim.x * W;
-    const int per = (P + NW - 1) / NW;
+    // Dynamic tail: a fraction of the stream in pieces of dyn_pages (none for
+    // small streams, where the static ranges are already short).
+    const int qd = a.dyn_pages;
+    const int Dp = (P >= 8 * NW * qd) ? (static_cast<int>(static_cast<long long>(P) * a.dyn_permille / 1000) / qd) * qd : 0;
+    const int A = P - Dp;
+    const int per = max(1, (A + NW - 1) / NW);
+    const int nd = Dp / qd;
     if (blockIdx.x == 0) {
         for (int i = threadIdx.x; i <= a.B; i += blockDim.x) a.ws_meta[kMetaHeader + i] = pre[i];
         if (threadIdx.x == 0) {
             a.ws_meta[0] = P;
             a.ws_meta[1] = per;
             a.ws_meta[2] = NW;
-            a.ws_meta[3] = 0;
+            // [3] is the dynamic-piece counter: zero on entry, reset by the merge.
+            a.ws_meta[4] = A;
+            a.ws_meta[5] = qd;
+            a.ws_meta[6] = nd;
         }
     }
     const int gw = blockIdx.x * W + warp;
-    const int x0 = gw * per;
-    const int x1 = min(x0 + per, P);
-    if (per == 0 || x0 >= x1) return;
-    const int S = a.stages;
     const uint32_t my_bars = bars0 + warp * S * 8;
+    const uint32_t my_meta = meta0 + warp * S * 16;
     const uint32_t my_ring = ring0 + static_cast<uint32_t>(warp * S * a.stage_bytes);
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(my_bars + 8 * s, 1);
@@ -515,26 +549,35 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
     }
     __syncwarp();
 
-    // Locate the first page of this warp's range.
-    Cursor cc;
-    {
+    auto claim = [&]() -> Range {
+        int j = 0;
+        if (lane == 0) j = atomicAdd(a.ws_meta + 3, 1);
+        j = __shfl_sync(0xffffffffu, j, 0);
+        if (j >= nd) return Range{-1, -1, -1};
+        return Range{A + j * qd, min(A + (j + 1) * qd, P), NW + j};
+    };
+    auto locate = [&](int x) {
         int lo = 0, hi = a.B - 1;
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (a.U * pre[mid] <= x0) lo = mid; else hi = mid - 1;
+            if (a.U * pre[mid] <= x) lo = mid; else hi = mid - 1;
         }
         const int nb = seq_pages(pre, lo);
-        const int off = x0 - a.U * pre[lo];
-        cc = Cursor{lo, off / nb, off % nb, nb};
-    }
-    Cursor ci = cc;
-    int xc = x0, xi = x0;  // global page index of the consume and issue cursors
+        const int off = x - a.U * pre[lo];
+        return Cursor{lo, off / nb, off % nb, nb};
+    };
+
+    Range ri{gw * per, min(gw * per + per, A), gw};
+    if (ri.x0 >= ri.x1) ri = claim();
+    if (ri.id < 0) return;
+    Cursor ci = locate(ri.x0);
+    int xi = ri.x0;
+    bool issue_done = false;
     const uint32_t page_bytes = 2u * BS * D * 2u;  // K + V of one page
     const uint64_t policy = policy_evict_first();
     int tb_row = -1, tb_base = -1, tbl = -1;  // table batch: entries [tb_base, tb_base+32) of row tb_row
     uint32_t badmask = 0, phase = 0;
 
-    auto chunk_pages = [&](const Cursor& c, int x) { return min(min(CP, c.nb - c.p), x1 - x); };
     auto table_entry = [&](int b, int p, int nb) {
         const int pbase = p & ~31;
         if (b != tb_row || pbase != tb_base) {
@@ -549,8 +592,8 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
 
     // Issue the chunk at the issue cursor into stage s; warp-collective.
     auto issue = [&](int s) {
-        const int n = chunk_pages(ci, xi);
-        const bool qstart = xi == x0 || ci.p == 0;
+        const int n = min(min(CP, ci.nb - ci.p), ri.x1 - xi);
+        const bool qstart = xi == ri.x0 || ci.p == 0;
         int phys[CP];
         bool bad = false;
 #pragma unroll
@@ -562,6 +605,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
         if (lane == 0) {
             const uint32_t bar = my_bars + 8 * s;
             const uint32_t stg = my_ring + static_cast<uint32_t>(s * a.stage_bytes);
+            sts_v4i(my_meta + 16 * s, ri.x0, ri.x1, ri.id);  // released by the arrive below
             const int kvh = ci.u / a.nslices, slice = ci.u - kvh * a.nslices;
             const int nh = min(a.GS, a.g - slice * a.GS);
             const uint32_t qbytes = qstart ? static_cast<uint32_t>(nh * D * 2) : 0u;
@@ -592,16 +636,28 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
         }
         for (int j = 0; j < n; ++j) advance(ci, pre, a.U, a.B);
         xi += n;
+        if (xi == ri.x1) {  // next range: a dynamic piece, if any is left
+            ri = claim();
+            if (ri.id < 0) {
+                issue_done = true;
+            } else {
+                ci = locate(ri.x0);
+                xi = ri.x0;
+            }
+        }
     };
 
     int n_issued = 0;
-    for (int s = 0; s < S && xi < x1; ++s, ++n_issued) issue(s);
+    for (int s = 0; s < S && !issue_done; ++s, ++n_issued) issue(s);
 
     State st;
+    Range rc{-1, -1, -1};
+    Cursor cc{0, 0, 0, 0};
+    int xc = 0;
     int p_first = 0, hq0 = 0, nh = 0;
     bool poison = false;
     int s = 0, n_done = 0;
-    while (xc < x1) {
+    while (n_done < n_issued) {
         const uint32_t bar = my_bars + 8 * s;
         const uint32_t stg = my_ring + static_cast<uint32_t>(s * a.stage_bytes);
         const bool ready = mbar_wait_bounded(bar, (phase >> s) & 1u, kWaitLimitNs);
@@ -615,8 +671,14 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
             return;
         }
         phase ^= 1u << s;
-        const int n = chunk_pages(cc, xc);
-        if (xc == x0 || cc.p == 0) {
+        const int4 m4 = lds_v4i(my_meta + 16 * s);
+        if (m4.z != rc.id) {  // first chunk of a new range
+            rc = Range{m4.x, m4.y, m4.z};
+            xc = rc.x0;
+            cc = locate(xc);
+        }
+        const int n = min(min(CP, cc.nb - cc.p), rc.x1 - xc);
+        if (xc == rc.x0 || cc.p == 0) {
             const int kvh = cc.u / a.nslices, slice = cc.u - kvh * a.nslices;
             nh = min(a.GS, a.g - slice * a.GS);
             hq0 = kvh * a.g + slice * a.GS;
@@ -631,15 +693,15 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
             st.page(stg, stg + CT * D * 2, nv, a.scale_log2, lane);
         }
         __syncwarp();
-        if (xi < x1) {
+        if (!issue_done) {
             fence_proxy_async_smem();
             issue(s);
             ++n_issued;
         }
         const int p_last = cc.p + n - 1;
-        if (p_last == cc.nb - 1 || xc + n == x1) {
+        if (p_last == cc.nb - 1 || xc + n == rc.x1) {
             const bool full = p_first == 0 && p_last == cc.nb - 1;
-            const int slot = gw * 2 + (p_first > 0 ? 0 : 1);
+            const int slot = rc.id * 2 + (p_first > 0 ? 0 : 1);
             st.finish(a, cc.b, hq0, nh, full, poison, slot, lane);
         }
         for (int j = 0; j < n; ++j) advance(cc, pre, a.U, a.B);
