@@ -37,8 +37,8 @@ L2_BYTES = 126 * 2**20
 # DRAM traffic of the split-attention kernel from an ncu capture (per launch,
 # scaled to the full workload), valid only for the kernel sources it was
 # measured on (sha256 of the split kernel's source files).
-TRAFFIC = {"source_sha": "f49ea8c3a94d378483ccb4e3e37c2d21818a0dfe286e90e70c7b90fc8b6855fa",
-           "workload": "llama3_8b_gqa", "bytes_per_launch": 2211840440}
+TRAFFIC = {"source_sha": "ebcc10d8c27f5b7c6ffa7a8b70c6fc892f9c28291717c2ab67fe0db47b7604d6",
+           "workload": "llama3_8b_gqa", "bytes_per_launch": 2205603584 + 5870080}
 
 
 def split_source_sha() -> str:
@@ -289,7 +289,10 @@ def run_ours(args, rank, world, local_rank):
     app_bytes = pa.append_bytes(wl.B, wl.Hkv, wl.D, eb)
     step_bytes = dec_bytes + app_bytes
 
-    # Timed region: K steps, split-kernel events per step.
+    # Timed region: K steps exactly as a caller issues them. The split and
+    # merge kernels start under programmatic dependent launch, which overlaps
+    # each launch with its predecessor's drain; an event recorded between two
+    # kernels would cancel that overlap, so the step loop carries none.
     ev_split = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
                 for _ in range(args.steps)]
     for a_, b_ in ev_split:       # create the underlying events before the timed region
@@ -305,12 +308,18 @@ def run_ours(args, rank, world, local_rank):
     w0 = time.time()
     ev0.record(stream)
     for i in range(args.steps):
-        plan.set_split_events(*ev_split[i])
         step()
     ev1.record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
     barrier()
+    # Kernel pass: the same K steps again, with events around every split
+    # launch, for the split kernel's average duration (the roofline figure).
+    for i in range(args.steps):
+        plan.set_split_events(*ev_split[i])
+        step()
+    torch.cuda.synchronize()
+    w2 = time.time()
     plan.set_split_events(None, None)
     time.sleep(0.25)
     sampler.stop()
@@ -388,7 +397,7 @@ def run_ours(args, rank, world, local_rank):
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["source_sha"] == sha and \
         TRAFFIC["workload"] == wl.name else None
     value = world * step_bytes / (ms_step * 1e-3) / 1e9
-    clocks = sampler.summary(w0, w1)
+    clocks = sampler.summary(w0, w2)
     path, blocks, warps = plan.info()
     plan.free()
     if rank == 0:
@@ -408,7 +417,9 @@ def run_ours(args, rank, world, local_rank):
             "roofline": {"bound": "hbm", "kernel": "split attention", "achieved": achieved,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
-                         "algorithmic_bytes": dec_bytes, "ms_per_launch": split_ms},
+                         "algorithmic_bytes": dec_bytes, "ms_per_launch": split_ms,
+                         "timing": "CUDA events around each split launch, in a second pass "
+                                   "of the K timed steps"},
             "e2e": {"value": world * step_bytes / e2e_s / 1e9, "unit": "GB/s",
                     "ms_per_step": e2e_s * 1e3, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},

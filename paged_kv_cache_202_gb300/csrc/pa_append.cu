@@ -5,6 +5,7 @@
 #include <algorithm>
 
 #include "pa_internal.h"
+#include "pa_ptx.cuh"
 
 namespace pa {
 namespace {
@@ -12,6 +13,7 @@ namespace {
 __device__ int g_append_error;  // library-wide word of append and block copies (per device)
 
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
+    griddep_launch_dependents();  // a following decode may start launching
     const int b = blockIdx.x;
     const int pos = a.cache_lens[b];
     if (pos < 0 || pos >= a.max_blocks * a.BS) {

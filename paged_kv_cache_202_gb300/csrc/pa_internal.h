@@ -74,7 +74,7 @@ struct MergeArgs {
     void* out;
     int B, Hq, g, GS, nslices, U, D;
     int out_bf16;
-    int wide;  // 1: eight warps per row (many partials per row), 0: one warp per row
+    int wide;  // 1: several warps per row (many partials per row), 0: one warp per row
 };
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 

@@ -1,13 +1,15 @@
 // Merge of split partials: for every (sequence, query head) whose segment was
 // cut across warps, combine the partials (m_i, l_i, acc_i) with
 //   m = max_i m_i,  l = sum_i l_i 2^(m_i - m),  o = sum_i acc_i 2^(m_i - m) / l
-// -- the two-partial rule of "39 · PagedAttention" §3 applied left to right,
-// with the value sums rescaled by the same factors; the maxima are in the log2
-// domain of the split kernel. Rows of invalid sequences are written as zeros,
+// -- the two-partial rule of "39 · PagedAttention" §3, applied to batches of
+// partials against a running maximum, with the value sums rescaled by the
+// same factors; the maxima are in the log2 domain of the split kernel. Rows of invalid sequences are written as zeros,
 // rows whose partial carries the poison marker (NaN max, a bad table entry)
 // too. Segments finished inside one range were already written by the split
 // kernel and are skipped. The merge also resets the split kernel's
 // dynamic-piece counter for the next call.
+#include <cstdlib>
+
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
 
@@ -15,24 +17,41 @@ namespace pa {
 namespace {
 
 // WPR warps per (sequence, query head) row, 8 / WPR rows per block of 8
-// warps. The warps of a row split its partials (warp w folds every WPR-th
-// one, with its loads unrolled so that several are in flight), then the
-// row's first warp folds the warps' results. Lane l owns elements
-// [l * D/32, (l+1) * D/32) of the row. Many warps per row pay off when
-// dynamic pieces cut long segments into many partials; one warp per row is
-// cheaper otherwise.
+// warps. Warp w of a row folds partials rf + w, rf + w + WPR, ... in batches
+// of kBatch: the loads of a whole batch are issued before any is used, then
+// the batch is folded into the warp's running (m, l, acc) with one rescale.
+// The warps of a row then combine their results through shared memory, on a
+// named barrier of their own, so rows of one block may leave at different
+// points. Lane l owns elements [l * D/32, (l+1) * D/32) of the row.
+// Launched as a programmatic dependent of the split kernel: it waits for the
+// split kernel's completion before reading anything.
 template <int D, int WPR>
 __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
     constexpr int DPL = D / 32;
-    constexpr int kMergeWarps = WPR;
+    constexpr int kBatch = 8;
     constexpr int kRowsPerBlock = 8 / WPR;
     __shared__ float sm_m[8], sm_l[8];
-    __shared__ float sm_acc[8][D];
+    __shared__ int sm_poison[8];
+    __shared__ float sm_acc[WPR > 1 ? 8 : 1][D];
     const int lane = threadIdx.x & 31;
     const int gwarp = threadIdx.x >> 5;
     const int warp = gwarp % WPR;            // warp within the row
     const int slotw = gwarp - warp;          // first warp of the row in this block
     const int row = blockIdx.x * kRowsPerBlock + gwarp / WPR;
+    // Barrier over the WPR warps of this row only: named barrier 1 + the row's
+    // index in the block (barrier 0 is the block's), ids kept immediate.
+    auto row_sync = [&] {
+        const int rb = gwarp / WPR;
+        if (rb == 0) asm volatile("bar.sync 1, %0;" ::"n"(WPR * 32) : "memory");
+        if constexpr (kRowsPerBlock > 1) {
+            if (rb == 1) asm volatile("bar.sync 2, %0;" ::"n"(WPR * 32) : "memory");
+        }
+        if constexpr (kRowsPerBlock > 2) {
+            if (rb == 2) asm volatile("bar.sync 3, %0;" ::"n"(WPR * 32) : "memory");
+            if (rb == 3) asm volatile("bar.sync 4, %0;" ::"n"(WPR * 32) : "memory");
+        }
+    };
+    griddep_wait();  // the split kernel's partials and metadata
     if (row >= a.B * a.Hq) return;
     const int b = row / a.Hq, hq = row - b * a.Hq;
     const int* pre = a.ws_meta + kMetaHeader;
@@ -80,78 +99,101 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
     // the head slots of the others (empty static ranges past A hold nothing).
     auto holds = [&](int r) { return r >= NW || static_cast<long long>(r) * per < A; };
     auto slot_of = [&](int r) { return r == rf ? r * 2 + 1 : r * 2; };
-    // Pass 1: the row maximum (and poison) over all partials.
-    float m = -INFINITY;
+
+    // This warp's partials, folded with a running maximum m (log2 domain).
+    float m = -INFINITY, l = 0.f;
     bool poison = false;
-    for (int r = rf + warp * 32 + lane; r <= rl; r += kMergeWarps * 32) {
-        if (!holds(r)) continue;
-        const float mi = a.ws_ml[(static_cast<size_t>(slot_of(r)) * a.GS + j) * 2];
-        poison |= mi != mi;
-        m = fmaxf(m, mi);
-    }
+    for (int r0 = rf + warp; r0 <= rl; r0 += kBatch * WPR) {
+        float mi[kBatch], li[kBatch], v[kBatch][DPL];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    poison = __any_sync(0xffffffffu, poison);
-    if constexpr (WPR > 1) {
-        if (lane == 0) {
-            sm_m[slotw + warp] = m;
-            sm_l[slotw + warp] = poison ? 1.f : 0.f;
-        }
-        __syncthreads();
-        m = sm_m[slotw];
-        poison = false;
+        for (int k = 0; k < kBatch; ++k) {
+            const int r = r0 + k * WPR;
+            mi[k] = -INFINITY;
+            li[k] = 0.f;
 #pragma unroll
-        for (int w = 0; w < kMergeWarps; ++w) {
-            m = fmaxf(m, sm_m[slotw + w]);
-            poison |= sm_l[slotw + w] != 0.f;
+            for (int i = 0; i < DPL; ++i) v[k][i] = 0.f;
+            if (r <= rl && holds(r)) {
+                const size_t base = static_cast<size_t>(slot_of(r)) * a.GS + j;
+                mi[k] = a.ws_ml[base * 2];
+                li[k] = a.ws_ml[base * 2 + 1];
+                const float* src = a.ws_acc + base * D + d0;
+                if constexpr (DPL == 4) {
+                    const float4 t = *reinterpret_cast<const float4*>(src);
+                    v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
+                } else {
+                    const float2 t = *reinterpret_cast<const float2*>(src);
+                    v[k][0] = t.x; v[k][1] = t.y;
+                }
+            }
         }
+        float mb = m;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            poison |= mi[k] != mi[k];   // the split kernel's poison marker
+            mb = fmaxf(mb, mi[k]);      // fmaxf passes over NaN
+        }
+        if (mb == -INFINITY) continue;  // nothing of the segment in this batch
+        const float fo = fast_exp2(m - mb);   // 0 while m is still -inf
+        l *= fo;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] *= fo;
+#pragma unroll
+        for (int k = 0; k < kBatch; ++k) {
+            const float f = fast_exp2(mi[k] - mb);  // 0 for the empty entries
+            l = fmaf(li[k], f, l);
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) acc[i] = fmaf(v[k][i], f, acc[i]);
+        }
+        m = mb;
     }
-    if (poison) {
-        if (warp == 0) store(acc);
-        return;
-    }
-    if constexpr (WPR > 1) __syncthreads();
-    // Pass 2: this warp's share of l and acc, rescaled to the row maximum.
-    float l = 0.f;
-#pragma unroll 4
-    for (int r = rf + warp; r <= rl; r += kMergeWarps) {
-        if (!holds(r)) continue;
-        const size_t base = static_cast<size_t>(slot_of(r)) * a.GS + j;
-        const float f = fast_exp2(a.ws_ml[base * 2] - m);
-        l = fmaf(a.ws_ml[base * 2 + 1], f, l);
-        const float* src = a.ws_acc + base * D + d0;
-        if constexpr (DPL == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(src);
-            acc[0] = fmaf(v.x, f, acc[0]);
-            acc[1] = fmaf(v.y, f, acc[1]);
-            acc[2] = fmaf(v.z, f, acc[2]);
-            acc[3] = fmaf(v.w, f, acc[3]);
+
+    if constexpr (WPR == 1) {
+        if (poison) {
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
         } else {
-            const float2 v = *reinterpret_cast<const float2*>(src);
-            acc[0] = fmaf(v.x, f, acc[0]);
-            acc[1] = fmaf(v.y, f, acc[1]);
-        }
-    }
-    if constexpr (WPR == 1) {  // every lane folded every partial: l is already the row's
-        const float inv = 1.f / l;
+            const float inv = 1.f / l;
 #pragma unroll
-        for (int i = 0; i < DPL; ++i) acc[i] *= inv;
+            for (int i = 0; i < DPL; ++i) acc[i] *= inv;
+        }
         store(acc);
     } else {
-        if (lane == 0) sm_l[slotw + warp] = l;
+        if (lane == 0) {
+            sm_m[slotw + warp] = m;
+            sm_l[slotw + warp] = l;
+            sm_poison[slotw + warp] = poison ? 1 : 0;
+        }
 #pragma unroll
         for (int i = 0; i < DPL; ++i) sm_acc[slotw + warp][d0 + i] = acc[i];
-        __syncthreads();
+        row_sync();
         if (warp != 0) return;
+        float M = -INFINITY;
+        bool bad = false;
+#pragma unroll
+        for (int w = 0; w < WPR; ++w) {
+            M = fmaxf(M, sm_m[slotw + w]);
+            bad |= sm_poison[slotw + w] != 0;
+        }
+        if (bad || M == -INFINITY) {
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+            store(acc);
+            return;
+        }
+        float f[WPR];
         float lt = 0.f;
 #pragma unroll
-        for (int w = 0; w < kMergeWarps; ++w) lt += sm_l[slotw + w];
+        for (int w = 0; w < WPR; ++w) {
+            f[w] = fast_exp2(sm_m[slotw + w] - M);  // 0 for a warp that held nothing
+            lt = fmaf(sm_l[slotw + w], f[w], lt);
+        }
+        const float inv = 1.f / lt;
 #pragma unroll
         for (int i = 0; i < DPL; ++i) {
-            float v = 0.f;
+            float t = 0.f;
 #pragma unroll
-            for (int w = 0; w < kMergeWarps; ++w) v += sm_acc[slotw + w][d0 + i];
-            acc[i] = v / lt;
+            for (int w = 0; w < WPR; ++w) t = fmaf(sm_acc[slotw + w][d0 + i], f[w], t);
+            acc[i] = t * inv;
         }
         store(acc);
     }
@@ -162,18 +204,34 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
     const int rows = a.B * a.Hq;
     if (rows == 0) return cudaSuccess;
-    const bool wide = a.wide;
-    const int blocks = wide ? rows : (rows + 7) / 8;
+    // Warps per row when dynamic pieces cut long segments into many partials
+    // (tuning override PA_MERGE_WARPS = 2, 4 or 8); one warp per row otherwise.
+    static const int wide_warps = [] {
+        const char* e = std::getenv("PA_MERGE_WARPS");
+        const int w = e ? std::atoi(e) : 4;
+        return (w == 2 || w == 4 || w == 8) ? w : 4;
+    }();
+    const int wpr = a.wide ? wide_warps : 1;
+    const int rows_per_block = 8 / wpr;
+    void (*fn)(MergeArgs) = nullptr;
     if (a.D == 128) {
-        if (wide) merge_kernel<128, 8><<<blocks, 256, 0, stream>>>(a);
-        else merge_kernel<128, 1><<<blocks, 256, 0, stream>>>(a);
+        fn = wpr == 1 ? merge_kernel<128, 1> : wpr == 2 ? merge_kernel<128, 2>
+           : wpr == 4 ? merge_kernel<128, 4> : merge_kernel<128, 8>;
     } else if (a.D == 64) {
-        if (wide) merge_kernel<64, 8><<<blocks, 256, 0, stream>>>(a);
-        else merge_kernel<64, 1><<<blocks, 256, 0, stream>>>(a);
+        fn = wpr == 1 ? merge_kernel<64, 1> : wpr == 2 ? merge_kernel<64, 2>
+           : wpr == 4 ? merge_kernel<64, 4> : merge_kernel<64, 8>;
     }
-    else
-        return cudaErrorInvalidValue;
-    return cudaGetLastError();
+    if (!fn) return cudaErrorInvalidValue;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((rows + rows_per_block - 1) / rows_per_block);
+    cfg.blockDim = dim3(256);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, a);
 }
 
 }  // namespace pa

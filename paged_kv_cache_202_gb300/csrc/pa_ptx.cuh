@@ -103,6 +103,21 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// ---------------------------------------------------------------- dependent launch
+
+// Programmatic dependent launch: a kernel launched with programmatic stream
+// serialization may start while the previous kernel of its stream drains;
+// griddep_wait() blocks until that kernel has completed and its memory
+// operations are visible. griddep_launch_dependents() lets the next such
+// kernel start launching early.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- shared loads
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,

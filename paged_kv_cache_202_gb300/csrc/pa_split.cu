@@ -61,8 +61,19 @@ cudaError_t launch_split(const SplitLaunch& L, const CUtensorMap& kmap, const CU
                          const SplitArgs& a, cudaStream_t stream) {
     split::KernelFn fn = split::select(L);
     if (!fn) return cudaErrorInvalidValue;
-    fn<<<L.blocks, L.warps * 32, L.smem, stream>>>(kmap, vmap, a);
-    return cudaGetLastError();
+    // Programmatic dependent launch: the kernel waits for its predecessor at
+    // griddep_wait(), so its launch can overlap the predecessor's drain.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L.blocks);
+    cfg.blockDim = dim3(L.warps * 32);
+    cfg.dynamicSmemBytes = L.smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, fn, kmap, vmap, a);
 }
 
 }  // namespace pa

@@ -515,6 +515,9 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
         prefetch_tensormap(kmap);
         prefetch_tensormap(vmap);
     }
+    // Everything below may read what the previous kernel of the stream wrote.
+    griddep_wait();
+    griddep_launch_dependents();
     const int limit = min(a.max_seq_len, a.max_blocks * BS);
     scan_lengths<BS>(a.seq_lens, a.B, limit, pre, len, a.err);
 
