@@ -5,24 +5,38 @@
 // pos = L_b - n_b + i attends causally to tokens t <= pos read through the
 // block table ("FlashAttention vs PagedAttention", "How prefill and decode
 // change the diagnosis"; exact attention as in "39 · PagedAttention" §1-§2).
-// Here the query side is a real dense contraction: one block takes 128 rows =
-// (128 / g) queries x the g query heads of one kv head, so every K/V chunk is
-// read once for all of them.
+// Here the query side is a real dense contraction: a query tile holds 128
+// rows = (128 / g) queries x the g query heads of one kv head, so every K/V
+// chunk is read once for all of them.
 //
-// Per block: the 128 x 128 query tile is written to shared memory in the
-// 128-byte-swizzled K-major layout; K and V chunks of 64 tokens (whole pages)
-// arrive by tiled bulk tensor copies into a two-stage ring. For each chunk one
-// thread issues S = Q K^T (M=128, N=64, K=128: eight k16 MMAs) into tensor
-// memory; every thread then owns one row: it loads its 64 scores from TMEM,
-// applies the scale (log2 domain), the causal mask by predicate and the online
-// softmax, writes its bf16 probabilities into a swizzled P tile (over the
-// chunk's consumed K stage), rescales its
-// row of the TMEM accumulator when the running max moved, and one thread
-// issues O += P V (M=128, N=128, K=64, V read MN-major). Rows past the last
-// valid token of the final chunk are zeroed in V before the product so that
-// slots beyond the sequence never reach a sum. Every mbarrier wait is bounded;
-// on expiry the block reports PA_DEVERR_TIMEOUT, waits for its copies and
-// MMAs in flight (bounded), frees its tensor memory and returns.
+// One block = two query tiles of the same (sequence, kv head) that share the
+// K/V stream, with specialised warps:
+//   * warp 8 (producer): tiled bulk tensor copies of 64-token K and V chunks
+//     (whole pages, through the block table) into a 3-stage ring;
+//   * warp 9 (MMA): one thread issues S_t = Q_t K^T (M=128, N=64, K=128)
+//     into tensor memory and O_t += P_t V (M=128, N=128, K=64, V read
+//     MN-major straight from the page layout), for both tiles t, and signals
+//     completion through tcgen05.commit on mbarriers. S is double-buffered:
+//     the scores of chunk c+1 are computed as soon as its keys land, while
+//     the softmax still works on chunk c;
+//   * warps 0-3 / 4-7 (softmax, one warpgroup per tile, one thread per row):
+//     load the row's 64 scores from tensor memory, scale (log2 domain), mask
+//     causally by predicate, run the online softmax and write the bf16
+//     probabilities P_t into a 128-byte-swizzled tile; at the end, read the
+//     row of O_t, normalise and store it.
+// While one warpgroup exponentiates, the tensor core works on the other
+// tile, so the two tiles take turns. The running maximum is raised only when
+// a chunk's maximum exceeds it by more than 2^8 (any fixed reference gives
+// the same quotient acc / l; this one keeps every probability below 256):
+// the accumulator rows in tensor memory are then rescaled, otherwise left.
+// V rows past the last token of the final chunk are zeroed before the
+// product so that slots beyond the sequence never reach a sum. Blocks are
+// ordered longest sequence first so that the long ones do not form the tail.
+//
+// Every mbarrier wait is bounded. A role that gives up raises a shared abort
+// flag (and PA_DEVERR_TIMEOUT); the others see it in their own waits. Before
+// the block leaves, the producer waits (bounded) for its copies in flight,
+// the MMA thread for its products, and the block frees its tensor memory.
 #include <cuda_bf16.h>
 
 #include "pa.h"
@@ -33,22 +47,46 @@
 namespace pa {
 namespace {
 
-constexpr int kRows = 128;    // M: query rows per block
-constexpr int kChunk = 64;    // tokens per K/V chunk
-constexpr int kD = 128;       // head dimension
-constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kColS = 0;   // scores: 64 columns
-constexpr uint32_t kColO = 64;  // output accumulator: 128 columns
+constexpr int kRows = 128;      // M: query rows per tile
+constexpr int kChunk = 64;      // tokens per K/V chunk
+constexpr int kD = 128;         // head dimension
+constexpr int kStages = 3;      // K/V ring depth
+constexpr int kSoftmaxThreads = 2 * kRows;
+constexpr int kWarpLoad = kSoftmaxThreads / 32;  // warp 8
+constexpr int kWarpMma = kWarpLoad + 1;          // warp 9
+constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kSortMax = 256;   // sequences ordered by length up to this batch size
+constexpr uint32_t kTmemCols = 512;
+// Tensor-memory columns: S of tile t, buffer j (64 each), then O of tile t (128 each).
+__host__ __device__ constexpr uint32_t col_s(int t, int j) { return 128u * t + 64u * j; }
+__host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
+constexpr float kRescaleLog2 = 8.f;  // raise the reference max only beyond 2^8
 
 // Shared-memory layout (byte offsets from a 1024-aligned base).
-// The probabilities of chunk c (128 rows x 128 B) are written over chunk c's
-// K stage, which is free once S = Q K^T has completed; that keeps a block at
-// ~97 KB so that two blocks share an SM.
-constexpr uint32_t kOffQ = 0;                       // 2 halves x 128 rows x 128 B
-constexpr uint32_t kOffK = 32768;                   // 2 stages x 2 halves x 64 rows x 128 B
-constexpr uint32_t kOffV = kOffK + 2 * 16384;
-constexpr uint32_t kOffBar = kOffV + 2 * 16384;     // 4 mbarriers + TMEM address slot
-constexpr uint32_t kOffTable = kOffBar + 64;        // the sequence's physical block ids
+constexpr uint32_t kTileQ = 32768;                    // 2 halves x 128 rows x 128 B
+constexpr uint32_t kStageKV = 16384;                  // 2 halves x 64 rows x 128 B
+constexpr uint32_t kTileP = 16384;                    // 128 rows x 64 bf16
+constexpr uint32_t kOffQ = 0;
+constexpr uint32_t kOffK = kOffQ + 2 * kTileQ;
+constexpr uint32_t kOffV = kOffK + kStages * kStageKV;
+constexpr uint32_t kOffP = kOffV + kStages * kStageKV;
+constexpr uint32_t kOffBar = kOffP + 2 * kTileP;
+// mbarriers (8 bytes each) and slots, at kOffBar + ...
+constexpr uint32_t kBarKvFull = 0;                    // [kStages]
+constexpr uint32_t kBarKvEmpty = kBarKvFull + 8 * kStages;
+constexpr uint32_t kBarS = kBarKvEmpty + 8 * kStages; // [tile][buffer]
+constexpr uint32_t kBarP = kBarS + 32;                // [tile], 128 arrivals each
+constexpr uint32_t kBarO = kBarP + 16;                // [tile]
+constexpr uint32_t kBarDrain = kBarO + 16;
+constexpr uint32_t kSlotTmem = kBarDrain + 8;
+constexpr uint32_t kSlotAbort = kSlotTmem + 4;
+constexpr uint32_t kSlotSeq = kSlotAbort + 4;
+constexpr uint32_t kOffLens = kOffBar + 256;          // [kSortMax] lengths, for the ordering
+constexpr uint32_t kSmemBytes = 1024 + kOffLens + 4 * kSortMax;
+static_assert(kSlotSeq + 4 <= kOffLens - kOffBar, "barrier area overlaps the length array");
+static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms");
+static_assert(kSmemBytes <= 227 * 1024 && 2 * kSmemBytes > 228 * 1024,
+              "one block per SM: it holds all 512 tensor-memory columns");
 
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kRows, kChunk, false, false);
 constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kRows, kD, false, true);
@@ -60,7 +98,7 @@ struct PrefillArgs {
     const int32_t* seq_lens;
     void* out;                // [T][Hq][D]
     int* err;
-    int B, Hq, Hkv, g, Qb;    // Qb = queries per block = 128 / g
+    int B, Hq, Hkv, g, Qb;    // Qb = queries per tile = 128 / g
     int max_blocks, num_blocks, max_seq_len;
     float scale_log2;
     int out_bf16;
@@ -76,54 +114,102 @@ __device__ __forceinline__ void write_row(const PrefillArgs& a, size_t row, cons
                                           int d0, int nd) {
     if (a.out_bf16) {
         uint16_t* o = static_cast<uint16_t*>(a.out) + row * kD + d0;
-        for (int i = 0; i < nd; i += 2)
-            *reinterpret_cast<uint32_t*>(o + i) = pack_bf16x2(v[i] * inv, v[i + 1] * inv);
+        for (int i = 0; i < nd; i += 8) {
+            uint4 w;
+            w.x = pack_bf16x2(v[i] * inv, v[i + 1] * inv);
+            w.y = pack_bf16x2(v[i + 2] * inv, v[i + 3] * inv);
+            w.z = pack_bf16x2(v[i + 4] * inv, v[i + 5] * inv);
+            w.w = pack_bf16x2(v[i + 6] * inv, v[i + 7] * inv);
+            *reinterpret_cast<uint4*>(o + i) = w;
+        }
     } else {
         float* o = static_cast<float*>(a.out) + row * kD + d0;
-        for (int i = 0; i < nd; ++i) o[i] = v[i] * inv;
+        for (int i = 0; i < nd; i += 4)
+            *reinterpret_cast<float4*>(o + i) =
+                make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
+    }
+}
+
+// Bounded wait that also gives up when another role raised the abort flag.
+__device__ __forceinline__ bool wait_role(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+            *abort_flag = 1;
+            atomicOr(err, kErrTimeout);
+            return false;
+        }
     }
 }
 
 template <int BS>
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                    const PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t raw = smem_addr(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* gbase = smem_raw + (base - raw);
-    int32_t* tbl = reinterpret_cast<int32_t*>(gbase + kOffTable);
-    const uint32_t bar_kv0 = base + kOffBar, bar_s = base + kOffBar + 16, bar_pv = base + kOffBar + 24;
-    const uint32_t tmem_slot = base + kOffBar + 32;
+    const uint32_t bars = base + kOffBar;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(gbase + kOffBar + kSlotAbort);
+    int* seq_slot = reinterpret_cast<int*>(gbase + kOffBar + kSlotSeq);
 
-    const int qb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+    // The sequence of this block: blockIdx.z is its rank by length (longest
+    // first, ties by index) when the batch is small enough to rank here.
+    int b = blockIdx.z;
+    if (a.B <= kSortMax) {
+        int* lens = reinterpret_cast<int*>(gbase + kOffLens);
+        for (int i = tid; i < a.B; i += kThreads) lens[i] = a.seq_lens[i];
+        __syncthreads();
+        for (int i = tid; i < a.B; i += kThreads) {
+            const int li = lens[i];
+            int r = 0;
+            for (int j = 0; j < a.B; ++j) {
+                const int lj = lens[j];
+                r += (lj > li) || (lj == li && j < i);
+            }
+            if (r == static_cast<int>(blockIdx.z)) *seq_slot = i;
+        }
+        __syncthreads();
+        b = *seq_slot;
+    }
+    const int h = blockIdx.y;
     const int qs = a.q_start[b];
     const int n = a.q_start[b + 1] - qs;
     const int L = a.seq_lens[b];
     const int limit = min(a.max_seq_len, a.max_blocks * BS);
-    const int q0 = qb * a.Qb;
     if (n < 1 || L < n || L > limit) {
-        if (qb == 0 && h == 0 && tid == 0) atomicOr(a.err, kErrSeqLen);
+        if (blockIdx.x == 0 && h == 0 && tid == 0) atomicOr(a.err, kErrSeqLen);
         return;  // rows of an invalid sequence are left untouched
     }
+    const int q0 = blockIdx.x * 2 * a.Qb;
     if (q0 >= n) return;
-    const int nq = min(a.Qb, n - q0);
-    const int ntok = L - n + q0 + nq;           // tokens any row of this block may see
+    const int nq0 = min(a.Qb, n - q0);
+    const int nq1 = max(0, min(a.Qb, n - q0 - a.Qb));
+    const bool two = nq1 > 0;
+    const int ntok = L - n + q0 + (two ? a.Qb + nq1 : nq0);  // tokens the last row sees
     const int nc = (ntok + kChunk - 1) / kChunk;
     const int nb = (ntok + BS - 1) / BS;
+    const int32_t* table = a.tables + static_cast<size_t>(b) * a.max_blocks;
 
-    // The table row of this sequence, validated once.
+    // This thread's query row (softmax warps): tile t, row r of the tile.
+    const int t = tid >> 7, row = tid & (kRows - 1);
+    const bool softmax = tid < kSoftmaxThreads;
+    const int qi = row / a.g, qj = row - qi * a.g;
+    const bool row_valid = softmax && qi < (t == 0 ? nq0 : nq1);
+    const size_t out_row = (static_cast<size_t>(qs) + q0 + t * a.Qb + qi) * a.Hq + h * a.g + qj;
+
+    // The table entries this block reads, validated once.
     bool bad = false;
-    for (int i = tid; i < nb; i += blockDim.x) {
-        const int p = a.tables[static_cast<size_t>(b) * a.max_blocks + i];
-        tbl[i] = p;
+    for (int i = tid; i < nb; i += kThreads) {
+        const int p = table[i];
         bad |= p < 0 || p >= a.num_blocks;
     }
-    const int row = tid;                         // this thread's query row
-    const int qi = row / a.g, qj = row - qi * a.g;
-    const bool row_valid = qi < nq;
-    const size_t out_row = (static_cast<size_t>(qs) + q0 + qi) * a.Hq + h * a.g + qj;
     if (__syncthreads_or(bad)) {
         if (tid == 0) atomicOr(a.err, kErrTable);
         if (row_valid) {
@@ -133,202 +219,266 @@ __global__ void __launch_bounds__(128, 2)
         return;
     }
     if (tid == 0) {
-        mbar_init(bar_kv0, 1);
-        mbar_init(bar_kv0 + 8, 1);
-        mbar_init(bar_s, 1);
-        mbar_init(bar_pv, 1);
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(bars + kBarKvFull + 8 * s, 1);
+            mbar_init(bars + kBarKvEmpty + 8 * s, 1);
+        }
+        for (int u = 0; u < 2; ++u) {
+            mbar_init(bars + kBarS + 16 * u, 1);
+            mbar_init(bars + kBarS + 16 * u + 8, 1);
+            mbar_init(bars + kBarP + 8 * u, kRows);
+            mbar_init(bars + kBarO + 8 * u, 1);
+        }
+        mbar_init(bars + kBarDrain, 1);
+        *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 0) {
-        tc::alloc(tmem_slot, kTmemCols);
+    if (warp == kWarpMma) {
+        tc::alloc(bars + kSlotTmem, kTmemCols);
         tc::relinquish();
     }
-    // Query rows -> swizzled K-major tile (two 64-column halves).
-    {
+    // Query rows -> swizzled K-major tiles (two 64-column halves each).
+    if (softmax) {
         const uint16_t* src = a.q + out_row * kD;
+        const uint32_t qt = base + kOffQ + t * kTileQ;
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
             const uint4 w = row_valid ? *reinterpret_cast<const uint4*>(src + c * 8)
                                       : make_uint4(0, 0, 0, 0);
             const int half = c >> 3, cc = c & 7;
-            st_shared_v4(base + kOffQ + half * 16384 + row * 128 + ((cc ^ (row & 7)) << 4), w);
+            st_shared_v4(qt + half * 16384 + row * 128 + ((cc ^ (row & 7)) << 4), w);
         }
     }
     fence_proxy_async_smem();
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + kOffBar + 32);
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    const uint64_t policy = policy_evict_first();
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + kOffBar + kSlotTmem);
 
-    auto issue_kv = [&](int c, int s) {
-        if (tid != 0) return;
-        const int p0 = c * (kChunk / BS);
-        const int np = min(kChunk / BS, nb - p0);
-        const uint32_t bar = bar_kv0 + 8 * s;
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np) * BS * kD * 2 * 2);
-        const uint32_t kst = base + kOffK + s * 16384, vst = base + kOffV + s * 16384;
-        for (int j = 0; j < np; ++j) {
-            const int r = tbl[p0 + j] * a.Hkv + h;
+    if (warp == kWarpLoad) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            const uint64_t policy = policy_evict_first();
+            int issued = 0;
+            for (int c = 0; c < nc; ++c) {
+                const int s = c % kStages;
+                if (c >= kStages &&
+                    !wait_role(bars + kBarKvEmpty + 8 * s, ((c / kStages) - 1) & 1, abort_flag, a.err))
+                    break;
+                const int p0 = c * (kChunk / BS);
+                const int np = min(kChunk / BS, nb - p0);
+                const uint32_t bar = bars + kBarKvFull + 8 * s;
+                mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np) * BS * kD * 2 * 2);
+                const uint32_t kst = base + kOffK + s * kStageKV, vst = base + kOffV + s * kStageKV;
+                for (int j = 0; j < np; ++j) {
+                    const int r = table[p0 + j] * a.Hkv + h;
 #pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                const uint32_t off = half * 8192 + j * BS * 128;
-                tma_load_3d(kst + off, &kmap, half * 64, 0, r, bar, policy);
-                tma_load_3d(vst + off, &vmap, half * 64, 0, r, bar, policy);
+                    for (int half = 0; half < 2; ++half) {
+                        const uint32_t off = half * 8192 + j * BS * 128;
+                        tma_load_3d(kst + off, &kmap, half * 64, 0, r, bar, policy);
+                        tma_load_3d(vst + off, &vmap, half * 64, 0, r, bar, policy);
+                    }
+                }
+                issued = c + 1;
+            }
+            if (*abort_flag) {
+                // Copies still in flight land before the block leaves: the
+                // last chunk issued on each stage (its phase is then final).
+                for (int c = max(0, issued - kStages); c < issued; ++c)
+                    mbar_wait_bounded(bars + kBarKvFull + 8 * (c % kStages), (c / kStages) & 1,
+                                      kWaitLimitNs);
             }
         }
-    };
-    // Bounded wait by every thread; false if any thread gave up.
-    auto wait_all = [&](uint32_t bar, uint32_t parity) {
-        const bool ok = mbar_wait_bounded(bar, parity, kWaitLimitNs);
-        return !__syncthreads_or(!ok);
-    };
-    uint32_t ph_kv = 0, ph_s = 0, ph_pv = 0;
-    int kv_issued = 0, kv_done = 0, s_issued = 0, s_done = 0, pv_issued = 0, pv_done = 0;
-    auto bail = [&]() {
-        if (tid == 0) {
-            atomicOr(a.err, kErrTimeout);
-            // Bounded waits for this block's copies and MMAs still in flight.
-            for (int k = kv_done; k < kv_issued; ++k)
-                mbar_wait_bounded(bar_kv0 + 8 * (k & 1), (ph_kv >> (k & 1)) & 1u, kWaitLimitNs);
-            if (s_issued > s_done) mbar_wait_bounded(bar_s, ph_s, kWaitLimitNs);
-            if (pv_issued > pv_done) mbar_wait_bounded(bar_pv, ph_pv, kWaitLimitNs);
+        __syncwarp();
+    } else if (warp == kWarpMma) {
+        // ------------------------------------------------------------ MMA issue
+        if (lane == 0) {
+            // Descriptor low words of every operand, built once; all share the
+            // high word (SBO = 1024, 128-byte swizzle).
+            const uint32_t hi = static_cast<uint32_t>(tc::smem_desc(base, 16, 1024) >> 32);
+            const uint32_t lo_q = tc::desc_lo(base + kOffQ, 16);
+            const uint32_t lo_k = tc::desc_lo(base + kOffK, 16);
+            const uint32_t lo_v = tc::desc_lo(base + kOffV, 8192);
+            const uint32_t lo_p = tc::desc_lo(base + kOffP, 16);
+            auto issue_s = [&](int u, int c) {
+                const int s = c % kStages;
+                const uint32_t a0 = lo_q + u * (kTileQ >> 4);
+                const uint32_t b0 = lo_k + s * (kStageKV >> 4);
+                const uint32_t d = tmem + col_s(u, c & 1);
+#pragma unroll
+                for (int kk = 0; kk < kD / 16; ++kk) {
+                    const uint32_t da = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
+                    const uint32_t db = (kk >> 2) * (8192 >> 4) + (kk & 3) * 2;
+                    tc::mma_bf16_lo(d, a0 + da, b0 + db, hi, kIdescS, kk > 0);
+                }
+                tc::commit(bars + kBarS + 16 * u + 8 * (c & 1));
+            };
+            auto issue_pv = [&](int u, int c) {
+                const int s = c % kStages;
+                const uint32_t a0 = lo_p + u * (kTileP >> 4);
+                const uint32_t b0 = lo_v + s * (kStageKV >> 4);
+                const uint32_t d = tmem + col_o(u);
+#pragma unroll
+                for (int kk = 0; kk < kChunk / 16; ++kk)
+                    tc::mma_bf16_lo(d, a0 + kk * 2, b0 + kk * (2048 >> 4), hi, kIdescO, c > 0 || kk > 0);
+                tc::commit(bars + kBarO + 8 * u);
+            };
+            // S of chunk c+1 (both tiles) goes in as soon as its keys land: its
+            // buffer was last read for chunk c-1, whose P has been published.
+            bool ok = wait_role(bars + kBarKvFull, 0, abort_flag, a.err);
+            if (ok) {
+                tc::fence_after_sync();
+                issue_s(0, 0);
+                if (two) issue_s(1, 0);
+            }
+            for (int c = 0; c < nc && ok; ++c) {
+                if (c + 1 < nc) {
+                    const int c1 = c + 1;
+                    ok = wait_role(bars + kBarKvFull + 8 * (c1 % kStages), (c1 / kStages) & 1,
+                                   abort_flag, a.err);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    issue_s(0, c1);
+                    if (two) issue_s(1, c1);
+                }
+                ok = wait_role(bars + kBarP, c & 1, abort_flag, a.err);
+                if (!ok) break;
+                tc::fence_after_sync();
+                issue_pv(0, c);
+                if (two) {
+                    ok = wait_role(bars + kBarP + 8, c & 1, abort_flag, a.err);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    issue_pv(1, c);
+                }
+                // The stage of chunk c is free once these products are done.
+                tc::commit(bars + kBarKvEmpty + 8 * (c % kStages));
+            }
+            if (*abort_flag) {
+                tc::commit(bars + kBarDrain);
+                mbar_wait_bounded(bars + kBarDrain, 0, kWaitLimitNs);
+            }
         }
-        tc::fence_before_sync();
-        __syncthreads();
-        if (warp == 0) tc::dealloc(tmem, kTmemCols);
-    };
-
-    issue_kv(0, 0);
-    kv_issued = 1;
-    const int pos_r = L - n + q0 + qi;
-    float m = -INFINITY, l = 0.f;
-    for (int c = 0; c < nc; ++c) {
-        const int s = c & 1;
-        if (!wait_all(bar_kv0 + 8 * s, (ph_kv >> s) & 1u)) { bail(); return; }
-        ph_kv ^= 1u << s;
-        ++kv_done;
-        // S = Q K^T into TMEM columns [0, 64).
-        if (tid == 0) {
+        __syncwarp();
+    } else if (t == 0 || two) {
+        // ------------------------------------------------------------ softmax (tile t)
+        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        const uint32_t s_addr = tmem + lane_base + col_s(t, 0);
+        const uint32_t o_addr = tmem + lane_base + col_o(t);
+        const uint32_t pt = base + kOffP + t * kTileP;
+        const int pos_r = L - n + q0 + t * a.Qb + qi;  // last token this row sees
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int c = 0; c < nc; ++c) {
+            ok = __all_sync(0xffffffffu, wait_role(bars + kBarS + 16 * t + 8 * (c & 1), (c >> 1) & 1,
+                                                   abort_flag, a.err));
+            if (!ok) break;
             tc::fence_after_sync();
-            const uint32_t kst = base + kOffK + s * 16384;
-#pragma unroll
-            for (int kk = 0; kk < kD / 16; ++kk) {
-                const uint32_t half = kk >> 2, off = (kk & 3) * 32;
-                const uint64_t ad = tc::smem_desc(base + kOffQ + half * 16384 + off, 16, 1024);
-                const uint64_t bd = tc::smem_desc(kst + half * 8192 + off, 16, 1024);
-                tc::mma_bf16(tmem + kColS, ad, bd, kIdescS, kk > 0);
-            }
-            tc::commit(bar_s);
-        }
-        ++s_issued;
-        if (!wait_all(bar_s, ph_s)) { bail(); return; }
-        ph_s ^= 1u;
-        ++s_done;
-        tc::fence_after_sync();
-        float sv[64];
-        {
-            float t0[32], t1[32];
-            tc::ld32(tmem + lane_base + kColS, t0);
-            tc::ld32(tmem + lane_base + kColS + 32, t1);
-            tc::wait_ld();
-#pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                sv[i] = t0[i];
-                sv[32 + i] = t1[i];
-            }
-        }
-        // Scale, causal mask by predicate, online softmax (this thread's row).
-        const int t0 = c * kChunk;
-        float mx = -INFINITY;
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-            const float v = (row_valid && t0 + i <= pos_r) ? sv[i] * a.scale_log2 : -INFINITY;
-            sv[i] = v;
-            mx = fmaxf(mx, v);
-        }
-        const float m_new = fmaxf(m, mx);
-        const float m_use = m_new == -INFINITY ? 0.f : m_new;
-        const float alpha = fast_exp2(m - m_use);
-        uint32_t pw[32];
-        float psum = 0.f;
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            pw[i] = pack_bf16x2(fast_exp2(sv[2 * i] - m_use), fast_exp2(sv[2 * i + 1] - m_use));
-            psum += bf16_lo(pw[i]) + bf16_hi(pw[i]);
-        }
-        l = l * alpha + psum;
-        m = m_new;
-        // The previous P V must be done before P and O are touched again.
-        if (c > 0) {
-            if (!wait_all(bar_pv, ph_pv)) { bail(); return; }
-            ph_pv ^= 1u;
-            ++pv_done;
-            tc::fence_after_sync();
-        }
-        if (c + 1 < nc) {
-            issue_kv(c + 1, s ^ 1);
-            ++kv_issued;
-        }
-        // P row -> swizzled K-major tile in this chunk's (consumed) K stage.
-        const uint32_t pst = base + kOffK + s * 16384;
-#pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-            st_shared_v4(pst + row * 128 + ((ch ^ (row & 7)) << 4),
-                         make_uint4(pw[4 * ch], pw[4 * ch + 1], pw[4 * ch + 2], pw[4 * ch + 3]));
-        // Rescale this row of the TMEM accumulator if its max moved.
-        if (c > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-#pragma unroll
-            for (int piece = 0; piece < kD / 32; ++piece) {
-                float o[32];
-                tc::ld32(tmem + lane_base + kColO + piece * 32, o);
+            float sv[64];
+            {
+                float t0[32], t1[32];
+                const uint32_t sa = s_addr + 64u * (c & 1);
+                tc::ld32(sa, t0);
+                tc::ld32(sa + 32, t1);
                 tc::wait_ld();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                tc::st32(tmem + lane_base + kColO + piece * 32, o);
+                for (int i = 0; i < 32; ++i) {
+                    sv[i] = t0[i];
+                    sv[32 + i] = t1[i];
+                }
             }
-            tc::wait_st();
-        }
-        // Final chunk: zero the V rows past the last token any row may see.
-        const int valid = min(kChunk, ntok - t0);
-        if (valid < kChunk) {
-            const uint32_t vst = base + kOffV + s * 16384;
-            for (int idx = tid; idx < (kChunk - valid) * 16; idx += blockDim.x) {
-                const int r = valid + (idx >> 4), half = (idx >> 3) & 1, ch = idx & 7;
-                st_shared_v4(vst + half * 8192 + r * 128 + ch * 16, make_uint4(0, 0, 0, 0));
-            }
-        }
-        fence_proxy_async_smem();
-        tc::fence_before_sync();
-        __syncthreads();
-        // O += P V into TMEM columns [64, 192).
-        if (tid == 0) {
-            tc::fence_after_sync();
-            const uint32_t vst = base + kOffV + s * 16384;
+            // Causal mask by predicate; the warp skips it when no row needs it.
+            const int tok0 = c * kChunk;
+            if (!__all_sync(0xffffffffu, row_valid && tok0 + kChunk - 1 <= pos_r)) {
 #pragma unroll
-            for (int kk = 0; kk < kChunk / 16; ++kk) {
-                const uint64_t ad = tc::smem_desc(pst + kk * 32, 16, 1024);
-                const uint64_t bd = tc::smem_desc(vst + kk * 2048, 8192, 1024);
-                tc::mma_bf16(tmem + kColO, ad, bd, kIdescO, c > 0 || kk > 0);
+                for (int i = 0; i < 64; ++i)
+                    sv[i] = (row_valid && tok0 + i <= pos_r) ? sv[i] : -INFINITY;
             }
-            tc::commit(bar_pv);
-        }
-        ++pv_issued;
-    }
-    if (!wait_all(bar_pv, ph_pv)) { bail(); return; }
-    tc::fence_after_sync();
-    const float inv = (row_valid && l > 0.f) ? 1.f / l : 0.f;
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four short chains
 #pragma unroll
-    for (int piece = 0; piece < kD / 32; ++piece) {
-        float o[32];
-        tc::ld32(tmem + lane_base + kColO + piece * 32, o);
-        tc::wait_ld();
-        if (row_valid) write_row(a, out_row, o, inv, piece * 32, 32);
+            for (int i = 0; i < 64; ++i) mq[i & 3] = fmaxf(mq[i & 3], sv[i]);
+            // scale > 0, so this is the max of the scaled scores
+            const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;
+            // Raise the reference max only when the chunk exceeds it by > 2^8.
+            float alpha = 1.f;
+            if (mx > m + kRescaleLog2) {
+                alpha = fast_exp2(m - mx);  // 0 while m is still -inf
+                m = mx;
+                l *= alpha;
+            }
+            const float m_use = m == -INFINITY ? 0.f : m;
+            uint32_t pw[32];
+            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const float p0 = fast_exp2(fmaf(sv[2 * i], a.scale_log2, -m_use));
+                const float p1 = fast_exp2(fmaf(sv[2 * i + 1], a.scale_log2, -m_use));
+                ps[i & 3] += p0 + p1;
+                pw[i] = pack_bf16x2(p0, p1);
+            }
+            l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+            // O_t += P_t V of chunk c-1 must be done before P_t and O_t change.
+            if (c > 0) {
+                ok = __all_sync(0xffffffffu,
+                                wait_role(bars + kBarO + 8 * t, (c - 1) & 1, abort_flag, a.err));
+                if (!ok) break;
+                tc::fence_after_sync();
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+                    for (int piece = 0; piece < kD / 32; ++piece) {
+                        float o[32];
+                        tc::ld32(o_addr + piece * 32, o);
+                        tc::wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                        tc::st32(o_addr + piece * 32, o);
+                    }
+                    tc::wait_st();
+                }
+            }
+            // Final chunk: tile 0 zeroes the V rows past the last token (both
+            // tiles' products run after tile 0 has published its P).
+            if (t == 0 && c == nc - 1) {
+                const int valid = ntok - tok0;
+                if (valid < kChunk) {
+                    const uint32_t vst = base + kOffV + (c % kStages) * kStageKV;
+                    for (int idx = tid; idx < (kChunk - valid) * 16; idx += kRows) {
+                        const int r = valid + (idx >> 4), half = (idx >> 3) & 1, ch = idx & 7;
+                        st_shared_v4(vst + half * 8192 + r * 128 + ch * 16, make_uint4(0, 0, 0, 0));
+                    }
+                }
+            }
+            // P row -> swizzled K-major tile.
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                st_shared_v4(pt + row * 128 + ((ch ^ (row & 7)) << 4),
+                             make_uint4(pw[4 * ch], pw[4 * ch + 1], pw[4 * ch + 2], pw[4 * ch + 3]));
+            fence_proxy_async_smem();
+            tc::fence_before_sync();
+            mbar_arrive(bars + kBarP + 8 * t);
+        }
+        if (ok) {
+            ok = __all_sync(0xffffffffu,
+                            wait_role(bars + kBarO + 8 * t, (nc - 1) & 1, abort_flag, a.err));
+            if (ok) {
+                tc::fence_after_sync();
+                const float inv = (row_valid && l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll
+                for (int piece = 0; piece < kD / 32; ++piece) {
+                    float o[32];
+                    tc::ld32(o_addr + piece * 32, o);
+                    tc::wait_ld();
+                    if (row_valid) write_row(a, out_row, o, inv, piece * 32, 32);
+                }
+            }
+        }
     }
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) tc::dealloc(tmem, kTmemCols);
+    if (warp == kWarpMma) {
+        tc::fence_after_sync();
+        tc::dealloc(tmem, kTmemCols);
+    }
 }
 
 }  // namespace
@@ -355,14 +505,14 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
     a.max_seq_len = max_seq_len;
     a.scale_log2 = scale_log2;
     a.out_bf16 = out_bf16;
-    const size_t smem = 1024 + kOffTable + static_cast<size_t>(max_blocks) * 4;
-    dim3 grid((max_q + a.Qb - 1) / a.Qb, Hkv, B);
+    if (B > 65535 || Hkv > 65535) return cudaErrorInvalidValue;
+    dim3 grid((max_q + 2 * a.Qb - 1) / (2 * a.Qb), Hkv, B);
     auto kern = block_size == 16 ? prefill_kernel<16> : prefill_kernel<32>;
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+                                         static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    kern<<<grid, 128, smem, stream>>>(kmap, vmap, a);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(kmap, vmap, a);
     return cudaGetLastError();
 }
 

@@ -1,7 +1,8 @@
 """GPU: causal paged multi-query attention (tcgen05 tensor cores) against the
 fp64 oracle, within the bf16 tolerance. Query counts that do not fill a block,
 partial final chunks, NaN-poisoned slots past each sequence, GQA group sizes
-1..16 and both block sizes are covered."""
+1..16, both block sizes, ties in the longest-first block order and batches
+past the size it is applied to are covered."""
 
 import numpy as np
 import pytest
@@ -20,6 +21,11 @@ pytestmark = pytest.mark.gpu
 def _built():
     import __graft_entry__
     __graft_entry__.build()
+
+
+_rng = np.random.default_rng(5)
+_MANY_LENS = [int(x) for x in _rng.integers(1, 80, size=300)]
+_MANY_NS = [int(min(x, y)) for x, y in zip(_MANY_LENS, _rng.integers(1, 20, size=300))]
 
 
 def _case(lens, ns, Hq=32, Hkv=8, bs=16, seed=0):
@@ -50,6 +56,8 @@ def _run(wl, q, qs, ns):
     (8, 8, 16, [300, 1], [150, 1]),                     # g = 1: 128 queries per block
     (16, 1, 16, [90, 640], [8, 40]),                    # g = 16 (MQA-like)
     (4, 2, 32, [64, 65, 66], [64, 65, 2]),              # g = 2, ragged edges
+    (32, 8, 16, [50] * 20 + [120] * 20, [10] * 40),     # equal lengths: the longest-first order breaks ties
+    (32, 8, 16, _MANY_LENS, _MANY_NS),                  # more sequences than are ordered by length
 ])
 def test_prefill_matches_oracle(Hq, Hkv, bs, lens, ns):
     wl, q, qs = _case(lens, ns, Hq=Hq, Hkv=Hkv, bs=bs)
