@@ -11,21 +11,28 @@
 //
 // One block = two query tiles of the same (sequence, kv head) that share the
 // K/V stream, with specialised warps:
-//   * warp 8 (producer): tiled bulk tensor copies of 64-token K and V chunks
-//     (whole pages, through the block table) into a 3-stage ring;
-//   * warp 9 (MMA): one thread issues S_t = Q_t K^T (M=128, N=64, K=128)
-//     into tensor memory and O_t += P_t V (M=128, N=128, K=64, V read
-//     MN-major straight from the page layout), for both tiles t, and signals
-//     completion through tcgen05.commit on mbarriers. S is double-buffered:
-//     the scores of chunk c+1 are computed as soon as its keys land, while
-//     the softmax still works on chunk c;
+//   * warp 8 (producer): tiled bulk tensor copies of 128-token K and V chunks
+//     (whole pages, through the block table) into a 3-stage K ring and a
+//     2-stage V ring (V one chunk behind K: it is needed one step later;
+//     V goes first at each step);
+//   * warp 9 (MMA): one thread issues S_t = Q_t K^T (M=128, N=128, K=128,
+//     both operands in shared memory) into tensor memory and
+//     O_t += P_t V (M=128, N=128, K=128) with P_t read from tensor memory and
+//     V read MN-major straight from the page layout, for both tiles t, and
+//     signals completion through tcgen05.commit on mbarriers;
 //   * warps 0-3 / 4-7 (softmax, one warpgroup per tile, one thread per row):
-//     load the row's 64 scores from tensor memory, scale (log2 domain), mask
-//     causally by predicate, run the online softmax and write the bf16
-//     probabilities P_t into a 128-byte-swizzled tile; at the end, read the
-//     row of O_t, normalise and store it.
-// While one warpgroup exponentiates, the tensor core works on the other
-// tile, so the two tiles take turns. The running maximum is raised only when
+//     load the row's 128 scores from tensor memory, scale (log2 domain), mask
+//     causally by predicate, run the online softmax and store the bf16
+//     probabilities P_t over the first 64 columns of the same scores (the
+//     A operand of the PV product); at the end, read the row of O_t,
+//     normalise and store it.
+// The MMA thread issues PV_0(c), S_0(c+1), PV_1(c), S_1(c+1), ...: one
+// thread's products run in issue order, so S_t(c+1) overwrites P_t(c) only
+// after PV_t(c) has read it, and its completion (one commit covers every
+// earlier product) also tells the softmax that PV_t(c) is done. While one
+// warpgroup exponentiates, the tensor core works on the other tile, so the
+// two tiles take turns. Keeping P out of shared memory leaves the shared
+// memory bandwidth to the S operands, V and the incoming copies. The running maximum is raised only when
 // a chunk's maximum exceeds it by more than 2^8 (any fixed reference gives
 // the same quotient acc / l; this one keeps every probability below 256):
 // the accumulator rows in tensor memory are then rescaled, otherwise left.
@@ -48,34 +55,36 @@ namespace pa {
 namespace {
 
 constexpr int kRows = 128;      // M: query rows per tile
-constexpr int kChunk = 64;      // tokens per K/V chunk
+constexpr int kChunk = 128;     // tokens per K/V chunk
 constexpr int kD = 128;         // head dimension
-constexpr int kStages = 3;      // K/V ring depth
+constexpr int kStagesK = 3;     // K ring depth
+constexpr int kStagesV = 2;     // V ring depth
 constexpr int kSoftmaxThreads = 2 * kRows;
 constexpr int kWarpLoad = kSoftmaxThreads / 32;  // warp 8
 constexpr int kWarpMma = kWarpLoad + 1;          // warp 9
 constexpr int kThreads = kSoftmaxThreads + 64;
 constexpr int kSortMax = 256;   // sequences ordered by length up to this batch size
 constexpr uint32_t kTmemCols = 512;
-// Tensor-memory columns: S of tile t, buffer j (64 each), then O of tile t (128 each).
-__host__ __device__ constexpr uint32_t col_s(int t, int j) { return 128u * t + 64u * j; }
+// Tensor-memory columns: S of tile t (128; P_t over its first 64), then O of tile t (128).
+__host__ __device__ constexpr uint32_t col_s(int t) { return 128u * t; }
 __host__ __device__ constexpr uint32_t col_o(int t) { return 256u + 128u * t; }
 constexpr float kRescaleLog2 = 8.f;  // raise the reference max only beyond 2^8
 
 // Shared-memory layout (byte offsets from a 1024-aligned base).
 constexpr uint32_t kTileQ = 32768;                    // 2 halves x 128 rows x 128 B
-constexpr uint32_t kStageKV = 16384;                  // 2 halves x 64 rows x 128 B
-constexpr uint32_t kTileP = 16384;                    // 128 rows x 64 bf16
+constexpr uint32_t kHalfKV = kChunk * 128;            // one 64-column half of a chunk
+constexpr uint32_t kStageKV = 2 * kHalfKV;            // 2 halves x 128 rows x 128 B
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + 2 * kTileQ;
-constexpr uint32_t kOffV = kOffK + kStages * kStageKV;
-constexpr uint32_t kOffP = kOffV + kStages * kStageKV;
-constexpr uint32_t kOffBar = kOffP + 2 * kTileP;
+constexpr uint32_t kOffV = kOffK + kStagesK * kStageKV;
+constexpr uint32_t kOffBar = kOffV + kStagesV * kStageKV;
 // mbarriers (8 bytes each) and slots, at kOffBar + ...
-constexpr uint32_t kBarKvFull = 0;                    // [kStages]
-constexpr uint32_t kBarKvEmpty = kBarKvFull + 8 * kStages;
-constexpr uint32_t kBarS = kBarKvEmpty + 8 * kStages; // [tile][buffer]
-constexpr uint32_t kBarP = kBarS + 32;                // [tile], 128 arrivals each
+constexpr uint32_t kBarKFull = 0;                     // [kStagesK]
+constexpr uint32_t kBarKEmpty = kBarKFull + 8 * kStagesK;
+constexpr uint32_t kBarVFull = kBarKEmpty + 8 * kStagesK;  // [kStagesV]
+constexpr uint32_t kBarVEmpty = kBarVFull + 8 * kStagesV;
+constexpr uint32_t kBarS = kBarVEmpty + 8 * kStagesV; // [tile]
+constexpr uint32_t kBarP = kBarS + 16;                // [tile], 128 arrivals each
 constexpr uint32_t kBarO = kBarP + 16;                // [tile]
 constexpr uint32_t kBarDrain = kBarO + 16;
 constexpr uint32_t kSlotTmem = kBarDrain + 8;
@@ -84,12 +93,12 @@ constexpr uint32_t kSlotSeq = kSlotAbort + 4;
 constexpr uint32_t kOffLens = kOffBar + 256;          // [kSortMax] lengths, for the ordering
 constexpr uint32_t kSmemBytes = 1024 + kOffLens + 4 * kSortMax;
 static_assert(kSlotSeq + 4 <= kOffLens - kOffBar, "barrier area overlaps the length array");
-static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0, "swizzle atoms");
+static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzle atoms");
 static_assert(kSmemBytes <= 227 * 1024 && 2 * kSmemBytes > 228 * 1024,
               "one block per SM: it holds all 512 tensor-memory columns");
 
 constexpr uint32_t kIdescS = tc::idesc_bf16_f32(kRows, kChunk, false, false);
-constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kRows, kD, false, true);
+constexpr uint32_t kIdescO = tc::idesc_bf16_f32(kRows, kD, false, true);  // A from tensor memory
 
 struct PrefillArgs {
     const uint16_t* q;        // [T][Hq][D] bf16
@@ -219,13 +228,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         return;
     }
     if (tid == 0) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(bars + kBarKvFull + 8 * s, 1);
-            mbar_init(bars + kBarKvEmpty + 8 * s, 1);
+        for (int s = 0; s < kStagesK; ++s) {
+            mbar_init(bars + kBarKFull + 8 * s, 1);
+            mbar_init(bars + kBarKEmpty + 8 * s, 1);
+        }
+        for (int s = 0; s < kStagesV; ++s) {
+            mbar_init(bars + kBarVFull + 8 * s, 1);
+            mbar_init(bars + kBarVEmpty + 8 * s, 1);
         }
         for (int u = 0; u < 2; ++u) {
-            mbar_init(bars + kBarS + 16 * u, 1);
-            mbar_init(bars + kBarS + 16 * u + 8, 1);
+            mbar_init(bars + kBarS + 8 * u, 1);
             mbar_init(bars + kBarP + 8 * u, kRows);
             mbar_init(bars + kBarO + 8 * u, 1);
         }
@@ -259,33 +271,45 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ producer
         if (lane == 0) {
             const uint64_t policy = policy_evict_first();
-            int issued = 0;
-            for (int c = 0; c < nc; ++c) {
-                const int s = c % kStages;
-                if (c >= kStages &&
-                    !wait_role(bars + kBarKvEmpty + 8 * s, ((c / kStages) - 1) & 1, abort_flag, a.err))
-                    break;
+            // One chunk of K or V (its pages, both 64-column halves) into a stage.
+            auto load = [&](const CUtensorMap* map, uint32_t stage, uint32_t bar, int c) {
                 const int p0 = c * (kChunk / BS);
                 const int np = min(kChunk / BS, nb - p0);
-                const uint32_t bar = bars + kBarKvFull + 8 * s;
-                mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np) * BS * kD * 2 * 2);
-                const uint32_t kst = base + kOffK + s * kStageKV, vst = base + kOffV + s * kStageKV;
+                mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np) * BS * kD * 2);
                 for (int j = 0; j < np; ++j) {
                     const int r = table[p0 + j] * a.Hkv + h;
 #pragma unroll
-                    for (int half = 0; half < 2; ++half) {
-                        const uint32_t off = half * 8192 + j * BS * 128;
-                        tma_load_3d(kst + off, &kmap, half * 64, 0, r, bar, policy);
-                        tma_load_3d(vst + off, &vmap, half * 64, 0, r, bar, policy);
-                    }
+                    for (int half = 0; half < 2; ++half)
+                        tma_load_3d(stage + half * kHalfKV + j * BS * 128, map, half * 64, 0, r, bar, policy);
                 }
-                issued = c + 1;
+            };
+            int issued_k = 0, issued_v = 0;
+            for (int c = 0; c <= nc; ++c) {
+                if (c >= 1) {  // V of chunk c - 1 (the MMA thread waits on it first)
+                    const int cv = c - 1, s = cv % kStagesV;
+                    if (cv >= kStagesV &&
+                        !wait_role(bars + kBarVEmpty + 8 * s, ((cv / kStagesV) - 1) & 1, abort_flag, a.err))
+                        break;
+                    load(&vmap, base + kOffV + s * kStageKV, bars + kBarVFull + 8 * s, cv);
+                    issued_v = cv + 1;
+                }
+                if (c < nc) {  // K of chunk c
+                    const int s = c % kStagesK;
+                    if (c >= kStagesK &&
+                        !wait_role(bars + kBarKEmpty + 8 * s, ((c / kStagesK) - 1) & 1, abort_flag, a.err))
+                        break;
+                    load(&kmap, base + kOffK + s * kStageKV, bars + kBarKFull + 8 * s, c);
+                    issued_k = c + 1;
+                }
             }
             if (*abort_flag) {
                 // Copies still in flight land before the block leaves: the
                 // last chunk issued on each stage (its phase is then final).
-                for (int c = max(0, issued - kStages); c < issued; ++c)
-                    mbar_wait_bounded(bars + kBarKvFull + 8 * (c % kStages), (c / kStages) & 1,
+                for (int c = max(0, issued_k - kStagesK); c < issued_k; ++c)
+                    mbar_wait_bounded(bars + kBarKFull + 8 * (c % kStagesK), (c / kStagesK) & 1,
+                                      kWaitLimitNs);
+                for (int c = max(0, issued_v - kStagesV); c < issued_v; ++c)
+                    mbar_wait_bounded(bars + kBarVFull + 8 * (c % kStagesV), (c / kStagesV) & 1,
                                       kWaitLimitNs);
             }
         }
@@ -293,66 +317,68 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kWarpMma) {
         // ------------------------------------------------------------ MMA issue
         if (lane == 0) {
-            // Descriptor low words of every operand, built once; all share the
-            // high word (SBO = 1024, 128-byte swizzle).
+            // Descriptor low words of every shared-memory operand, built once;
+            // all share the high word (SBO = 1024, 128-byte swizzle).
             const uint32_t hi = static_cast<uint32_t>(tc::smem_desc(base, 16, 1024) >> 32);
             const uint32_t lo_q = tc::desc_lo(base + kOffQ, 16);
             const uint32_t lo_k = tc::desc_lo(base + kOffK, 16);
-            const uint32_t lo_v = tc::desc_lo(base + kOffV, 8192);
-            const uint32_t lo_p = tc::desc_lo(base + kOffP, 16);
+            const uint32_t lo_v = tc::desc_lo(base + kOffV, kHalfKV);
             auto issue_s = [&](int u, int c) {
-                const int s = c % kStages;
                 const uint32_t a0 = lo_q + u * (kTileQ >> 4);
-                const uint32_t b0 = lo_k + s * (kStageKV >> 4);
-                const uint32_t d = tmem + col_s(u, c & 1);
+                const uint32_t b0 = lo_k + (c % kStagesK) * (kStageKV >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kD / 16; ++kk) {
                     const uint32_t da = (kk >> 2) * (16384 >> 4) + (kk & 3) * 2;
-                    const uint32_t db = (kk >> 2) * (8192 >> 4) + (kk & 3) * 2;
-                    tc::mma_bf16_lo(d, a0 + da, b0 + db, hi, kIdescS, kk > 0);
+                    const uint32_t db = (kk >> 2) * (kHalfKV >> 4) + (kk & 3) * 2;
+                    tc::mma_bf16_lo(tmem + col_s(u), a0 + da, b0 + db, hi, kIdescS, kk > 0);
                 }
-                tc::commit(bars + kBarS + 16 * u + 8 * (c & 1));
+                tc::commit(bars + kBarS + 8 * u);
             };
             auto issue_pv = [&](int u, int c) {
-                const int s = c % kStages;
-                const uint32_t a0 = lo_p + u * (kTileP >> 4);
-                const uint32_t b0 = lo_v + s * (kStageKV >> 4);
-                const uint32_t d = tmem + col_o(u);
+                const uint32_t b0 = lo_v + (c % kStagesV) * (kStageKV >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kChunk / 16; ++kk)
-                    tc::mma_bf16_lo(d, a0 + kk * 2, b0 + kk * (2048 >> 4), hi, kIdescO, c > 0 || kk > 0);
-                tc::commit(bars + kBarO + 8 * u);
+                for (int kk = 0; kk < kChunk / 16; ++kk)   // 16 tokens = 8 columns of P
+                    tc::mma_bf16_ts(tmem + col_o(u), tmem + col_s(u) + kk * 8, b0 + kk * (2048 >> 4), hi,
+                                    kIdescO, c > 0 || kk > 0);
             };
-            // S of chunk c+1 (both tiles) goes in as soon as its keys land: its
-            // buffer was last read for chunk c-1, whose P has been published.
-            bool ok = wait_role(bars + kBarKvFull, 0, abort_flag, a.err);
+            bool ok = wait_role(bars + kBarKFull, 0, abort_flag, a.err);
             if (ok) {
                 tc::fence_after_sync();
                 issue_s(0, 0);
                 if (two) issue_s(1, 0);
+                tc::commit(bars + kBarKEmpty);  // K stage of chunk 0 free once both S are done
             }
             for (int c = 0; c < nc && ok; ++c) {
-                if (c + 1 < nc) {
-                    const int c1 = c + 1;
-                    ok = wait_role(bars + kBarKvFull + 8 * (c1 % kStages), (c1 / kStages) & 1,
-                                   abort_flag, a.err);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    issue_s(0, c1);
-                    if (two) issue_s(1, c1);
-                }
-                ok = wait_role(bars + kBarP, c & 1, abort_flag, a.err);
+                const int c1 = c + 1;
+                ok = wait_role(bars + kBarP, c & 1, abort_flag, a.err) &&
+                     wait_role(bars + kBarVFull + 8 * (c % kStagesV), (c / kStagesV) & 1, abort_flag, a.err);
                 if (!ok) break;
                 tc::fence_after_sync();
                 issue_pv(0, c);
+                if (c1 < nc) {
+                    ok = wait_role(bars + kBarKFull + 8 * (c1 % kStagesK), (c1 / kStagesK) & 1,
+                                   abort_flag, a.err);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    issue_s(0, c1);  // after PV_0(c) in issue order: P_0(c) is read first
+                    if (!two) tc::commit(bars + kBarKEmpty + 8 * (c1 % kStagesK));
+                }
                 if (two) {
                     ok = wait_role(bars + kBarP + 8, c & 1, abort_flag, a.err);
                     if (!ok) break;
                     tc::fence_after_sync();
                     issue_pv(1, c);
                 }
-                // The stage of chunk c is free once these products are done.
-                tc::commit(bars + kBarKvEmpty + 8 * (c % kStages));
+                // The V stage of chunk c is free once these products are done.
+                tc::commit(bars + kBarVEmpty + 8 * (c % kStagesV));
+                if (two && c1 < nc) {
+                    issue_s(1, c1);
+                    tc::commit(bars + kBarKEmpty + 8 * (c1 % kStagesK));
+                }
+            }
+            if (ok) {
+                tc::commit(bars + kBarO);
+                if (two) tc::commit(bars + kBarO + 8);
             }
             if (*abort_flag) {
                 tc::commit(bars + kBarDrain);
@@ -363,40 +389,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (t == 0 || two) {
         // ------------------------------------------------------------ softmax (tile t)
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t s_addr = tmem + lane_base + col_s(t, 0);
+        const uint32_t s_addr = tmem + lane_base + col_s(t);
         const uint32_t o_addr = tmem + lane_base + col_o(t);
-        const uint32_t pt = base + kOffP + t * kTileP;
         const int pos_r = L - n + q0 + t * a.Qb + qi;  // last token this row sees
         float m = -INFINITY, l = 0.f;
         bool ok = true;
         for (int c = 0; c < nc; ++c) {
-            ok = __all_sync(0xffffffffu, wait_role(bars + kBarS + 16 * t + 8 * (c & 1), (c >> 1) & 1,
-                                                   abort_flag, a.err));
+            // S_t(c) done; its commit also covers PV_t(c-1).
+            ok = __all_sync(0xffffffffu, wait_role(bars + kBarS + 8 * t, c & 1, abort_flag, a.err));
             if (!ok) break;
             tc::fence_after_sync();
-            float sv[64];
-            {
-                float t0[32], t1[32];
-                const uint32_t sa = s_addr + 64u * (c & 1);
-                tc::ld32(sa, t0);
-                tc::ld32(sa + 32, t1);
-                tc::wait_ld();
+            float sv[kChunk];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    sv[i] = t0[i];
-                    sv[32 + i] = t1[i];
-                }
-            }
+            for (int i = 0; i < kChunk / 32; ++i)
+                tc::ld32(s_addr + 32 * i, *reinterpret_cast<float(*)[32]>(sv + 32 * i));
+            tc::wait_ld();
             // Causal mask by predicate; the warp skips it when no row needs it.
             const int tok0 = c * kChunk;
             if (!__all_sync(0xffffffffu, row_valid && tok0 + kChunk - 1 <= pos_r)) {
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
+                for (int i = 0; i < kChunk; ++i)
                     sv[i] = (row_valid && tok0 + i <= pos_r) ? sv[i] : -INFINITY;
             }
             float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four short chains
 #pragma unroll
-            for (int i = 0; i < 64; ++i) mq[i & 3] = fmaxf(mq[i & 3], sv[i]);
+            for (int i = 0; i < kChunk; ++i) mq[i & 3] = fmaxf(mq[i & 3], sv[i]);
             // scale > 0, so this is the max of the scaled scores
             const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;
             // Raise the reference max only when the chunk exceeds it by > 2^8.
@@ -407,59 +424,56 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l *= alpha;
             }
             const float m_use = m == -INFINITY ? 0.f : m;
-            uint32_t pw[32];
+            // P (bf16 pairs) over the first 64 columns of this row's scores.
             float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const float p0 = fast_exp2(fmaf(sv[2 * i], a.scale_log2, -m_use));
-                const float p1 = fast_exp2(fmaf(sv[2 * i + 1], a.scale_log2, -m_use));
-                ps[i & 3] += p0 + p1;
-                pw[i] = pack_bf16x2(p0, p1);
+            for (int h2 = 0; h2 < kChunk / 64; ++h2) {
+                uint32_t pw[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                    const float p0 = fast_exp2(fmaf(sv[64 * h2 + 2 * i], a.scale_log2, -m_use));
+                    const float p1 = fast_exp2(fmaf(sv[64 * h2 + 2 * i + 1], a.scale_log2, -m_use));
+                    ps[i & 3] += p0 + p1;
+                    pw[i] = pack_bf16x2(p0, p1);
+                }
+                tc::st32u(s_addr + 32 * h2, pw);
             }
             l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-            // O_t += P_t V of chunk c-1 must be done before P_t and O_t change.
-            if (c > 0) {
-                ok = __all_sync(0xffffffffu,
-                                wait_role(bars + kBarO + 8 * t, (c - 1) & 1, abort_flag, a.err));
-                if (!ok) break;
-                tc::fence_after_sync();
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            // Rescale this row of O_t if the reference max moved (PV_t(c-1) is done).
+            if (c > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                    for (int piece = 0; piece < kD / 32; ++piece) {
-                        float o[32];
-                        tc::ld32(o_addr + piece * 32, o);
-                        tc::wait_ld();
+                for (int piece = 0; piece < kD / 32; ++piece) {
+                    float o[32];
+                    tc::ld32(o_addr + piece * 32, o);
+                    tc::wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                        tc::st32(o_addr + piece * 32, o);
-                    }
-                    tc::wait_st();
+                    for (int i = 0; i < 32; ++i) o[i] *= alpha;
+                    tc::st32(o_addr + piece * 32, o);
                 }
             }
             // Final chunk: tile 0 zeroes the V rows past the last token (both
             // tiles' products run after tile 0 has published its P).
             if (t == 0 && c == nc - 1) {
                 const int valid = ntok - tok0;
+                // V of this chunk arrives on its own barrier.
+                ok = __all_sync(0xffffffffu, wait_role(bars + kBarVFull + 8 * (c % kStagesV),
+                                                       (c / kStagesV) & 1, abort_flag, a.err));
+                if (!ok) break;
                 if (valid < kChunk) {
-                    const uint32_t vst = base + kOffV + (c % kStages) * kStageKV;
+                    const uint32_t vst = base + kOffV + (c % kStagesV) * kStageKV;
                     for (int idx = tid; idx < (kChunk - valid) * 16; idx += kRows) {
                         const int r = valid + (idx >> 4), half = (idx >> 3) & 1, ch = idx & 7;
-                        st_shared_v4(vst + half * 8192 + r * 128 + ch * 16, make_uint4(0, 0, 0, 0));
+                        st_shared_v4(vst + half * kHalfKV + r * 128 + ch * 16, make_uint4(0, 0, 0, 0));
                     }
                 }
+                fence_proxy_async_smem();
             }
-            // P row -> swizzled K-major tile.
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                st_shared_v4(pt + row * 128 + ((ch ^ (row & 7)) << 4),
-                             make_uint4(pw[4 * ch], pw[4 * ch + 1], pw[4 * ch + 2], pw[4 * ch + 3]));
-            fence_proxy_async_smem();
+            tc::wait_st();
             tc::fence_before_sync();
             mbar_arrive(bars + kBarP + 8 * t);
         }
         if (ok) {
-            ok = __all_sync(0xffffffffu,
-                            wait_role(bars + kBarO + 8 * t, (nc - 1) & 1, abort_flag, a.err));
+            ok = __all_sync(0xffffffffu, wait_role(bars + kBarO + 8 * t, 0, abort_flag, a.err));
             if (ok) {
                 tc::fence_after_sync();
                 const float inv = (row_valid && l > 0.f) ? 1.f / l : 0.f;
