@@ -411,11 +411,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < kChunk; ++i)
                     sv[i] = (row_valid && tok0 + i <= pos_r) ? sv[i] : -INFINITY;
             }
-            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};  // four short chains
+            // Row max: three-input max over pairs, four short chains.
+            float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < kChunk; ++i) mq[i & 3] = fmaxf(mq[i & 3], sv[i]);
+            for (int i = 0; i < kChunk / 2; ++i) mq[i & 3] = max3(mq[i & 3], sv[2 * i], sv[2 * i + 1]);
             // scale > 0, so this is the max of the scaled scores
-            const float mx = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])) * a.scale_log2;
+            const float mx = max3(mq[0], mq[1], fmaxf(mq[2], mq[3])) * a.scale_log2;
             // Raise the reference max only when the chunk exceeds it by > 2^8.
             float alpha = 1.f;
             if (mx > m + kRescaleLog2) {
@@ -424,21 +425,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l *= alpha;
             }
             const float m_use = m == -INFINITY ? 0.f : m;
-            // P (bf16 pairs) over the first 64 columns of this row's scores.
-            float ps[4] = {0.f, 0.f, 0.f, 0.f};
+            // P = 2^(s * scale - m) (bf16 pairs) over the first 64 columns of
+            // this row's scores; the arguments and the row sum two at a time.
+            const uint64_t sc2 = f32x2(a.scale_log2, a.scale_log2), nm2 = f32x2(-m_use, -m_use);
+            uint64_t ps2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
             for (int h2 = 0; h2 < kChunk / 64; ++h2) {
                 uint32_t pw[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) {
-                    const float p0 = fast_exp2(fmaf(sv[64 * h2 + 2 * i], a.scale_log2, -m_use));
-                    const float p1 = fast_exp2(fmaf(sv[64 * h2 + 2 * i + 1], a.scale_log2, -m_use));
-                    ps[i & 3] += p0 + p1;
+                    const float2 x = f32x2_split(
+                        fma_f32x2(f32x2(sv[64 * h2 + 2 * i], sv[64 * h2 + 2 * i + 1]), sc2, nm2));
+                    const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
+                    ps2[i & 1] = add_f32x2(ps2[i & 1], f32x2(p0, p1));
                     pw[i] = pack_bf16x2(p0, p1);
                 }
                 tc::st32u(s_addr + 32 * h2, pw);
             }
-            l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+            {
+                const float2 s0 = f32x2_split(ps2[0]), s1 = f32x2_split(ps2[1]);
+                l += (s0.x + s0.y) + (s1.x + s1.y);
+            }
             // Rescale this row of O_t if the reference max moved (PV_t(c-1) is done).
             if (c > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
