@@ -201,6 +201,21 @@ def oracle_sample_gbs(wl, budget_s: float, min_pairs: int = 1, appended: bool = 
     return done_bytes / elapsed / 1e9, elapsed, pairs, threads
 
 
+def aggregate_over_ranks(world: int, seconds: float, units: float, device) -> tuple[float, float]:
+    """Whole-job figures of `world` replica ranks (one process per GPU, no
+    data exchange): the slowest rank's time and the sum of the units every
+    rank processed. With one rank the inputs come back unchanged. Every rank
+    must call it (it is a collective when world > 1)."""
+    if world == 1:
+        return seconds, units
+    import torch.distributed as dist
+    t = torch.tensor([seconds], dtype=torch.float64, device=device)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
 def run_reference(args, rank):
     if rank != 0:
         return
@@ -323,11 +338,9 @@ def run_ours(args, rank, world, local_rank):
     plan.set_split_events(None, None)
     time.sleep(0.25)
     sampler.stop()
-    ms_total = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_total = float(t.item())
+    # Slowest rank's time, every rank's bytes and query rows.
+    ms_total, job_bytes = aggregate_over_ranks(world, ev0.elapsed_time(ev1), step_bytes, dev)
+    _, job_qheads = aggregate_over_ranks(world, 0.0, wl.B * wl.Hq, dev)
     ms_step = ms_total / args.steps
     split_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ev_split)
     err = pa.pa_last_device_error(plan)
@@ -380,7 +393,7 @@ def run_ours(args, rank, world, local_rank):
     for _ in range(e2e_steps):
         e2e_step()
     torch.cuda.synchronize()
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s, _ = aggregate_over_ranks(world, (time.perf_counter() - t0) / e2e_steps, 0, dev)
     barrier()
 
     cpu = None
@@ -396,7 +409,7 @@ def run_ours(args, rank, world, local_rank):
     sha = split_source_sha()
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["source_sha"] == sha and \
         TRAFFIC["workload"] == wl.name else None
-    value = world * step_bytes / (ms_step * 1e-3) / 1e9
+    value = job_bytes / (ms_step * 1e-3) / 1e9
     clocks = sampler.summary(w0, w2)
     path, blocks, warps = plan.info()
     plan.free()
@@ -413,14 +426,14 @@ def run_ours(args, rank, world, local_rank):
                              f"of pools vs {L2_BYTES / 2**20:.0f} MiB L2), no flush",
                        "step": "pa_append_kv + pa_decode", "parallelism": f"replicas x{world}"},
             "pct_of_peak": 100.0 * value / world / peak,
-            "qheads_per_s": world * wl.B * wl.Hq / (ms_step * 1e-3),
+            "qheads_per_s": job_qheads / (ms_step * 1e-3),
             "roofline": {"bound": "hbm", "kernel": "split attention", "achieved": achieved,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes": dec_bytes, "ms_per_launch": split_ms,
                          "timing": "CUDA events around each split launch, in a second pass "
                                    "of the K timed steps"},
-            "e2e": {"value": world * step_bytes / e2e_s / 1e9, "unit": "GB/s",
+            "e2e": {"value": job_bytes / e2e_s / 1e9, "unit": "GB/s",
                     "ms_per_step": e2e_s * 1e3, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": 3 * args.steps,
