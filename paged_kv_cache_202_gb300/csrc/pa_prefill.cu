@@ -11,10 +11,10 @@
 //
 // One block = two query tiles of the same (sequence, kv head) that share the
 // K/V stream, with specialised warps:
-//   * warp 8 (producer): tiled bulk tensor copies of 128-token K and V chunks
-//     (whole pages, through the block table) into a 3-stage K ring and a
-//     2-stage V ring (V one chunk behind K: it is needed one step later;
-//     V goes first at each step);
+//   * warps 8 and 10 (producers): tiled bulk tensor copies of 128-token K
+//     and V chunks (whole pages, through the block table) into a 3-stage K
+//     ring and a 2-stage V ring, each stream on its own warp so that a wait
+//     for a free V stage never holds back the next K;
 //   * warp 9 (MMA): one thread issues S_t = Q_t K^T (M=128, N=128, K=128,
 //     both operands in shared memory) into tensor memory and
 //     O_t += P_t V (M=128, N=128, K=128) with P_t read from tensor memory and
@@ -60,9 +60,10 @@ constexpr int kD = 128;         // head dimension
 constexpr int kStagesK = 3;     // K ring depth
 constexpr int kStagesV = 2;     // V ring depth
 constexpr int kSoftmaxThreads = 2 * kRows;
-constexpr int kWarpLoad = kSoftmaxThreads / 32;  // warp 8
+constexpr int kWarpLoad = kSoftmaxThreads / 32;  // warp 8: K copies
 constexpr int kWarpMma = kWarpLoad + 1;          // warp 9
-constexpr int kThreads = kSoftmaxThreads + 64;
+constexpr int kWarpLoadV = kWarpMma + 1;         // warp 10: V copies
+constexpr int kThreads = kSoftmaxThreads + 96;
 constexpr int kSortMax = 256;   // sequences ordered by length up to this batch size
 constexpr uint32_t kTmemCols = 512;
 // Tensor-memory columns: S of tile t (128; P_t over its first 64), then O of tile t (128).
@@ -267,14 +268,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + kOffBar + kSlotTmem);
 
-    if (warp == kWarpLoad) {
-        // ------------------------------------------------------------ producer
+    if (warp == kWarpLoad || warp == kWarpLoadV) {
+        // ------------------------------------------------------------ producers (K, V)
         if (lane == 0) {
+            const bool is_k = warp == kWarpLoad;
+            const int nst = is_k ? kStagesK : kStagesV;
+            const uint32_t full = bars + (is_k ? kBarKFull : kBarVFull);
+            const uint32_t empty = bars + (is_k ? kBarKEmpty : kBarVEmpty);
+            const uint32_t ring = base + (is_k ? kOffK : kOffV);
+            const CUtensorMap* map = is_k ? &kmap : &vmap;
             const uint64_t policy = policy_evict_first();
-            // One chunk of K or V (its pages, both 64-column halves) into a stage.
-            auto load = [&](const CUtensorMap* map, uint32_t stage, uint32_t bar, int c) {
+            int issued = 0;
+            for (int c = 0; c < nc; ++c) {
+                const int s = c % nst;
+                if (c >= nst && !wait_role(empty + 8 * s, ((c / nst) - 1) & 1, abort_flag, a.err)) break;
+                // One chunk (its pages, both 64-column halves) into the stage.
                 const int p0 = c * (kChunk / BS);
                 const int np = min(kChunk / BS, nb - p0);
+                const uint32_t bar = full + 8 * s, stage = ring + s * kStageKV;
                 mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np) * BS * kD * 2);
                 for (int j = 0; j < np; ++j) {
                     const int r = table[p0 + j] * a.Hkv + h;
@@ -282,35 +293,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int half = 0; half < 2; ++half)
                         tma_load_3d(stage + half * kHalfKV + j * BS * 128, map, half * 64, 0, r, bar, policy);
                 }
-            };
-            int issued_k = 0, issued_v = 0;
-            for (int c = 0; c <= nc; ++c) {
-                if (c >= 1) {  // V of chunk c - 1 (the MMA thread waits on it first)
-                    const int cv = c - 1, s = cv % kStagesV;
-                    if (cv >= kStagesV &&
-                        !wait_role(bars + kBarVEmpty + 8 * s, ((cv / kStagesV) - 1) & 1, abort_flag, a.err))
-                        break;
-                    load(&vmap, base + kOffV + s * kStageKV, bars + kBarVFull + 8 * s, cv);
-                    issued_v = cv + 1;
-                }
-                if (c < nc) {  // K of chunk c
-                    const int s = c % kStagesK;
-                    if (c >= kStagesK &&
-                        !wait_role(bars + kBarKEmpty + 8 * s, ((c / kStagesK) - 1) & 1, abort_flag, a.err))
-                        break;
-                    load(&kmap, base + kOffK + s * kStageKV, bars + kBarKFull + 8 * s, c);
-                    issued_k = c + 1;
-                }
+                issued = c + 1;
             }
             if (*abort_flag) {
                 // Copies still in flight land before the block leaves: the
                 // last chunk issued on each stage (its phase is then final).
-                for (int c = max(0, issued_k - kStagesK); c < issued_k; ++c)
-                    mbar_wait_bounded(bars + kBarKFull + 8 * (c % kStagesK), (c / kStagesK) & 1,
-                                      kWaitLimitNs);
-                for (int c = max(0, issued_v - kStagesV); c < issued_v; ++c)
-                    mbar_wait_bounded(bars + kBarVFull + 8 * (c % kStagesV), (c / kStagesV) & 1,
-                                      kWaitLimitNs);
+                for (int c = max(0, issued - nst); c < issued; ++c)
+                    mbar_wait_bounded(full + 8 * (c % nst), (c / nst) & 1, kWaitLimitNs);
             }
         }
         __syncwarp();
