@@ -12,8 +12,8 @@
 // One block = two query tiles of the same (sequence, kv head) that share the
 // K/V stream, with specialised warps:
 //   * warps 8 and 10 (producers): tiled bulk tensor copies of 128-token K
-//     and V chunks (whole pages, through the block table) into a 3-stage K
-//     ring and a 2-stage V ring, each stream on its own warp so that a wait
+//     and V chunks (whole pages, through the block table) into a 2-stage K
+//     ring and a 3-stage V ring, each stream on its own warp so that a wait
 //     for a free V stage never holds back the next K;
 //   * warp 9 (MMA): one thread issues S_t = Q_t K^T (M=128, N=128, K=128,
 //     both operands in shared memory) into tensor memory and
@@ -57,8 +57,8 @@ namespace {
 constexpr int kRows = 128;      // M: query rows per tile
 constexpr int kChunk = 128;     // tokens per K/V chunk
 constexpr int kD = 128;         // head dimension
-constexpr int kStagesK = 3;     // K ring depth
-constexpr int kStagesV = 2;     // V ring depth
+constexpr int kStagesK = 2;     // K ring depth
+constexpr int kStagesV = 3;     // V ring depth (PV waits on V last)
 constexpr int kSoftmaxThreads = 2 * kRows;
 constexpr int kWarpLoad = kSoftmaxThreads / 32;  // warp 8: K copies
 constexpr int kWarpMma = kWarpLoad + 1;          // warp 9
