@@ -37,8 +37,8 @@ L2_BYTES = 126 * 2**20
 # DRAM traffic of the split-attention kernel from an ncu capture (per launch,
 # scaled to the full workload), valid only for the kernel sources it was
 # measured on (sha256 of the split kernel's source files).
-TRAFFIC = {"source_sha": "ebcc10d8c27f5b7c6ffa7a8b70c6fc892f9c28291717c2ab67fe0db47b7604d6",
-           "workload": "llama3_8b_gqa", "bytes_per_launch": 2205603584 + 5870080}
+TRAFFIC = {"source_sha": "63797715d93a054d8af3c7e1cc4422b66bcadbaa9decc8f0b9ffc6981ca90f4a",
+           "workload": "llama3_8b_gqa", "bytes_per_launch": 2205526528 + 5707520}
 
 
 def split_source_sha() -> str:
