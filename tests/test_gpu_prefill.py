@@ -93,3 +93,31 @@ def test_prefill_bad_lengths_and_table():
     ref = oracle.prefill(q[:10], wl.k_pool, wl.v_pool, wl.block_tables[:1], wl.seq_lens[:1],
                          qs[:2], wl.scale)
     assert np.abs(got[:10] - ref).max() <= BF16_TOL
+
+
+@pytest.mark.parametrize("name", ["prefill_gqa", "llama3_8b_gqa"])
+def test_prefill_full_size_sampled_rows(name):
+    """The benchmark's workloads at full size (the newest 256 tokens of every
+    sequence are queries): sampled query rows, each checked against the
+    oracle on its own (query i of sequence b sees its first L - n + i + 1
+    tokens), including the first and last query row of every sequence."""
+    wl = make_workload(name)
+    wl.append_in_place()
+    ns = np.minimum(wl.seq_lens, 256).astype(np.int64)
+    qs = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
+    T = int(qs[-1])
+    q = bf16_bits(np.random.default_rng(11).standard_normal((T, wl.Hq, wl.D)).astype(np.float32))
+    got, err = _run(wl, q, qs, [int(x) for x in ns])
+    assert err == 0
+    rng = np.random.default_rng(12)
+    rows = set(rng.choice(T, size=48, replace=False).tolist())
+    rows |= set(qs[:-1].tolist()) | set((qs[1:] - 1).tolist())
+    worst = 0.0
+    for r in sorted(rows):
+        b = int(np.searchsorted(qs, r, side="right") - 1)
+        i = r - int(qs[b])
+        ref = oracle.prefill(q[r:r + 1], wl.k_pool, wl.v_pool, wl.block_tables[b:b + 1],
+                             [int(wl.seq_lens[b] - ns[b] + i + 1)], [0, 1], wl.scale)
+        assert np.isfinite(got[r]).all()
+        worst = max(worst, float(np.abs(got[r] - ref[0]).max()))
+    assert worst <= BF16_TOL, f"max abs error {worst:.3e}"
