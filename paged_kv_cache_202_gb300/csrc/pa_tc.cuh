@@ -42,21 +42,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_ma
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-// D(tmem) (+)= A(smem) * B(smem); issued by one thread.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, bool accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}"
-        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(static_cast<uint32_t>(accumulate))
-        : "memory");
-}
-
-// The same product with each descriptor passed as two 32-bit words. Every
-// descriptor built by smem_desc() with SBO = 1024 has the same high word; the
-// low word holds the start address (16-byte units, bits 0-13) and the LBO, so
-// stepping through a tile is one 32-bit add on the low word.
+// D(tmem) (+)= A(smem) * B(smem), issued by one thread, with each descriptor
+// passed as two 32-bit words. Every descriptor built by smem_desc() with
+// SBO = 1024 has the same high word; the low word holds the start address
+// (16-byte units, bits 0-13) and the LBO, so stepping through a tile is one
+// 32-bit add on the low word.
 __device__ __forceinline__ void mma_bf16_lo(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t hi,
                                             uint32_t idesc, uint32_t accumulate) {
     asm volatile(
