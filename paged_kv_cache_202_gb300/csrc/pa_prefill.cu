@@ -32,17 +32,18 @@
 // earlier product) also tells the softmax that PV_t(c) is done. While one
 // warpgroup exponentiates, the tensor core works on the other tile, so the
 // two tiles take turns. Keeping P out of shared memory leaves the shared
-// memory bandwidth to the S operands, V and the incoming copies. The running maximum is raised only when
-// a chunk's maximum exceeds it by more than 2^8 (any fixed reference gives
-// the same quotient acc / l; this one keeps every probability below 256):
-// the accumulator rows in tensor memory are then rescaled, otherwise left.
+// memory bandwidth to the S operands, V and the incoming copies.
+// The running maximum is raised only when a chunk's maximum exceeds it by
+// more than 2^8 (any fixed reference gives the same quotient acc / l; this
+// one keeps every probability below 256): the accumulator rows in tensor
+// memory are then rescaled, otherwise left.
 // V rows past the last token of the final chunk are zeroed before the
 // product so that slots beyond the sequence never reach a sum. Blocks are
 // ordered longest sequence first so that the long ones do not form the tail.
 //
 // Every mbarrier wait is bounded. A role that gives up raises a shared abort
 // flag (and PA_DEVERR_TIMEOUT); the others see it in their own waits. Before
-// the block leaves, the producer waits (bounded) for its copies in flight,
+// the block leaves, each producer waits (bounded) for its copies in flight,
 // the MMA thread for its products, and the block frees its tensor memory.
 #include <cuda_bf16.h>
 
