@@ -329,10 +329,20 @@ def run_ours(args, rank, world, local_rank):
     w1 = time.time()
     barrier()
     # Kernel pass: the same K steps again, with events around every split
-    # launch, for the split kernel's average duration (the roofline figure).
+    # launch, for the split kernel's average duration (the roofline figure),
+    # and around the append and the whole decode call.
+    ev_parts = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    for evs in ev_parts:
+        for e in evs:
+            e.record(stream)
+    torch.cuda.synchronize()
     for i in range(args.steps):
         plan.set_split_events(*ev_split[i])
-        step()
+        ev_parts[i][0].record(stream)
+        pa.pa_append_kv(k_new, v_new, k_pool, v_pool, tables, cache_lens, stream)
+        ev_parts[i][1].record(stream)
+        pa.pa_decode(q, k_pool, v_pool, tables, seq_lens, wl.scale, out, max_len, plan, stream)
+        ev_parts[i][2].record(stream)
     torch.cuda.synchronize()
     w2 = time.time()
     plan.set_split_events(None, None)
@@ -343,6 +353,8 @@ def run_ours(args, rank, world, local_rank):
     _, job_qheads = aggregate_over_ranks(world, 0.0, wl.B * wl.Hq, dev)
     ms_step = ms_total / args.steps
     split_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ev_split)
+    append_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev_parts)
+    decode_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev_parts)
     err = pa.pa_last_device_error(plan)
 
     # Parity of the timed output against the oracle on sampled rows (rank 0).
@@ -429,6 +441,9 @@ def run_ours(args, rank, world, local_rank):
                        "step": "pa_append_kv + pa_decode", "parallelism": f"replicas x{world}"},
             "pct_of_peak": 100.0 * value / world / peak,
             "qheads_per_s": job_qheads / (ms_step * 1e-3),
+            "parts_ms": {"append": append_ms, "decode": decode_ms, "split_kernel": split_ms,
+                         "timing": "CUDA events around each call in the kernel pass (events "
+                                   "between calls, so no launch overlap); rank 0"},
             "roofline": {"bound": "hbm", "kernel": "split attention", "achieved": achieved,
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
