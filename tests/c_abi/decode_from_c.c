@@ -1,0 +1,162 @@
+/*
+ * The C boundary used from C: one decode step (pa_append_kv, then pa_decode)
+ * on device memory from cudaMalloc, with no Python or PyTorch involved,
+ * checked against the fp64 oracle (linked from oracle/ as test
+ * infrastructure). Inputs are deterministic (an integer hash), the pools hold
+ * NaN in every slot past each sequence, and the tables name a shuffled set of
+ * physical blocks with -1 past each sequence.
+ *
+ * Exit status 0 when the appended pools match the oracle's bit for bit and
+ * the attention output is within the bf16 tolerance (1.5e-2 absolute).
+ */
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include "pa.h"
+
+/* The oracle's C entry points (oracle/oracle.cpp). */
+int oracle_decode(const void* q, const void* kpool, const void* vpool, const int32_t* table,
+                  int max_blocks, const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int bs,
+                  int num_blocks, float scale, int dtype, double* out, const int32_t* pairs,
+                  int npairs, int nthreads);
+int oracle_append(const void* k_new, const void* v_new, void* kpool, void* vpool,
+                  const int32_t* table, int max_blocks, const int32_t* cache_lens, int B, int Hkv,
+                  int D, int bs, int num_blocks, int elem_bytes);
+
+enum { B = 3, HQ = 8, HKV = 2, D = 128, BS = 16, MAXB = 20, SPARE = 5 };
+static const int kLens[B] = {1, 37, 300}; /* tokens after the append */
+
+static uint32_t hash32(uint32_t x) {
+    x ^= x >> 16; x *= 0x7feb352dU; x ^= x >> 15; x *= 0x846ca68bU; x ^= x >> 16;
+    return x;
+}
+
+/* A value in [-1, 1) as bf16 bits (round to nearest even). */
+static uint16_t bf16_of(uint32_t key) {
+    float f = (float)((double)(hash32(key) >> 8) / 8388608.0 - 1.0);
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)((u + 0x7FFFu + ((u >> 16) & 1u)) >> 16);
+}
+
+static float f32_of_bf16(uint16_t h) {
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+#define CHECK_CUDA(x) do { cudaError_t e_ = (x); if (e_ != cudaSuccess) { \
+    fprintf(stderr, "%s: %s\n", #x, cudaGetErrorString(e_)); return 2; } } while (0)
+#define CHECK_PA(x) do { pa_status s_ = (x); if (s_ != PA_OK) { \
+    fprintf(stderr, "%s: %s\n", #x, pa_status_str(s_)); return 3; } } while (0)
+
+int main(void) {
+    int used = 0;
+    for (int b = 0; b < B; ++b) used += (kLens[b] + BS - 1) / BS;
+    const int NB = used + SPARE;
+    const size_t pool_elems = (size_t)NB * HKV * BS * D;
+
+    /* Shuffled physical blocks, consumed in order; -1 past each sequence. */
+    int32_t* perm = malloc(sizeof(int32_t) * NB);
+    for (int i = 0; i < NB; ++i) perm[i] = i;
+    for (int i = NB - 1; i > 0; --i) {
+        const int j = (int)(hash32(0xB10C0000u + (uint32_t)i) % (uint32_t)(i + 1));
+        const int32_t t = perm[i]; perm[i] = perm[j]; perm[j] = t;
+    }
+    int32_t table[B * MAXB];
+    int32_t seq_lens[B], cache_lens[B];
+    int next = 0;
+    for (int b = 0; b < B; ++b) {
+        const int nb = (kLens[b] + BS - 1) / BS;
+        for (int p = 0; p < MAXB; ++p) table[b * MAXB + p] = p < nb ? perm[next++] : -1;
+        seq_lens[b] = kLens[b];
+        cache_lens[b] = kLens[b] - 1;
+    }
+
+    /* Pools: hashed values, NaN in every slot past each sequence's cached tokens. */
+    uint16_t* kpool = malloc(pool_elems * 2);
+    uint16_t* vpool = malloc(pool_elems * 2);
+    for (size_t i = 0; i < pool_elems; ++i) {
+        kpool[i] = bf16_of(0x10000000u + (uint32_t)i);
+        vpool[i] = bf16_of(0x20000000u + (uint32_t)i);
+    }
+    for (int b = 0; b < B; ++b)
+        for (int t = cache_lens[b]; t < (kLens[b] + BS - 1) / BS * BS; ++t) {
+            const int blk = table[b * MAXB + t / BS];
+            for (int h = 0; h < HKV; ++h)
+                for (int d = 0; d < D; ++d) {
+                    const size_t i = (((size_t)blk * HKV + h) * BS + t % BS) * D + d;
+                    kpool[i] = vpool[i] = 0x7FC0; /* NaN */
+                }
+        }
+    uint16_t q[B * HQ * D], k_new[B * HKV * D], v_new[B * HKV * D];
+    for (int i = 0; i < B * HQ * D; ++i) q[i] = bf16_of(0x30000000u + (uint32_t)i);
+    for (int i = 0; i < B * HKV * D; ++i) {
+        k_new[i] = bf16_of(0x40000000u + (uint32_t)i);
+        v_new[i] = bf16_of(0x50000000u + (uint32_t)i);
+    }
+
+    void *dk, *dv, *dq, *dkn, *dvn, *dout;
+    int32_t *dtab, *dsl, *dcl;
+    CHECK_CUDA(cudaMalloc(&dk, pool_elems * 2));
+    CHECK_CUDA(cudaMalloc(&dv, pool_elems * 2));
+    CHECK_CUDA(cudaMalloc(&dq, sizeof q));
+    CHECK_CUDA(cudaMalloc(&dkn, sizeof k_new));
+    CHECK_CUDA(cudaMalloc(&dvn, sizeof v_new));
+    CHECK_CUDA(cudaMalloc(&dout, (size_t)B * HQ * D * 2));
+    CHECK_CUDA(cudaMalloc((void**)&dtab, sizeof table));
+    CHECK_CUDA(cudaMalloc((void**)&dsl, sizeof seq_lens));
+    CHECK_CUDA(cudaMalloc((void**)&dcl, sizeof cache_lens));
+    CHECK_CUDA(cudaMemcpy(dk, kpool, pool_elems * 2, cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemcpy(dv, vpool, pool_elems * 2, cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemcpy(dq, q, sizeof q, cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemcpy(dkn, k_new, sizeof k_new, cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemcpy(dvn, v_new, sizeof v_new, cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemcpy(dtab, table, sizeof table, cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemcpy(dsl, seq_lens, sizeof seq_lens, cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemcpy(dcl, cache_lens, sizeof cache_lens, cudaMemcpyHostToDevice));
+
+    const float scale = 1.0f / sqrtf((float)D);
+    pa_plan* plan = NULL;
+    CHECK_PA(pa_append_kv(dkn, dvn, dk, dv, dtab, MAXB, dcl, B, HKV, D, BS, NB, PA_BF16, NULL));
+    CHECK_PA(pa_decode(dq, dk, dv, dtab, MAXB, dsl, B, HQ, HKV, D, BS, NB, MAXB * BS, scale, PA_BF16,
+                       dout, PA_BF16, &plan, NULL));
+    CHECK_CUDA(cudaDeviceSynchronize());
+    int derr = -1, aerr = -1;
+    CHECK_PA(pa_last_device_error(plan, &derr));
+    CHECK_PA(pa_last_device_error(NULL, &aerr));
+
+    uint16_t* kgot = malloc(pool_elems * 2);
+    uint16_t* vgot = malloc(pool_elems * 2);
+    uint16_t out[B * HQ * D];
+    CHECK_CUDA(cudaMemcpy(kgot, dk, pool_elems * 2, cudaMemcpyDeviceToHost));
+    CHECK_CUDA(cudaMemcpy(vgot, dv, pool_elems * 2, cudaMemcpyDeviceToHost));
+    CHECK_CUDA(cudaMemcpy(out, dout, sizeof out, cudaMemcpyDeviceToHost));
+    CHECK_PA(pa_free(plan));
+
+    /* The oracle: append on the host pools, then fp64 attention. */
+    if (oracle_append(k_new, v_new, kpool, vpool, table, MAXB, cache_lens, B, HKV, D, BS, NB, 2) != 0)
+        return 4;
+    double ref[B * HQ * D];
+    if (oracle_decode(q, kpool, vpool, table, MAXB, seq_lens, B, HQ, HKV, D, BS, NB, scale, 1, ref,
+                      NULL, 0, 4) != 0)
+        return 4;
+    const int pools_equal = memcmp(kgot, kpool, pool_elems * 2) == 0 &&
+                            memcmp(vgot, vpool, pool_elems * 2) == 0;
+    double worst = 0.0;
+    int finite = 1;
+    for (int i = 0; i < B * HQ * D; ++i) {
+        const double g = (double)f32_of_bf16(out[i]);
+        finite &= isfinite(g) != 0;
+        const double e = fabs(g - ref[i]);
+        if (e > worst) worst = e;
+    }
+    printf("device errors %d/%d, pools equal %d, finite %d, max abs error %.3e\n", derr, aerr,
+           pools_equal, finite, worst);
+    return (derr == 0 && aerr == 0 && pools_equal && finite && worst <= 1.5e-2) ? 0 : 1;
+}
