@@ -466,6 +466,60 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.destroy_process_group()
 
 
+def row_cpu_baseline(row, wl, budget_s, prefill_q=None, prefill_qs=None, prefill_ns=None):
+    """The oracle, as it stands, on a bounded random sample of the row's
+    workload on the host cores (about budget_s of CPU work)."""
+    import oracle
+    rng = np.random.default_rng(5)
+    elapsed, units, n = 0.0, 0.0, 0
+    if row == "prefill":
+        threads = os.cpu_count() or 1
+        T = int(prefill_qs[-1])
+        for r in rng.permutation(T):
+            b = int(np.searchsorted(prefill_qs, r, side="right") - 1)
+            npos = int(wl.seq_lens[b] - prefill_ns[b] + (r - prefill_qs[b]) + 1)
+            t = time.perf_counter()
+            oracle.prefill(prefill_q[r:r + 1], wl.k_pool, wl.v_pool, wl.block_tables[b:b + 1],
+                           [npos], [0, 1], wl.scale, nthreads=threads)
+            elapsed += time.perf_counter() - t
+            units += 4 * wl.D * wl.Hq * npos
+            n += 1
+            if elapsed >= budget_s:
+                break
+        return {"value": units / elapsed / 1e12, "unit": "TFLOP/s", "cores": threads,
+                "kind": "oracle", "sample": f"{n} query rows (all {wl.Hq} heads each, random "
+                                            f"order), {elapsed:.1f} s"}
+    eb = wl.elem_bytes
+    if row == "copy_blocks":
+        block_bytes = wl.Hkv * wl.block_size * wl.D * eb
+        perm = rng.permutation(wl.num_blocks).astype(np.int32)
+        half = wl.num_blocks // 2
+        batch = 0
+        while elapsed < budget_s:
+            k = batch % max(1, half // 64)
+            batch += 1
+            src, dst = perm[64 * k:64 * k + 64], perm[half + 64 * k:half + 64 * k + 64]
+            t = time.perf_counter()
+            oracle.copy_blocks(wl.k_pool, wl.v_pool, src, dst)
+            elapsed += time.perf_counter() - t
+            units += 2 * len(src) * block_bytes * 2
+            n += len(src)
+        what = f"{n} random block pairs in batches of 64"
+    else:
+        for b in np.tile(rng.permutation(wl.B), 1000):
+            L = int(wl.seq_lens[b])
+            t = time.perf_counter()
+            oracle.page_scores(wl.k_pool, wl.v_pool, wl.block_tables[b:b + 1], wl.seq_lens[b:b + 1])
+            elapsed += time.perf_counter() - t
+            units += 2 * wl.Hkv * wl.D * eb * L
+            n += 1
+            if elapsed >= budget_s:
+                break
+        what = f"{n} sequences one at a time, random order"
+    return {"value": units / elapsed / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"{what}, {elapsed:.1f} s"}
+
+
 def run_row(args, local_rank):
     """Measure one of the other hot-path kernels on the workload: whole-pool
     block copies (copy on write) or PagedEviction page scores."""
@@ -568,6 +622,8 @@ def run_row(args, local_rank):
                 got = out[r].float().cpu().numpy().astype(np.float64)
                 err = max(err, float(np.abs(got - sub[0]).max()))
             parity = {"rows": int(len(rows)), "max_abs_err": err, "tol": 1.5e-2}
+        cpu = None if args.no_cpu_baseline else row_cpu_baseline(
+            "prefill", wl, args.cpu_budget, prefill_q=qh, prefill_qs=qs, prefill_ns=ns)
         print(json.dumps({
             "row": "prefill", "metric": "prefill: achieved bf16 TFLOP/s", "value": tfs,
             "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
@@ -576,9 +632,10 @@ def run_row(args, local_rank):
             "roofline": {"bound": "tensor", "achieved": tfs, "peak": tpeak, "peak_kind": tkind,
                          "unit": "TFLOP/s", "frac": tfs / tpeak, "algorithmic_flops": flops,
                          "hbm_gbs": gbs},
-            "parity": parity, "gpu_launches": args.steps,
+            "parity": parity, "gpu_launches": args.steps, "cpu_baseline": cpu,
         }), flush=True)
         return
+    cpu = None if args.no_cpu_baseline else row_cpu_baseline(args.row, wl, args.cpu_budget)
     print(json.dumps({
         "row": args.row, "metric": f"{args.row}: achieved HBM GB/s", "value": gbs, "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -588,6 +645,7 @@ def run_row(args, local_rank):
         "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": gbs / peak, "algorithmic_bytes": nbytes},
         "gpu_launches": (1 if args.row == "copy_blocks" else 2) * args.steps,
+        "cpu_baseline": cpu,
     }), flush=True)
 
 
