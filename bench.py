@@ -472,21 +472,25 @@ def row_cpu_baseline(row, wl, budget_s, prefill_q=None, prefill_qs=None, prefill
     import oracle
     rng = np.random.default_rng(5)
     elapsed, units, n = 0.0, 0.0, 0
-    if row == "prefill":
+    if row in ("prefill", "spec"):
         threads = os.cpu_count() or 1
         T = int(prefill_qs[-1])
-        for r in rng.permutation(T):
+        for r in np.tile(rng.permutation(T), max(1, 100000 // max(T, 1))):  # cycles until the budget
             b = int(np.searchsorted(prefill_qs, r, side="right") - 1)
             npos = int(wl.seq_lens[b] - prefill_ns[b] + (r - prefill_qs[b]) + 1)
             t = time.perf_counter()
             oracle.prefill(prefill_q[r:r + 1], wl.k_pool, wl.v_pool, wl.block_tables[b:b + 1],
                            [npos], [0, 1], wl.scale, nthreads=threads)
             elapsed += time.perf_counter() - t
-            units += 4 * wl.D * wl.Hq * npos
+            if row == "prefill":
+                units += 4 * wl.D * wl.Hq * npos
+            else:  # bytes: the sequence's K and V once, shared by its query rows
+                units += 2 * wl.Hkv * wl.D * wl.elem_bytes * int(wl.seq_lens[b]) / prefill_ns[b]
             n += 1
             if elapsed >= budget_s:
                 break
-        return {"value": units / elapsed / 1e12, "unit": "TFLOP/s", "cores": threads,
+        scale, unit = (1e12, "TFLOP/s") if row == "prefill" else (1e9, "GB/s")
+        return {"value": units / elapsed / scale, "unit": unit, "cores": threads,
                 "kind": "oracle", "sample": f"{n} query rows (all {wl.Hq} heads each, random "
                                             f"order), {elapsed:.1f} s"}
     eb = wl.elem_bytes
@@ -541,7 +545,7 @@ def run_row(args, local_rank):
     tables = torch.from_numpy(wl.block_tables).to(dev)
     seq_lens = torch.from_numpy(wl.seq_lens).to(dev)
     eb = wl.elem_bytes
-    if args.row == "prefill":
+    if args.row in ("prefill", "spec"):
         n_new = int(CONFIGS_NEW_TOKENS(args.workload))
         wl.append_in_place()
         k_pool, v_pool = to_dev(wl.k_pool), to_dev(wl.v_pool)
@@ -560,9 +564,16 @@ def run_row(args, local_rank):
         flops = 4 * wl.D * wl.Hq * toks
         nbytes = 2 * wl.Hkv * wl.D * eb * int(wl.seq_lens.sum()) + 2 * T * wl.Hq * wl.D * 2
 
-        def call():
-            pa.pa_prefill(q, q_start, k_pool, v_pool, tables, seq_lens, wl.scale, out,
-                          int(ns.max()), wl.max_seq_len)
+        if args.row == "prefill":
+            def call():
+                pa.pa_prefill(q, q_start, k_pool, v_pool, tables, seq_lens, wl.scale, out,
+                              int(ns.max()), wl.max_seq_len)
+        else:
+            plan = pa.Plan()
+
+            def call():
+                pa.pa_decode_multi(q, q_start, k_pool, v_pool, tables, seq_lens, wl.scale, out,
+                                   int(ns.max()), wl.max_seq_len, plan)
         what = f"{T} query rows ({n_new} newest tokens per sequence), causal"
     elif args.row == "copy_blocks":
         n = min(8192, wl.num_blocks // 2)
@@ -605,9 +616,12 @@ def run_row(args, local_rank):
     ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ev)
     peak, peak_kind = measured_peak_gbs()
     gbs = nbytes / (ms * 1e-3) / 1e9
-    if args.row == "prefill":
+    if args.row in ("prefill", "spec"):
         tpeak, tkind = measured_peak_tflops()
         tfs = flops / (ms * 1e-3) / 1e12
+        # Bound by arithmetic intensity: few queries per sequence (speculative
+        # verification) make the pass HBM-bound, many (chunked prefill) tensor-bound.
+        hbm_bound = flops / nbytes < tpeak * 1e12 / (peak * 1e9)
         parity = None
         if not args.no_parity:
             import oracle
@@ -623,16 +637,23 @@ def run_row(args, local_rank):
                 err = max(err, float(np.abs(got - sub[0]).max()))
             parity = {"rows": int(len(rows)), "max_abs_err": err, "tol": 1.5e-2}
         cpu = None if args.no_cpu_baseline else row_cpu_baseline(
-            "prefill", wl, args.cpu_budget, prefill_q=qh, prefill_qs=qs, prefill_ns=ns)
+            args.row, wl, args.cpu_budget, prefill_q=qh, prefill_qs=qs, prefill_ns=ns)
         print(json.dumps({
-            "row": "prefill", "metric": "prefill: achieved bf16 TFLOP/s", "value": tfs,
-            "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+            "row": args.row,
+            **({"metric": "prefill: achieved bf16 TFLOP/s", "value": tfs, "unit": "TFLOP/s"}
+               if args.row == "prefill" else
+               {"metric": "speculative verification (pa_decode_multi): achieved HBM GB/s",
+                "value": gbs, "unit": "GB/s"}), "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": wl.name, "what": what},
-            "roofline": {"bound": "tensor", "achieved": tfs, "peak": tpeak, "peak_kind": tkind,
-                         "unit": "TFLOP/s", "frac": tfs / tpeak, "algorithmic_flops": flops,
-                         "hbm_gbs": gbs},
-            "parity": parity, "gpu_launches": args.steps, "cpu_baseline": cpu,
+            "roofline": ({"bound": "hbm", "achieved": gbs, "peak": peak, "peak_kind": peak_kind,
+                          "unit": "GB/s", "frac": gbs / peak, "algorithmic_bytes": nbytes,
+                          "tflops": tfs} if hbm_bound else
+                         {"bound": "tensor", "achieved": tfs, "peak": tpeak, "peak_kind": tkind,
+                          "unit": "TFLOP/s", "frac": tfs / tpeak, "algorithmic_flops": flops,
+                          "hbm_gbs": gbs}),
+            "parity": parity, "gpu_launches": (2 if args.row == "spec" else 1) * args.steps,
+            "cpu_baseline": cpu,
         }), flush=True)
         return
     cpu = None if args.no_cpu_baseline else row_cpu_baseline(args.row, wl, args.cpu_budget)
@@ -662,12 +683,12 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--row", default="decode",
-                    choices=["decode", "copy_blocks", "page_scores", "prefill"])
+                    choices=["decode", "copy_blocks", "page_scores", "prefill", "spec"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.workload is None:
-        args.workload = "prefill_gqa" if args.row == "prefill" else "llama3_8b_gqa"
+        args.workload = {"prefill": "prefill_gqa", "spec": "spec_gqa"}.get(args.row, "llama3_8b_gqa")
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         run_reference(args, rank)

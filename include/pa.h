@@ -209,6 +209,40 @@ pa_status pa_prefill(const void* q, const int32_t* q_start, const void* k_pool, 
                      int max_seq_len, float scale, pa_dtype kv_dtype, void* out, pa_dtype out_dtype,
                      int* device_error, struct CUstream_st* stream);
 
+/*
+ * pa_decode_multi -- paged decode attention for a few new queries per
+ * sequence (speculative verification of drafted tokens).
+ *
+ * Computes what pa_prefill computes -- the newest n_b = q_start[b+1] -
+ * q_start[b] tokens of sequence b are queries, query i at position
+ * L_b - n_b + i attends to the tokens up to its position ("FlashAttention vs
+ * PagedAttention", "How prefill and decode change the diagnosis") -- on the
+ * split decode kernels of pa_decode: the (query, head) pairs of a kv head
+ * share one tensor-core tile and the pages are streamed once for all of
+ * them, so a step with few queries runs at the decode's bandwidth. Partials
+ * across the split are combined as in pa_decode ("39 · PagedAttention" §3).
+ *
+ *   q, q_start, out   as for pa_prefill; num_queries = q_start[B] (host)
+ *   max_q     host bound on every n_b; max_q * (Hq / Hkv) <= 16
+ *   plan_inout  as for pa_decode (the plan's forced path does not apply:
+ *             this call always uses the tensor-core tiles)
+ *   other arguments   as for pa_decode
+ *
+ * Supported: bf16 pools (PA_ERR_DTYPE otherwise), D in {64, 128}, block_size
+ * 16 or 32. max_q * (Hq / Hkv) > 16 returns PA_ERR_SHAPE (use pa_prefill).
+ * A sequence with n_b < 1, n_b > max_q, n_b > L_b, rows outside
+ * [0, num_queries) or L_b out of range raises PA_DEVERR_SEQ_LEN in the plan's
+ * error word and gets zero rows (q_start must still be nondecreasing); a table
+ * entry outside the pool raises PA_DEVERR_TABLE and zeroes that sequence's
+ * rows of the affected kv head. num_queries = 0 or B = 0 is a no-op.
+ */
+pa_status pa_decode_multi(const void* q, const int32_t* q_start, int num_queries, int max_q,
+                          const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                          int max_blocks, const int32_t* seq_lens, int B, int Hq, int Hkv, int D,
+                          int block_size, int num_blocks, int max_seq_len, float scale,
+                          pa_dtype kv_dtype, void* out, pa_dtype out_dtype, pa_plan** plan_inout,
+                          struct CUstream_st* stream);
+
 /* ------------------------------------------------------------------------
  * Block management: free list, sharing and copy on write.
  *

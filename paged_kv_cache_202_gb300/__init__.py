@@ -87,6 +87,9 @@ def lib() -> ctypes.CDLL:
     L.pa_prefill.argtypes = [vp, vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf, ci, vp,
                              ci, vp, vp]
     L.pa_prefill.restype = ci
+    L.pa_decode_multi.argtypes = [vp, vp, ci, ci, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, ci, cf,
+                                  ci, vp, ci, ctypes.POINTER(vp), vp]
+    L.pa_decode_multi.restype = ci
     L.pa_page_scores.argtypes = [vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, ci, vp, vp, vp, vp]
     L.pa_page_scores.restype = ci
     for name in ("pa_bm_create", "pa_bm_destroy", "pa_bm_alloc", "pa_bm_fork", "pa_bm_release",
@@ -190,6 +193,27 @@ def pa_decode(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                          int(max_seq_len), float(scale), _dtype(k_pool), _ptr(out), _dtype(out),
                          ctypes.byref(plan.handle), _stream(stream))
     _check(st, "pa_decode")
+    return out
+
+
+def pa_decode_multi(q: torch.Tensor, q_start: torch.Tensor, k_pool: torch.Tensor,
+                    v_pool: torch.Tensor, block_tables: torch.Tensor, seq_lens: torch.Tensor,
+                    scale: float, out: torch.Tensor, max_q: int, max_seq_len: int, plan: Plan,
+                    stream=None) -> torch.Tensor:
+    """Decode attention for a few new queries per sequence into ``out``; returns ``out``.
+
+    ``q`` and ``out`` are ``[T, Hq, D]`` with sequence b's queries (its
+    newest tokens) at rows ``q_start[b] .. q_start[b+1]``; ``q_start`` is a
+    device int32 tensor of B + 1 entries and ``max_q`` bounds every count.
+    """
+    T, Hq, D = q.shape
+    NB, Hkv, bs, _ = k_pool.shape
+    B = seq_lens.shape[0]
+    st = lib().pa_decode_multi(_ptr(q), _ptr(q_start), T, int(max_q), _ptr(k_pool), _ptr(v_pool),
+                               _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, Hq,
+                               Hkv, D, bs, NB, int(max_seq_len), float(scale), _dtype(k_pool),
+                               _ptr(out), _dtype(out), ctypes.byref(plan.handle), _stream(stream))
+    _check(st, "pa_decode_multi")
     return out
 
 

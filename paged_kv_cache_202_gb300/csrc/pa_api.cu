@@ -19,6 +19,7 @@ using pa::SplitLaunch;
 
 constexpr size_t kSmemLimit = 232448;     // opt-in dynamic shared memory per block on sm_10x
 constexpr int kDefaultWarps = 3;           // warps per block of the split kernels
+constexpr int kMultiWarps = 4;             // ... with several queries per sequence
 constexpr int kDefaultStages = 1;          // pipeline stages per warp
 constexpr int kDynPermille = 150;          // share of the page stream scheduled dynamically
 constexpr int kDynMinPages = 1024;         // ... when a sequence may have this many pages
@@ -38,6 +39,7 @@ struct OccKey {
     int kind, D, BS, NT, warps;
     size_t smem;
     int blocks_per_sm;
+    int mq;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -162,11 +164,15 @@ pa_status pa_append_kv(const void* k_new, const void* v_new, void* k_pool, void*
                : PA_ERR_CUDA;
 }
 
-pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
-                    const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int B,
-                    int Hq, int Hkv, int D, int block_size, int num_blocks, int max_seq_len,
-                    float scale, pa_dtype kv_dtype, void* out, pa_dtype out_dtype,
-                    pa_plan** plan_inout, struct CUstream_st* stream_) {
+namespace {
+
+// The decode of pa_decode and, with q_start != null (T query rows, at most
+// nq per sequence), of pa_decode_multi.
+pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, const void* k_pool,
+                      const void* v_pool, const int32_t* block_tables, int max_blocks,
+                      const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
+                      int num_blocks, int max_seq_len, float scale, pa_dtype kv_dtype, void* out,
+                      pa_dtype out_dtype, pa_plan** plan_inout, struct CUstream_st* stream_) {
     if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out || !plan_inout)
         return PA_ERR_NULL;
     if ((kv_dtype != PA_F32 && kv_dtype != PA_BF16) || (out_dtype != PA_F32 && out_dtype != PA_BF16))
@@ -180,6 +186,13 @@ pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
         return PA_ERR_SHAPE;
     if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
         return PA_ERR_ALIGN;
+    if (q_start) {
+        // Several queries per sequence run on the tensor-core tiles only: up to
+        // 16 (query, head) columns per kv head, bf16 pools.
+        if (kv_dtype != PA_BF16) return PA_ERR_DTYPE;
+        if (T < 0 || nq < 1 || nq * (Hq / Hkv) > 16) return PA_ERR_SHAPE;
+        if (T == 0) return PA_OK;
+    }
     if (B == 0) return PA_OK;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
@@ -202,7 +215,7 @@ pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
     if (plan->device != dev) return PA_ERR_CUDA;  // a plan belongs to one device
 
     const int g = Hq / Hkv;
-    int path = plan->forced_path;
+    int path = q_start ? PA_PATH_MMA : plan->forced_path;
     if (path == PA_PATH_AUTO) {
         path = kv_dtype == PA_F32 ? PA_PATH_SIMPLE : (g == 1 ? PA_PATH_FMA : PA_PATH_MMA);
     }
@@ -228,6 +241,11 @@ pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
         kind = pa::kSplitFma;
         nslices = g;  // one query head per kv unit
         GS = 1;
+    } else if (q_start) {
+        kind = pa::kSplitMma;
+        nslices = 1;  // one tile: nq queries x g heads of the kv head
+        GS = nq * g;
+        NT = (GS + 7) / 8;
     } else {
         kind = pa::kSplitMma;
         nslices = (g + kHeadSlice - 1) / kHeadSlice;
@@ -245,7 +263,11 @@ pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
     // Many warps with one stage each: a warp waits for its chunk while the other
     // warps of the SM compute, so bytes in flight scale with the warp count
     // (3 warps per block, up to 4 blocks per SM at 32-token stages).
-    int warps = kDefaultWarps;
+    // With 9-16 (query, head) columns the multi-query kernel holds two
+    // n-tiles of state (~235 registers a thread), which limits an SM to two
+    // blocks: four warps each keep eight warps' stages in flight (measured
+    // 5.77 vs 4.96 TB/s with three on the speculative-verification workload).
+    int warps = (q_start && NT == 2) ? kMultiWarps : kDefaultWarps;
     int stages = kDefaultStages;
     tuning_override(&warps, &stages);
     if (stages < 1) stages = 1;
@@ -256,17 +278,18 @@ pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
     if (smem > kSmemLimit) return PA_ERR_SHAPE;
 
     SplitLaunch L{kind, D, block_size, NT, warps, 0, smem};
+    L.mq = q_start ? 1 : 0;
     int per_sm = 0;
     for (const OccKey& o : plan->occ) {
         if (o.kind == kind && o.D == D && o.BS == block_size && o.NT == NT && o.warps == warps &&
-            o.smem == smem)
+            o.smem == smem && o.mq == L.mq)
             per_sm = o.blocks_per_sm;
     }
     if (per_sm == 0) {
         cudaError_t e;
         per_sm = pa::split_blocks_per_sm(L, &e);
         if (e != cudaSuccess || per_sm < 1) return PA_ERR_CUDA;
-        plan->occ.push_back(OccKey{kind, D, block_size, NT, warps, smem, per_sm});
+        plan->occ.push_back(OccKey{kind, D, block_size, NT, warps, smem, per_sm, L.mq});
     }
     const int64_t need = (P_max + static_cast<int64_t>(warps) * kMinPagesPerWarp - 1) /
                          (static_cast<int64_t>(warps) * kMinPagesPerWarp);
@@ -343,18 +366,45 @@ pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
     a.lens_bytes = static_cast<int>(lens_bytes);
     a.dyn_permille = dyn_permille;
     a.dyn_pages = dyn_pages;
+    a.q_start = q_start;
+    a.nq = nq;
+    a.num_q = T;
 
     if (plan->ev_start) cudaEventRecord(plan->ev_start, stream);
     cudaError_t e = pa::launch_split(L, plan->kmap, plan->vmap, a, stream);
     if (plan->ev_stop) cudaEventRecord(plan->ev_stop, stream);
     if (e != cudaSuccess) return PA_ERR_CUDA;
     pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, GS, nslices, U, D, out_dtype == PA_BF16,
-                    dyn_permille > 0};
+                    dyn_permille > 0, (q_start ? T : B) * Hq, q_start};
     e = pa::launch_merge(m, stream);
     plan->last_path = path;
     plan->last_blocks = L.blocks;
     plan->last_warps = NW;
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
+                    const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int B,
+                    int Hq, int Hkv, int D, int block_size, int num_blocks, int max_seq_len,
+                    float scale, pa_dtype kv_dtype, void* out, pa_dtype out_dtype,
+                    pa_plan** plan_inout, struct CUstream_st* stream) {
+    return decode_impl(q, nullptr, B, 1, k_pool, v_pool, block_tables, max_blocks, seq_lens, B,
+                       Hq, Hkv, D, block_size, num_blocks, max_seq_len, scale, kv_dtype, out,
+                       out_dtype, plan_inout, stream);
+}
+
+pa_status pa_decode_multi(const void* q, const int32_t* q_start, int num_queries, int max_q,
+                          const void* k_pool, const void* v_pool, const int32_t* block_tables,
+                          int max_blocks, const int32_t* seq_lens, int B, int Hq, int Hkv, int D,
+                          int block_size, int num_blocks, int max_seq_len, float scale,
+                          pa_dtype kv_dtype, void* out, pa_dtype out_dtype, pa_plan** plan_inout,
+                          struct CUstream_st* stream) {
+    if (!q_start) return PA_ERR_NULL;
+    return decode_impl(q, q_start, num_queries, max_q, k_pool, v_pool, block_tables, max_blocks,
+                       seq_lens, B, Hq, Hkv, D, block_size, num_blocks, max_seq_len, scale, kv_dtype,
+                       out, out_dtype, plan_inout, stream);
 }
 
 pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* copy_src,

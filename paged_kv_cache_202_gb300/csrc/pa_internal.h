@@ -51,6 +51,12 @@ struct SplitArgs {
     int lens_bytes;            // bytes of the per-sequence arrays at the front of shared memory
     int dyn_permille;          // fraction of the page stream handed out dynamically (1/1000)
     int dyn_pages;             // pages per dynamic piece
+    // Several queries per sequence (speculative verification): q and out are
+    // [T][Hq][D] with sequence b's queries at rows q_start[b] .. q_start[b+1)
+    // (at most nq), the newest tokens of the sequence; null for one query.
+    const int32_t* q_start;
+    int nq;
+    int num_q;                 // T: rows of q and out
 };
 
 struct SplitLaunch {
@@ -59,6 +65,7 @@ struct SplitLaunch {
     int warps;     // warps per block
     int blocks;    // grid size
     size_t smem;   // dynamic shared memory bytes
+    int mq = 0;    // 1: several queries per sequence (tensor-core path only)
 };
 
 // Returns the resident blocks per SM of a split-kernel variant at the given
@@ -75,6 +82,8 @@ struct MergeArgs {
     int B, Hq, g, GS, nslices, U, D;
     int out_bf16;
     int wide;  // 1: several warps per row (many partials per row), 0: one warp per row
+    int rows;  // output rows: B * Hq, or T * Hq with several queries per sequence
+    const int32_t* q_start;  // several queries per sequence (see SplitArgs), else null
 };
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream);
 

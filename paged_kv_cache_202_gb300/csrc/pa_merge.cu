@@ -52,8 +52,23 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
         }
     };
     griddep_wait();  // the split kernel's partials and metadata
-    if (row >= a.B * a.Hq) return;
-    const int b = row / a.Hq, hq = row - b * a.Hq;
+    if (row >= a.rows) return;
+    // Row -> (sequence b, query head hq, column j of the kv unit's partials).
+    int b, hq, qcol = 0;
+    if (a.q_start) {  // several queries per sequence: row = t * Hq + hq
+        const int t = row / a.Hq;
+        hq = row - t * a.Hq;
+        int lo = 0, hi = a.B - 1;  // the sequence whose query rows hold t
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (a.q_start[mid] <= t) lo = mid; else hi = mid - 1;
+        }
+        b = lo;
+        qcol = (t - a.q_start[b]) * a.g;  // column of query (t - q_start[b]), head 0
+    } else {
+        b = row / a.Hq;
+        hq = row - b * a.Hq;
+    }
     const int* pre = a.ws_meta + kMetaHeader;
     const int per = a.ws_meta[1], NW = a.ws_meta[2], A = a.ws_meta[4], qd = a.ws_meta[5];
     if (row == 0 && threadIdx.x == 0) a.ws_meta[3] = 0;  // dynamic-piece counter, for the next call
@@ -87,7 +102,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
         return;
     }
     const int kvh = hq / a.g, hr = hq - kvh * a.g;
-    const int slice = hr / a.GS, j = hr - slice * a.GS;
+    const int slice = hr / a.GS, j = qcol + hr - slice * a.GS;
     const int u = kvh * a.nslices + slice;
     const int sb = a.U * pre[b] + u * nb;
     // Range of page x: static ranges of `per` pages up to A, then pieces of qd.
@@ -202,7 +217,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
 }  // namespace
 
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
-    const int rows = a.B * a.Hq;
+    const int rows = a.rows;
     if (rows == 0) return cudaSuccess;
     // Warps per row when dynamic pieces cut long segments into many partials
     // (tuning override PA_MERGE_WARPS = 2, 4 or 8); one warp per row otherwise.

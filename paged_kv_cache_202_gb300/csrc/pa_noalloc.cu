@@ -264,6 +264,6 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     a.dyn_pages = dyn_pages;
     if (pa::launch_split(L, kmap, vmap, a, stream) != cudaSuccess) return PA_ERR_CUDA;
     pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, GS, nslices, U, D, out_dtype == PA_BF16,
-                    dyn_permille > 0};
+                    dyn_permille > 0, B * Hq, nullptr};
     return pa::launch_merge(m, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }

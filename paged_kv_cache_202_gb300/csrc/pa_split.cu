@@ -18,11 +18,24 @@ __global__ void __launch_bounds__(256, 1)
     split_body<D, BS, MmaState<D, kChunkTokens, NT>>(&kmap, &vmap, a);
 }
 
+// Several queries per sequence (speculative verification) on the same tiles.
+template <int D, int BS, int NT>
+__global__ void __launch_bounds__(256, 1)
+    mma_mq_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
+                  const SplitArgs a) {
+    split_body<D, BS, MmaState<D, kChunkTokens, NT>, true>(&kmap, &vmap, a);
+}
+
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, SplitArgs);
 
 KernelFn select(const SplitLaunch& L) {
 #define PA_CASE(D_, BS_)                                                        \
     if (L.D == D_ && L.BS == BS_) {                                             \
+        if (L.mq) {                                                             \
+            if (L.kind == kSplitMma && L.NT == 1) return mma_mq_kernel<D_, BS_, 1>; \
+            if (L.kind == kSplitMma && L.NT == 2) return mma_mq_kernel<D_, BS_, 2>; \
+            return nullptr;                                                     \
+        }                                                                       \
         if (L.kind == kSplitFma) return fma_kernel<D_, BS_>;                    \
         if (L.kind == kSplitMma && L.NT == 1) return mma_kernel<D_, BS_, 1>;    \
         if (L.kind == kSplitMma && L.NT == 2) return mma_kernel<D_, BS_, 2>;    \

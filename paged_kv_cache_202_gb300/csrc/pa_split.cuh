@@ -68,10 +68,14 @@ __device__ __forceinline__ void advance(Cursor& c, const int* pre, int U, int B)
 
 // Block-wide: validate the lengths and build the page prefix sums pre[0..B]
 // and the attended lengths len[0..B) in shared memory. Invalid lengths count
-// as zero pages (their rows are written as zeros by the merge kernel).
+// as zero pages (their rows are written as zeros by the merge kernel). With
+// several queries per sequence (q_start != null), a sequence is also invalid
+// unless it has 1 .. nq queries, at least as many tokens, and its query rows
+// lie within the num_q rows of q and out.
 template <int BS>
 __device__ void scan_lengths(const int32_t* __restrict__ seq_lens, int B, int limit, int* pre,
-                             int* len, int* err) {
+                             int* len, int* err, const int32_t* q_start = nullptr, int nq = 0,
+                             int num_q = 0) {
     __shared__ int warp_tot[32];
     const int T = blockDim.x, tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5, nwarps = T >> 5;
@@ -81,7 +85,11 @@ __device__ void scan_lengths(const int32_t* __restrict__ seq_lens, int B, int li
     bool bad = false;
     for (int b = lo; b < hi; ++b) {
         const int L = seq_lens[b];
-        const bool ok = L >= 1 && L <= limit;
+        bool ok = L >= 1 && L <= limit;
+        if (q_start) {
+            const int nqb = q_start[b + 1] - q_start[b];
+            ok = ok && nqb >= 1 && nqb <= nq && nqb <= L && q_start[b] >= 0 && q_start[b + 1] <= num_q;
+        }
         bad |= !ok;
         len[b] = ok ? L : 0;
         sum += ok ? (L + BS - 1) / BS : 0;
@@ -282,8 +290,25 @@ struct MmaState {
         }
     }
 
+    // nv: tokens of this chunk before the end of the sequence. With MQ, column
+    // c of the tile is query c / g (of nqb, the newest tokens) and head c % g,
+    // and query i sees only the tokens before rem - (nqb - 1 - i), rem being
+    // the tokens from the chunk's start to the end of the sequence.
+    template <bool MQ = false>
     __device__ __forceinline__ void page(uint32_t kst, uint32_t vst, int nv, float scale_log2,
-                                         int lane) {
+                                         int lane, int rem = 0, int nqb = 0, int g = 1) {
+        int lim[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                if constexpr (MQ) {
+                    const int col = nt * 8 + 2 * (lane & 3) + j;
+                    lim[nt][j] = min(nv, rem - (nqb - 1 - col / g));
+                } else {
+                    lim[nt][j] = nv;
+                }
+            }
         float s[TILES][NT][4];
 #pragma unroll
         for (int t = 0; t < TILES; ++t)
@@ -319,7 +344,7 @@ struct MmaState {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int tk = tok + (i >= 2 ? 8 : 0);
-                    const float v = tk < nv ? s[t][nt][i] * scale_log2 : -INFINITY;
+                    const float v = tk < lim[nt][i & 1] ? s[t][nt][i] * scale_log2 : -INFINITY;
                     s[t][nt][i] = v;
                     mx[nt][i & 1] = fmaxf(mx[nt][i & 1], v);
                 }
@@ -413,8 +438,11 @@ struct MmaState {
         }
     }
 
+    // With MQ, column `head` is query head / g of the sequence (row qrow0 + it
+    // of out) and head hq0 + head % g; otherwise head hq0 + head of row b.
+    template <bool MQ = false>
     __device__ __forceinline__ void finish(const SplitArgs& a, int b, int hq0, int nh, bool full,
-                                           bool poison, int slot, int lane) {
+                                           bool poison, int slot, int lane, int qrow0 = 0) {
         float lt[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -435,7 +463,11 @@ struct MmaState {
                 if (head >= nh) continue;
                 if (full) {
                     const float inv = poison ? 0.f : 1.f / lt[nt][j];
-                    const size_t row = (static_cast<size_t>(b) * a.Hq + hq0 + head) * D;
+                    size_t row;
+                    if constexpr (MQ)
+                        row = ((static_cast<size_t>(qrow0) + head / a.g) * a.Hq + hq0 + head % a.g) * D;
+                    else
+                        row = (static_cast<size_t>(b) * a.Hq + hq0 + head) * D;
 #pragma unroll
                     for (int mt = 0; mt < KS; ++mt) {
 #pragma unroll
@@ -494,7 +526,7 @@ __device__ __forceinline__ int4 lds_v4i(uint32_t addr) {
     return v;
 }
 
-template <int D, int BS, typename State>
+template <int D, int BS, typename State, bool MQ = false>
 __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtensorMap* vmap,
                                            const SplitArgs& a) {
     constexpr int CT = kChunkTokens;
@@ -519,7 +551,10 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
     griddep_wait();
     griddep_launch_dependents();
     const int limit = min(a.max_seq_len, a.max_blocks * BS);
-    scan_lengths<BS>(a.seq_lens, a.B, limit, pre, len, a.err);
+    if constexpr (MQ)
+        scan_lengths<BS>(a.seq_lens, a.B, limit, pre, len, a.err, a.q_start, a.nq, a.num_q);
+    else
+        scan_lengths<BS>(a.seq_lens, a.B, limit, pre, len, a.err);
 
     const int P = a.U * pre[a.B];
     const int NW = gridDim.x * W;
@@ -610,7 +645,13 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
             const uint32_t stg = my_ring + static_cast<uint32_t>(s * a.stage_bytes);
             sts_v4i(my_meta + 16 * s, ri.x0, ri.x1, ri.id);  // released by the arrive below
             const int kvh = ci.u / a.nslices, slice = ci.u - kvh * a.nslices;
-            const int nh = min(a.GS, a.g - slice * a.GS);
+            int nh, qrow0 = 0;
+            if constexpr (MQ) {
+                qrow0 = a.q_start[ci.b];
+                nh = (a.q_start[ci.b + 1] - qrow0) * a.g;  // validated: 1 .. nq queries
+            } else {
+                nh = min(a.GS, a.g - slice * a.GS);
+            }
             const uint32_t qbytes = qstart ? static_cast<uint32_t>(nh * D * 2) : 0u;
             if (bad) {
                 atomicOr(a.err, kErrTable);
@@ -632,9 +673,18 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
                 }
             }
             if (qstart) {
-                const uint16_t* src =
-                    a.q + (static_cast<size_t>(ci.b) * a.Hq + kvh * a.g + slice * a.GS) * D;
-                bulk_load(stg + 2 * CT * D * 2, src, qbytes, bar);
+                if constexpr (MQ) {
+                    // Query i's g heads of this kv head: rows qrow0 + i of q.
+                    const uint32_t run = static_cast<uint32_t>(a.g * D * 2);
+                    for (int i = 0; i < nh / a.g; ++i) {
+                        const uint16_t* src = a.q + ((static_cast<size_t>(qrow0) + i) * a.Hq + kvh * a.g) * D;
+                        bulk_load(stg + 2 * CT * D * 2 + i * run, src, run, bar);
+                    }
+                } else {
+                    const uint16_t* src =
+                        a.q + (static_cast<size_t>(ci.b) * a.Hq + kvh * a.g + slice * a.GS) * D;
+                    bulk_load(stg + 2 * CT * D * 2, src, qbytes, bar);
+                }
             }
         }
         for (int j = 0; j < n; ++j) advance(ci, pre, a.U, a.B);
@@ -657,7 +707,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
     Range rc{-1, -1, -1};
     Cursor cc{0, 0, 0, 0};
     int xc = 0;
-    int p_first = 0, hq0 = 0, nh = 0;
+    int p_first = 0, hq0 = 0, nh = 0, qrow0 = 0, nqb = 0;
     bool poison = false;
     int s = 0, n_done = 0;
     while (n_done < n_issued) {
@@ -683,8 +733,15 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
         const int n = min(min(CP, cc.nb - cc.p), rc.x1 - xc);
         if (xc == rc.x0 || cc.p == 0) {
             const int kvh = cc.u / a.nslices, slice = cc.u - kvh * a.nslices;
-            nh = min(a.GS, a.g - slice * a.GS);
-            hq0 = kvh * a.g + slice * a.GS;
+            if constexpr (MQ) {
+                qrow0 = a.q_start[cc.b];
+                nqb = a.q_start[cc.b + 1] - qrow0;
+                nh = nqb * a.g;
+                hq0 = kvh * a.g;
+            } else {
+                nh = min(a.GS, a.g - slice * a.GS);
+                hq0 = kvh * a.g + slice * a.GS;
+            }
             st.start(stg + 2 * CT * D * 2, nh, lane);
             p_first = cc.p;
             poison = false;
@@ -692,8 +749,12 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
         if ((badmask >> s) & 1u) {
             poison = true;
         } else {
-            const int nv = min(n * BS, len[cc.b] - cc.p * BS);
-            st.page(stg, stg + CT * D * 2, nv, a.scale_log2, lane);
+            const int rem = len[cc.b] - cc.p * BS;  // tokens from the chunk start to the end
+            const int nv = min(n * BS, rem);
+            if constexpr (MQ)
+                st.template page<true>(stg, stg + CT * D * 2, nv, a.scale_log2, lane, rem, nqb, a.g);
+            else
+                st.page(stg, stg + CT * D * 2, nv, a.scale_log2, lane);
         }
         __syncwarp();
         if (!issue_done) {
@@ -705,7 +766,10 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
         if (p_last == cc.nb - 1 || xc + n == rc.x1) {
             const bool full = p_first == 0 && p_last == cc.nb - 1;
             const int slot = rc.id * 2 + (p_first > 0 ? 0 : 1);
-            st.finish(a, cc.b, hq0, nh, full, poison, slot, lane);
+            if constexpr (MQ)
+                st.template finish<true>(a, cc.b, hq0, nh, full, poison, slot, lane, qrow0);
+            else
+                st.finish(a, cc.b, hq0, nh, full, poison, slot, lane);
         }
         for (int j = 0; j < n; ++j) advance(cc, pre, a.U, a.B);
         xc += n;

@@ -29,6 +29,9 @@ name                  shape
 ``mixed_shared``      B=256, 32 q / 8 kv heads, D=128, bf16, block 16,
                       lengths geometric (mean 1024) clipped to [1, 8192];
                       even sequences share the same first 64 physical blocks
+``spec_gqa``          the ``llama3_8b_gqa`` batch (its own seed); the newest 4
+                      tokens of each sequence are queries (speculative
+                      verification of 4 drafted tokens)
 ====================  ====================================================
 
 Every workload is one decode step: the pools hold ``cache_len = L - 1``
@@ -48,7 +51,7 @@ import torch
 
 # numpy PCG64 seeds: 1000 + the workload's ordinal.
 _ORDINAL = {"tiny_worked_60": 1, "llama7b_mha": 2, "llama3_8b_gqa": 3, "long_splitk": 4,
-            "mixed_shared": 5, "prefill_gqa": 6}
+            "mixed_shared": 5, "prefill_gqa": 6, "spec_gqa": 7}
 
 CONFIGS = {
     "tiny_worked_60": dict(B=1, Hq=1, Hkv=1, D=64, block_size=16, dtype="f32",
@@ -68,6 +71,9 @@ CONFIGS = {
     "mixed_shared": dict(B=256, Hq=32, Hkv=8, D=128, block_size=16, dtype="bf16",
                          lengths=("geometric", 1.0 / 1024.0, 1, 8192), pool=("factor", 1.1),
                          max_len=8192, shared_prefix_blocks=64),
+    "spec_gqa": dict(B=64, Hq=32, Hkv=8, D=128, block_size=16, dtype="bf16",
+                     lengths=("loguniform", 512, 32768), pool=("factor", 1.1), max_len=32768,
+                     new_tokens=4),
 }
 
 

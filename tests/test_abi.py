@@ -79,6 +79,38 @@ def test_decode_empty_batch_is_a_no_op(lib):
     assert _decode(lib, B=0) == pa.PA_OK
 
 
+def _decode_multi(lib, **kw):
+    args = dict(q=ALIGNED, qs=ALIGNED, T=8, maxq=4, k=ALIGNED, v=ALIGNED, bt=ALIGNED, mb=4,
+                sl=ALIGNED, B=2, Hq=8, Hkv=2, D=128, bs=16, NB=64, maxlen=64, scale=0.1,
+                kvdt=pa.PA_BF16, out=ALIGNED, odt=pa.PA_BF16)
+    args.update(kw)
+    plan = ctypes.c_void_p(None)
+    st = lib.pa_decode_multi(args["q"], args["qs"], args["T"], args["maxq"], args["k"], args["v"],
+                             args["bt"], args["mb"], args["sl"], args["B"], args["Hq"], args["Hkv"],
+                             args["D"], args["bs"], args["NB"], args["maxlen"], args["scale"],
+                             args["kvdt"], args["out"], args["odt"], ctypes.byref(plan), None)
+    assert plan.value is None, "an argument error must not create a plan"
+    return st
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(qs=None), pa.PA_ERR_NULL),
+    (dict(q=None), pa.PA_ERR_NULL),
+    (dict(kvdt=pa.PA_F32), pa.PA_ERR_DTYPE),       # tensor-core tiles take bf16 pools
+    (dict(maxq=5), pa.PA_ERR_SHAPE),                # 5 queries x 4 heads > 16 columns
+    (dict(maxq=0), pa.PA_ERR_SHAPE),
+    (dict(T=-1), pa.PA_ERR_SHAPE),
+    (dict(q=ALIGNED + 8), pa.PA_ERR_ALIGN),
+])
+def test_decode_multi_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _decode_multi(lib, **kw) == status
+
+
+def test_decode_multi_without_queries_is_a_no_op(lib):
+    assert _decode_multi(lib, T=0) == pa.PA_OK
+    assert _decode_multi(lib, B=0) == pa.PA_OK
+
+
 def _append(lib, **kw):
     args = dict(kn=ALIGNED, vn=ALIGNED, k=ALIGNED, v=ALIGNED, bt=ALIGNED, mb=4, cl=ALIGNED, B=2,
                 Hkv=2, D=128, bs=16, NB=64, dt=pa.PA_BF16)
