@@ -199,7 +199,9 @@ pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
  *             pa_last_device_error(NULL, ...)): PA_DEVERR_* bits
  *
  * Supported: bf16 pools, D = 128, block_size 16 or 32, Hq / Hkv dividing 128,
- * max_blocks <= 16384. n_b < 1, n_b > L_b or L_b out of range raise
+ * max_blocks <= 16384. Built for many queries per sequence (chunked prefill);
+ * with a few (max_q * Hq / Hkv <= 16, e.g. speculative verification)
+ * pa_decode_multi computes the same rows at the decode's bandwidth. n_b < 1, n_b > L_b or L_b out of range raise
  * PA_DEVERR_SEQ_LEN and leave that sequence's rows untouched; a table entry
  * outside the pool raises PA_DEVERR_TABLE and zeroes the affected rows.
  */
