@@ -1,13 +1,14 @@
 /*
  * The C boundary used from C: one decode step (pa_append_kv, then pa_decode)
- * on device memory from cudaMalloc, with no Python or PyTorch involved,
- * checked against the fp64 oracle (linked from oracle/ as test
- * infrastructure). Inputs are deterministic (an integer hash), the pools hold
+ * and a verification step for the newest two tokens of every sequence
+ * (pa_decode_multi) on device memory from cudaMalloc, with no Python or
+ * PyTorch involved, checked against the fp64 oracle (linked from oracle/ as
+ * test infrastructure). Inputs are deterministic (an integer hash), the pools hold
  * NaN in every slot past each sequence, and the tables name a shuffled set of
  * physical blocks with -1 past each sequence.
  *
  * Exit status 0 when the appended pools match the oracle's bit for bit and
- * the attention output is within the bf16 tolerance (1.5e-2 absolute).
+ * both attention outputs are within the bf16 tolerance (1.5e-2 absolute).
  */
 #include <cuda_runtime.h>
 #include <math.h>
@@ -26,6 +27,10 @@ int oracle_decode(const void* q, const void* kpool, const void* vpool, const int
 int oracle_append(const void* k_new, const void* v_new, void* kpool, void* vpool,
                   const int32_t* table, int max_blocks, const int32_t* cache_lens, int B, int Hkv,
                   int D, int bs, int num_blocks, int elem_bytes);
+int oracle_prefill(const void* q, const void* kpool, const void* vpool, const int32_t* table,
+                   int max_blocks, const int32_t* seq_lens, const int32_t* q_start, int B, int Hq,
+                   int Hkv, int D, int bs, int num_blocks, float scale, int dtype, double* out,
+                   int nthreads);
 
 enum { B = 3, HQ = 8, HKV = 2, D = 128, BS = 16, MAXB = 20, SPARE = 5 };
 static const int kLens[B] = {1, 37, 300}; /* tokens after the append */
@@ -137,6 +142,28 @@ int main(void) {
     CHECK_CUDA(cudaMemcpy(kgot, dk, pool_elems * 2, cudaMemcpyDeviceToHost));
     CHECK_CUDA(cudaMemcpy(vgot, dv, pool_elems * 2, cudaMemcpyDeviceToHost));
     CHECK_CUDA(cudaMemcpy(out, dout, sizeof out, cudaMemcpyDeviceToHost));
+
+    /* Verification step: the newest min(2, L_b) tokens of each sequence. */
+    int32_t q_start[B + 1];
+    q_start[0] = 0;
+    for (int b = 0; b < B; ++b) q_start[b + 1] = q_start[b] + (kLens[b] < 2 ? kLens[b] : 2);
+    const int T = q_start[B];
+    uint16_t q2[2 * B * HQ * D];
+    for (int i = 0; i < T * HQ * D; ++i) q2[i] = bf16_of(0x60000000u + (uint32_t)i);
+    void *dq2, *dout2;
+    int32_t* dqs;
+    CHECK_CUDA(cudaMalloc(&dq2, (size_t)T * HQ * D * 2));
+    CHECK_CUDA(cudaMalloc(&dout2, (size_t)T * HQ * D * 2));
+    CHECK_CUDA(cudaMalloc((void**)&dqs, sizeof q_start));
+    CHECK_CUDA(cudaMemcpy(dq2, q2, (size_t)T * HQ * D * 2, cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemcpy(dqs, q_start, sizeof q_start, cudaMemcpyHostToDevice));
+    CHECK_PA(pa_decode_multi(dq2, dqs, T, 2, dk, dv, dtab, MAXB, dsl, B, HQ, HKV, D, BS, NB,
+                             MAXB * BS, scale, PA_BF16, dout2, PA_BF16, &plan, NULL));
+    CHECK_CUDA(cudaDeviceSynchronize());
+    int merr = -1;
+    CHECK_PA(pa_last_device_error(plan, &merr));
+    uint16_t out2[2 * B * HQ * D];
+    CHECK_CUDA(cudaMemcpy(out2, dout2, (size_t)T * HQ * D * 2, cudaMemcpyDeviceToHost));
     CHECK_PA(pa_free(plan));
 
     /* The oracle: append on the host pools, then fp64 attention. */
@@ -145,6 +172,10 @@ int main(void) {
     double ref[B * HQ * D];
     if (oracle_decode(q, kpool, vpool, table, MAXB, seq_lens, B, HQ, HKV, D, BS, NB, scale, 1, ref,
                       NULL, 0, 4) != 0)
+        return 4;
+    double ref2[2 * B * HQ * D];
+    if (oracle_prefill(q2, kpool, vpool, table, MAXB, seq_lens, q_start, B, HQ, HKV, D, BS, NB,
+                       scale, 1, ref2, 4) != 0)
         return 4;
     const int pools_equal = memcmp(kgot, kpool, pool_elems * 2) == 0 &&
                             memcmp(vgot, vpool, pool_elems * 2) == 0;
@@ -156,7 +187,17 @@ int main(void) {
         const double e = fabs(g - ref[i]);
         if (e > worst) worst = e;
     }
-    printf("device errors %d/%d, pools equal %d, finite %d, max abs error %.3e\n", derr, aerr,
-           pools_equal, finite, worst);
-    return (derr == 0 && aerr == 0 && pools_equal && finite && worst <= 1.5e-2) ? 0 : 1;
+    double worst2 = 0.0;
+    for (int i = 0; i < T * HQ * D; ++i) {
+        const double g = (double)f32_of_bf16(out2[i]);
+        finite &= isfinite(g) != 0;
+        const double e = fabs(g - ref2[i]);
+        if (e > worst2) worst2 = e;
+    }
+    printf("device errors %d/%d/%d, pools equal %d, finite %d, max abs error %.3e / %.3e\n", derr,
+           aerr, merr, pools_equal, finite, worst, worst2);
+    return (derr == 0 && aerr == 0 && merr == 0 && pools_equal && finite && worst <= 1.5e-2 &&
+            worst2 <= 1.5e-2)
+               ? 0
+               : 1;
 }
