@@ -366,7 +366,10 @@ struct MmaState {
             }
         }
         // Probabilities as a bf16 pair hi + lo (hi = bf16(p), lo = bf16(p - hi)),
-        // transposed in registers into the B operand of P V.
+        // transposed in registers into the B operand of P V. With MQ (twice
+        // the columns, so twice the products per page) only hi is used, as in
+        // the prefill kernel: 8 significant bits of p, well inside the bf16
+        // output's tolerance.
         uint32_t pb[TILES][NT][2][2];  // [tile][n-tile][hi/lo][token half]
         float ps[NT][2];
 #pragma unroll
@@ -385,12 +388,14 @@ struct MmaState {
                 ps[nt][1] += p[1] + p[3];
                 const uint32_t top = pack_bf16x2(p[0], p[1]);
                 const uint32_t bot = pack_bf16x2(p[2], p[3]);
-                const uint32_t top_lo = pack_bf16x2(p[0] - bf16_lo(top), p[1] - bf16_hi(top));
-                const uint32_t bot_lo = pack_bf16x2(p[2] - bf16_lo(bot), p[3] - bf16_hi(bot));
                 pb[t][nt][0][0] = movmatrix_trans(top);
                 pb[t][nt][0][1] = movmatrix_trans(bot);
-                pb[t][nt][1][0] = movmatrix_trans(top_lo);
-                pb[t][nt][1][1] = movmatrix_trans(bot_lo);
+                if constexpr (!MQ) {
+                    const uint32_t top_lo = pack_bf16x2(p[0] - bf16_lo(top), p[1] - bf16_hi(top));
+                    const uint32_t bot_lo = pack_bf16x2(p[2] - bf16_lo(bot), p[3] - bf16_hi(bot));
+                    pb[t][nt][1][0] = movmatrix_trans(top_lo);
+                    pb[t][nt][1][1] = movmatrix_trans(bot_lo);
+                }
             }
         }
         bool rescale = false;
@@ -432,7 +437,8 @@ struct MmaState {
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
                     mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, pb[t][nt][0][0], pb[t][nt][0][1]);
-                    mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, pb[t][nt][1][0], pb[t][nt][1][1]);
+                    if constexpr (!MQ)
+                        mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, pb[t][nt][1][0], pb[t][nt][1][1]);
                 }
             }
         }
