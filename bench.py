@@ -37,8 +37,8 @@ L2_BYTES = 126 * 2**20
 # DRAM traffic of the split-attention kernel from an ncu capture (per launch,
 # scaled to the full workload), valid only for the kernel sources it was
 # measured on (sha256 of the split kernel's source files).
-TRAFFIC = {"source_sha": "a9c9b2750ff691f5bc8d65fd6d788f86c4edc5e5e9ecdd8ad7e7ade6e4c0b341",
-           "workload": "llama3_8b_gqa", "bytes_per_launch": 2205528064 + 5833216}
+TRAFFIC = {"source_sha": "d4814fa4f71f1cfbd0c50196e28bdacc90a1a2ae084f53f59b21b3dbc2da9e34",
+           "workload": "llama3_8b_gqa", "bytes_per_launch": 2205587200 + 5779968}
 
 
 def split_source_sha() -> str:
