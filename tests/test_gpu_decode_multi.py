@@ -126,3 +126,29 @@ def test_speculative_workload_full_size_sampled_rows():
         assert np.isfinite(got[r]).all()
         worst = max(worst, float(np.abs(got[r] - ref[0]).max()))
     assert worst <= BF16_TOL, f"max abs error {worst:.3e}"
+
+
+def test_one_plan_alternates_decode_and_multi():
+    # The two calls need different workspace sizes (the multi-query tile is
+    # wider); a plan serves both in turn, growing its workspace once.
+    lens = [20000, 300, 17000, 64]
+    wl, q1, _ = _case(lens, [1] * len(lens), seed=6)
+    ns = [4, 2, 4, 3]
+    q = bf16_bits(np.random.default_rng(16).standard_normal((sum(ns), wl.Hq, wl.D)).astype(np.float32))
+    qs = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
+    ds = DeviceStep(wl)
+    want_multi, _ = _run(wl, q, qs, 4)
+    out1 = torch.empty((len(lens), wl.Hq, wl.D), dtype=torch.bfloat16, device="cuda")
+    with pa.Plan() as fresh:
+        pa.pa_decode(to_dev(q1, "bf16"), ds.k_pool, ds.v_pool, ds.tables, ds.seq_lens, wl.scale,
+                     out1, wl.max_seq_len, fresh)
+        torch.cuda.synchronize()
+    want_dec = out_f64(out1)
+    with pa.Plan() as plan:
+        for _ in range(2):
+            pa.pa_decode(to_dev(q1, "bf16"), ds.k_pool, ds.v_pool, ds.tables, ds.seq_lens, wl.scale,
+                         out1, wl.max_seq_len, plan)
+            torch.cuda.synchronize()
+            assert np.array_equal(out_f64(out1), want_dec)
+            got, err = _run(wl, q, qs, 4, plan=plan)
+            assert err == 0 and np.array_equal(got, want_multi)
