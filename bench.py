@@ -166,8 +166,8 @@ def _copy_appended(wl):
     return dataclasses.replace(wl, k_pool=kp, v_pool=vp)
 
 
-def oracle_sample_gbs(wl, budget_s: float, min_pairs: int = 1, appended: bool = False):
-    """Time the fp64 oracle on (b, h) pairs of the workload for about budget_s.
+def oracle_sample_gbs(wl, sample_s: float, min_pairs: int = 1, appended: bool = False):
+    """Time the fp64 oracle on (b, h) pairs of the workload for about sample_s.
 
     Returns (GB/s of algorithmic bytes, seconds, pairs, threads). The bytes of
     one (b, h) pair are sequence b's decode bytes divided by Hq.
@@ -182,10 +182,10 @@ def oracle_sample_gbs(wl, budget_s: float, min_pairs: int = 1, appended: bool = 
     per_seq = [pa.decode_bytes([int(L)], wl.Hq, wl.Hkv, wl.D, wl.block_size, eb, eb) / wl.Hq
                for L in wl.seq_lens]
     order = np.random.default_rng(0).permutation(wl.B * wl.Hq)
-    # Random rows, cycling through the whole workload until the budget is spent.
+    # Random rows, cycling through the whole workload until the time is spent.
     pairs, done_bytes, elapsed, i = 0, 0.0, 0.0, 0
     chunk = max(min_pairs, threads)
-    while elapsed < budget_s or pairs < min_pairs:
+    while elapsed < sample_s or pairs < min_pairs:
         if i >= order.size:
             i = 0
         sel = order[i:i + chunk]
@@ -424,7 +424,7 @@ def run_ours(args, rank, world, local_rank):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, el, pairs, threads = oracle_sample_gbs(wl, args.cpu_budget, appended=True)
+        gbs, el, pairs, threads = oracle_sample_gbs(wl, args.cpu_seconds, appended=True)
         cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
                "sample": f"{pairs} (sequence, q-head) rows ({pairs / (wl.B * wl.Hq):.1f} passes "
                          f"over the workload in random order), {el:.1f} s; bytes per row = its "
@@ -481,16 +481,16 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.destroy_process_group()
 
 
-def row_cpu_baseline(row, wl, budget_s, prefill_q=None, prefill_qs=None, prefill_ns=None):
+def row_cpu_baseline(row, wl, sample_s, prefill_q=None, prefill_qs=None, prefill_ns=None):
     """The oracle, as it stands, on a bounded random sample of the row's
-    workload on the host cores (about budget_s of CPU work)."""
+    workload on the host cores (about sample_s of CPU work)."""
     import oracle
     rng = np.random.default_rng(5)
     elapsed, units, n = 0.0, 0.0, 0
     if row in ("prefill", "spec"):
         threads = os.cpu_count() or 1
         T = int(prefill_qs[-1])
-        for r in np.tile(rng.permutation(T), max(1, 100000 // max(T, 1))):  # cycles until the budget
+        for r in np.tile(rng.permutation(T), max(1, 100000 // max(T, 1))):  # cycles until the time is spent
             b = int(np.searchsorted(prefill_qs, r, side="right") - 1)
             npos = int(wl.seq_lens[b] - prefill_ns[b] + (r - prefill_qs[b]) + 1)
             t = time.perf_counter()
@@ -502,7 +502,7 @@ def row_cpu_baseline(row, wl, budget_s, prefill_q=None, prefill_qs=None, prefill
             else:  # bytes: the sequence's K and V once, shared by its query rows
                 units += 2 * wl.Hkv * wl.D * wl.elem_bytes * int(wl.seq_lens[b]) / prefill_ns[b]
             n += 1
-            if elapsed >= budget_s:
+            if elapsed >= sample_s:
                 break
         scale, unit = (1e12, "TFLOP/s") if row == "prefill" else (1e9, "GB/s")
         return {"value": units / elapsed / scale, "unit": unit, "cores": threads,
@@ -514,7 +514,7 @@ def row_cpu_baseline(row, wl, budget_s, prefill_q=None, prefill_qs=None, prefill
         perm = rng.permutation(wl.num_blocks).astype(np.int32)
         half = wl.num_blocks // 2
         batch = 0
-        while elapsed < budget_s:
+        while elapsed < sample_s:
             k = batch % max(1, half // 64)
             batch += 1
             src, dst = perm[64 * k:64 * k + 64], perm[half + 64 * k:half + 64 * k + 64]
@@ -532,7 +532,7 @@ def row_cpu_baseline(row, wl, budget_s, prefill_q=None, prefill_qs=None, prefill
             elapsed += time.perf_counter() - t
             units += 2 * wl.Hkv * wl.D * eb * L
             n += 1
-            if elapsed >= budget_s:
+            if elapsed >= sample_s:
                 break
         what = f"{n} sequences one at a time, random order"
     return {"value": units / elapsed / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
@@ -652,7 +652,7 @@ def run_row(args, local_rank):
                 err = max(err, float(np.abs(got - sub[0]).max()))
             parity = {"rows": int(len(rows)), "max_abs_err": err, "tol": 1.5e-2}
         cpu = None if args.no_cpu_baseline else row_cpu_baseline(
-            args.row, wl, args.cpu_budget, prefill_q=qh, prefill_qs=qs, prefill_ns=ns)
+            args.row, wl, args.cpu_seconds, prefill_q=qh, prefill_qs=qs, prefill_ns=ns)
         print(json.dumps({
             "row": args.row,
             **({"metric": "prefill: achieved bf16 TFLOP/s", "value": tfs, "unit": "TFLOP/s"}
@@ -671,7 +671,7 @@ def run_row(args, local_rank):
             "cpu_baseline": cpu,
         }), flush=True)
         return
-    cpu = None if args.no_cpu_baseline else row_cpu_baseline(args.row, wl, args.cpu_budget)
+    cpu = None if args.no_cpu_baseline else row_cpu_baseline(args.row, wl, args.cpu_seconds)
     print(json.dumps({
         "row": args.row, "metric": f"{args.row}: achieved HBM GB/s", "value": gbs, "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -694,7 +694,7 @@ def main():
     ap.add_argument("--workload", default=None,
                     help="default: llama3_8b_gqa (prefill row: prefill_gqa)")
     ap.add_argument("--seed", type=int, default=None)
-    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
     ap.add_argument("--row", default="decode",
