@@ -135,7 +135,9 @@ pa_status pa_append_kv(const void* k_new, const void* v_new, void* k_pool, void*
  *   plan_inout    in/out: *plan_inout == NULL makes the library create a plan
  *                 (device workspace allocation, the only allocation); a plan
  *                 is reused by later calls and grows its workspace only when
- *                 a call needs more. Release it with pa_free.
+ *                 a call needs more. Release it with pa_free. A call that
+ *                 returns an argument error (PA_ERR_NULL, _SHAPE, _DTYPE,
+ *                 _BLOCK_SIZE, _ALIGN) creates no plan and launches nothing.
  *
  * Device-side violations (seq_len out of range, table entry outside the pool)
  * write zeros for the affected (b, h) rows and raise bits in the plan's error

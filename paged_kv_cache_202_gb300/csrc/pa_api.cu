@@ -196,6 +196,60 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     if (B == 0) return PA_OK;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
+    // Everything that depends on the arguments alone is checked before a plan
+    // exists, so that an argument error never creates one.
+    const int g = Hq / Hkv;
+    int path = q_start ? PA_PATH_MMA : (*plan_inout ? (*plan_inout)->forced_path : PA_PATH_AUTO);
+    if (path == PA_PATH_AUTO) {
+        path = kv_dtype == PA_F32 ? PA_PATH_SIMPLE : (g == 1 ? PA_PATH_FMA : PA_PATH_MMA);
+    }
+    if (kv_dtype == PA_F32 && path != PA_PATH_SIMPLE) return PA_ERR_DTYPE;
+    const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+
+    // Split paths (bf16 pools): kv units, tile width and block shape.
+    int nslices = 0, GS = 0, NT = 0, kind = 0, warps = 0, stages = 0;
+    int64_t max_pages = 0, P_max = 0;
+    size_t stage_bytes = 0, lens_bytes = 0, smem = 0;
+    if (path != PA_PATH_SIMPLE) {
+        if (path == PA_PATH_FMA) {
+            kind = pa::kSplitFma;
+            nslices = g;  // one query head per kv unit
+            GS = 1;
+        } else if (q_start) {
+            kind = pa::kSplitMma;
+            nslices = 1;  // one tile: nq queries x g heads of the kv head
+            GS = nq * g;
+            NT = (GS + 7) / 8;
+        } else {
+            kind = pa::kSplitMma;
+            nslices = (g + kHeadSlice - 1) / kHeadSlice;
+            GS = (g + nslices - 1) / nslices;
+            NT = (GS + 7) / 8;
+        }
+        max_pages = (static_cast<int64_t>(std::min(max_seq_len, max_blocks * block_size)) +
+                     block_size - 1) / block_size;
+        P_max = static_cast<int64_t>(B) * Hkv * nslices * max_pages;
+        if (P_max > INT32_MAX) return PA_ERR_SHAPE;
+
+        stage_bytes = round_up(2u * pa::kChunkTokens * D * 2u + static_cast<size_t>(GS) * D * 2u, 1024);
+        lens_bytes = round_up(static_cast<size_t>(2 * B + 1) * 4u, 1024);
+        // Many warps with one stage each: a warp waits for its chunk while the other
+        // warps of the SM compute, so bytes in flight scale with the warp count
+        // (3 warps per block, up to 4 blocks per SM at 32-token stages).
+        // With 9-16 (query, head) columns the multi-query kernel holds two
+        // n-tiles of state (~235 registers a thread), which limits an SM to two
+        // blocks: four warps each keep eight warps' stages in flight (measured
+        // 5.77 vs 4.96 TB/s with three on the speculative-verification workload).
+        warps = (q_start && NT == 2) ? kMultiWarps : kDefaultWarps;
+        stages = kDefaultStages;
+        tuning_override(&warps, &stages);
+        // ring, mbarriers (8 B each, padded to 16 B), per-stage range records (16 B each)
+        smem = 1024 + lens_bytes + static_cast<size_t>(warps) * stages * stage_bytes +
+               round_up(static_cast<size_t>(warps) * stages * 8, 16) +
+               static_cast<size_t>(warps) * stages * 16;
+        if (smem > kSmemLimit) return PA_ERR_SHAPE;
+    }
+
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
     pa_plan* plan = *plan_inout;
@@ -214,14 +268,6 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     }
     if (plan->device != dev) return PA_ERR_CUDA;  // a plan belongs to one device
 
-    const int g = Hq / Hkv;
-    int path = q_start ? PA_PATH_MMA : plan->forced_path;
-    if (path == PA_PATH_AUTO) {
-        path = kv_dtype == PA_F32 ? PA_PATH_SIMPLE : (g == 1 ? PA_PATH_FMA : PA_PATH_MMA);
-    }
-    if (kv_dtype == PA_F32 && path != PA_PATH_SIMPLE) return PA_ERR_DTYPE;
-    const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-
     if (path == PA_PATH_SIMPLE) {
         pa::SimpleArgs a{q, k_pool, v_pool, block_tables, seq_lens, out, plan->err,
                          B, Hq, Hkv, D, block_size, max_blocks, num_blocks, max_seq_len,
@@ -235,48 +281,7 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
         return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     }
 
-    // Split paths (bf16 pools).
-    int nslices, GS, NT = 0, kind;
-    if (path == PA_PATH_FMA) {
-        kind = pa::kSplitFma;
-        nslices = g;  // one query head per kv unit
-        GS = 1;
-    } else if (q_start) {
-        kind = pa::kSplitMma;
-        nslices = 1;  // one tile: nq queries x g heads of the kv head
-        GS = nq * g;
-        NT = (GS + 7) / 8;
-    } else {
-        kind = pa::kSplitMma;
-        nslices = (g + kHeadSlice - 1) / kHeadSlice;
-        GS = (g + nslices - 1) / nslices;
-        NT = (GS + 7) / 8;
-    }
     const int U = Hkv * nslices;
-    const int64_t max_pages = (static_cast<int64_t>(std::min(max_seq_len, max_blocks * block_size)) +
-                               block_size - 1) / block_size;
-    const int64_t P_max = static_cast<int64_t>(B) * U * max_pages;
-    if (P_max > INT32_MAX) return PA_ERR_SHAPE;
-
-    const size_t stage_bytes = round_up(2u * pa::kChunkTokens * D * 2u + static_cast<size_t>(GS) * D * 2u, 1024);
-    const size_t lens_bytes = round_up(static_cast<size_t>(2 * B + 1) * 4u, 1024);
-    // Many warps with one stage each: a warp waits for its chunk while the other
-    // warps of the SM compute, so bytes in flight scale with the warp count
-    // (3 warps per block, up to 4 blocks per SM at 32-token stages).
-    // With 9-16 (query, head) columns the multi-query kernel holds two
-    // n-tiles of state (~235 registers a thread), which limits an SM to two
-    // blocks: four warps each keep eight warps' stages in flight (measured
-    // 5.77 vs 4.96 TB/s with three on the speculative-verification workload).
-    int warps = (q_start && NT == 2) ? kMultiWarps : kDefaultWarps;
-    int stages = kDefaultStages;
-    tuning_override(&warps, &stages);
-    if (stages < 1) stages = 1;
-    // ring, mbarriers (8 B each, padded to 16 B), per-stage range records (16 B each)
-    const size_t smem = 1024 + lens_bytes + static_cast<size_t>(warps) * stages * stage_bytes +
-                        round_up(static_cast<size_t>(warps) * stages * 8, 16) +
-                        static_cast<size_t>(warps) * stages * 16;
-    if (smem > kSmemLimit) return PA_ERR_SHAPE;
-
     SplitLaunch L{kind, D, block_size, NT, warps, 0, smem};
     L.mq = q_start ? 1 : 0;
     int per_sm = 0;

@@ -75,6 +75,15 @@ def test_decode_rejects_bad_arguments_on_host(lib, kw, status):
     assert _decode(lib, **kw) == status
 
 
+def test_decode_late_shape_errors_create_no_plan(lib, monkeypatch):
+    # Rejected from the sizes alone, before any CUDA call: the page count
+    # over all (sequence, kv head) units overflows 32 bits ...
+    assert _decode(lib, B=8192, Hq=64, Hkv=64, mb=65536, maxlen=1 << 20) == pa.PA_ERR_SHAPE
+    # ... or a forced block shape needs more shared memory than a block has.
+    monkeypatch.setenv("PA_SPLIT_TUNING", "8,16")
+    assert _decode(lib) == pa.PA_ERR_SHAPE
+
+
 def test_decode_empty_batch_is_a_no_op(lib):
     assert _decode(lib, B=0) == pa.PA_OK
 
