@@ -17,7 +17,6 @@ namespace {
 
 using pa::SplitLaunch;
 
-constexpr size_t kSmemLimit = 232448;     // opt-in dynamic shared memory per block on sm_10x
 constexpr int kDefaultWarps = 3;           // warps per block of the split kernels
 constexpr int kMultiWarps = 4;             // ... with several queries per sequence
 constexpr int kDefaultStages = 1;          // pipeline stages per warp
@@ -25,7 +24,6 @@ constexpr int kDynPermille = 150;          // share of the page stream scheduled
 constexpr int kDynMinPages = 1024;         // ... when a sequence may have this many pages
 constexpr int kMinPagesPerWarp = 4;
 constexpr int kHeadSlice = 16;             // query heads per kv unit on the tensor-core path
-constexpr int kMaxBatch = 8192;            // per-sequence arrays live in shared memory
 
 struct MapKey {
     const void* ptr = nullptr;
@@ -56,22 +54,6 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
     });
     return fn;
-}
-
-// View a [NB][Hkv][BS][D] bf16 pool as a 3-D tensor (D, BS, NB*Hkv) whose
-// boxes are [64 columns][BS rows][1 page] with the 128-byte swizzle.
-bool encode_pool_map(CUtensorMap* map, const void* pool, int rows, int D, int BS) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(BS),
-                          static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(BS) * D * 2};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BS), 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides,
-                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS;
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -110,6 +92,103 @@ struct DeviceGuard {
 };
 
 }  // namespace
+
+namespace pa {
+
+bool encode_pool_map(CUtensorMap* map, const void* pool, int rows, int D, int BS) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(BS),
+                          static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(BS) * D * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BS), 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+bool split_shape(int kind, int nq, int B, int Hq, int Hkv, int D, int block_size, int max_blocks,
+                 int max_seq_len, bool tunable, SplitShape* out) {
+    SplitShape s;
+    const int g = Hq / Hkv;
+    s.kind = kind;
+    s.mq = nq > 0 ? 1 : 0;
+    if (kind == kSplitFma) {
+        s.nslices = g;  // one query head per kv unit
+        s.GS = 1;
+    } else if (s.mq) {
+        s.nslices = 1;  // one tile: nq queries x g heads of the kv head
+        s.GS = nq * g;
+        s.NT = (s.GS + 7) / 8;
+    } else {
+        s.nslices = (g + kHeadSlice - 1) / kHeadSlice;
+        s.GS = (g + s.nslices - 1) / s.nslices;
+        s.NT = (s.GS + 7) / 8;
+    }
+    s.U = Hkv * s.nslices;
+    s.max_pages = (static_cast<int64_t>(std::min(max_seq_len, max_blocks * block_size)) +
+                   block_size - 1) / block_size;
+    s.P_max = static_cast<int64_t>(B) * s.U * s.max_pages;
+    if (s.P_max > INT32_MAX) return false;
+
+    s.stage_bytes = round_up(2u * kChunkTokens * D * 2u + static_cast<size_t>(s.GS) * D * 2u, 1024);
+    s.lens_bytes = round_up(static_cast<size_t>(2 * B + 1) * 4u, 1024);
+    // Many warps with one stage each: a warp waits for its chunk while the other
+    // warps of the SM compute, so bytes in flight scale with the warp count
+    // (3 warps per block, up to 4 blocks per SM at 32-token stages).
+    // With 9-16 (query, head) columns the multi-query kernel holds two
+    // n-tiles of state (~235 registers a thread), which limits an SM to two
+    // blocks: four warps each keep eight warps' stages in flight (measured
+    // 5.77 vs 4.96 TB/s with three on the speculative-verification workload).
+    s.warps = (s.mq && s.NT == 2) ? kMultiWarps : kDefaultWarps;
+    s.stages = kDefaultStages;
+    if (tunable) tuning_override(&s.warps, &s.stages);
+    // ring, mbarriers (8 B each, padded to 16 B), per-stage range records (16 B each)
+    s.smem = 1024 + s.lens_bytes + static_cast<size_t>(s.warps) * s.stages * s.stage_bytes +
+             round_up(static_cast<size_t>(s.warps) * s.stages * 8, 16) +
+             static_cast<size_t>(s.warps) * s.stages * 16;
+    if (s.smem > kSmemLimit) return false;
+    *out = s;
+    return true;
+}
+
+SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int num_sms, int per_sm,
+                     bool tunable) {
+    SplitGrid gr;
+    const int64_t need = (s.P_max + static_cast<int64_t>(s.warps) * kMinPagesPerWarp - 1) /
+                         (static_cast<int64_t>(s.warps) * kMinPagesPerWarp);
+    gr.blocks = static_cast<int>(std::max<int64_t>(
+        1, std::min<int64_t>(need, static_cast<int64_t>(num_sms) * per_sm)));
+    gr.NW = gr.blocks * s.warps;
+    // Dynamic tail: dyn_permille of the page stream in pieces of 256 tokens,
+    // only when sequences can be long (many pages per segment): there the
+    // static split leaves an uneven finish; short segments balance already
+    // and would only pay for the wider merge.
+    gr.dyn_permille = s.max_pages >= kDynMinPages ? kDynPermille : 0;
+    gr.dyn_pages = 256 / block_size;
+    if (tunable) dynamic_override(&gr.dyn_permille, &gr.dyn_pages);
+    const int64_t max_pieces = s.P_max * gr.dyn_permille / 1000 / gr.dyn_pages + 1;
+    gr.ranges = static_cast<int64_t>(gr.NW) + max_pieces;
+    gr.meta_bytes = round_up(static_cast<size_t>(kMetaHeader + B + 1) * 4u, 256);
+    gr.ml_bytes = round_up(static_cast<size_t>(2) * gr.ranges * s.GS * 2 * 4u, 256);
+    gr.acc_bytes = round_up(static_cast<size_t>(2) * gr.ranges * s.GS * D * 4u, 256);
+    return gr;
+}
+
+void set_split_plan(SplitArgs* a, const SplitShape& s, const SplitGrid& gr) {
+    a->GS = s.GS;
+    a->nslices = s.nslices;
+    a->U = s.U;
+    a->stages = s.stages;
+    a->stage_bytes = static_cast<int>(s.stage_bytes);
+    a->lens_bytes = static_cast<int>(s.lens_bytes);
+    a->dyn_permille = gr.dyn_permille;
+    a->dyn_pages = gr.dyn_pages;
+}
+
+}  // namespace pa
 
 struct pa_plan {
     int device = -1;
@@ -179,7 +258,7 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
         return PA_ERR_DTYPE;
     if (block_size != 16 && block_size != 32) return PA_ERR_BLOCK_SIZE;
     if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (D != 64 && D != 128) || num_blocks < 1 ||
-        max_blocks < 1 || max_seq_len < 1 || !std::isfinite(scale) || B > kMaxBatch)
+        max_blocks < 1 || max_seq_len < 1 || !std::isfinite(scale) || B > pa::kMaxBatch)
         return PA_ERR_SHAPE;
     if (static_cast<int64_t>(num_blocks) * Hkv > INT32_MAX ||
         static_cast<int64_t>(max_blocks) * block_size > INT32_MAX)
@@ -205,50 +284,11 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     }
     if (kv_dtype == PA_F32 && path != PA_PATH_SIMPLE) return PA_ERR_DTYPE;
     const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-
-    // Split paths (bf16 pools): kv units, tile width and block shape.
-    int nslices = 0, GS = 0, NT = 0, kind = 0, warps = 0, stages = 0;
-    int64_t max_pages = 0, P_max = 0;
-    size_t stage_bytes = 0, lens_bytes = 0, smem = 0;
-    if (path != PA_PATH_SIMPLE) {
-        if (path == PA_PATH_FMA) {
-            kind = pa::kSplitFma;
-            nslices = g;  // one query head per kv unit
-            GS = 1;
-        } else if (q_start) {
-            kind = pa::kSplitMma;
-            nslices = 1;  // one tile: nq queries x g heads of the kv head
-            GS = nq * g;
-            NT = (GS + 7) / 8;
-        } else {
-            kind = pa::kSplitMma;
-            nslices = (g + kHeadSlice - 1) / kHeadSlice;
-            GS = (g + nslices - 1) / nslices;
-            NT = (GS + 7) / 8;
-        }
-        max_pages = (static_cast<int64_t>(std::min(max_seq_len, max_blocks * block_size)) +
-                     block_size - 1) / block_size;
-        P_max = static_cast<int64_t>(B) * Hkv * nslices * max_pages;
-        if (P_max > INT32_MAX) return PA_ERR_SHAPE;
-
-        stage_bytes = round_up(2u * pa::kChunkTokens * D * 2u + static_cast<size_t>(GS) * D * 2u, 1024);
-        lens_bytes = round_up(static_cast<size_t>(2 * B + 1) * 4u, 1024);
-        // Many warps with one stage each: a warp waits for its chunk while the other
-        // warps of the SM compute, so bytes in flight scale with the warp count
-        // (3 warps per block, up to 4 blocks per SM at 32-token stages).
-        // With 9-16 (query, head) columns the multi-query kernel holds two
-        // n-tiles of state (~235 registers a thread), which limits an SM to two
-        // blocks: four warps each keep eight warps' stages in flight (measured
-        // 5.77 vs 4.96 TB/s with three on the speculative-verification workload).
-        warps = (q_start && NT == 2) ? kMultiWarps : kDefaultWarps;
-        stages = kDefaultStages;
-        tuning_override(&warps, &stages);
-        // ring, mbarriers (8 B each, padded to 16 B), per-stage range records (16 B each)
-        smem = 1024 + lens_bytes + static_cast<size_t>(warps) * stages * stage_bytes +
-               round_up(static_cast<size_t>(warps) * stages * 8, 16) +
-               static_cast<size_t>(warps) * stages * 16;
-        if (smem > kSmemLimit) return PA_ERR_SHAPE;
-    }
+    pa::SplitShape sh;
+    if (path != PA_PATH_SIMPLE &&
+        !pa::split_shape(path == PA_PATH_FMA ? pa::kSplitFma : pa::kSplitMma, q_start ? nq : 0, B,
+                         Hq, Hkv, D, block_size, max_blocks, max_seq_len, true, &sh))
+        return PA_ERR_SHAPE;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return PA_ERR_CUDA;
@@ -281,40 +321,26 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
         return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     }
 
-    const int U = Hkv * nslices;
-    SplitLaunch L{kind, D, block_size, NT, warps, 0, smem};
-    L.mq = q_start ? 1 : 0;
+    // Split paths (bf16 pools).
+    SplitLaunch L{sh.kind, D, block_size, sh.NT, sh.warps, 0, sh.smem};
+    L.mq = sh.mq;
     int per_sm = 0;
     for (const OccKey& o : plan->occ) {
-        if (o.kind == kind && o.D == D && o.BS == block_size && o.NT == NT && o.warps == warps &&
-            o.smem == smem && o.mq == L.mq)
+        if (o.kind == L.kind && o.D == D && o.BS == block_size && o.NT == L.NT &&
+            o.warps == L.warps && o.smem == L.smem && o.mq == L.mq)
             per_sm = o.blocks_per_sm;
     }
     if (per_sm == 0) {
         cudaError_t e;
         per_sm = pa::split_blocks_per_sm(L, &e);
         if (e != cudaSuccess || per_sm < 1) return PA_ERR_CUDA;
-        plan->occ.push_back(OccKey{kind, D, block_size, NT, warps, smem, per_sm, L.mq});
+        plan->occ.push_back(OccKey{L.kind, D, block_size, L.NT, L.warps, L.smem, per_sm, L.mq});
     }
-    const int64_t need = (P_max + static_cast<int64_t>(warps) * kMinPagesPerWarp - 1) /
-                         (static_cast<int64_t>(warps) * kMinPagesPerWarp);
-    L.blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(need, static_cast<int64_t>(plan->num_sms) * per_sm)));
-    const int NW = L.blocks * warps;
-    // Dynamic tail: dyn_permille of the page stream in pieces of 256 tokens,
-    // only when sequences can be long (many pages per segment): there the
-    // static split leaves an uneven finish; short segments balance already
-    // and would only pay for the wider merge.
-    int dyn_permille = max_pages >= kDynMinPages ? kDynPermille : 0;
-    int dyn_pages = 256 / block_size;
-    dynamic_override(&dyn_permille, &dyn_pages);
-    const int64_t max_pieces = P_max * dyn_permille / 1000 / dyn_pages + 1;
-    const int64_t ranges = static_cast<int64_t>(NW) + max_pieces;
+    const pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size, plan->num_sms, per_sm, true);
+    L.blocks = gr.blocks;
 
     // Workspace: metadata, partial (m, l), partial value sums.
-    const size_t meta_bytes = round_up(static_cast<size_t>(pa::kMetaHeader + B + 1) * 4u, 256);
-    const size_t ml_bytes = round_up(static_cast<size_t>(2) * ranges * GS * 2 * 4u, 256);
-    const size_t acc_bytes = round_up(static_cast<size_t>(2) * ranges * GS * D * 4u, 256);
-    const size_t need_ws = meta_bytes + ml_bytes + acc_bytes;
+    const size_t need_ws = gr.workspace_bytes();
     if (plan->ws_bytes < need_ws) {
         if (plan->ws) cudaFree(plan->ws);
         plan->ws = nullptr;
@@ -325,20 +351,20 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     }
     char* ws = static_cast<char*>(plan->ws);
     int* meta = reinterpret_cast<int*>(ws);
-    float* ml = reinterpret_cast<float*>(ws + meta_bytes);
-    float* acc = reinterpret_cast<float*>(ws + meta_bytes + ml_bytes);
+    float* ml = reinterpret_cast<float*>(ws + gr.meta_bytes);
+    float* acc = reinterpret_cast<float*>(ws + gr.meta_bytes + gr.ml_bytes);
 
     const int rows = num_blocks * Hkv;
     MapKey kk{k_pool, rows, D, block_size}, vk{v_pool, rows, D, block_size};
     if (!(plan->kkey == kk)) {
-        if (!encode_pool_map(&plan->kmap, k_pool, rows, D, block_size)) {
+        if (!pa::encode_pool_map(&plan->kmap, k_pool, rows, D, block_size)) {
             plan->kkey = MapKey{};
             return PA_ERR_CUDA;
         }
         plan->kkey = kk;
     }
     if (!(plan->vkey == vk)) {
-        if (!encode_pool_map(&plan->vmap, v_pool, rows, D, block_size)) {
+        if (!pa::encode_pool_map(&plan->vmap, v_pool, rows, D, block_size)) {
             plan->vkey = MapKey{};
             return PA_ERR_CUDA;
         }
@@ -358,19 +384,12 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     a.Hq = Hq;
     a.Hkv = Hkv;
     a.g = g;
-    a.GS = GS;
-    a.nslices = nslices;
-    a.U = U;
     a.max_blocks = max_blocks;
     a.num_blocks = num_blocks;
     a.max_seq_len = max_seq_len;
     a.scale_log2 = scale_log2;
     a.out_bf16 = out_dtype == PA_BF16;
-    a.stages = stages;
-    a.stage_bytes = static_cast<int>(stage_bytes);
-    a.lens_bytes = static_cast<int>(lens_bytes);
-    a.dyn_permille = dyn_permille;
-    a.dyn_pages = dyn_pages;
+    pa::set_split_plan(&a, sh, gr);
     a.q_start = q_start;
     a.nq = nq;
     a.num_q = T;
@@ -379,12 +398,12 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     cudaError_t e = pa::launch_split(L, plan->kmap, plan->vmap, a, stream);
     if (plan->ev_stop) cudaEventRecord(plan->ev_stop, stream);
     if (e != cudaSuccess) return PA_ERR_CUDA;
-    pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, GS, nslices, U, D, out_dtype == PA_BF16,
-                    dyn_permille > 0, (q_start ? T : B) * Hq, q_start};
+    pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, sh.GS, sh.nslices, sh.U, D,
+                    out_dtype == PA_BF16, gr.dyn_permille > 0, (q_start ? T : B) * Hq, q_start};
     e = pa::launch_merge(m, stream);
     plan->last_path = path;
     plan->last_blocks = L.blocks;
-    plan->last_warps = NW;
+    plan->last_warps = gr.NW;
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -452,8 +471,8 @@ pa_status pa_prefill(const void* q, const int32_t* q_start, const void* k_pool,
         return PA_ERR_ALIGN;
     if (B == 0) return PA_OK;
     CUtensorMap kmap, vmap;
-    if (!encode_pool_map(&kmap, k_pool, num_blocks * Hkv, D, block_size) ||
-        !encode_pool_map(&vmap, v_pool, num_blocks * Hkv, D, block_size))
+    if (!pa::encode_pool_map(&kmap, k_pool, num_blocks * Hkv, D, block_size) ||
+        !pa::encode_pool_map(&vmap, v_pool, num_blocks * Hkv, D, block_size))
         return PA_ERR_CUDA;
     int* err = device_error;
     if (!err && pa::append_error_address(&err) != cudaSuccess) return PA_ERR_CUDA;

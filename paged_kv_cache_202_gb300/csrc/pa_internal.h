@@ -74,6 +74,46 @@ int split_blocks_per_sm(const SplitLaunch& L, cudaError_t* status);
 cudaError_t launch_split(const SplitLaunch& L, const CUtensorMap& kmap, const CUtensorMap& vmap,
                          const SplitArgs& a, cudaStream_t stream);
 
+// Host-side planning of a split launch, shared by pa_decode,
+// pa_decode_multi and pa_decode_noalloc.
+constexpr size_t kSmemLimit = 232448;  // opt-in dynamic shared memory per block on sm_10x
+constexpr int kMaxBatch = 8192;        // per-sequence arrays live in shared memory
+
+// Kv units, tile width and block shape, from the sizes alone.
+struct SplitShape {
+    int kind = 0, mq = 0;          // SplitKind; several queries per sequence
+    int nslices = 0, GS = 0, NT = 0, U = 0;
+    int warps = 0, stages = 0;
+    int64_t max_pages = 0;         // pages of the longest possible sequence
+    int64_t P_max = 0;             // pages over all (sequence, kv unit) segments, at most
+    size_t stage_bytes = 0, lens_bytes = 0, smem = 0;
+};
+// kind: kSplitFma (one query head per kv unit) or kSplitMma; nq > 0 selects
+// the multi-query tile (nq queries x g heads, tensor cores). tunable: honour
+// the PA_SPLIT_TUNING override of the block shape. Returns false when the
+// sizes do not fit (page count over 32 bits, shared memory over the limit).
+bool split_shape(int kind, int nq, int B, int Hq, int Hkv, int D, int block_size, int max_blocks,
+                 int max_seq_len, bool tunable, SplitShape* s);
+
+// Grid, dynamic tail and workspace carve-up at per_sm resident blocks.
+struct SplitGrid {
+    int blocks = 0, NW = 0;        // grid size, warps in the grid
+    int dyn_permille = 0, dyn_pages = 0;
+    int64_t ranges = 0;            // partial records: static ranges + dynamic pieces
+    size_t meta_bytes = 0, ml_bytes = 0, acc_bytes = 0;
+    size_t workspace_bytes() const { return meta_bytes + ml_bytes + acc_bytes; }
+};
+// tunable: honour the PA_SPLIT_DYNAMIC override of the dynamic tail.
+SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int num_sms, int per_sm,
+                     bool tunable);
+
+// Copies the planned fields (shape, grid, tail) into a.
+void set_split_plan(SplitArgs* a, const SplitShape& s, const SplitGrid& gr);
+
+// View a [NB][Hkv][BS][D] bf16 pool as a 3-D tensor (D, BS, rows = NB*Hkv)
+// whose boxes are [64 columns][BS rows][1 page] with the 128-byte swizzle.
+bool encode_pool_map(CUtensorMap* map, const void* pool, int rows, int D, int BS);
+
 struct MergeArgs {
     int* ws_meta;
     const float* ws_acc;

@@ -38,14 +38,6 @@ namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
 constexpr int kMaxDevices = 64;
-constexpr int kDefaultWarps = 3;
-constexpr int kDefaultStages = 1;
-constexpr int kDynPermille = 150;
-constexpr int kDynMinPages = 1024;
-constexpr size_t kSmemLimit = 232448;
-constexpr int kMinPagesPerWarp = 4;
-constexpr int kHeadSlice = 16;
-constexpr int kMaxBatch = 8192;
 
 }  // namespace
 
@@ -102,35 +94,6 @@ int blocks_per_sm(int dev, const pa::SplitLaunch& L, cudaError_t* status) {
     return n;
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-bool encode_pool(CUtensorMap* map, const void* pool, int rows, int D, int BS) {
-    auto fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(BS),
-                          static_cast<cuuint64_t>(rows)};
-    cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, static_cast<cuuint64_t>(BS) * D * 2};
-    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(BS), 1};
-    cuuint32_t estr[3] = {1, 1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(pool), dims, strides,
-              box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
-void dynamic_override(int*, int*) {}  // the no-alloc entry point always uses the default
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 }  // namespace
@@ -146,7 +109,7 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     if (kv_dtype != PA_BF16 || (out_dtype != PA_F32 && out_dtype != PA_BF16)) return PA_ERR_DTYPE;
     if (block_size != 16 && block_size != 32) return PA_ERR_BLOCK_SIZE;
     if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || (D != 64 && D != 128) || num_blocks < 1 ||
-        max_blocks < 1 || max_seq_len < 1 || !std::isfinite(scale) || B > kMaxBatch)
+        max_blocks < 1 || max_seq_len < 1 || !std::isfinite(scale) || B > pa::kMaxBatch)
         return PA_ERR_SHAPE;
     if (static_cast<int64_t>(num_blocks) * Hkv > INT32_MAX ||
         static_cast<int64_t>(max_blocks) * block_size > INT32_MAX)
@@ -156,6 +119,15 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     if (B == 0) return PA_OK;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
+    // Same planning as pa_decode's automatic choice (one query head per kv
+    // unit when the group has one head, tensor-core tiles otherwise), at the
+    // default block shape and dynamic tail.
+    const int g = Hq / Hkv;
+    pa::SplitShape sh;
+    if (!pa::split_shape(g == 1 ? pa::kSplitFma : pa::kSplitMma, 0, B, Hq, Hkv, D, block_size,
+                         max_blocks, max_seq_len, false, &sh))
+        return PA_ERR_SHAPE;
+
     int dev = 0, num_sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -164,65 +136,20 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     char* scratch = static_cast<char*>(scratch_address(dev, &st));
     if (!scratch) return PA_ERR_CUDA;
 
-    // Same planning as pa_decode's automatic choice: one query head per kv
-    // unit when the group has one head, tensor-core tiles otherwise.
-    const int g = Hq / Hkv;
-    int kind, nslices, GS, NT = 0;
-    if (g == 1) {
-        kind = pa::kSplitFma;
-        nslices = 1;
-        GS = 1;
-    } else {
-        kind = pa::kSplitMma;
-        nslices = (g + kHeadSlice - 1) / kHeadSlice;
-        GS = (g + nslices - 1) / nslices;
-        NT = (GS + 7) / 8;
-    }
-    const int U = Hkv * nslices;
-    const int64_t max_pages =
-        (static_cast<int64_t>(std::min(max_seq_len, max_blocks * block_size)) + block_size - 1) /
-        block_size;
-    const int64_t P_max = static_cast<int64_t>(B) * U * max_pages;
-    if (P_max > INT32_MAX) return PA_ERR_SHAPE;
-    const size_t stage_bytes =
-        round_up(2u * pa::kChunkTokens * D * 2u + static_cast<size_t>(GS) * D * 2u, 1024);
-    const size_t lens_bytes = round_up(static_cast<size_t>(2 * B + 1) * 4u, 1024);
-    const int warps = kDefaultWarps;
-    const int stages = kDefaultStages;
-    // ring, mbarriers (8 B each, padded to 16 B), per-stage range records (16 B each)
-    const size_t smem = 1024 + lens_bytes + static_cast<size_t>(warps) * stages * stage_bytes +
-                        round_up(static_cast<size_t>(warps) * stages * 8, 16) +
-                        static_cast<size_t>(warps) * stages * 16;
-    if (smem > kSmemLimit) return PA_ERR_SHAPE;
-    pa::SplitLaunch L{kind, D, block_size, NT, warps, 0, smem};
+    pa::SplitLaunch L{sh.kind, D, block_size, sh.NT, sh.warps, 0, sh.smem};
     const int per_sm = blocks_per_sm(dev, L, &st);
     if (st != cudaSuccess || per_sm < 1) return PA_ERR_CUDA;
-    const int64_t need = (P_max + static_cast<int64_t>(warps) * kMinPagesPerWarp - 1) /
-                         (static_cast<int64_t>(warps) * kMinPagesPerWarp);
-    L.blocks = static_cast<int>(
-        std::max<int64_t>(1, std::min<int64_t>(need, static_cast<int64_t>(num_sms) * per_sm)));
-    const int NW = L.blocks * warps;
-    // Dynamic tail: dyn_permille of the page stream in pieces of 256 tokens,
-    // only when sequences can be long (many pages per segment): there the
-    // static split leaves an uneven finish; short segments balance already
-    // and would only pay for the wider merge.
-    int dyn_permille = max_pages >= kDynMinPages ? kDynPermille : 0;
-    int dyn_pages = 256 / block_size;
-    dynamic_override(&dyn_permille, &dyn_pages);
-    const int64_t max_pieces = P_max * dyn_permille / 1000 / dyn_pages + 1;
-    const int64_t ranges = static_cast<int64_t>(NW) + max_pieces;
+    const pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size, num_sms, per_sm, false);
+    L.blocks = gr.blocks;
 
-    // Scratch layout: fallback error word, metadata, partial (m, l), partial sums.
+    // Scratch layout: fallback error word, then the workspace (metadata,
+    // partial (m, l), partial sums).
     const size_t err_bytes = 256;
-    const size_t meta_bytes = round_up(static_cast<size_t>(pa::kMetaHeader + B + 1) * 4u, 256);
-    const size_t ml_bytes = round_up(static_cast<size_t>(2) * ranges * GS * 2 * 4u, 256);
-    const size_t acc_bytes = round_up(static_cast<size_t>(2) * ranges * GS * D * 4u, 256);
-    if (err_bytes + meta_bytes + ml_bytes + acc_bytes > kNoAllocScratchBytes)
-        return PA_ERR_WORKSPACE;
+    if (err_bytes + gr.workspace_bytes() > kNoAllocScratchBytes) return PA_ERR_WORKSPACE;
     int* err = reinterpret_cast<int*>(scratch);
     int* meta = reinterpret_cast<int*>(scratch + err_bytes);
-    float* ml = reinterpret_cast<float*>(scratch + err_bytes + meta_bytes);
-    float* acc = reinterpret_cast<float*>(scratch + err_bytes + meta_bytes + ml_bytes);
+    float* ml = reinterpret_cast<float*>(scratch + err_bytes + gr.meta_bytes);
+    float* acc = reinterpret_cast<float*>(scratch + err_bytes + gr.meta_bytes + gr.ml_bytes);
     if (!device_error) {
         if (cudaMemsetAsync(err, 0, sizeof(int), stream) != cudaSuccess) return PA_ERR_CUDA;
         device_error = err;
@@ -232,8 +159,8 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
 
     CUtensorMap kmap, vmap;
     const int rows = num_blocks * Hkv;
-    if (!encode_pool(&kmap, k_pool, rows, D, block_size) ||
-        !encode_pool(&vmap, v_pool, rows, D, block_size))
+    if (!pa::encode_pool_map(&kmap, k_pool, rows, D, block_size) ||
+        !pa::encode_pool_map(&vmap, v_pool, rows, D, block_size))
         return PA_ERR_CUDA;
 
     pa::SplitArgs a{};
@@ -249,21 +176,14 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     a.Hq = Hq;
     a.Hkv = Hkv;
     a.g = g;
-    a.GS = GS;
-    a.nslices = nslices;
-    a.U = U;
     a.max_blocks = max_blocks;
     a.num_blocks = num_blocks;
     a.max_seq_len = max_seq_len;
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     a.out_bf16 = out_dtype == PA_BF16;
-    a.stages = stages;
-    a.stage_bytes = static_cast<int>(stage_bytes);
-    a.lens_bytes = static_cast<int>(lens_bytes);
-    a.dyn_permille = dyn_permille;
-    a.dyn_pages = dyn_pages;
+    pa::set_split_plan(&a, sh, gr);
     if (pa::launch_split(L, kmap, vmap, a, stream) != cudaSuccess) return PA_ERR_CUDA;
-    pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, GS, nslices, U, D, out_dtype == PA_BF16,
-                    dyn_permille > 0, B * Hq, nullptr};
+    pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, sh.GS, sh.nslices, sh.U, D,
+                    out_dtype == PA_BF16, gr.dyn_permille > 0, B * Hq, nullptr};
     return pa::launch_merge(m, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
