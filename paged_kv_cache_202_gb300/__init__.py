@@ -129,6 +129,42 @@ def _ptr(t: torch.Tensor) -> int:
     return t.data_ptr()
 
 
+def _on_one_device(*ts) -> None:
+    """Every tensor the kernels read or write is CUDA memory of one device."""
+    dev = None
+    for t in ts:
+        if t is None:
+            continue
+        if not t.is_cuda:
+            raise ValueError("tensors must be on a CUDA device")
+        if dev is None:
+            dev = t.device
+        elif t.device != dev:
+            raise ValueError(f"tensors on {dev} and {t.device}: all must be on one device")
+
+
+def _expect(t: torch.Tensor, name: str, shape: tuple, dtype: torch.dtype | None = None) -> None:
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} is {t.dtype}, expected {dtype}")
+
+
+def _pools(k_pool: torch.Tensor, v_pool: torch.Tensor) -> tuple[int, int, int, int]:
+    if k_pool.dim() != 4:
+        raise ValueError("pools are [num_blocks, Hkv, block_size, D]")
+    _expect(v_pool, "v_pool", tuple(k_pool.shape), k_pool.dtype)
+    return tuple(k_pool.shape)
+
+
+def _error_word(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    if t.dtype != torch.int32 or t.numel() < 1:
+        raise TypeError("device_error must be an int32 tensor of at least one element")
+    return _ptr(t)
+
+
 def _stream(stream) -> int:
     if stream is None:
         return torch.cuda.current_stream().cuda_stream
@@ -170,12 +206,30 @@ class Plan:
         self.free()
 
 
+def _check_decode(q, k_pool, v_pool, block_tables, seq_lens, out, B: int) -> None:
+    """Devices, dtypes and shapes shared by the attention calls (q and out
+    have the same [rows, Hq, D] shape; q has the pools' element type)."""
+    _on_one_device(q, k_pool, v_pool, block_tables, seq_lens, out)
+    if q.dim() != 3:
+        raise ValueError("q is [rows, Hq, D]")
+    if q.dtype != k_pool.dtype:
+        raise TypeError(f"q is {q.dtype}, the pools are {k_pool.dtype}")
+    _expect(out, "out", tuple(q.shape))
+    _expect(block_tables, "block_tables", (B, block_tables.shape[-1]), torch.int32)
+    _expect(seq_lens, "seq_lens", (B,), torch.int32)
+
+
 def pa_append_kv(k_new: torch.Tensor, v_new: torch.Tensor, k_pool: torch.Tensor,
                  v_pool: torch.Tensor, block_tables: torch.Tensor, cache_lens: torch.Tensor,
                  stream=None) -> None:
     """Write each sequence's new K/V token into its tail block (in place)."""
-    NB, Hkv, bs, D = k_pool.shape
+    NB, Hkv, bs, D = _pools(k_pool, v_pool)
     B = cache_lens.shape[0]
+    _on_one_device(k_new, v_new, k_pool, v_pool, block_tables, cache_lens)
+    _expect(k_new, "k_new", (B, Hkv, D), k_pool.dtype)
+    _expect(v_new, "v_new", (B, Hkv, D), k_pool.dtype)
+    _expect(cache_lens, "cache_lens", (B,), torch.int32)
+    _expect(block_tables, "block_tables", (B, block_tables.shape[-1]), torch.int32)
     st = lib().pa_append_kv(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
                             _ptr(block_tables), block_tables.shape[1], _ptr(cache_lens), B, Hkv,
                             D, bs, NB, _dtype(k_pool), _stream(stream))
@@ -187,7 +241,8 @@ def pa_decode(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
               out: torch.Tensor, max_seq_len: int, plan: Plan, stream=None) -> torch.Tensor:
     """Paged decode attention into ``out``; returns ``out``."""
     B, Hq, D = q.shape
-    NB, Hkv, bs, _ = k_pool.shape
+    NB, Hkv, bs, _ = _pools(k_pool, v_pool)
+    _check_decode(q, k_pool, v_pool, block_tables, seq_lens, out, B)
     st = lib().pa_decode(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
                          block_tables.shape[1], _ptr(seq_lens), B, Hq, Hkv, D, bs, NB,
                          int(max_seq_len), float(scale), _dtype(k_pool), _ptr(out), _dtype(out),
@@ -207,8 +262,11 @@ def pa_decode_multi(q: torch.Tensor, q_start: torch.Tensor, k_pool: torch.Tensor
     device int32 tensor of B + 1 entries and ``max_q`` bounds every count.
     """
     T, Hq, D = q.shape
-    NB, Hkv, bs, _ = k_pool.shape
+    NB, Hkv, bs, _ = _pools(k_pool, v_pool)
     B = seq_lens.shape[0]
+    _check_decode(q, k_pool, v_pool, block_tables, seq_lens, out, B)
+    _on_one_device(q, q_start)
+    _expect(q_start, "q_start", (B + 1,), torch.int32)
     st = lib().pa_decode_multi(_ptr(q), _ptr(q_start), T, int(max_q), _ptr(k_pool), _ptr(v_pool),
                                _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, Hq,
                                Hkv, D, bs, NB, int(max_seq_len), float(scale), _dtype(k_pool),
@@ -227,8 +285,10 @@ def pa_decode_noalloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
     given, is an int32 device tensor of one element that receives error bits.
     """
     B, Hq, D = q.shape
-    NB, Hkv, bs, _ = k_pool.shape
-    err = _ptr(device_error) if device_error is not None else None
+    NB, Hkv, bs, _ = _pools(k_pool, v_pool)
+    _check_decode(q, k_pool, v_pool, block_tables, seq_lens, out, B)
+    _on_one_device(q, device_error)
+    err = _error_word(device_error)
     st = lib().pa_decode_noalloc(_ptr(q), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
                                  block_tables.shape[1], _ptr(seq_lens), B, Hq, Hkv, D, bs, NB,
                                  int(max_seq_len), float(scale), _dtype(k_pool), _ptr(out),
@@ -240,10 +300,11 @@ def pa_decode_noalloc(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tenso
 def pa_copy_blocks(k_pool: torch.Tensor, v_pool: torch.Tensor, copy_src: torch.Tensor,
                    copy_dst: torch.Tensor, stream=None) -> None:
     """Copy whole blocks copy_src[i] -> copy_dst[i] of both pools (int32 device tensors)."""
-    NB, Hkv, bs, D = k_pool.shape
+    NB, Hkv, bs, D = _pools(k_pool, v_pool)
     n = copy_src.numel()
-    if copy_dst.numel() != n:
-        raise ValueError("copy_src and copy_dst differ in length")
+    _on_one_device(k_pool, v_pool, copy_src, copy_dst)
+    _expect(copy_src, "copy_src", (n,), torch.int32)
+    _expect(copy_dst, "copy_dst", (n,), torch.int32)
     st = lib().pa_copy_blocks(_ptr(k_pool), _ptr(v_pool), _ptr(copy_src) if n else None,
                               _ptr(copy_dst) if n else None, n, Hkv, D, bs, NB, _dtype(k_pool),
                               _stream(stream))
@@ -256,9 +317,12 @@ def pa_prefill(q: torch.Tensor, q_start: torch.Tensor, k_pool: torch.Tensor,
                device_error: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Causal paged multi-query attention (bf16 pools, D = 128); returns ``out``."""
     T, Hq, D = q.shape
-    NB, Hkv, bs, _ = k_pool.shape
+    NB, Hkv, bs, _ = _pools(k_pool, v_pool)
     B, MB = block_tables.shape
-    err = _ptr(device_error) if device_error is not None else None
+    _check_decode(q, k_pool, v_pool, block_tables, seq_lens, out, B)
+    _on_one_device(q, q_start, device_error)
+    _expect(q_start, "q_start", (B + 1,), torch.int32)
+    err = _error_word(device_error)
     st = lib().pa_prefill(_ptr(q), _ptr(q_start), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
                           MB, _ptr(seq_lens), B, Hq, Hkv, D, bs, NB, int(max_q),
                           int(max_seq_len), float(scale), _dtype(k_pool), _ptr(out), _dtype(out),
@@ -272,9 +336,14 @@ def pa_page_scores(k_pool: torch.Tensor, v_pool: torch.Tensor, block_tables: tor
                    victims: torch.Tensor, device_error: torch.Tensor | None = None,
                    stream=None) -> None:
     """PagedEviction page scores (float32 [B, max_blocks]) and victims (int32 [B])."""
-    NB, Hkv, bs, D = k_pool.shape
+    NB, Hkv, bs, D = _pools(k_pool, v_pool)
     B, MB = block_tables.shape
-    err = _ptr(device_error) if device_error is not None else None
+    _on_one_device(k_pool, v_pool, block_tables, seq_lens, scores, victims, device_error)
+    _expect(block_tables, "block_tables", (B, MB), torch.int32)
+    _expect(seq_lens, "seq_lens", (B,), torch.int32)
+    _expect(scores, "scores", (B, MB), torch.float32)
+    _expect(victims, "victims", (B,), torch.int32)
+    err = _error_word(device_error)
     st = lib().pa_page_scores(_ptr(k_pool), _ptr(v_pool), _ptr(block_tables), MB, _ptr(seq_lens),
                               B, Hkv, D, bs, NB, int(max_seq_len), _dtype(k_pool), _ptr(scores),
                               _ptr(victims), err, _stream(stream))

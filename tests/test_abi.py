@@ -171,3 +171,36 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(pa, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="missing"):
         pa.lib()
+
+
+def _host_tensors(B=2, Hq=8, Hkv=2, D=128, bs=16, NB=16, MB=4):
+    import torch
+    bf = torch.bfloat16
+    return dict(q=torch.zeros(B, Hq, D, dtype=bf), k=torch.zeros(NB, Hkv, bs, D, dtype=bf),
+                v=torch.zeros(NB, Hkv, bs, D, dtype=bf),
+                bt=torch.zeros(B, MB, dtype=torch.int32), sl=torch.ones(B, dtype=torch.int32),
+                qs=torch.arange(B + 1, dtype=torch.int32), out=torch.zeros(B, Hq, D, dtype=bf),
+                kn=torch.zeros(B, Hkv, D, dtype=bf), sc=torch.zeros(B, MB),
+                vic=torch.zeros(B, dtype=torch.int32))
+
+
+def test_binding_rejects_host_tensors():
+    # A host pointer must never reach a kernel: every entry point refuses
+    # tensors that are not CUDA memory before it calls the library.
+    t = _host_tensors()
+    plan = pa.Plan()
+    calls = [
+        lambda: pa.pa_decode(t["q"], t["k"], t["v"], t["bt"], t["sl"], 0.1, t["out"], 64, plan),
+        lambda: pa.pa_decode_multi(t["q"], t["qs"], t["k"], t["v"], t["bt"], t["sl"], 0.1,
+                                   t["out"], 1, 64, plan),
+        lambda: pa.pa_decode_noalloc(t["q"], t["k"], t["v"], t["bt"], t["sl"], 0.1, t["out"], 64),
+        lambda: pa.pa_append_kv(t["kn"], t["kn"], t["k"], t["v"], t["bt"], t["sl"]),
+        lambda: pa.pa_prefill(t["q"], t["qs"], t["k"], t["v"], t["bt"], t["sl"], 0.1, t["out"],
+                              1, 64),
+        lambda: pa.pa_page_scores(t["k"], t["v"], t["bt"], t["sl"], 64, t["sc"], t["vic"]),
+        lambda: pa.pa_copy_blocks(t["k"], t["v"], t["vic"], t["vic"]),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError, match="CUDA device"):
+            call()
+    assert plan.handle.value is None
