@@ -70,8 +70,11 @@ def _load():
     global _lib
     if _lib is not None:
         return _lib
-    build()
-    lib = ctypes.CDLL(_LIB_PATH)
+    # ORACLE_LIB names another build of oracle.cpp to load instead; the
+    # mutation test points it at deliberately broken copies to show that the
+    # pins catch them.
+    path = os.environ.get("ORACLE_LIB") or build()
+    lib = ctypes.CDLL(path)
     vp, i32p, f64p = ctypes.c_void_p, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_double)
     ci, cf, ci64 = ctypes.c_int, ctypes.c_float, ctypes.c_int64
     lib.oracle_num_blocks.argtypes = [ci64, ci64]
