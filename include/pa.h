@@ -354,9 +354,11 @@ pa_status pa_page_scores(const void* k_pool, const void* v_pool, const int32_t* 
  *                 (the caller clears it); NULL = errors are not reported.
  *
  * Limits and rules:
- *   - a call whose partials need more than 16 MiB (about 2 x warps x query
- *     heads per kv unit x D x 4 bytes: with 16 query heads per kv head at
- *     D = 128, a plan of more than about 1020 warps) returns
+ *   - when the partials of pa_decode's dynamic tail would not fit in the
+ *     array, the call runs on static ranges alone (one partial pair per
+ *     warp); a call whose partials need more than 16 MiB even then (about
+ *     2 x warps x query heads per kv unit x D x 4 bytes: with 16 query heads
+ *     per kv head at D = 128, a plan of more than about 1020 warps) returns
  *     PA_ERR_WORKSPACE and launches nothing;
  *   - every call shares the array and it keeps the last call's contents;
  *     calls whose work overlaps on the GPU (unordered streams) race on it and

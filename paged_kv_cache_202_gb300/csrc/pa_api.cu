@@ -22,6 +22,8 @@ constexpr int kMultiWarps = 4;             // ... with several queries per seque
 constexpr int kDefaultStages = 1;          // pipeline stages per warp
 constexpr int kDynPermille = 150;          // share of the page stream scheduled dynamically
 constexpr int kDynMinPages = 1024;         // ... when a sequence may have this many pages
+constexpr int kDynShortPermille = 500;     // ... on the one-head path with shorter sequences
+constexpr int kMergeRowsPerSm = 16;        // rows one SM merges at once with 4 warps per row
 constexpr int kMinPagesPerWarp = 4;
 constexpr int kHeadSlice = 16;             // query heads per kv unit on the tensor-core path
 
@@ -155,20 +157,39 @@ bool split_shape(int kind, int nq, int B, int Hq, int Hkv, int D, int block_size
 }
 
 SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int num_sms, int per_sm,
-                     bool tunable) {
+                     bool tunable, bool dynamic) {
     SplitGrid gr;
     const int64_t need = (s.P_max + static_cast<int64_t>(s.warps) * kMinPagesPerWarp - 1) /
                          (static_cast<int64_t>(s.warps) * kMinPagesPerWarp);
     gr.blocks = static_cast<int>(std::max<int64_t>(
         1, std::min<int64_t>(need, static_cast<int64_t>(num_sms) * per_sm)));
     gr.NW = gr.blocks * s.warps;
-    // Dynamic tail: dyn_permille of the page stream in pieces of 256 tokens,
-    // only when sequences can be long (many pages per segment): there the
-    // static split leaves an uneven finish; short segments balance already
-    // and would only pay for the wider merge.
-    gr.dyn_permille = s.max_pages >= kDynMinPages ? kDynPermille : 0;
-    gr.dyn_pages = 256 / block_size;
-    if (tunable) dynamic_override(&gr.dyn_permille, &gr.dyn_pages);
+    // Dynamic tail: part of the page stream handed out in pieces through an
+    // atomic counter, so that warps whose pages arrive early take more of the
+    // end. When sequences can be long (many pages per segment): 15 % in
+    // pieces of 256 tokens. On the one-head path with shorter sequences: half
+    // the stream in pieces of 64 tokens (its partials are one head wide, so
+    // small pieces stay cheap), provided the merge of their partials, four
+    // warps per row, fits in one wave. Measured: the Llama-7B MHA step (1024
+    // rows) takes 102.0 us with it and 104.8 us without; on the mixed
+    // shared-prefix workload (8192 rows, tensor-core path) every tail tried
+    // made the step slower (162-182 vs 150 us): there the wider merge costs
+    // more than the balance gains.
+    const int64_t rows = static_cast<int64_t>(B) * s.U * s.GS;
+    if (!dynamic) {
+        gr.dyn_permille = 0;
+        gr.dyn_pages = 256 / block_size;
+    } else if (s.max_pages >= kDynMinPages) {
+        gr.dyn_permille = kDynPermille;
+        gr.dyn_pages = 256 / block_size;
+    } else if (s.kind == kSplitFma && rows <= static_cast<int64_t>(num_sms) * kMergeRowsPerSm) {
+        gr.dyn_permille = kDynShortPermille;
+        gr.dyn_pages = 64 / block_size;
+    } else {
+        gr.dyn_permille = 0;
+        gr.dyn_pages = 256 / block_size;
+    }
+    if (tunable && dynamic) dynamic_override(&gr.dyn_permille, &gr.dyn_pages);
     const int64_t max_pieces = s.P_max * gr.dyn_permille / 1000 / gr.dyn_pages + 1;
     gr.ranges = static_cast<int64_t>(gr.NW) + max_pieces;
     gr.meta_bytes = round_up(static_cast<size_t>(kMetaHeader + B + 1) * 4u, 256);

@@ -17,8 +17,8 @@
 // call (the only word that must start at zero, the fallback error word, is
 // cleared by each call). Calls whose kernels overlap on the GPU (different
 // streams without ordering) race on the array: serialise them. A call whose
-// partials would not fit in the array returns PA_ERR_WORKSPACE before any
-// launch.
+// dynamic-tail partials would not fit runs on static ranges alone; one whose
+// partials do not fit even then returns PA_ERR_WORKSPACE before any launch.
 //
 // Set-up. The device address of the array is looked up once per device with
 // cudaGetSymbolAddress, on the first call made while that device is current;
@@ -139,13 +139,15 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     pa::SplitLaunch L{sh.kind, D, block_size, sh.NT, sh.warps, 0, sh.smem};
     const int per_sm = blocks_per_sm(dev, L, &st);
     if (st != cudaSuccess || per_sm < 1) return PA_ERR_CUDA;
-    const pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size, num_sms, per_sm, false);
-    L.blocks = gr.blocks;
-
     // Scratch layout: fallback error word, then the workspace (metadata,
-    // partial (m, l), partial sums).
+    // partial (m, l), partial sums). A dynamic tail adds partials; when they
+    // do not fit, the call runs on static ranges alone.
     const size_t err_bytes = 256;
+    pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size, num_sms, per_sm, false);
+    if (err_bytes + gr.workspace_bytes() > kNoAllocScratchBytes)
+        gr = pa::split_grid(sh, B, D, block_size, num_sms, per_sm, false, false);
     if (err_bytes + gr.workspace_bytes() > kNoAllocScratchBytes) return PA_ERR_WORKSPACE;
+    L.blocks = gr.blocks;
     int* err = reinterpret_cast<int*>(scratch);
     int* meta = reinterpret_cast<int*>(scratch + err_bytes);
     float* ml = reinterpret_cast<float*>(scratch + err_bytes + gr.meta_bytes);

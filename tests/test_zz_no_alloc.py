@@ -72,3 +72,23 @@ def test_noalloc_rejects_or_matches_at_the_largest_footprint():
         return
     torch.cuda.synchronize()
     assert np.abs(out_f64(out) - ref).max() <= tol(wl)
+
+
+def test_noalloc_runs_without_the_dynamic_tail_when_it_does_not_fit():
+    # One query head per kv unit, 32 x 32 heads and a 2048-token bound: the
+    # dynamic tail pa_decode plans here needs about 19 MB of partials, more
+    # than the fixed scratch, so the no-alloc call runs on static ranges
+    # alone, and must still match pa_decode.
+    wl = make_workload("llama7b_mha", seed=24, B=32, lengths=("uniform", 1, 200), max_len=2048,
+                       pool=("fixed", 1024))
+    ds = DeviceStep(wl)
+    ds.append()
+    with pa.Plan() as plan:
+        ref = out_f64(ds.decode(plan, max_seq_len=2048))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out = torch.full_like(ds.out, float("nan"))
+    pa.pa_decode_noalloc(ds.q, ds.k_pool, ds.v_pool, ds.tables, ds.seq_lens, wl.scale, out, 2048,
+                         device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert np.abs(out_f64(out) - ref).max() <= tol(wl)
