@@ -12,9 +12,28 @@ namespace {
 
 __device__ int g_append_error;  // library-wide word of append and block copies (per device)
 
+// blockIdx.x = sequence; each thread moves one 16-byte vector of the
+// sequence's new K and V rows (blockIdx.y picks the group of 256 vectors).
+// The vector's load does not depend on where it goes, so it is issued first
+// and its latency overlaps the two dependent index loads (cache length, then
+// table entry).
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
     griddep_launch_dependents();  // a following decode may start launching
     const int b = blockIdx.x;
+    const int row_bytes = a.D * a.elem_bytes;
+    const int chunks = row_bytes / 16;        // 16-byte vectors per head row
+    const int per_pool = a.Hkv * chunks;
+    const int i = blockIdx.y * blockDim.x + threadIdx.x;
+    const bool mine = i < 2 * per_pool;
+    const int which = i / per_pool;           // 0 = K, 1 = V
+    const int r = i - which * per_pool;
+    const int h = r / chunks, c = r - h * chunks;
+    uint4 w = make_uint4(0, 0, 0, 0);
+    if (mine) {
+        const char* src = static_cast<const char*>(which ? a.v_new : a.k_new) +
+                          (static_cast<size_t>(b) * a.Hkv + h) * row_bytes + c * 16;
+        w = *reinterpret_cast<const uint4*>(src);
+    }
     const int pos = a.cache_lens[b];
     if (pos < 0 || pos >= a.max_blocks * a.BS) {
         if (threadIdx.x == 0) atomicOr(&g_append_error, kErrCacheLen);
@@ -25,19 +44,11 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
         if (threadIdx.x == 0) atomicOr(&g_append_error, kErrTable);
         return;
     }
-    const int row_bytes = a.D * a.elem_bytes;
-    const int chunks = row_bytes / 16;        // 16-byte vectors per head row
-    const int per_pool = a.Hkv * chunks;
-    const int slot = pos % a.BS;
-    for (int i = threadIdx.x; i < 2 * per_pool; i += blockDim.x) {
-        const int which = i / per_pool;       // 0 = K, 1 = V
-        const int r = i - which * per_pool;
-        const int h = r / chunks, c = r - h * chunks;
-        const char* src = static_cast<const char*>(which ? a.v_new : a.k_new) +
-                          (static_cast<size_t>(b) * a.Hkv + h) * row_bytes + c * 16;
+    if (mine) {
         char* dst = static_cast<char*>(which ? a.vpool : a.kpool) +
-                    ((static_cast<size_t>(phys) * a.Hkv + h) * a.BS + slot) * row_bytes + c * 16;
-        *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(src);
+                    ((static_cast<size_t>(phys) * a.Hkv + h) * a.BS + pos % a.BS) * row_bytes +
+                    c * 16;
+        *reinterpret_cast<uint4*>(dst) = w;
     }
 }
 
@@ -82,9 +93,11 @@ cudaError_t launch_copy_blocks(const CopyArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     if (a.B == 0) return cudaSuccess;
-    const int per_seq = 2 * a.Hkv * (a.D * a.elem_bytes / 16);
+    const int per_seq = 2 * a.Hkv * (a.D * a.elem_bytes / 16);  // 16-byte vectors
     const int threads = per_seq >= 256 ? 256 : ((per_seq + 31) / 32) * 32;
-    append_kernel<<<a.B, threads, 0, stream>>>(a);
+    const int groups = (per_seq + threads - 1) / threads;
+    if (groups > 65535) return cudaErrorInvalidValue;
+    append_kernel<<<dim3(a.B, groups), threads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
