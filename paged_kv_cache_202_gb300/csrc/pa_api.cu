@@ -156,8 +156,8 @@ bool split_shape(int kind, int nq, int B, int Hq, int Hkv, int D, int block_size
     return true;
 }
 
-SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int num_sms, int per_sm,
-                     bool tunable, bool dynamic) {
+SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t rows, int num_sms,
+                     int per_sm, bool tunable, bool dynamic) {
     SplitGrid gr;
     const int64_t need = (s.P_max + static_cast<int64_t>(s.warps) * kMinPagesPerWarp - 1) /
                          (static_cast<int64_t>(s.warps) * kMinPagesPerWarp);
@@ -166,28 +166,27 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int num_
     gr.NW = gr.blocks * s.warps;
     // Dynamic tail: part of the page stream handed out in pieces through an
     // atomic counter, so that warps whose pages arrive early take more of the
-    // end. When sequences can be long (many pages per segment): 15 % in
-    // pieces of 256 tokens. On the one-head path with shorter sequences: half
-    // the stream in pieces of 64 tokens (its partials are one head wide, so
-    // small pieces stay cheap), provided the merge of their partials, four
-    // warps per row, fits in one wave. Measured: the Llama-7B MHA step (1024
-    // rows) takes 102.0 us with it and 104.8 us without; on the mixed
-    // shared-prefix workload (8192 rows, tensor-core path) every tail tried
-    // made the step slower (162-182 vs 150 us): there the wider merge costs
-    // more than the balance gains.
-    const int64_t rows = static_cast<int64_t>(B) * s.U * s.GS;
-    if (!dynamic) {
-        gr.dyn_permille = 0;
-        gr.dyn_pages = 256 / block_size;
-    } else if (s.max_pages >= kDynMinPages) {
-        gr.dyn_permille = kDynPermille;
-        gr.dyn_pages = 256 / block_size;
-    } else if (s.kind == kSplitFma && rows <= static_cast<int64_t>(num_sms) * kMergeRowsPerSm) {
-        gr.dyn_permille = kDynShortPermille;
-        gr.dyn_pages = 64 / block_size;
-    } else {
-        gr.dyn_permille = 0;
-        gr.dyn_pages = 256 / block_size;
+    // end. Its partials are merged with four warps per row, which pays only
+    // while the merge of all rows fits in one wave; past that the wider merge
+    // costs more than the balance gains. Within it: 15 % of the stream in
+    // 256-token pieces when sequences can be long (many pages per segment);
+    // on the one-head path with shorter sequences, half the stream in 64-token
+    // pieces (its partials are one head wide, so small pieces stay cheap).
+    // Measured (split + merge, or whole step): Llama-3-8B GQA decode, 2048
+    // rows, 310 vs 326 us split; Llama-7B MHA, 1024 rows, step 102.0 vs
+    // 104.8 us; mixed shared prefix, 8192 rows, step 150 us without a tail
+    // against 162-182 with one; four queries per sequence on the GQA batch,
+    // 8192 rows, 348 us without against 361-370 with one.
+    const bool merge_fits = rows <= static_cast<int64_t>(num_sms) * kMergeRowsPerSm;
+    gr.dyn_permille = 0;
+    gr.dyn_pages = 256 / block_size;
+    if (dynamic && merge_fits) {
+        if (s.max_pages >= kDynMinPages) {
+            gr.dyn_permille = kDynPermille;
+        } else if (s.kind == kSplitFma) {
+            gr.dyn_permille = kDynShortPermille;
+            gr.dyn_pages = 64 / block_size;
+        }
     }
     if (tunable && dynamic) dynamic_override(&gr.dyn_permille, &gr.dyn_pages);
     const int64_t max_pieces = s.P_max * gr.dyn_permille / 1000 / gr.dyn_pages + 1;
@@ -357,7 +356,9 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
         if (e != cudaSuccess || per_sm < 1) return PA_ERR_CUDA;
         plan->occ.push_back(OccKey{L.kind, D, block_size, L.NT, L.warps, L.smem, per_sm, L.mq});
     }
-    const pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size, plan->num_sms, per_sm, true);
+    const pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size,
+                                            static_cast<int64_t>(q_start ? T : B) * Hq,
+                                            plan->num_sms, per_sm, true);
     L.blocks = gr.blocks;
 
     // Workspace: metadata, partial (m, l), partial value sums.

@@ -103,10 +103,11 @@ struct SplitGrid {
     size_t meta_bytes = 0, ml_bytes = 0, acc_bytes = 0;
     size_t workspace_bytes() const { return meta_bytes + ml_bytes + acc_bytes; }
 };
-// tunable: honour the PA_SPLIT_DYNAMIC override of the dynamic tail;
-// dynamic = false plans static ranges only (the fewest partials).
-SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int num_sms, int per_sm,
-                     bool tunable, bool dynamic = true);
+// rows: output rows the merge writes (B * Hq, or T * Hq with several queries
+// per sequence). tunable: honour the PA_SPLIT_DYNAMIC override of the dynamic
+// tail; dynamic = false plans static ranges only (the fewest partials).
+SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t rows, int num_sms,
+                     int per_sm, bool tunable, bool dynamic = true);
 
 // Copies the planned fields (shape, grid, tail) into a.
 void set_split_plan(SplitArgs* a, const SplitShape& s, const SplitGrid& gr);

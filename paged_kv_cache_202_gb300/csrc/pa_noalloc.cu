@@ -143,9 +143,10 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     // partial (m, l), partial sums). A dynamic tail adds partials; when they
     // do not fit, the call runs on static ranges alone.
     const size_t err_bytes = 256;
-    pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size, num_sms, per_sm, false);
+    const int64_t out_rows = static_cast<int64_t>(B) * Hq;
+    pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size, out_rows, num_sms, per_sm, false);
     if (err_bytes + gr.workspace_bytes() > kNoAllocScratchBytes)
-        gr = pa::split_grid(sh, B, D, block_size, num_sms, per_sm, false, false);
+        gr = pa::split_grid(sh, B, D, block_size, out_rows, num_sms, per_sm, false, false);
     if (err_bytes + gr.workspace_bytes() > kNoAllocScratchBytes) return PA_ERR_WORKSPACE;
     L.blocks = gr.blocks;
     int* err = reinterpret_cast<int*>(scratch);
