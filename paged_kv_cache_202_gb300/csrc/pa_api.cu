@@ -166,24 +166,27 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t 
     gr.NW = gr.blocks * s.warps;
     // Dynamic tail: part of the page stream handed out in pieces through an
     // atomic counter, so that warps whose pages arrive early take more of the
-    // end. Its partials are merged with four warps per row, which pays only
-    // while the merge of all rows fits in one wave; past that the wider merge
-    // costs more than the balance gains. Within it: 15 % of the stream in
-    // 256-token pieces when sequences can be long (many pages per segment);
-    // on the one-head path with shorter sequences, half the stream in 64-token
-    // pieces (its partials are one head wide, so small pieces stay cheap).
-    // Measured (split + merge, or whole step): Llama-3-8B GQA decode, 2048
-    // rows, 310 vs 326 us split; Llama-7B MHA, 1024 rows, step 102.0 vs
-    // 104.8 us; mixed shared prefix, 8192 rows, step 150 us without a tail
-    // against 162-182 with one; four queries per sequence on the GQA batch,
-    // 8192 rows, 348 us without against 361-370 with one.
+    // end; its partials are merged with four warps per row. Measured (whole
+    // decode call, or step):
+    //  * one query per sequence, sequences up to 1024 pages or more: 15 % in
+    //    256-token pieces; Llama-3-8B GQA batches of 64 / 96 / 128 / 192 / 256
+    //    long sequences ran 3-5 % faster with it (DRAM-saturating kernels
+    //    finish unevenly without it).
+    //  * the one-head path with shorter sequences: half the stream in 64-token
+    //    pieces (one-head partials stay cheap), while the merge of all rows
+    //    fits in one wave; Llama-7B MHA (1024 rows) step 102.0 vs 104.8 us.
+    //    The tensor-core path with shorter sequences gains nothing (mixed
+    //    shared prefix: 142 vs 141 us split, and a slower merge).
+    //  * several queries per sequence: none. That kernel finishes evenly
+    //    without it (335.8 vs 335.6-339.7 us split on four queries per
+    //    sequence of the GQA batch) and its merge took 30-34 instead of 16 us.
     const bool merge_fits = rows <= static_cast<int64_t>(num_sms) * kMergeRowsPerSm;
     gr.dyn_permille = 0;
     gr.dyn_pages = 256 / block_size;
-    if (dynamic && merge_fits) {
+    if (dynamic && !s.mq) {
         if (s.max_pages >= kDynMinPages) {
             gr.dyn_permille = kDynPermille;
-        } else if (s.kind == kSplitFma) {
+        } else if (s.kind == kSplitFma && merge_fits) {
             gr.dyn_permille = kDynShortPermille;
             gr.dyn_pages = 64 / block_size;
         }

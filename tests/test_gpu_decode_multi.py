@@ -67,9 +67,13 @@ def test_decode_multi_matches_oracle(Hq, Hkv, bs, D, lens, ns):
     assert e <= BF16_TOL, f"max abs error {e:.3e}"
 
 
-def test_long_sequences_merge_many_partials():
-    # Sequences past 1024 pages switch on the dynamically scheduled tail, so
-    # their rows are merged from many partials.
+@pytest.mark.parametrize("tail", [None, "150,1"])
+def test_long_sequences_merge_many_partials(tail, monkeypatch):
+    # Long rows are cut by many static ranges; with a forced dynamic tail of
+    # one-page pieces (the tuning override) they are also cut into many
+    # pieces and merged four warps per row.
+    if tail:
+        monkeypatch.setenv("PA_SPLIT_DYNAMIC", tail)
     lens, ns = [20000, 17000, 300, 9000], [4, 2, 4, 1]
     wl, q, qs = _case(lens, ns, seed=3)
     got, err = _run(wl, q, qs, 4)
