@@ -22,6 +22,7 @@ constexpr int kMultiWarps = 4;             // ... with several queries per seque
 constexpr int kDefaultStages = 1;          // pipeline stages per warp
 constexpr int kDynPermille = 150;          // share of the page stream scheduled dynamically
 constexpr int kDynMinPages = 1024;         // ... when a sequence may have this many pages
+constexpr int kDynPiecePages = 16;         // ... in pieces of this many pages
 constexpr int kDynShortPermille = 500;     // ... on the one-head path with shorter sequences
 constexpr int kMergeRowsPerSm = 16;        // rows one SM merges at once with 4 warps per row
 constexpr int kMinPagesPerWarp = 4;
@@ -169,9 +170,10 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t 
     // end; its partials are merged with four warps per row. Measured (whole
     // decode call, or step):
     //  * one query per sequence, sequences up to 1024 pages or more: 15 % in
-    //    256-token pieces; Llama-3-8B GQA batches of 64 / 96 / 128 / 192 / 256
-    //    long sequences ran 3-5 % faster with it (DRAM-saturating kernels
-    //    finish unevenly without it).
+    //    16-page pieces; Llama-3-8B GQA batches of 64 / 96 / 128 / 192 / 256
+    //    long sequences ran 2-5 % faster with it (DRAM-saturating kernels
+    //    finish unevenly without it). 16 pages beat 8 and 32 on both the GQA
+    //    batch (block size 16) and the 128k-token one (block size 32).
     //  * the one-head path with shorter sequences: half the stream in 64-token
     //    pieces (one-head partials stay cheap), while the merge of all rows
     //    fits in one wave; Llama-7B MHA (1024 rows) step 102.0 vs 104.8 us.
@@ -182,7 +184,7 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t 
     //    sequence of the GQA batch) and its merge took 30-34 instead of 16 us.
     const bool merge_fits = rows <= static_cast<int64_t>(num_sms) * kMergeRowsPerSm;
     gr.dyn_permille = 0;
-    gr.dyn_pages = 256 / block_size;
+    gr.dyn_pages = kDynPiecePages;
     if (dynamic && !s.mq) {
         if (s.max_pages >= kDynMinPages) {
             gr.dyn_permille = kDynPermille;
