@@ -18,7 +18,7 @@ namespace {
 using pa::SplitLaunch;
 
 constexpr int kDefaultWarps = 3;           // warps per block of the split kernels
-constexpr int kMultiWarps = 4;             // ... with several queries per sequence
+constexpr int kMultiWarps = 5;             // ... with several queries per sequence
 constexpr int kDefaultStages = 1;          // pipeline stages per warp
 constexpr int kDynPermille = 150;          // share of the page stream scheduled dynamically
 constexpr int kDynMinPages = 1024;         // ... when a sequence may have this many pages
@@ -136,18 +136,23 @@ bool split_shape(int kind, int nq, int B, int Hq, int Hkv, int D, int block_size
     s.P_max = static_cast<int64_t>(B) * s.U * s.max_pages;
     if (s.P_max > INT32_MAX) return false;
 
-    s.stage_bytes = round_up(2u * kChunkTokens * D * 2u + static_cast<size_t>(s.GS) * D * 2u, 1024);
+    // K and V of a chunk, then the query rows (padded rows on the multi-query
+    // path, which rereads them at every chunk).
+    const size_t q_row = s.mq ? static_cast<size_t>(mq_q_pitch(D)) : static_cast<size_t>(D) * 2u;
+    s.stage_bytes = round_up(2u * kChunkTokens * D * 2u + static_cast<size_t>(s.GS) * q_row, 1024);
     s.lens_bytes = round_up(static_cast<size_t>(2 * B + 1) * 4u, 1024);
     // Many warps with one stage each: a warp waits for its chunk while the other
     // warps of the SM compute, so bytes in flight scale with the warp count
     // (3 warps per block, up to 4 blocks per SM at 32-token stages).
-    // With 9-16 (query, head) columns the multi-query kernel holds two
-    // n-tiles of state (~235 registers a thread), which limits an SM to two
-    // blocks: four warps each keep eight warps' stages in flight (measured
-    // 5.77 vs 4.96 TB/s with three on the speculative-verification workload).
+    // With 9-16 (query, head) columns the multi-query kernel's 21.5 KB stages
+    // allow ten warps per SM: two blocks of five (168 registers a thread).
     s.warps = (s.mq && s.NT == 2) ? kMultiWarps : kDefaultWarps;
     s.stages = kDefaultStages;
     if (tunable) tuning_override(&s.warps, &s.stages);
+    if (s.mq) {
+        s.stages = 1;  // its query rows stay in the stage for the whole segment
+        s.warps = std::min(s.warps, kMultiWarps);  // the kernel's launch bound: 5 warps
+    }
     // ring, mbarriers (8 B each, padded to 16 B), per-stage range records (16 B each)
     s.smem = 1024 + s.lens_bytes + static_cast<size_t>(s.warps) * s.stages * s.stage_bytes +
              round_up(static_cast<size_t>(s.warps) * s.stages * 8, 16) +

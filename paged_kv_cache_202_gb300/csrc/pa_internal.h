@@ -31,6 +31,12 @@ enum SplitKind { kSplitFma = 0, kSplitMma = 1 };
 // 32-token page of the same (sequence, kv unit) segment.
 constexpr int kChunkTokens = 32;
 
+// Row pitch (bytes) of the query rows in a stage of the multi-query kernel,
+// which reads its query fragments from shared memory at every chunk: 16
+// bytes past a row of D bf16 values, so that the 8 rows of a fragment load
+// fall in different banks.
+__host__ __device__ constexpr int mq_q_pitch(int D) { return D * 2 + 16; }
+
 // Arguments of the split-attention kernels (bf16 KV).
 struct SplitArgs {
     const uint16_t* q;         // [B][Hq][D] bf16 bits

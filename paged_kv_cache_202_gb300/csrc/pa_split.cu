@@ -18,12 +18,14 @@ __global__ void __launch_bounds__(256, 1)
     split_body<D, BS, MmaState<D, kChunkTokens, NT>>(&kmap, &vmap, a);
 }
 
-// Several queries per sequence (speculative verification) on the same tiles.
+// Several queries per sequence (speculative verification) on the same tiles,
+// query fragments read from shared memory at every chunk; at most 204
+// registers a thread, so that two blocks of five warps fit an SM.
 template <int D, int BS, int NT>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(160, 2)
     mma_mq_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const SplitArgs a) {
-    split_body<D, BS, MmaState<D, kChunkTokens, NT>, true>(&kmap, &vmap, a);
+    split_body<D, BS, MmaState<D, kChunkTokens, NT, true>, true>(&kmap, &vmap, a);
 }
 
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, SplitArgs);

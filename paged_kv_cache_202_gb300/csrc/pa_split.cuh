@@ -260,23 +260,35 @@ struct FmaState {
 };
 
 // ------------------------------------------------------------------ MMA path
-template <int D, int BS, int NT>
+// QS: the query fragments are read from the stage's query rows (row pitch
+// mq_q_pitch(D)) at every chunk instead of being held in registers for the
+// whole segment; the multi-query kernel, whose 16-column tile would otherwise
+// hold 32 more registers, does this (its stage keeps the segment's query rows
+// because it runs one stage per warp).
+template <int D, int BS, int NT, bool QS = false>
 struct MmaState {
     static constexpr int KS = D / 16;     // k-steps of the score product, m-tiles of the value product
     static constexpr int TILES = BS / 16; // 16-token tiles per page
-    uint32_t qb[KS][NT][2];               // Q^T fragments (B operand)
+    static constexpr int QP = QS ? mq_q_pitch(D) : D * 2;  // query row pitch in the stage
+    uint32_t qb[QS ? 1 : KS][NT][2];      // Q^T fragments (B operand), held unless QS
     float o[KS][NT][4];                   // O^T accumulators
     float m[NT][2], l[NT][2];
+
+    // Fragment (kk, nt) of Q^T from the stage: rows past nh read as zero.
+    __device__ __forceinline__ void q_frag(uint32_t qst, int nh, int lane, int kk, int nt,
+                                           uint32_t& b0, uint32_t& b1) const {
+        const int row = nt * 8 + (lane >> 2);
+        const uint32_t addr = qst + row * QP + (16 * kk + 2 * (lane & 3)) * 2;
+        b0 = row < nh ? lds_u32(addr) : 0u;
+        b1 = row < nh ? lds_u32(addr + 16) : 0u;
+    }
 
     __device__ __forceinline__ void start(uint32_t qst, int nh, int lane) {
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const int row = nt * 8 + (lane >> 2);
+            if constexpr (!QS) {
 #pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                const uint32_t addr = qst + row * (D * 2) + (16 * kk + 2 * (lane & 3)) * 2;
-                qb[kk][nt][0] = row < nh ? lds_u32(addr) : 0u;
-                qb[kk][nt][1] = row < nh ? lds_u32(addr + 16) : 0u;
+                for (int kk = 0; kk < KS; ++kk) q_frag(qst, nh, lane, kk, nt, qb[kk][nt][0], qb[kk][nt][1]);
             }
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
@@ -296,7 +308,8 @@ struct MmaState {
     // the tokens from the chunk's start to the end of the sequence.
     template <bool MQ = false>
     __device__ __forceinline__ void page(uint32_t kst, uint32_t vst, int nv, float scale_log2,
-                                         int lane, int rem = 0, int nqb = 0, int g = 1) {
+                                         int lane, int rem = 0, int nqb = 0, int g = 1,
+                                         uint32_t qst = 0, int nh = 0) {
         int lim[NT][2];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt)
@@ -317,16 +330,34 @@ struct MmaState {
 #pragma unroll
                 for (int i = 0; i < 4; ++i) s[t][nt][i] = 0.f;
         // Scores S^T = K Q^T.
-#pragma unroll
-        for (int t = 0; t < TILES; ++t) {
-            const int tok = t * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+        if constexpr (QS) {
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(swz(kst, 2 * kk + (lane >> 4), tok, BS), a0, a1, a2, a3);
+                uint32_t b[NT][2];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    mma_bf16_16816(s[t][nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+                for (int nt = 0; nt < NT; ++nt) q_frag(qst, nh, lane, kk, nt, b[nt][0], b[nt][1]);
+#pragma unroll
+                for (int t = 0; t < TILES; ++t) {
+                    const int tok = t * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(swz(kst, 2 * kk + (lane >> 4), tok, BS), a0, a1, a2, a3);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_bf16_16816(s[t][nt], a0, a1, a2, a3, b[nt][0], b[nt][1]);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int t = 0; t < TILES; ++t) {
+                const int tok = t * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+                    uint32_t a0, a1, a2, a3;
+                    ldsm_x4(swz(kst, 2 * kk + (lane >> 4), tok, BS), a0, a1, a2, a3);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+                        mma_bf16_16816(s[t][nt], a0, a1, a2, a3, qb[kk][nt][0], qb[kk][nt][1]);
+                }
             }
         }
         // Scale to the log2 domain, mask the tail, column maxima over the tokens.
@@ -680,11 +711,13 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
             }
             if (qstart) {
                 if constexpr (MQ) {
-                    // Query i's g heads of this kv head: rows qrow0 + i of q.
-                    const uint32_t run = static_cast<uint32_t>(a.g * D * 2);
-                    for (int i = 0; i < nh / a.g; ++i) {
-                        const uint16_t* src = a.q + ((static_cast<size_t>(qrow0) + i) * a.Hq + kvh * a.g) * D;
-                        bulk_load(stg + 2 * CT * D * 2 + i * run, src, run, bar);
+                    // Column c = i * g + j: head kvh * g + j of query row
+                    // qrow0 + i, one row of D values per copy at the padded pitch.
+                    for (int c = 0; c < nh; ++c) {
+                        const int i = c / a.g, j = c - i * a.g;
+                        const uint16_t* src =
+                            a.q + ((static_cast<size_t>(qrow0) + i) * a.Hq + kvh * a.g + j) * D;
+                        bulk_load(stg + 2 * CT * D * 2 + c * mq_q_pitch(D), src, D * 2, bar);
                     }
                 } else {
                     const uint16_t* src =
@@ -758,7 +791,8 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
             const int rem = len[cc.b] - cc.p * BS;  // tokens from the chunk start to the end
             const int nv = min(n * BS, rem);
             if constexpr (MQ)
-                st.template page<true>(stg, stg + CT * D * 2, nv, a.scale_log2, lane, rem, nqb, a.g);
+                st.template page<true>(stg, stg + CT * D * 2, nv, a.scale_log2, lane, rem, nqb, a.g,
+                                       stg + 2 * CT * D * 2, nh);
             else
                 st.page(stg, stg + CT * D * 2, nv, a.scale_log2, lane);
         }
