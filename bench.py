@@ -37,8 +37,8 @@ L2_BYTES = 126 * 2**20
 # DRAM traffic of the split-attention kernel from an ncu capture (per launch,
 # scaled to the full workload), valid only for the kernel sources it was
 # measured on (sha256 of the split kernel's source files).
-TRAFFIC = {"source_sha": "9bd2f856e452c16f5ea428b14d10aa1f79f235abfc0b72e494f4949dfbd6525c",
-           "workload": "llama3_8b_gqa", "bytes_per_launch": 2205524736 + 5805056}
+TRAFFIC = {"source_sha": "3a8bec0b37495f3882534aff9dbd3d0fe60e4223f68b0f1ff843af5e6fa792ee",
+           "workload": "llama3_8b_gqa", "bytes_per_launch": 2205654272 + 5797888}
 
 
 def split_source_sha() -> str:

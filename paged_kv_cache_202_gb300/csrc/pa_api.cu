@@ -136,22 +136,24 @@ bool split_shape(int kind, int nq, int B, int Hq, int Hkv, int D, int block_size
     s.P_max = static_cast<int64_t>(B) * s.U * s.max_pages;
     if (s.P_max > INT32_MAX) return false;
 
-    // K and V of a chunk, then the query rows (padded rows on the multi-query
-    // path, which rereads them at every chunk).
-    const size_t q_row = s.mq ? static_cast<size_t>(mq_q_pitch(D)) : static_cast<size_t>(D) * 2u;
+    // K and V of a chunk, then the query rows (padded rows for the tiles that
+    // reread them at every chunk: several queries per sequence, or two
+    // n-tiles).
+    const bool qs = s.mq || s.NT == 2;
+    const size_t q_row = qs ? static_cast<size_t>(mq_q_pitch(D)) : static_cast<size_t>(D) * 2u;
     s.stage_bytes = round_up(2u * kChunkTokens * D * 2u + static_cast<size_t>(s.GS) * q_row, 1024);
     s.lens_bytes = round_up(static_cast<size_t>(2 * B + 1) * 4u, 1024);
     // Many warps with one stage each: a warp waits for its chunk while the other
     // warps of the SM compute, so bytes in flight scale with the warp count
     // (3 warps per block, up to 4 blocks per SM at 32-token stages).
-    // With 9-16 (query, head) columns the multi-query kernel's 21.5 KB stages
-    // allow ten warps per SM: two blocks of five (168 registers a thread).
-    s.warps = (s.mq && s.NT == 2) ? kMultiWarps : kDefaultWarps;
+    // With 9-16 (query, head) columns the 21.5 KB stages allow ten warps per
+    // SM: two blocks of five (about 168 registers a thread).
+    s.warps = s.NT == 2 ? kMultiWarps : kDefaultWarps;
     s.stages = kDefaultStages;
     if (tunable) tuning_override(&s.warps, &s.stages);
-    if (s.mq) {
-        s.stages = 1;  // its query rows stay in the stage for the whole segment
-        s.warps = std::min(s.warps, kMultiWarps);  // the kernel's launch bound: 5 warps
+    if (qs) {
+        s.stages = 1;  // the query rows stay in the stage for the whole segment
+        s.warps = std::min(s.warps, kMultiWarps);  // the kernels' launch bound: 5 warps
     }
     // ring, mbarriers (8 B each, padded to 16 B), per-stage range records (16 B each)
     s.smem = 1024 + s.lens_bytes + static_cast<size_t>(s.warps) * s.stages * s.stage_bytes +

@@ -11,11 +11,14 @@ __global__ void __launch_bounds__(256, 1)
     split_body<D, BS, FmaState<D, kChunkTokens>>(&kmap, &vmap, a);
 }
 
+// Two n-tiles (9-16 query heads per kv head) read their query fragments
+// from shared memory at every chunk, as the multi-query kernel does, and run
+// two blocks of five warps per SM.
 template <int D, int BS, int NT>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(NT == 2 ? 160 : 256, NT == 2 ? 2 : 1)
     mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                const SplitArgs a) {
-    split_body<D, BS, MmaState<D, kChunkTokens, NT>>(&kmap, &vmap, a);
+    split_body<D, BS, MmaState<D, kChunkTokens, NT, NT == 2>>(&kmap, &vmap, a);
 }
 
 // Several queries per sequence (speculative verification) on the same tiles,

@@ -131,6 +131,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t region, int chunk, int tok, int
 // ------------------------------------------------------------------ FMA path
 template <int D, int BS>
 struct FmaState {
+    static constexpr bool kQS = false;   // query rows staged contiguously, read once per segment
     static constexpr int HALF = D / 2;   // query elements per lane
     static constexpr int DPL = D / 32;   // output elements per lane
     static constexpr int TPL = BS / 16;  // tokens per lane
@@ -262,11 +263,13 @@ struct FmaState {
 // ------------------------------------------------------------------ MMA path
 // QS: the query fragments are read from the stage's query rows (row pitch
 // mq_q_pitch(D)) at every chunk instead of being held in registers for the
-// whole segment; the multi-query kernel, whose 16-column tile would otherwise
-// hold 32 more registers, does this (its stage keeps the segment's query rows
-// because it runs one stage per warp).
+// whole segment. Tiles of two n-tiles (9-16 columns: several queries per
+// sequence, or 9-16 query heads per kv head) do this, which saves 32
+// registers a thread; their stage keeps the segment's query rows because
+// they run one stage per warp.
 template <int D, int BS, int NT, bool QS = false>
 struct MmaState {
+    static constexpr bool kQS = QS;
     static constexpr int KS = D / 16;     // k-steps of the score product, m-tiles of the value product
     static constexpr int TILES = BS / 16; // 16-token tiles per page
     static constexpr int QP = QS ? mq_q_pitch(D) : D * 2;  // query row pitch in the stage
@@ -566,6 +569,7 @@ __device__ __forceinline__ int4 lds_v4i(uint32_t addr) {
 template <int D, int BS, typename State, bool MQ = false>
 __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtensorMap* vmap,
                                            const SplitArgs& a) {
+    static_assert(!MQ || State::kQS, "the multi-query tile reads its query rows from the stage");
     constexpr int CT = kChunkTokens;
     constexpr int CP = CT / BS;  // pages per chunk
     extern __shared__ uint8_t smem_raw[];
@@ -710,14 +714,19 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
                 }
             }
             if (qstart) {
-                if constexpr (MQ) {
-                    // Column c = i * g + j: head kvh * g + j of query row
-                    // qrow0 + i, one row of D values per copy at the padded pitch.
+                if constexpr (State::kQS) {
+                    // One row of D values per copy at the padded pitch. With MQ,
+                    // column c = i * g + j is head kvh * g + j of query row
+                    // qrow0 + i; otherwise head kvh * g + slice * GS + c of row b.
                     for (int c = 0; c < nh; ++c) {
-                        const int i = c / a.g, j = c - i * a.g;
-                        const uint16_t* src =
-                            a.q + ((static_cast<size_t>(qrow0) + i) * a.Hq + kvh * a.g + j) * D;
-                        bulk_load(stg + 2 * CT * D * 2 + c * mq_q_pitch(D), src, D * 2, bar);
+                        size_t row;
+                        if constexpr (MQ) {
+                            const int i = c / a.g, j = c - i * a.g;
+                            row = (static_cast<size_t>(qrow0) + i) * a.Hq + kvh * a.g + j;
+                        } else {
+                            row = static_cast<size_t>(ci.b) * a.Hq + kvh * a.g + slice * a.GS + c;
+                        }
+                        bulk_load(stg + 2 * CT * D * 2 + c * mq_q_pitch(D), a.q + row * D, D * 2, bar);
                     }
                 } else {
                     const uint16_t* src =
@@ -793,6 +802,9 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
             if constexpr (MQ)
                 st.template page<true>(stg, stg + CT * D * 2, nv, a.scale_log2, lane, rem, nqb, a.g,
                                        stg + 2 * CT * D * 2, nh);
+            else if constexpr (State::kQS)
+                st.page(stg, stg + CT * D * 2, nv, a.scale_log2, lane, 0, 0, 1,
+                        stg + 2 * CT * D * 2, nh);
             else
                 st.page(stg, stg + CT * D * 2, nv, a.scale_log2, lane);
         }

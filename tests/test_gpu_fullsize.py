@@ -22,9 +22,14 @@ def _built():
     __graft_entry__.build()
 
 
-@pytest.mark.parametrize("name", ["llama7b_mha", "llama3_8b_gqa", "long_splitk", "mixed_shared"])
-def test_full_size_sampled_rows(name):
-    wl = make_workload(name)
+@pytest.mark.parametrize("name,extra", [
+    ("llama7b_mha", {}), ("llama3_8b_gqa", {}), ("long_splitk", {}), ("mixed_shared", {}),
+    # 16 query heads per kv head: the two-column-tile decode (query fragments
+    # reread from shared memory), with the dynamic tail and many partials.
+    ("llama3_8b_gqa", {"Hq": 128}),
+])
+def test_full_size_sampled_rows(name, extra):
+    wl = make_workload(name, **extra)
     ds = DeviceStep(wl)
     torch.cuda.synchronize()
     wl.append_in_place()
