@@ -356,10 +356,12 @@ pa_status pa_page_scores(const void* k_pool, const void* v_pool, const int32_t* 
  * Limits and rules:
  *   - when the partials of pa_decode's dynamic tail would not fit in the
  *     array, the call runs on static ranges alone (one partial pair per
- *     warp); a call whose partials need more than 16 MiB even then (about
- *     2 x warps x query heads per kv unit x D x 4 bytes: with 16 query heads
- *     per kv head at D = 128, a plan of more than about 1020 warps) returns
- *     PA_ERR_WORKSPACE and launches nothing;
+ *     warp, about 2 x query heads per kv unit x D x 4 bytes); when those do
+ *     not fit either (16 query heads per kv head at D = 128 need more than
+ *     about 1000 warps' worth), on fewer blocks, as many as the array holds
+ *     partials for. PA_ERR_WORKSPACE (nothing launched) remains for a call
+ *     whose partials would not fit for a single block, which no shape within
+ *     the limits above reaches;
  *   - every call shares the array and it keeps the last call's contents;
  *     calls whose work overlaps on the GPU (unordered streams) race on it and
  *     must be serialised by the caller;

@@ -165,12 +165,13 @@ bool split_shape(int kind, int nq, int B, int Hq, int Hkv, int D, int block_size
 }
 
 SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t rows, int num_sms,
-                     int per_sm, bool tunable, bool dynamic) {
+                     int per_sm, bool tunable, bool dynamic, int max_blocks) {
     SplitGrid gr;
     const int64_t need = (s.P_max + static_cast<int64_t>(s.warps) * kMinPagesPerWarp - 1) /
                          (static_cast<int64_t>(s.warps) * kMinPagesPerWarp);
-    gr.blocks = static_cast<int>(std::max<int64_t>(
-        1, std::min<int64_t>(need, static_cast<int64_t>(num_sms) * per_sm)));
+    int64_t cap = static_cast<int64_t>(num_sms) * per_sm;
+    if (max_blocks > 0) cap = std::min<int64_t>(cap, max_blocks);
+    gr.blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(need, cap)));
     gr.NW = gr.blocks * s.warps;
     // Dynamic tail: part of the page stream handed out in pieces through an
     // atomic counter, so that warps whose pages arrive early take more of the

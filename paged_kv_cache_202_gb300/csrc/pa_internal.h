@@ -111,9 +111,10 @@ struct SplitGrid {
 };
 // rows: output rows the merge writes (B * Hq, or T * Hq with several queries
 // per sequence). tunable: honour the PA_SPLIT_DYNAMIC override of the dynamic
-// tail; dynamic = false plans static ranges only (the fewest partials).
+// tail; dynamic = false plans static ranges only (the fewest partials);
+// max_blocks > 0 caps the grid (fewer warps, fewer partials).
 SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t rows, int num_sms,
-                     int per_sm, bool tunable, bool dynamic = true);
+                     int per_sm, bool tunable, bool dynamic = true, int max_blocks = 0);
 
 // Copies the planned fields (shape, grid, tail) into a.
 void set_split_plan(SplitArgs* a, const SplitShape& s, const SplitGrid& gr);

@@ -17,8 +17,9 @@
 // call (the only word that must start at zero, the fallback error word, is
 // cleared by each call). Calls whose kernels overlap on the GPU (different
 // streams without ordering) race on the array: serialise them. A call whose
-// dynamic-tail partials would not fit runs on static ranges alone; one whose
-// partials do not fit even then returns PA_ERR_WORKSPACE before any launch.
+// dynamic-tail partials would not fit runs on static ranges alone, and if
+// those do not fit either, on fewer blocks; only a call whose partials would
+// not fit for one block returns PA_ERR_WORKSPACE, before any launch.
 //
 // Set-up. The device address of the array is looked up once per device with
 // cudaGetSymbolAddress, on the first call made while that device is current;
@@ -141,13 +142,28 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     if (st != cudaSuccess || per_sm < 1) return PA_ERR_CUDA;
     // Scratch layout: fallback error word, then the workspace (metadata,
     // partial (m, l), partial sums). A dynamic tail adds partials; when they
-    // do not fit, the call runs on static ranges alone.
+    // do not fit, the call runs on static ranges alone, and when those do not
+    // fit either, on as many blocks as the scratch holds partials for.
     const size_t err_bytes = 256;
     const int64_t out_rows = static_cast<int64_t>(B) * Hq;
+    auto fits = [&](const pa::SplitGrid& g) {
+        return err_bytes + g.workspace_bytes() <= kNoAllocScratchBytes;
+    };
     pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size, out_rows, num_sms, per_sm, false);
-    if (err_bytes + gr.workspace_bytes() > kNoAllocScratchBytes)
-        gr = pa::split_grid(sh, B, D, block_size, out_rows, num_sms, per_sm, false, false);
-    if (err_bytes + gr.workspace_bytes() > kNoAllocScratchBytes) return PA_ERR_WORKSPACE;
+    if (!fits(gr)) gr = pa::split_grid(sh, B, D, block_size, out_rows, num_sms, per_sm, false, false);
+    if (!fits(gr)) {
+        // Static ranges only: two partial slots of GS rows of (D sums + m, l)
+        // per warp, plus one spare range; 256 bytes of rounding per array.
+        const size_t per_warp = static_cast<size_t>(2) * sh.GS * (D + 2) * 4u;
+        const size_t head = err_bytes + gr.meta_bytes + 512;
+        const int64_t warps_fit =
+            head < kNoAllocScratchBytes ? static_cast<int64_t>((kNoAllocScratchBytes - head) / per_warp) - 1 : 0;
+        const int blocks_fit = static_cast<int>(std::min<int64_t>(warps_fit / sh.warps, INT32_MAX));
+        if (blocks_fit >= 1)
+            gr = pa::split_grid(sh, B, D, block_size, out_rows, num_sms, per_sm, false, false,
+                                blocks_fit);
+    }
+    if (!fits(gr)) return PA_ERR_WORKSPACE;
     L.blocks = gr.blocks;
     int* err = reinterpret_cast<int*>(scratch);
     int* meta = reinterpret_cast<int*>(scratch + err_bytes);

@@ -51,26 +51,23 @@ def test_noalloc_matches_decode_on_two_calls_in_a_row():
         assert np.abs(got - ref).max() <= tol(wl)
 
 
-def test_noalloc_rejects_or_matches_at_the_largest_footprint():
+def test_noalloc_matches_at_the_largest_footprint():
     # 16 query heads per kv head at D = 128 is the largest partial footprint:
-    # the call either fits the fixed scratch and matches pa_decode, or is
-    # rejected with PA_ERR_WORKSPACE before anything is launched.
+    # here even static ranges over the full grid (1025 warps) need more than
+    # the fixed scratch, so the call runs on fewer blocks and must still
+    # match pa_decode.
     wl = make_workload("llama3_8b_gqa", seed=23, B=4, Hq=32, Hkv=2, lengths=("fixed", 100),
                        max_len=8192)
     ds = DeviceStep(wl)
     ds.append()
     with pa.Plan() as plan:
         ref = out_f64(ds.decode(plan, max_seq_len=8192))
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = torch.full_like(ds.out, float("nan"))
-    try:
-        pa.pa_decode_noalloc(ds.q, ds.k_pool, ds.v_pool, ds.tables, ds.seq_lens, wl.scale, out,
-                             8192)
-    except pa.PagedAttentionError as e:
-        assert e.status == pa.PA_ERR_WORKSPACE
-        torch.cuda.synchronize()
-        assert torch.isnan(out.float()).all(), "a rejected call must launch nothing"
-        return
+    pa.pa_decode_noalloc(ds.q, ds.k_pool, ds.v_pool, ds.tables, ds.seq_lens, wl.scale, out, 8192,
+                         device_error=err)
     torch.cuda.synchronize()
+    assert int(err.item()) == 0
     assert np.abs(out_f64(out) - ref).max() <= tol(wl)
 
 
