@@ -156,3 +156,21 @@ def test_one_plan_alternates_decode_and_multi():
             assert np.array_equal(out_f64(out1), want_dec)
             got, err = _run(wl, q, qs, 4, plan=plan)
             assert err == 0 and np.array_equal(got, want_multi)
+
+
+def test_launch_shape_and_clamped_override(monkeypatch):
+    # 16 columns (4 queries x 4 heads) run two blocks of five warps per SM,
+    # the kernel's launch bound; a tuning override asking for more warps per
+    # block is clamped to it rather than failing the launch.
+    lens, ns = [700, 300, 2000], [4, 4, 3]
+    wl, q, qs = _case(lens, ns, seed=12)
+    ref = oracle.prefill(q, wl.k_pool, wl.v_pool, wl.block_tables, wl.seq_lens, qs, wl.scale)
+    for override in (None, "8,1"):
+        if override:
+            monkeypatch.setenv("PA_SPLIT_TUNING", override)
+        with pa.Plan() as plan:
+            got, err = _run(wl, q, qs, 4, plan)
+            path, blocks, warps = plan.info()
+        assert err == 0 and path == pa.PA_PATH_MMA
+        assert warps == 5 * blocks
+        assert np.abs(got - ref).max() <= BF16_TOL

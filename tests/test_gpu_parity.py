@@ -105,6 +105,22 @@ def test_auto_path_choice():
             assert plan.info()[0] == want
 
 
+@pytest.mark.parametrize("Hq,Hkv,warps_per_block", [(32, 8, 3), (64, 4, 5), (128, 8, 5), (8, 8, 3)])
+def test_launch_shape(Hq, Hkv, warps_per_block):
+    # Up to 8 query heads per kv head: blocks of three warps; 9-16 (two
+    # n-tiles, query fragments reread from shared memory): blocks of five.
+    wl = _exact(Hq, Hkv, 128, 16, [300, 1200], seed=77)
+    ref, _, _ = _reference(wl)
+    ds = DeviceStep(wl)
+    ds.append()
+    with pa.Plan() as plan:
+        out = ds.decode(plan)
+        torch.cuda.synchronize()
+        _, blocks, warps = plan.info()
+    assert warps == warps_per_block * blocks
+    assert np.abs(out_f64(out) - ref).max() <= tol(wl)
+
+
 # ---------------------------------------------------------------- invariances
 
 @pytest.mark.parametrize("key", ["gqa_small", "mha_small", "long_small"])
