@@ -321,7 +321,10 @@ pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* copy_src,
  *   scores    device float [B][max_blocks]: entry p < ceil(L_b / block_size)
  *             receives page p's mean (over its valid tokens); others untouched
  *   victims   device int32 [B]: the logical page to evict, or -1 (no full
- *             newest page this step, or a bad table entry in the sequence)
+ *             newest page this step, or a bad table entry in the sequence);
+ *             until the victims are written, victims[0] is the score
+ *             kernel's work counter (stream-ordered, so the caller sees only
+ *             the results)
  *   device_error  device int or NULL: receives PA_DEVERR_SEQ_LEN /
  *             PA_DEVERR_TABLE bits (the caller clears it)
  *

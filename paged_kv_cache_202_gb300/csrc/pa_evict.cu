@@ -30,11 +30,22 @@ struct ScoreArgs {
     const int32_t* tables;
     const int32_t* seq_lens;
     float* scores;
-    int32_t* victims;
+    int32_t* victims;  // victims[0] is also the score kernel's piece counter (zeroed before it)
     int* err;
     int B, Hkv, D, max_blocks, num_blocks, max_seq_len;
     int stages, stage_bytes, lens_bytes;
 };
+
+// Dynamic tail of the score kernel: the last 15 % of the page list in pieces
+// of 2 logical pages (all kv heads of a page stay with one warp, so a piece
+// leaves nothing to merge), claimed through a counter by whichever warp is
+// free, so that warps whose pages arrive early take more of the end.
+constexpr int kScoreDynPermille = 150;
+constexpr int kScoreDynPages = 2;
+
+__device__ __forceinline__ void sts_u32(uint32_t addr, uint32_t v) {
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 
 __device__ __forceinline__ void report(int* err, int bit) {
     if (err) atomicOr(err, bit);
@@ -62,10 +73,12 @@ __device__ __forceinline__ float sumsq16<float>(const uint4 w) {
 }
 
 // Score kernel: persistent blocks of kWarps warps; the flattened page list is
-// cut into equal ranges, one per warp (as in the split decode). A warp streams
-// its pages head by head through a ring of shared-memory stages: one stage =
-// the K and V pages of one (block, kv head), each a contiguous run moved by a
-// 1-D bulk copy that completes on the stage's mbarrier. Lane (half, token)
+// cut into equal static ranges, one per warp, followed by small pieces that
+// free warps claim (as in the split decode). A warp streams its pages head by
+// head through a ring of shared-memory stages: one stage = the K and V pages
+// of one (block, kv head), each a contiguous run moved by a 1-D bulk copy
+// that completes on the stage's mbarrier, with the stage's page index
+// recorded beside it. Lane (half, token)
 // sums the squares of its half row, rotating the 16-byte column order by the
 // token so that the eight rows a quarter-warp reads hit different banks; after
 // the last head of a page the halves are joined, the token ratios formed and
@@ -88,13 +101,32 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 1) page_score_kernel(const S
 
     const int P = pre[a.B];
     const int NW = gridDim.x * kScoreWarps;
-    const int per = (P + NW - 1) / NW;
-    const int x0 = (blockIdx.x * kScoreWarps + warp) * per;
-    const int x1 = min(x0 + per, P);
-    if (per == 0 || x0 >= x1) return;
+    // Static ranges over the first part of the page list, then pieces of qd
+    // pages (none for small lists, whose static ranges are already short).
+    const int qd = kScoreDynPages;
+    const int Dp = (P >= 8 * NW * qd)
+                       ? (static_cast<int>(static_cast<long long>(P) * kScoreDynPermille / 1000) / qd) * qd
+                       : 0;
+    const int A = P - Dp, nd = Dp / qd;
+    const int per = (A + NW - 1) / NW;
+    const int gw = blockIdx.x * kScoreWarps + warp;
     const int S = a.stages, H = a.Hkv;
     const uint32_t my_bars = bars0 + warp * S * 8;
+    const uint32_t my_xs = bars0 + kScoreWarps * S * 8 + warp * S * 4;  // page of each stage
     const uint32_t my_ring = ring0 + warp * S * a.stage_bytes;
+
+    // Issue range [ix, ix1): the warp's static range, then claimed pieces.
+    int ix = min(gw * per, A), ix1 = min(gw * per + per, A);
+    auto claim = [&]() -> bool {  // warp-collective
+        int j = 0;
+        if (lane == 0) j = atomicAdd(a.victims, 1);
+        j = __shfl_sync(0xffffffffu, j, 0);
+        if (j >= nd) return false;
+        ix = A + j * qd;
+        ix1 = min(ix + qd, P);
+        return true;
+    };
+    if (ix >= ix1 && !claim()) return;
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(my_bars + 8 * s, 1);
         fence_barrier_init();
@@ -103,7 +135,7 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 1) page_score_kernel(const S
     const uint32_t row_bytes = a.D * sizeof(T);
     const uint32_t page_bytes = BS * row_bytes;  // one pool, one (block, head)
 
-    // Page cursors (sequence, logical page) for issue and consume.
+    // Page x -> (sequence, logical page).
     auto locate = [&](int x, int& b, int& p) {
         int lo = 0, hi = a.B - 1;
         while (lo < hi) {
@@ -113,19 +145,20 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 1) page_score_kernel(const S
         b = lo;
         p = x - pre[lo];
     };
-    int ib, ip, ih = 0, ix = x0;  // issue cursor: page x = (ib, ip), head ih
-    locate(x0, ib, ip);
+    int ib, ip, ih = 0;  // issue cursor: page ix = (ib, ip), head ih
+    locate(ix, ib, ip);
     int iphys = a.tables[static_cast<int64_t>(ib) * a.max_blocks + ip];
     uint32_t badmask = 0, phase = 0;
-    const int nitems = (x1 - x0) * H;
     int n_issued = 0;
+    bool issue_done = false;
 
-    auto issue = [&](int s) {
+    auto issue = [&](int s) {  // warp-collective
         const bool bad = iphys < 0 || iphys >= a.num_blocks;
         badmask = bad ? (badmask | (1u << s)) : (badmask & ~(1u << s));
         if (lane == 0) {
             const uint32_t bar = my_bars + 8 * s;
             const uint32_t stg = my_ring + s * a.stage_bytes;
+            sts_u32(my_xs + 4 * s, static_cast<uint32_t>(ix));  // released by the arrive below
             if (bad) {
                 mbar_arrive(bar);
             } else {
@@ -135,43 +168,48 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 1) page_score_kernel(const S
                 bulk_load(stg + page_bytes, static_cast<const char*>(a.vpool) + off, page_bytes, bar);
             }
         }
-        if (++ih == H) {
-            ih = 0;
-            if (++ix < x1) {
-                if (++ip == pre[ib + 1] - pre[ib]) locate(ix, ib, ip);
-                iphys = a.tables[static_cast<int64_t>(ib) * a.max_blocks + ip];
-            }
-        }
         ++n_issued;
+        if (++ih < H) return;
+        ih = 0;
+        if (++ix == ix1) {
+            if (!claim()) {
+                issue_done = true;
+                return;
+            }
+            locate(ix, ib, ip);
+        } else if (++ip == pre[ib + 1] - pre[ib]) {
+            locate(ix, ib, ip);
+        }
+        iphys = a.tables[static_cast<int64_t>(ib) * a.max_blocks + ip];
     };
-    for (int s = 0; s < S && n_issued < nitems; ++s) issue(s);
+    for (int s = 0; s < S && !issue_done; ++s) issue(s);
 
     const int hh = lane >> 4, tl = lane & 15;
     const int CH = row_bytes / 32;  // 16-byte columns in half a row
-    int cb, cp;
-    locate(x0, cb, cp);
+    int cb = 0, cp = 0;
     float kk[TPL], vv[TPL];
     bool poison = false;
-    int s = 0;
-    for (int k = 0; k < nitems; ++k) {
-        const int h = k % H;
-        if (h == 0) {
-#pragma unroll
-            for (int j = 0; j < TPL; ++j) kk[j] = vv[j] = 0.f;
-            poison = false;
-        }
+    int s = 0, n_done = 0;
+    while (n_done < n_issued) {
+        const int h = n_done % H;  // every page issues its H heads in a row
         const uint32_t bar = my_bars + 8 * s;
         const uint32_t stg = my_ring + s * a.stage_bytes;
         const bool ready = mbar_wait_bounded(bar, (phase >> s) & 1u, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ready)) {
             if (lane == 0) report(a.err, kErrTimeout);
-            for (int j = k; j < n_issued; ++j) {
+            for (int j = n_done; j < n_issued; ++j) {
                 const int sj = j % S;
                 mbar_wait_bounded(my_bars + 8 * sj, (phase >> sj) & 1u, kWaitLimitNs);
             }
             return;
         }
         phase ^= 1u << s;
+        if (h == 0) {
+            locate(static_cast<int>(lds_u32(my_xs + 4 * s)), cb, cp);
+#pragma unroll
+            for (int j = 0; j < TPL; ++j) kk[j] = vv[j] = 0.f;
+            poison = false;
+        }
         const int n = min(BS, len[cb] - cp * BS);
         if ((badmask >> s) & 1u) {
             poison = true;
@@ -189,7 +227,7 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 1) page_score_kernel(const S
             }
         }
         __syncwarp();
-        if (n_issued < nitems) {
+        if (!issue_done) {
             fence_proxy_async_smem();
             issue(s);
         }
@@ -213,8 +251,8 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 1) page_score_kernel(const S
                     *out = sum / static_cast<float>(n);
                 }
             }
-            if (k + 1 < nitems && ++cp == pre[cb + 1] - pre[cb]) locate(x0 + (k + 1) / H, cb, cp);
         }
+        ++n_done;
         if (++s == S) s = 0;
     }
 }
@@ -263,7 +301,7 @@ cudaError_t launch_scores(ScoreArgs a, bool bf16, int num_sms, cudaStream_t stre
     a.lens_bytes = static_cast<int>((static_cast<size_t>(2 * a.B + 1) * 4 + 127) / 128 * 128);
     a.stages = std::max(1, std::min(8, (192 * 1024) / (kScoreWarps * a.stage_bytes)));
     const size_t smem = 128 + a.lens_bytes + static_cast<size_t>(kScoreWarps) * a.stages * a.stage_bytes +
-                        static_cast<size_t>(kScoreWarps) * a.stages * 8;
+                        static_cast<size_t>(kScoreWarps) * a.stages * (8 + 4);
     auto kern = bf16 ? page_score_kernel<BS, uint16_t> : page_score_kernel<BS, float>;
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -278,6 +316,10 @@ cudaError_t launch_scores(ScoreArgs a, bool bf16, int num_sms, cudaStream_t stre
     const int64_t need = (max_pages + kScoreWarps * 4 - 1) / (kScoreWarps * 4);
     const int blocks = static_cast<int>(std::max<int64_t>(
         1, std::min<int64_t>(need, static_cast<int64_t>(std::max(per_sm, 1)) * num_sms)));
+    // victims[0] counts the claimed pieces during the score kernel; the victim
+    // kernel overwrites it afterwards.
+    e = cudaMemsetAsync(a.victims, 0, sizeof(int32_t), stream);
+    if (e != cudaSuccess) return e;
     kern<<<blocks, kScoreWarps * 32, smem, stream>>>(a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
