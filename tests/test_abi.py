@@ -204,3 +204,115 @@ def test_binding_rejects_host_tensors():
         with pytest.raises(ValueError, match="CUDA device"):
             call()
     assert plan.handle.value is None
+
+
+# Host-side argument errors of the other entry points: a status before any
+# CUDA call, so these run without a GPU.
+
+def _prefill(lib, **kw):
+    args = dict(q=ALIGNED, qs=ALIGNED, k=ALIGNED, v=ALIGNED, bt=ALIGNED, mb=4, sl=ALIGNED, B=2,
+                Hq=8, Hkv=2, D=128, bs=16, NB=64, maxq=4, maxlen=64, scale=0.1, kvdt=pa.PA_BF16,
+                out=ALIGNED, odt=pa.PA_BF16)
+    args.update(kw)
+    return lib.pa_prefill(args["q"], args["qs"], args["k"], args["v"], args["bt"], args["mb"],
+                          args["sl"], args["B"], args["Hq"], args["Hkv"], args["D"], args["bs"],
+                          args["NB"], args["maxq"], args["maxlen"], args["scale"], args["kvdt"],
+                          args["out"], args["odt"], None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(qs=None), pa.PA_ERR_NULL),
+    (dict(out=None), pa.PA_ERR_NULL),
+    (dict(kvdt=pa.PA_F32), pa.PA_ERR_DTYPE),      # tensor-core tiles take bf16 pools
+    (dict(bs=8), pa.PA_ERR_BLOCK_SIZE),
+    (dict(D=64), pa.PA_ERR_SHAPE),                # the tcgen05 tiles are built for D = 128
+    (dict(Hq=24, Hkv=8), pa.PA_ERR_SHAPE),        # g = 3 does not divide the 128-row tile
+    (dict(maxq=0), pa.PA_ERR_SHAPE),
+    (dict(scale=float("inf")), pa.PA_ERR_SHAPE),
+    (dict(k=ALIGNED + 4), pa.PA_ERR_ALIGN),
+])
+def test_prefill_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _prefill(lib, **kw) == status
+
+
+def test_prefill_empty_batch_is_a_no_op(lib):
+    assert _prefill(lib, B=0) == pa.PA_OK
+
+
+def _scores(lib, **kw):
+    args = dict(k=ALIGNED, v=ALIGNED, bt=ALIGNED, mb=4, sl=ALIGNED, B=2, Hkv=2, D=128, bs=16,
+                NB=64, maxlen=64, dt=pa.PA_BF16, sc=ALIGNED, vic=ALIGNED)
+    args.update(kw)
+    return lib.pa_page_scores(args["k"], args["v"], args["bt"], args["mb"], args["sl"], args["B"],
+                              args["Hkv"], args["D"], args["bs"], args["NB"], args["maxlen"],
+                              args["dt"], args["sc"], args["vic"], None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(vic=None), pa.PA_ERR_NULL),
+    (dict(sc=None), pa.PA_ERR_NULL),
+    (dict(dt=5), pa.PA_ERR_DTYPE),
+    (dict(bs=64), pa.PA_ERR_BLOCK_SIZE),
+    (dict(D=96), pa.PA_ERR_SHAPE),
+    (dict(B=9000), pa.PA_ERR_SHAPE),
+    (dict(v=ALIGNED + 8), pa.PA_ERR_ALIGN),
+])
+def test_page_scores_reject_bad_arguments_on_host(lib, kw, status):
+    assert _scores(lib, **kw) == status
+
+
+def test_page_scores_empty_batch_is_a_no_op(lib):
+    assert _scores(lib, B=0) == pa.PA_OK
+
+
+def _copies(lib, **kw):
+    args = dict(k=ALIGNED, v=ALIGNED, src=ALIGNED, dst=ALIGNED, n=3, Hkv=2, D=128, bs=16, NB=64,
+                dt=pa.PA_BF16)
+    args.update(kw)
+    return lib.pa_copy_blocks(args["k"], args["v"], args["src"], args["dst"], args["n"],
+                              args["Hkv"], args["D"], args["bs"], args["NB"], args["dt"], None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(src=None), pa.PA_ERR_NULL),
+    (dict(k=None), pa.PA_ERR_NULL),
+    (dict(dt=2), pa.PA_ERR_DTYPE),
+    (dict(bs=24), pa.PA_ERR_BLOCK_SIZE),
+    (dict(n=-1), pa.PA_ERR_SHAPE),
+    (dict(NB=0), pa.PA_ERR_SHAPE),
+    (dict(v=ALIGNED + 2), pa.PA_ERR_ALIGN),
+])
+def test_copy_blocks_reject_bad_arguments_on_host(lib, kw, status):
+    assert _copies(lib, **kw) == status
+
+
+def test_copy_blocks_without_pairs_is_a_no_op(lib):
+    assert _copies(lib, n=0, src=None, dst=None) == pa.PA_OK
+
+
+def _noalloc(lib, **kw):
+    args = dict(q=ALIGNED, k=ALIGNED, v=ALIGNED, bt=ALIGNED, mb=4, sl=ALIGNED, B=2, Hq=8, Hkv=2,
+                D=128, bs=16, NB=64, maxlen=64, scale=0.1, kvdt=pa.PA_BF16, out=ALIGNED,
+                odt=pa.PA_BF16)
+    args.update(kw)
+    return lib.pa_decode_noalloc(args["q"], args["k"], args["v"], args["bt"], args["mb"],
+                                 args["sl"], args["B"], args["Hq"], args["Hkv"], args["D"],
+                                 args["bs"], args["NB"], args["maxlen"], args["scale"],
+                                 args["kvdt"], args["out"], args["odt"], None, None)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=None), pa.PA_ERR_NULL),
+    (dict(kvdt=pa.PA_F32), pa.PA_ERR_DTYPE),      # the split kernels take bf16 pools
+    (dict(bs=8), pa.PA_ERR_BLOCK_SIZE),
+    (dict(Hq=6, Hkv=4), pa.PA_ERR_SHAPE),
+    (dict(B=8193), pa.PA_ERR_SHAPE),
+    (dict(B=8192, Hq=64, Hkv=64, mb=65536, maxlen=1 << 20), pa.PA_ERR_SHAPE),  # pages over 32 bits
+    (dict(out=ALIGNED + 2), pa.PA_ERR_ALIGN),
+])
+def test_noalloc_rejects_bad_arguments_on_host(lib, kw, status):
+    assert _noalloc(lib, **kw) == status
+
+
+def test_noalloc_empty_batch_is_a_no_op(lib):
+    assert _noalloc(lib, B=0) == pa.PA_OK
