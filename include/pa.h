@@ -75,7 +75,7 @@ enum {
 
 /* Kernel selection for pa_decode (pa_plan_set_path). */
 enum {
-    PA_PATH_AUTO = 0,    /* bf16 with g = 1: FMA path; bf16 with g >= 2: tensor-core path; f32: simple */
+    PA_PATH_AUTO = 0,    /* bf16: tensor-core path (any g); f32: simple */
     PA_PATH_SIMPLE = 1,  /* one warp per (sequence, q head), plain loads, no split */
     PA_PATH_FMA = 2,     /* bf16 only: bulk-staged pages, CUDA-core dot products */
     PA_PATH_MMA = 3      /* bf16 only: bulk-staged pages, GQA group through bf16 mma tiles */

@@ -182,11 +182,11 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t 
     //    long sequences ran 2-5 % faster with it (DRAM-saturating kernels
     //    finish unevenly without it). 16 pages beat 8 and 32 on both the GQA
     //    batch (block size 16) and the 128k-token one (block size 32).
-    //  * the one-head path with shorter sequences: half the stream in 64-token
-    //    pieces (one-head partials stay cheap), while the merge of all rows
-    //    fits in one wave; Llama-7B MHA (1024 rows) step 102.0 vs 104.8 us.
-    //    The tensor-core path with shorter sequences gains nothing (mixed
-    //    shared prefix: 142 vs 141 us split, and a slower merge).
+    //  * one query head per kv unit with shorter sequences: half the stream
+    //    in 64-token pieces (one-head partials stay cheap), while the merge of
+    //    all rows fits in one wave; Llama-7B MHA (1024 rows) step 102.0 vs
+    //    104.8 us. Wider partials with shorter sequences gain nothing (mixed
+    //    shared prefix, 4 heads: 142 vs 141 us split, and a slower merge).
     //  * several queries per sequence: none. That kernel finishes evenly
     //    without it (335.8 vs 335.6-339.7 us split on four queries per
     //    sequence of the GQA batch) and its merge took 30-34 instead of 16 us.
@@ -196,7 +196,7 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t 
     if (dynamic && !s.mq) {
         if (s.max_pages >= kDynMinPages) {
             gr.dyn_permille = kDynPermille;
-        } else if (s.kind == kSplitFma && merge_fits) {
+        } else if (s.GS == 1 && merge_fits) {
             gr.dyn_permille = kDynShortPermille;
             gr.dyn_pages = 64 / block_size;
         }
@@ -312,9 +312,11 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     // exists, so that an argument error never creates one.
     const int g = Hq / Hkv;
     int path = q_start ? PA_PATH_MMA : (*plan_inout ? (*plan_inout)->forced_path : PA_PATH_AUTO);
-    if (path == PA_PATH_AUTO) {
-        path = kv_dtype == PA_F32 ? PA_PATH_SIMPLE : (g == 1 ? PA_PATH_FMA : PA_PATH_MMA);
-    }
+    // bf16 pools run on the tensor-core tile for every group size, one query
+    // head per kv head included (one real column of eight: with the dynamic
+    // tail it measured 94.9-95.0 us against 96.2 us for the CUDA-core path on
+    // the Llama-7B MHA workload; PA_PATH_FMA still selects the latter).
+    if (path == PA_PATH_AUTO) path = kv_dtype == PA_F32 ? PA_PATH_SIMPLE : PA_PATH_MMA;
     if (kv_dtype == PA_F32 && path != PA_PATH_SIMPLE) return PA_ERR_DTYPE;
     const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     pa::SplitShape sh;

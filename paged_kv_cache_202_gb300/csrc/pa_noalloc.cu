@@ -120,13 +120,12 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     if (B == 0) return PA_OK;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
-    // Same planning as pa_decode's automatic choice (one query head per kv
-    // unit when the group has one head, tensor-core tiles otherwise), at the
-    // default block shape and dynamic tail.
+    // Same planning as pa_decode's automatic choice (the tensor-core tiles),
+    // at the default block shape and dynamic tail.
     const int g = Hq / Hkv;
     pa::SplitShape sh;
-    if (!pa::split_shape(g == 1 ? pa::kSplitFma : pa::kSplitMma, 0, B, Hq, Hkv, D, block_size,
-                         max_blocks, max_seq_len, false, &sh))
+    if (!pa::split_shape(pa::kSplitMma, 0, B, Hq, Hkv, D, block_size, max_blocks, max_seq_len,
+                         false, &sh))
         return PA_ERR_SHAPE;
 
     int dev = 0, num_sms = 0;

@@ -96,7 +96,7 @@ def test_decode_matches_oracle(key, path):
 
 
 def test_auto_path_choice():
-    for key, want in (("tiny_worked_60", pa.PA_PATH_SIMPLE), ("mha_small", pa.PA_PATH_FMA),
+    for key, want in (("tiny_worked_60", pa.PA_PATH_SIMPLE), ("mha_small", pa.PA_PATH_MMA),
                       ("gqa_small", pa.PA_PATH_MMA), ("long_small", pa.PA_PATH_MMA)):
         wl = _wl(key)
         ds = DeviceStep(wl)
