@@ -78,7 +78,7 @@ enum {
     PA_PATH_AUTO = 0,    /* bf16: tensor-core path (any g); f32: simple */
     PA_PATH_SIMPLE = 1,  /* one warp per (sequence, q head), plain loads, no split */
     PA_PATH_FMA = 2,     /* bf16 only: bulk-staged pages, CUDA-core dot products */
-    PA_PATH_MMA = 3      /* bf16 only: bulk-staged pages, GQA group through bf16 mma tiles */
+    PA_PATH_MMA = 3      /* bf16 only: bulk-staged pages, a kv head's query heads (any g) through bf16 mma tiles */
 };
 
 /* Opaque: split plan, device workspace and device error word. */
