@@ -187,13 +187,17 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t 
     //    all rows fits in one wave; Llama-7B MHA (1024 rows) step 102.0 vs
     //    104.8 us. Wider partials with shorter sequences gain nothing (mixed
     //    shared prefix, 4 heads: 142 vs 141 us split, and a slower merge).
-    //  * several queries per sequence: none. That kernel finishes evenly
-    //    without it (335.8 vs 335.6-339.7 us split on four queries per
-    //    sequence of the GQA batch) and its merge took 30-34 instead of 16 us.
+    //  * tiles of two n-tiles (9-16 columns), several queries per sequence
+    //    included: none. Those kernels (ten warps per SM, DRAM about 84 %)
+    //    finish evenly without it, and it only adds partials: four queries
+    //    per sequence of the GQA batch, split 335.8 vs 335.6-339.7 us and a
+    //    merge of 30-34 instead of 16 us; 16 query heads per kv head
+    //    (Llama-3-405B's grouping), split 281.7 us either way, step 290.7-
+    //    290.9 us without against 303.3-304.0 with.
     const bool merge_fits = rows <= static_cast<int64_t>(num_sms) * kMergeRowsPerSm;
     gr.dyn_permille = 0;
     gr.dyn_pages = kDynPiecePages;
-    if (dynamic && !s.mq) {
+    if (dynamic && !s.mq && s.NT <= 1) {
         if (s.max_pages >= kDynMinPages) {
             gr.dyn_permille = kDynPermille;
         } else if (s.GS == 1 && merge_fits) {

@@ -32,6 +32,8 @@ name                  shape
 ``spec_gqa``          the ``llama3_8b_gqa`` batch (its own seed); the newest 4
                       tokens of each sequence are queries (speculative
                       verification of 4 drafted tokens)
+``llama3_405b_gqa``   the ``llama3_8b_gqa`` recipe (its own seed) with
+                      Llama-3-405B's grouping: 128 q / 8 kv heads
 ====================  ====================================================
 
 Every workload is one decode step: the pools hold ``cache_len = L - 1``
@@ -51,7 +53,7 @@ import torch
 
 # numpy PCG64 seeds: 1000 + the workload's ordinal.
 _ORDINAL = {"tiny_worked_60": 1, "llama7b_mha": 2, "llama3_8b_gqa": 3, "long_splitk": 4,
-            "mixed_shared": 5, "prefill_gqa": 6, "spec_gqa": 7}
+            "mixed_shared": 5, "prefill_gqa": 6, "spec_gqa": 7, "llama3_405b_gqa": 8}
 
 CONFIGS = {
     "tiny_worked_60": dict(B=1, Hq=1, Hkv=1, D=64, block_size=16, dtype="f32",
@@ -74,6 +76,9 @@ CONFIGS = {
     "spec_gqa": dict(B=64, Hq=32, Hkv=8, D=128, block_size=16, dtype="bf16",
                      lengths=("loguniform", 512, 32768), pool=("factor", 1.1), max_len=32768,
                      new_tokens=4),
+    "llama3_405b_gqa": dict(B=64, Hq=128, Hkv=8, D=128, block_size=16, dtype="bf16",
+                            lengths=("loguniform", 512, 32768), pool=("factor", 1.1),
+                            max_len=32768),
 }
 
 

@@ -25,8 +25,9 @@ def _built():
 @pytest.mark.parametrize("name,extra", [
     ("llama7b_mha", {}), ("llama3_8b_gqa", {}), ("long_splitk", {}), ("mixed_shared", {}),
     # 16 query heads per kv head: the two-column-tile decode (query fragments
-    # reread from shared memory), with the dynamic tail and many partials.
-    ("llama3_8b_gqa", {"Hq": 128}),
+    # reread from shared memory, five-warp blocks), long rows merged from many
+    # static-range partials.
+    ("llama3_405b_gqa", {}),
 ])
 def test_full_size_sampled_rows(name, extra):
     wl = make_workload(name, **extra)
