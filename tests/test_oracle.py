@@ -240,6 +240,25 @@ def test_merge_of_random_splits_equals_one_pass(seed):
         np.testing.assert_allclose(out, full[b, h], rtol=1e-12, atol=1e-13)
 
 
+def test_merge_with_leading_and_inner_empty_partials():
+    # A partition of the tokens is still a partition when some pieces are
+    # empty: two empty pieces first, one in the middle and one at the end
+    # must merge to the one-pass result (an empty partial contributes
+    # nothing, even before any non-empty one has been folded in).
+    wl = _small("bs32_bf16")
+    kp, vp = wl.pools_after_append()
+    full = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale)
+    b, h = 1, 3
+    L = int(wl.seq_lens[b])
+    mid = L // 2
+    bounds = [0, 0, 0, mid, mid, L, L]
+    parts = [oracle.partial(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale, b, h, lo, hi)
+             for lo, hi in zip(bounds[:-1], bounds[1:])]
+    assert parts[0][0] == -math.inf and parts[0][1] == 0.0
+    out = oracle.merge([p[0] for p in parts], [p[1] for p in parts], [p[2] for p in parts])
+    np.testing.assert_allclose(out, full[b, h], rtol=1e-12, atol=1e-13)
+
+
 def test_two_partial_merge_rule():
     # Two partials with different maxima: the rule must rescale both l and acc.
     m = [3.0, -1.5]

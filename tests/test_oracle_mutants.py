@@ -47,6 +47,8 @@ MUTANTS = {
         "const int32_t phys = p.table[static_cast<int64_t>(p.B - 1 - b) * p.max_blocks + "
         "logical_block];"),
     "merge: sum not rescaled": ("ll = ll * f_old + l[i] * f_new;", "ll = ll + l[i];"),
+    "merge: two empty partials not skipped": (
+        "        if (mn == -std::numeric_limits<double>::infinity()) continue;  // both empty\n", ""),
     "merge: values not rescaled": (
         "aa[static_cast<size_t>(d)] * f_old + acc[static_cast<int64_t>(i) * D + d] * f_new;",
         "aa[static_cast<size_t>(d)] + acc[static_cast<int64_t>(i) * D + d];"),
@@ -69,6 +71,12 @@ MUTANTS = {
     "eviction ratio inverted": ("sum += kk > 0.0 ? std::sqrt(vv) / std::sqrt(kk)",
                                 "sum += kk > 0.0 ? std::sqrt(kk) / std::sqrt(vv)"),
     "evicts the highest page": ("if (victim < 0 || sp < scores[", "if (victim < 0 || sp > scores["),
+    "ties go to the highest page": ("if (victim < 0 || sp < scores[", "if (victim < 0 || sp <= scores["),
+    "eviction ratio without roots": ("sum += kk > 0.0 ? std::sqrt(vv) / std::sqrt(kk)",
+                                     "sum += kk > 0.0 ? vv / kk"),
+    "append into the next block": (
+        "const int32_t phys = table[static_cast<int64_t>(b) * max_blocks + pos / bs];",
+        "const int32_t phys = table[static_cast<int64_t>(b) * max_blocks + (pos / bs + 1) % max_blocks];"),
     "page mean over the block size": ("= sum / static_cast<double>(n);",
                                       "= sum / static_cast<double>(bs);"),
     "no causal mask": ("row_len[static_cast<size_t>(q_start[b] + i)] = seq_lens[b] - n + i + 1;",
