@@ -86,6 +86,22 @@ def test_decode_bytes_counts_kv_table_q_lens_out(golden_dir):
         == 2 * 64 * 4 + 4
 
 
+def test_decode_bytes_equal_the_arrays_a_decode_touches():
+    # bf16 pools and an f32 output, so the query and output element sizes
+    # differ: the counter must equal the bytes of the K and V rows the decode
+    # attends, the table entries of its attended blocks, and the q, length
+    # and output arrays as allocated.
+    wl = _small("gqa_bf16")
+    out = np.zeros((wl.B, wl.Hq, wl.D), dtype=np.float32)
+    lens = [int(x) for x in wl.seq_lens]
+    kv = 2 * sum(lens) * wl.Hkv * wl.k_pool[0, 0, 0].nbytes
+    table = sum(-(-L // wl.block_size) for L in lens) * wl.block_tables.itemsize
+    want = kv + table + wl.q.nbytes + wl.seq_lens.nbytes + out.nbytes
+    got = oracle.decode_bytes(wl.seq_lens, wl.Hq, wl.Hkv, wl.D, wl.block_size,
+                              wl.k_pool.itemsize, out.itemsize)
+    assert got == want
+
+
 # ---------------------------------------------------------------- the worked 60-token request
 
 def _worked_problem(golden_dir, seed=7):

@@ -68,6 +68,23 @@ MUTANTS = {
     "keys only per token": ("return 2 * kv_heads * head_dim * layers;",
                             "return kv_heads * head_dim * layers;"),
     "bytes without table entries": ("        total += 4 * oracle_num_blocks(L, bs);\n", ""),
+    "queries counted at the output size": (
+        "total += static_cast<int64_t>(B) * Hq * D * kv_elem_bytes;  // queries",
+        "total += static_cast<int64_t>(B) * Hq * D * out_elem_bytes;  // queries"),
+    "dot product drops its last element": ("        for (int d = 0; d < p.D; ++d) {\n            dot +=",
+                                           "        for (int d = 0; d < p.D - 1; ++d) {\n            dot +="),
+    "values skip the newest token": (
+        "    for (int64_t t = 0; t < L; ++t) {\n        const int64_t voff = token_offset(p, b, j, t);",
+        "    for (int64_t t = 0; t + 1 < L; ++t) {\n        const int64_t voff = token_offset(p, b, j, t);"),
+    "partial sums squared weights": ("        l += e;\n", "        l += e * e;\n"),
+    "append reads new rows transposed": (
+        "const int64_t src = (static_cast<int64_t>(b) * Hkv + j) * D;",
+        "const int64_t src = (static_cast<int64_t>(j) * B + b) * D;"),
+    "block copy direction swapped": (
+        "        std::memmove(k + dst[i] * block_bytes, k + src[i] * block_bytes, "
+        "static_cast<size_t>(block_bytes));",
+        "        std::memmove(k + src[i] * block_bytes, k + dst[i] * block_bytes, "
+        "static_cast<size_t>(block_bytes));"),
     "eviction ratio inverted": ("sum += kk > 0.0 ? std::sqrt(vv) / std::sqrt(kk)",
                                 "sum += kk > 0.0 ? std::sqrt(kk) / std::sqrt(vv)"),
     "evicts the highest page": ("if (victim < 0 || sp < scores[", "if (victim < 0 || sp > scores["),
