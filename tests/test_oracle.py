@@ -332,6 +332,20 @@ def test_uniform_weights_give_mean_of_values(how):
                                atol=1e-14)
 
 
+@pytest.mark.parametrize("L", [16, 48])
+def test_sequence_that_fills_its_table(L):
+    # The largest length a table allows: every entry names a full block
+    # (max_blocks * block_size tokens). It must be attended like any other,
+    # equal to softmax(q K^T s) V on the contiguous K and V.
+    q, Kc, Vc, perm, NB = _one_seq(L)
+    assert perm.size * 16 == L
+    scale = 0.3
+    out = oracle.decode(q, _pack(Kc, perm, NB), _pack(Vc, perm, NB), perm[None], [L], scale)
+    s = (Kc[0].astype(np.float64) @ q[0, 0].astype(np.float64)) * np.float64(np.float32(scale))
+    w = softmax(s)
+    np.testing.assert_allclose(out[0, 0], w @ Vc[0].astype(np.float64), rtol=1e-12, atol=1e-13)
+
+
 def test_one_dominant_key_selects_its_value():
     L = 40
     q, Kc, Vc, perm, NB = _one_seq(L)

@@ -77,6 +77,17 @@ MUTANTS = {
         "    for (int64_t t = 0; t < L; ++t) {\n        const int64_t voff = token_offset(p, b, j, t);",
         "    for (int64_t t = 0; t + 1 < L; ++t) {\n        const int64_t voff = token_offset(p, b, j, t);"),
     "partial sums squared weights": ("        l += e;\n", "        l += e * e;\n"),
+    "merge multiplies by the sum": ("out[d] = aa[static_cast<size_t>(d)] / ll;",
+                                    "out[d] = aa[static_cast<size_t>(d)] * ll;"),
+    "a full table refused": (
+        "return L >= 1 && static_cast<int64_t>(L) <= static_cast<int64_t>(p.max_blocks) * p.bs;",
+        "return L >= 1 && static_cast<int64_t>(L) < static_cast<int64_t>(p.max_blocks) * p.bs;"),
+    "bf16 widened without its shift": ("    const uint32_t wide = static_cast<uint32_t>(bits) << 16;",
+                                       "    const uint32_t wide = static_cast<uint32_t>(bits);"),
+    "eviction norms not squared": ("                        kk += k * k;\n",
+                                   "                        kk += k;\n"),
+    "victim when the newest page is not full": ("        if (L % bs == 0) {\n",
+                                                "        if (L % bs != 0) {\n"),
     "append reads new rows transposed": (
         "const int64_t src = (static_cast<int64_t>(b) * Hkv + j) * D;",
         "const int64_t src = (static_cast<int64_t>(j) * B + b) * D;"),
