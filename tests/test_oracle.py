@@ -457,6 +457,28 @@ def test_oracle_rejects_bad_inputs():
         oracle.decode(q, kp, vp, perm[None], [33], 1.0)   # needs a third table entry
 
 
+def test_append_takes_the_last_slot_of_the_table_and_no_further():
+    # Tables of two 16-token blocks hold positions 0 .. 31: position 31 is
+    # slot 15 of a sequence's second block; position 32 has no block and is
+    # refused (the next row of the table is another sequence's).
+    rng = np.random.default_rng(5)
+    NB, Hkv, bs, D = 4, 2, 16, 8
+    kp = rng.standard_normal((NB, Hkv, bs, D)).astype(np.float32)
+    vp = rng.standard_normal((NB, Hkv, bs, D)).astype(np.float32)
+    kn = rng.standard_normal((2, Hkv, D)).astype(np.float32)
+    vn = rng.standard_normal((2, Hkv, D)).astype(np.float32)
+    table = np.array([[2, 0], [1, 3]], dtype=np.int32)
+    k2, v2 = kp.copy(), vp.copy()
+    oracle.append(kn, vn, k2, v2, table, [31, 0])
+    assert np.array_equal(k2[0, :, 15], kn[0]) and np.array_equal(v2[0, :, 15], vn[0])
+    assert np.array_equal(k2[1, :, 0], kn[1]) and np.array_equal(v2[1, :, 0], vn[1])
+    k2[0, :, 15], v2[0, :, 15] = kp[0, :, 15], vp[0, :, 15]
+    k2[1, :, 0], v2[1, :, 0] = kp[1, :, 0], vp[1, :, 0]
+    assert np.array_equal(k2, kp) and np.array_equal(v2, vp)
+    with pytest.raises(ValueError):
+        oracle.append(kn, vn, kp.copy(), vp.copy(), table, [32, 0])
+
+
 def test_bf16_storage_is_widened_exactly():
     x = np.array([1.0, -2.5, 3.140625, 1e-3, 65504.0], dtype=np.float32)
     bits = bf16_bits(x)

@@ -57,3 +57,17 @@ def test_no_pairs_is_a_no_op():
     k0, v0 = k.copy(), v.copy()
     oracle.copy_blocks(k, v, np.zeros(0, np.int32), np.zeros(0, np.int32))
     assert k.tobytes() == k0.tobytes() and v.tobytes() == v0.tobytes()
+
+
+def test_ids_must_name_a_block_of_the_pool():
+    # Ids run 0 .. NB-1: the last block copies; an id equal to NB is refused.
+    import pytest
+    NB = 6
+    k, v = _pools(NB, 2, 16, 8, "f32", seed=9)
+    kr, vr = k.copy(), v.copy()
+    oracle.copy_blocks(k, v, np.array([NB - 1], np.int32), np.array([0], np.int32))
+    assert np.array_equal(k[0], kr[NB - 1]) and np.array_equal(v[0], vr[NB - 1])
+    for src, dst in ((NB, 0), (0, NB)):
+        with pytest.raises(ValueError):
+            oracle.copy_blocks(k.copy(), v.copy(), np.array([src], np.int32),
+                               np.array([dst], np.int32))

@@ -103,3 +103,13 @@ def test_bf16_storage():
     vf = (vb.astype(np.uint32) << 16).view(np.float32)
     s2, _ = oracle.page_scores(kf, vf, [[3, 0]], [32])
     assert np.array_equal(s, s2)
+
+
+def test_table_entries_must_name_a_block_of_the_pool():
+    # The last block of the pool is scored; an entry equal to NB is refused.
+    NB, Hkv, bs, D = 3, 2, 4, 8
+    k, v = _pool(NB, Hkv, bs, D, seed=4)
+    scores, _ = oracle.page_scores(k, v, [[NB - 1]], [bs])
+    assert np.isfinite(scores[0, 0])
+    with pytest.raises(ValueError):
+        oracle.page_scores(k, v, [[NB]], [bs])

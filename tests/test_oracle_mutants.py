@@ -86,6 +86,13 @@ MUTANTS = {
                                        "    const uint32_t wide = static_cast<uint32_t>(bits);"),
     "eviction norms not squared": ("                        kk += k * k;\n",
                                    "                        kk += k;\n"),
+    "append past the table": ("if (pos < 0 || pos >= static_cast<int64_t>(max_blocks) * bs) return -2;",
+                              "if (pos < 0 || pos > static_cast<int64_t>(max_blocks) * bs) return -2;"),
+    "copy accepts the pool size as an id": ("if (src[i] < 0 || src[i] >= num_blocks ||",
+                                            "if (src[i] < 0 || src[i] > num_blocks ||"),
+    "scores accept the pool size as an entry": (
+        "            if (phys < 0 || phys >= num_blocks) return -3;\n            const int64_t n = std::min",
+        "            if (phys < 0 || phys > num_blocks) return -3;\n            const int64_t n = std::min"),
     "victim when the newest page is not full": ("        if (L % bs == 0) {\n",
                                                 "        if (L % bs != 0) {\n"),
     "append reads new rows transposed": (
