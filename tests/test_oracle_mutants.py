@@ -114,6 +114,16 @@ MUTANTS = {
         "const int32_t phys = table[static_cast<int64_t>(b) * max_blocks + (pos / bs + 1) % max_blocks];"),
     "page mean over the block size": ("= sum / static_cast<double>(n);",
                                       "= sum / static_cast<double>(bs);"),
+    "sampled (sequence, head) pairs read transposed": (
+        "            const int b = pairs ? pairs[2 * i] : static_cast<int>(i / Hq);\n"
+        "            const int h = pairs ? pairs[2 * i + 1] : static_cast<int>(i % Hq);\n"
+        "            if (!attend_one",
+        "            const int b = pairs ? pairs[2 * i + 1] % B : static_cast<int>(i / Hq);\n"
+        "            const int h = pairs ? pairs[2 * i] % Hq : static_cast<int>(i % Hq);\n"
+        "            if (!attend_one"),
+    "prefill query positions counted from the end": (
+        "row_len[static_cast<size_t>(q_start[b] + i)] = seq_lens[b] - n + i + 1;\n",
+        "row_len[static_cast<size_t>(q_start[b] + i)] = seq_lens[b] - i;\n"),
     "no causal mask": ("row_len[static_cast<size_t>(q_start[b] + i)] = seq_lens[b] - n + i + 1;",
                        "row_len[static_cast<size_t>(q_start[b] + i)] = seq_lens[b];"),
     "causal mask one token short": (
