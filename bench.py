@@ -160,22 +160,26 @@ def dist_env():
             int(os.environ.get("LOCAL_RANK", 0)))
 
 
-def _copy_appended(wl):
+def oracle_step_state(wl):
+    """CPU-baseline leg: the workload after the step's append, as the oracle
+    computes it (``oracle.append`` on copies of the host pools)."""
     import dataclasses
-    kp, vp = wl.pools_after_append()
+    import oracle
+    oracle.build()
+    kp, vp = wl.k_pool.copy(), wl.v_pool.copy()
+    oracle.append(wl.k_new, wl.v_new, kp, vp, wl.block_tables, wl.cache_lens)
     return dataclasses.replace(wl, k_pool=kp, v_pool=vp)
 
 
-def oracle_sample_gbs(wl, sample_s: float, min_pairs: int = 1, appended: bool = False):
+def oracle_sample_gbs(wl, sample_s: float, min_pairs: int = 1):
     """Time the fp64 oracle on (b, h) pairs of the workload for about sample_s.
 
-    Returns (GB/s of algorithmic bytes, seconds, pairs, threads). The bytes of
-    one (b, h) pair are sequence b's decode bytes divided by Hq.
+    ``wl`` holds the pools after the append (``oracle_step_state``). Returns
+    (GB/s of algorithmic bytes, seconds, pairs, threads). The bytes of one
+    (b, h) pair are sequence b's decode bytes divided by Hq.
     """
     import oracle
     import paged_kv_cache_202_gb300 as pa
-    if not appended:
-        wl = _copy_appended(wl)
     kp, vp = wl.k_pool, wl.v_pool
     threads = os.cpu_count() or 1
     eb = wl.elem_bytes
@@ -216,14 +220,21 @@ def aggregate_over_ranks(world: int, seconds: float, units: float, device) -> tu
     return float(t.item()), float(u.item())
 
 
-def run_reference(args, rank):
+def decode_config(wl, world: int) -> dict:
+    """The ``config`` of a decode-step line, the same for both arms."""
+    return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
+            "block_size": wl.block_size, "num_blocks": wl.num_blocks,
+            "tokens": int(wl.seq_lens.sum()), "kv_dtype": wl.dtype,
+            "l2": f"inputs larger than L2 ({2 * wl.k_pool.nbytes / 2**30:.2f} GiB of pools vs "
+                  f"{L2_BYTES / 2**20:.0f} MiB L2), no flush",
+            "step": "pa_append_kv + pa_decode", "parallelism": f"replicas x{world}"}
+
+
+def run_reference(args, rank, world):
     if rank != 0:
         return
     from paged_kv_cache_202_gb300.workloads import make_workload
-    import oracle
-    oracle.build()
-    wl = make_workload(args.workload)
-    wl.append_in_place()
+    wl = oracle_step_state(make_workload(args.workload))
     total = args.steps + args.warmup
     per_step = max(0.05, min(20.0, 120.0 / max(total, 1)))
     vals = []
@@ -231,7 +242,7 @@ def run_reference(args, rank):
     pairs_all = 0
     threads = 1
     for step in range(total):
-        gbs, el, pairs, threads = oracle_sample_gbs(wl, per_step, appended=True)
+        gbs, el, pairs, threads = oracle_sample_gbs(wl, per_step)
         if step >= args.warmup:
             vals.append(gbs)
             t_all += el
@@ -242,9 +253,7 @@ def run_reference(args, rank):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * t_all / max(len(vals), 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
-                   "block_size": wl.block_size, "kv_dtype": wl.dtype,
-                   "l2": "inputs larger than L2"},
+        "config": decode_config(wl, world),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"{pairs_all} random (sequence, q-head) rows over "
                                    f"{len(vals)} steps, ~{per_step:.2f} s each"},
@@ -252,6 +261,35 @@ def run_reference(args, rank):
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+def cpu_baseline_leg(wl, out, args, bf: bool):
+    """The oracle on the host cores: timed on a bounded sample of the
+    workload (the CPU baseline), and its values on 64 sampled rows compared
+    with the timed GPU output."""
+    ref_wl = oracle_step_state(wl)
+    parity = None
+    if not args.no_parity:
+        import oracle
+        rng = np.random.default_rng(1)
+        idx = rng.choice(wl.B * wl.Hq, size=min(64, wl.B * wl.Hq), replace=False)
+        pr = np.stack([idx // wl.Hq, idx % wl.Hq], axis=1).astype(np.int32)
+        ref = oracle.decode(ref_wl.q, ref_wl.k_pool, ref_wl.v_pool, wl.block_tables, wl.seq_lens,
+                            wl.scale, pairs=pr)
+        got = out.float().cpu().numpy()[pr[:, 0], pr[:, 1]].astype(np.float64)
+        parity = {"rows": int(len(pr)), "max_abs_err": float(np.abs(got - ref).max()),
+                  "tol": 1.5e-2 if bf else 2e-3}
+    gbs, el, pairs, threads = oracle_sample_gbs(ref_wl, args.cpu_seconds)
+    cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
+           "sample": f"{pairs} (sequence, q-head) rows ({pairs / (wl.B * wl.Hq):.1f} passes "
+                     f"over the workload in random order), {el:.1f} s; bytes per row = its "
+                     f"sequence's decode bytes / Hq"}
+    return cpu, parity
+
+
+# Seconds the timed region spans at least: the K-step loop is repeated until
+# it does, so that the clock sampler (one sample per 100 ms) sees it.
+TIMED_SPAN_S = 2.0
 
 
 def run_ours(args, rank, world, local_rank):
@@ -283,7 +321,6 @@ def run_ours(args, rank, world, local_rank):
     seq_lens = torch.from_numpy(wl.seq_lens).to(dev)
     cache_lens = torch.from_numpy(wl.cache_lens).to(dev)
     torch.cuda.synchronize()
-    wl.append_in_place()   # host copy now holds the post-append state the oracle reads
     out_dtype = torch.bfloat16 if bf else torch.float32
     out = torch.empty(wl.B, wl.Hq, wl.D, dtype=out_dtype, device=dev)
     plan = pa.Plan()
@@ -304,39 +341,56 @@ def run_ours(args, rank, world, local_rank):
     app_bytes = pa.append_bytes(wl.B, wl.Hkv, wl.D, eb)
     step_bytes = dec_bytes + app_bytes
 
-    # Timed region: K steps exactly as a caller issues them. The split and
-    # merge kernels start under programmatic dependent launch, which overlaps
-    # each launch with its predecessor's drain; an event recorded between two
-    # kernels would cancel that overlap, so the step loop carries none.
-    ev_split = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-                for _ in range(args.steps)]
-    for a_, b_ in ev_split:       # create the underlying events before the timed region
+    # Repeats of the K-step loop: enough to span TIMED_SPAN_S, from a probe of
+    # one K-step loop (the same on every rank: the slowest rank's probe).
+    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_a.record(stream)
+    for _ in range(args.steps):
+        step()
+    e_b.record(stream)
+    torch.cuda.synchronize()
+    probe_ms, _ = aggregate_over_ranks(world, e_a.elapsed_time(e_b), 0, dev)
+    repeats = max(1, min(100000, math.ceil(TIMED_SPAN_S * 1e3 / max(probe_ms, 1e-3))))
+
+    # Timed region: R repeats of exactly K steps, each bracketed by a barrier
+    # and a synchronize, issued exactly as a caller issues them. The split
+    # and merge kernels start under programmatic dependent launch, which
+    # overlaps each launch with its predecessor's drain; an event recorded
+    # between two kernels would cancel that overlap, so the step loop carries
+    # none.
+    rep_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(repeats)]
+    for a_, b_ in rep_ev:         # create the underlying events before the timed region
         a_.record(stream)
         b_.record(stream)
     torch.cuda.synchronize()
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
     w0 = time.time()
-    ev0.record(stream)
-    for i in range(args.steps):
-        step()
-    ev1.record(stream)
-    torch.cuda.synchronize()
+    for a_, b_ in rep_ev:
+        barrier()
+        torch.cuda.synchronize()
+        a_.record(stream)
+        for _ in range(args.steps):
+            step()
+        b_.record(stream)
+        torch.cuda.synchronize()
     w1 = time.time()
     barrier()
-    # Kernel pass: the same K steps again, with events around every split
-    # launch, for the split kernel's average duration (the roofline figure),
-    # and around the append and the whole decode call.
-    ev_parts = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    for evs in ev_parts:
-        for e in evs:
+    # Kernel pass: the same number of steps again, with events around every
+    # split launch, for the split kernel's average duration (the roofline
+    # figure), and around the append and the whole decode call.
+    k_steps = max(args.steps, min(repeats * args.steps, 3000))
+    ev_split = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(k_steps)]
+    ev_parts = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(k_steps)]
+    for i in range(k_steps):
+        for e in (*ev_split[i], *ev_parts[i]):
             e.record(stream)
     torch.cuda.synchronize()
-    for i in range(args.steps):
+    w2 = time.time()
+    for i in range(k_steps):
         plan.set_split_events(*ev_split[i])
         ev_parts[i][0].record(stream)
         pa.pa_append_kv(k_new, v_new, k_pool, v_pool, tables, cache_lens, stream)
@@ -344,31 +398,22 @@ def run_ours(args, rank, world, local_rank):
         pa.pa_decode(q, k_pool, v_pool, tables, seq_lens, wl.scale, out, max_len, plan, stream)
         ev_parts[i][2].record(stream)
     torch.cuda.synchronize()
-    w2 = time.time()
+    w3 = time.time()
     plan.set_split_events(None, None)
     time.sleep(0.25)
     sampler.stop()
-    # Slowest rank's time, every rank's bytes and query rows.
-    ms_total, job_bytes = aggregate_over_ranks(world, ev0.elapsed_time(ev1), step_bytes, dev)
+    # Per repeat: the slowest rank's time for K steps; every rank's bytes and query rows.
+    rep_ms = []
+    for a_, b_ in rep_ev:
+        t, _ = aggregate_over_ranks(world, a_.elapsed_time(b_), 0, dev)
+        rep_ms.append(t / args.steps)
+    _, job_bytes = aggregate_over_ranks(world, 0.0, step_bytes, dev)
     _, job_qheads = aggregate_over_ranks(world, 0.0, wl.B * wl.Hq, dev)
-    ms_step = ms_total / args.steps
+    ms_step = statistics.median(rep_ms)
     split_ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ev_split)
     append_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in ev_parts)
     decode_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in ev_parts)
     err = pa.pa_last_device_error(plan)
-
-    # Parity of the timed output against the oracle on sampled rows (rank 0).
-    parity = None
-    if rank == 0 and not args.no_parity:
-        import oracle
-        kp, vp = wl.k_pool, wl.v_pool
-        rng = np.random.default_rng(1)
-        idx = rng.choice(wl.B * wl.Hq, size=min(64, wl.B * wl.Hq), replace=False)
-        pr = np.stack([idx // wl.Hq, idx % wl.Hq], axis=1).astype(np.int32)
-        ref = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale, pairs=pr)
-        got = out.float().cpu().numpy()[pr[:, 0], pr[:, 1]].astype(np.float64)
-        parity = {"rows": int(len(pr)), "max_abs_err": float(np.abs(got - ref).max()),
-                  "tol": 1.5e-2 if bf else 2e-3}
 
     # End to end through the public API: inputs from pinned host memory each step,
     # result read back each step. The step's inputs (q, k_new, v_new, tables,
@@ -390,7 +435,7 @@ def run_ours(args, rank, world, local_rank):
     h_out = torch.empty_like(out, device="cpu").pin_memory()
     h2d = total
     d2h = h_out.numel() * h_out.element_size()
-    e2e_steps = max(1, min(args.steps, 200))
+    e2e_steps = max(args.steps, min(2000, math.ceil(TIMED_SPAN_S * 1e3 / max(ms_step, 1e-3))))
 
     def e2e_calls(s):
         d_in.copy_(h_in, non_blocking=True)
@@ -422,13 +467,9 @@ def run_ours(args, rank, world, local_rank):
     e2e_s, _ = aggregate_over_ranks(world, (time.perf_counter() - t0) / e2e_steps, 0, dev)
     barrier()
 
-    cpu = None
+    cpu, parity = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        gbs, el, pairs, threads = oracle_sample_gbs(wl, args.cpu_seconds, appended=True)
-        cpu = {"value": gbs, "unit": "GB/s", "cores": threads, "kind": "oracle",
-               "sample": f"{pairs} (sequence, q-head) rows ({pairs / (wl.B * wl.Hq):.1f} passes "
-                         f"over the workload in random order), {el:.1f} s; bytes per row = its "
-                         f"sequence's decode bytes / Hq"}
+        cpu, parity = cpu_baseline_leg(wl, out, args, bf)
 
     peak, peak_kind = measured_peak_gbs()
     achieved = dec_bytes / (split_ms * 1e-3) / 1e9
@@ -436,21 +477,22 @@ def run_ours(args, rank, world, local_rank):
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["source_sha"] == sha and \
         TRAFFIC["workload"] == wl.name else None
     value = job_bytes / (ms_step * 1e-3) / 1e9
-    clocks = sampler.summary(w0, w2)
+    clocks = sampler.summary(w0, w1)
+    clocks_kernel_pass = sampler.summary(w2, w3)
     path, blocks, warps = plan.info()
     plan.free()
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+            "ms_per_step_min": min(rep_ms), "ms_per_step_max": max(rep_ms),
+            "repeats": repeats,
+            "timing": f"median over {repeats} repeats of the K-step loop (each bracketed by a "
+                      f"barrier and a synchronize, timed by CUDA events on the launching "
+                      f"stream), {1e-3 * sum(rep_ms) * args.steps:.2f} s timed in all",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
             if bf else "f32", "data": "synthetic",
-            "config": {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
-                       "block_size": wl.block_size, "num_blocks": wl.num_blocks,
-                       "tokens": int(wl.seq_lens.sum()), "kv_dtype": wl.dtype,
-                       "l2": f"inputs larger than L2 ({2 * wl.k_pool.nbytes / 2**30:.2f} GiB "
-                             f"of pools vs {L2_BYTES / 2**20:.0f} MiB L2), no flush",
-                       "step": "pa_append_kv + pa_decode", "parallelism": f"replicas x{world}"},
+            "config": decode_config(wl, world),
             "pct_of_peak": 100.0 * value / world / peak,
             "qheads_per_s": job_qheads / (ms_step * 1e-3),
             "parts_ms": {"append": append_ms, "decode": decode_ms, "split_kernel": split_ms,
@@ -460,17 +502,18 @@ def run_ours(args, rank, world, local_rank):
                          "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                          "frac": achieved / peak, "traffic": traffic,
                          "algorithmic_bytes": dec_bytes, "ms_per_launch": split_ms,
-                         "timing": "CUDA events around each split launch, in a second pass "
-                                   "of the K timed steps"},
+                         "timing": f"CUDA events around each of {k_steps} split launches, in "
+                                   f"a second pass of as many steps"},
             "e2e": {"value": job_bytes / e2e_s / 1e9, "unit": "GB/s",
                     "ms_per_step": e2e_s * 1e3, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h,
+                    "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                     "how": "per step: the inputs from pinned host memory (one staging copy), "
                            "pa_append_kv, pa_decode, the output back, captured once in a CUDA "
                            "graph and replayed, then a wait for the result"},
-            "gpu_launches": 3 * args.steps,
+            "gpu_launches": 3 * args.steps * repeats,
             "cpu_baseline": cpu,
             "clocks": clocks,
+            "clocks_kernel_pass": clocks_kernel_pass,
             "parity": parity,
             "device_error": err,
             "kernel": {"path": {1: "simple", 2: "fma", 3: "mma"}.get(path, path),
@@ -481,9 +524,36 @@ def run_ours(args, rank, world, local_rank):
         torch.distributed.destroy_process_group()
 
 
+def row_cpu_baseline_leg(args, wl, out, qh, qs, ns):
+    """CPU-baseline leg of the multi-query rows: the oracle's state after the
+    step's append, its values on 24 sampled query rows compared with the
+    GPU output, and the oracle timed on a bounded sample of the workload."""
+    import oracle
+    ref_wl = oracle_step_state(wl)
+    parity = None
+    if not args.no_parity:
+        rng = np.random.default_rng(3)
+        T = int(qs[-1])
+        rows = rng.choice(T, size=min(24, T), replace=False)
+        seq_of = np.searchsorted(qs, rows, side="right") - 1
+        err = 0.0
+        for r, b in zip(rows, seq_of):
+            i = r - qs[b]
+            sub = oracle.prefill(qh[r:r + 1], ref_wl.k_pool, ref_wl.v_pool,
+                                 wl.block_tables[b:b + 1], [int(wl.seq_lens[b] - ns[b] + i + 1)],
+                                 [0, 1], wl.scale)
+            got = out[r].float().cpu().numpy().astype(np.float64)
+            err = max(err, float(np.abs(got - sub[0]).max()))
+        parity = {"rows": int(len(rows)), "max_abs_err": err, "tol": 1.5e-2}
+    cpu = row_cpu_baseline(args.row, ref_wl, args.cpu_seconds, prefill_q=qh, prefill_qs=qs,
+                           prefill_ns=ns)
+    return cpu, parity
+
+
 def row_cpu_baseline(row, wl, sample_s, prefill_q=None, prefill_qs=None, prefill_ns=None):
     """The oracle, as it stands, on a bounded random sample of the row's
-    workload on the host cores (about sample_s of CPU work)."""
+    workload on the host cores (about sample_s of CPU work). For the
+    multi-query rows ``wl`` holds the pools after the step's append."""
     import oracle
     rng = np.random.default_rng(5)
     elapsed, units, n = 0.0, 0.0, 0
@@ -560,10 +630,14 @@ def run_row(args, local_rank):
     tables = torch.from_numpy(wl.block_tables).to(dev)
     seq_lens = torch.from_numpy(wl.seq_lens).to(dev)
     eb = wl.elem_bytes
+    if args.row != "copy_blocks":
+        # The step's token goes into the device pools through the library's
+        # append: every token a query or a page score reads is then cached.
+        pa.pa_append_kv(to_dev(wl.k_new), to_dev(wl.v_new), k_pool, v_pool, tables,
+                        torch.from_numpy(wl.cache_lens).to(dev))
+        torch.cuda.synchronize()
     if args.row in ("prefill", "spec"):
         n_new = int(CONFIGS_NEW_TOKENS(args.workload))
-        wl.append_in_place()
-        k_pool, v_pool = to_dev(wl.k_pool), to_dev(wl.v_pool)
         ns = np.minimum(wl.seq_lens, n_new).astype(np.int64)
         qs = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
         T = int(qs[-1])
@@ -637,22 +711,9 @@ def run_row(args, local_rank):
         # Bound by arithmetic intensity: few queries per sequence (speculative
         # verification) make the pass HBM-bound, many (chunked prefill) tensor-bound.
         hbm_bound = flops / nbytes < tpeak * 1e12 / (peak * 1e9)
-        parity = None
-        if not args.no_parity:
-            import oracle
-            rng = np.random.default_rng(3)
-            rows = rng.choice(T, size=min(24, T), replace=False)
-            seq_of = np.searchsorted(qs, rows, side="right") - 1
-            err = 0.0
-            for r, b in zip(rows, seq_of):
-                i = r - qs[b]
-                sub = oracle.prefill(qh[r:r + 1], wl.k_pool, wl.v_pool, wl.block_tables[b:b + 1],
-                                     [int(wl.seq_lens[b] - ns[b] + i + 1)], [0, 1], wl.scale)
-                got = out[r].float().cpu().numpy().astype(np.float64)
-                err = max(err, float(np.abs(got - sub[0]).max()))
-            parity = {"rows": int(len(rows)), "max_abs_err": err, "tol": 1.5e-2}
-        cpu = None if args.no_cpu_baseline else row_cpu_baseline(
-            args.row, wl, args.cpu_seconds, prefill_q=qh, prefill_qs=qs, prefill_ns=ns)
+        cpu, parity = None, None
+        if not args.no_cpu_baseline:
+            cpu, parity = row_cpu_baseline_leg(args, wl, out, qh, qs, ns)
         print(json.dumps({
             "row": args.row,
             **({"metric": "prefill: achieved bf16 TFLOP/s", "value": tfs, "unit": "TFLOP/s"}
@@ -671,7 +732,8 @@ def run_row(args, local_rank):
             "cpu_baseline": cpu,
         }), flush=True)
         return
-    cpu = None if args.no_cpu_baseline else row_cpu_baseline(args.row, wl, args.cpu_seconds)
+    cpu = None if args.no_cpu_baseline else row_cpu_baseline(
+        args.row, wl if args.row == "copy_blocks" else oracle_step_state(wl), args.cpu_seconds)
     print(json.dumps({
         "row": args.row, "metric": f"{args.row}: achieved HBM GB/s", "value": gbs, "unit": "GB/s",
         "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
@@ -688,7 +750,7 @@ def run_row(args, local_rank):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default=None,
@@ -706,7 +768,7 @@ def main():
         args.workload = {"prefill": "prefill_gqa", "spec": "spec_gqa"}.get(args.row, "llama3_8b_gqa")
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
-        run_reference(args, rank)
+        run_reference(args, rank, world)
     elif args.row != "decode":
         run_row(args, local_rank)
     else:

@@ -76,10 +76,16 @@ enum {
 /* Kernel selection for pa_decode (pa_plan_set_path). */
 enum {
     PA_PATH_AUTO = 0,    /* bf16: tensor-core path (any g); f32: simple */
-    PA_PATH_SIMPLE = 1,  /* one warp per (sequence, q head), plain loads, no split */
+    PA_PATH_SIMPLE = 1,  /* one warp per (sequence, q head), plain loads, no split;
+                            max_seq_len <= PA_SIMPLE_MAX_SEQ_LEN */
     PA_PATH_FMA = 2,     /* bf16 only: bulk-staged pages, CUDA-core dot products */
     PA_PATH_MMA = 3      /* bf16 only: bulk-staged pages, a kv head's query heads (any g) through bf16 mma tiles */
 };
+
+/* Longest max_seq_len the unsplit kernel (float32 pools, or PA_PATH_SIMPLE)
+ * accepts: each (sequence, q head) row is one warp walking every token, so a
+ * longer row would serialise; longer calls return PA_ERR_SHAPE. */
+#define PA_SIMPLE_MAX_SEQ_LEN 8192
 
 /* Opaque: split plan, device workspace and device error word. */
 typedef struct pa_plan pa_plan;
@@ -129,7 +135,10 @@ pa_status pa_append_kv(const void* k_new, const void* v_new, void* k_pool, void*
  *   block_tables  device, int32 [B][max_blocks]
  *   seq_lens      device, int32 [B]: tokens attended, >= 1 (includes the token
  *                 appended this step); must be <= max_seq_len
- *   max_seq_len   host bound on every seq_lens[b]; sizes the launch
+ *   max_seq_len   host bound on every seq_lens[b]; sizes the launch. With
+ *                 float32 pools (which run on the unsplit one-warp-per-row
+ *                 kernel) it must be <= PA_SIMPLE_MAX_SEQ_LEN: longer returns
+ *                 PA_ERR_SHAPE
  *   scale         score scale (normally 1/sqrt(D))
  *   out           device, [B][Hq][D] out_dtype (bf16 rounded to nearest even)
  *   plan_inout    in/out: *plan_inout == NULL makes the library create a plan
@@ -169,6 +178,25 @@ pa_status pa_last_device_error(pa_plan* plan, int* err);
  * A forced path that does not support a call's shape makes that call return
  * PA_ERR_DTYPE. */
 pa_status pa_plan_set_path(pa_plan* plan, int path);
+
+/* Test hook for the failure handling. While enable != 0, every kernel this
+ * library launches (decode, multi-query decode, no-alloc decode, prefill,
+ * page scores) makes its first pipeline wait on an mbarrier that nothing
+ * completes, bounded by 20 us, so that the wait expires: the kernel raises
+ * PA_DEVERR_TIMEOUT, waits (bounded) for its own copies and tensor-core
+ * products in flight, frees its tensor memory and returns. The outputs of
+ * such calls are unspecified; the device stays usable and the next call with
+ * the hook off computes normally. Off by default; process-wide (it is read
+ * when a call launches its kernels). Nothing ever waits without a bound. */
+pa_status pa_debug_set_wait_probe(int enable);
+
+/* Force the dynamic tail of later pa_decode / pa_decode_multi calls on this
+ * plan: the last dyn_permille / 1000 of the page stream (0..500) is handed
+ * out in pieces of dyn_pages pages (1..4096) to whichever warp is free, for
+ * any tile; dyn_permille = 0 runs static ranges only. dyn_permille < 0
+ * restores the automatic choice. A test and benchmark hook: the automatic
+ * choice is the measured best for the shapes it was measured on. */
+pa_status pa_plan_set_schedule(pa_plan* plan, int dyn_permille, int dyn_pages);
 
 /* The path the last pa_decode call on this plan launched (PA_PATH_*), the
  * number of thread blocks and warps of its split kernel. Any output pointer
@@ -369,8 +397,15 @@ pa_status pa_page_scores(const void* k_pool, const void* v_pool, const int32_t* 
  *     calls whose work overlaps on the GPU (unordered streams) race on it and
  *     must be serialised by the caller;
  *   - the first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current; a failed lookup (for
+ *     example inside a stream capture) returns PA_ERR_CUDA and is retried by
+ *     the next call;
+ *   - the array is reserved on a device when the library's device code is
+ *     loaded there; with lazy module loading (the CUDA default) that can be
+ *     the first call, which then takes the 16 MiB and may synchronise. Make
+ *     one warm-up call on each device at start-up, before sizing the KV pool
+ *     from the free memory and before any stream capture; later calls
+ *     allocate nothing.
  */
 pa_status pa_decode_noalloc(const void* q, const void* k_pool, const void* v_pool,
                             const int32_t* block_tables, int max_blocks, const int32_t* seq_lens,

@@ -32,6 +32,7 @@ PA_F32, PA_BF16 = 0, 1
 PA_DEVERR_SEQ_LEN, PA_DEVERR_TABLE, PA_DEVERR_TIMEOUT, PA_DEVERR_CACHE_LEN = 1, 2, 4, 8
 PA_DEVERR_COPY = 16
 PA_PATH_AUTO, PA_PATH_SIMPLE, PA_PATH_FMA, PA_PATH_MMA = 0, 1, 2, 3
+PA_SIMPLE_MAX_SEQ_LEN = 8192   # longest max_seq_len of the unsplit kernel (float32 pools)
 
 _lib = None
 
@@ -65,6 +66,10 @@ def lib() -> ctypes.CDLL:
     L.pa_last_device_error.restype = ci
     L.pa_plan_set_path.argtypes = [vp, ci]
     L.pa_plan_set_path.restype = ci
+    L.pa_debug_set_wait_probe.argtypes = [ci]
+    L.pa_debug_set_wait_probe.restype = ci
+    L.pa_plan_set_schedule.argtypes = [vp, ci, ci]
+    L.pa_plan_set_schedule.restype = ci
     L.pa_plan_info.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci), ctypes.POINTER(ci)]
     L.pa_plan_info.restype = ci
     L.pa_plan_set_split_events.argtypes = [vp, vp, vp]
@@ -184,6 +189,12 @@ class Plan:
 
     def set_path(self, path: int) -> None:
         _check(lib().pa_plan_set_path(self.handle, int(path)), "pa_plan_set_path")
+
+    def set_schedule(self, dyn_permille: int, dyn_pages: int = 1) -> None:
+        """Force the dynamic tail (per mille of the page stream, pages per piece);
+        a negative share restores the automatic choice."""
+        _check(lib().pa_plan_set_schedule(self.handle, int(dyn_permille), int(dyn_pages)),
+               "pa_plan_set_schedule")
 
     def info(self) -> tuple[int, int, int]:
         p, b, w = ctypes.c_int(), ctypes.c_int(), ctypes.c_int()
@@ -420,6 +431,12 @@ class BlockManager:
                                           int(block_size), self._i32p(src), self._i32p(dst),
                                           ctypes.byref(n)), "pa_bm_prepare_append")
         return src[:n.value].copy(), dst[:n.value].copy()
+
+
+def pa_debug_set_wait_probe(enable: bool) -> None:
+    """Test hook: while on, each kernel's first pipeline wait expires (bounded),
+    so the kernel reports PA_DEVERR_TIMEOUT and takes its give-up path."""
+    _check(lib().pa_debug_set_wait_probe(1 if enable else 0), "pa_debug_set_wait_probe")
 
 
 def pa_free(plan: Plan) -> None:

@@ -6,6 +6,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -61,27 +62,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Optional override "warps,stages" of the split kernel's block shape.
-void tuning_override(int* warps, int* stages) {
-    const char* s = std::getenv("PA_SPLIT_TUNING");
-    if (!s) return;
-    int w = 0, st = 0;
-    if (std::sscanf(s, "%d,%d", &w, &st) == 2 && w >= 1 && w <= 8 && st >= 1 && st <= 16) {
-        *warps = w;
-        *stages = st;
-    }
-}
-
-// Optional override "permille[,pages]" of the dynamically scheduled share of
-// the page stream (0..500 per mille) and of the pages per dynamic piece.
-void dynamic_override(int* permille, int* pages) {
-    const char* s = std::getenv("PA_SPLIT_DYNAMIC");
-    if (!s) return;
-    int v = -1, p = -1;
-    const int n = std::sscanf(s, "%d,%d", &v, &p);
-    if (n >= 1 && v >= 0 && v <= 500) *permille = v;
-    if (n == 2 && p >= 1 && p <= 4096) *pages = p;
-}
+std::atomic<int> g_wait_probe{0};
 
 struct DeviceGuard {
     int prev = -1;
@@ -98,6 +79,8 @@ struct DeviceGuard {
 
 namespace pa {
 
+int wait_probe() { return g_wait_probe.load(std::memory_order_relaxed); }
+
 bool encode_pool_map(CUtensorMap* map, const void* pool, int rows, int D, int BS) {
     auto fn = encode_fn();
     if (!fn) return false;
@@ -113,7 +96,7 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int rows, int D, int BS
 }
 
 bool split_shape(int kind, int nq, int B, int Hq, int Hkv, int D, int block_size, int max_blocks,
-                 int max_seq_len, bool tunable, SplitShape* out) {
+                 int max_seq_len, SplitShape* out) {
     SplitShape s;
     const int g = Hq / Hkv;
     s.kind = kind;
@@ -150,22 +133,23 @@ bool split_shape(int kind, int nq, int B, int Hq, int Hkv, int D, int block_size
     // SM: two blocks of five (about 168 registers a thread).
     s.warps = s.NT == 2 ? kMultiWarps : kDefaultWarps;
     s.stages = kDefaultStages;
-    if (tunable) tuning_override(&s.warps, &s.stages);
     if (qs) {
         s.stages = 1;  // the query rows stay in the stage for the whole segment
         s.warps = std::min(s.warps, kMultiWarps);  // the kernels' launch bound: 5 warps
     }
-    // ring, mbarriers (8 B each, padded to 16 B), per-stage range records (16 B each)
+    // ring, mbarriers (8 B each, padded to 16 B), per-stage range records (16 B
+    // each), the wait-probe mbarrier (16 B)
     s.smem = 1024 + s.lens_bytes + static_cast<size_t>(s.warps) * s.stages * s.stage_bytes +
              round_up(static_cast<size_t>(s.warps) * s.stages * 8, 16) +
-             static_cast<size_t>(s.warps) * s.stages * 16;
+             static_cast<size_t>(s.warps) * s.stages * 16 + 16;
     if (s.smem > kSmemLimit) return false;
     *out = s;
     return true;
 }
 
 SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t rows, int num_sms,
-                     int per_sm, bool tunable, bool dynamic, int max_blocks) {
+                     int per_sm, bool dynamic, int max_blocks, int force_permille,
+                     int force_pages) {
     SplitGrid gr;
     const int64_t need = (s.P_max + static_cast<int64_t>(s.warps) * kMinPagesPerWarp - 1) /
                          (static_cast<int64_t>(s.warps) * kMinPagesPerWarp);
@@ -205,7 +189,10 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t 
             gr.dyn_pages = 64 / block_size;
         }
     }
-    if (tunable && dynamic) dynamic_override(&gr.dyn_permille, &gr.dyn_pages);
+    if (dynamic && force_permille >= 0) {
+        gr.dyn_permille = force_permille;
+        gr.dyn_pages = force_pages;
+    }
     const int64_t max_pieces = s.P_max * gr.dyn_permille / 1000 / gr.dyn_pages + 1;
     gr.ranges = static_cast<int64_t>(gr.NW) + max_pieces;
     gr.meta_bytes = round_up(static_cast<size_t>(kMetaHeader + B + 1) * 4u, 256);
@@ -234,6 +221,7 @@ struct pa_plan {
     size_t ws_bytes = 0;
     int* err = nullptr;
     int forced_path = PA_PATH_AUTO;
+    int sched_permille = -1, sched_pages = 0;  // forced dynamic tail (pa_plan_set_schedule)
     int last_path = 0, last_blocks = 0, last_warps = 0;
     cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
     MapKey kkey, vkey;
@@ -322,11 +310,12 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     // the Llama-7B MHA workload; PA_PATH_FMA still selects the latter).
     if (path == PA_PATH_AUTO) path = kv_dtype == PA_F32 ? PA_PATH_SIMPLE : PA_PATH_MMA;
     if (kv_dtype == PA_F32 && path != PA_PATH_SIMPLE) return PA_ERR_DTYPE;
+    if (path == PA_PATH_SIMPLE && max_seq_len > PA_SIMPLE_MAX_SEQ_LEN) return PA_ERR_SHAPE;
     const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     pa::SplitShape sh;
     if (path != PA_PATH_SIMPLE &&
         !pa::split_shape(path == PA_PATH_FMA ? pa::kSplitFma : pa::kSplitMma, q_start ? nq : 0, B,
-                         Hq, Hkv, D, block_size, max_blocks, max_seq_len, true, &sh))
+                         Hq, Hkv, D, block_size, max_blocks, max_seq_len, &sh))
         return PA_ERR_SHAPE;
 
     int dev = 0;
@@ -377,7 +366,8 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     }
     const pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size,
                                             static_cast<int64_t>(q_start ? T : B) * Hq,
-                                            plan->num_sms, per_sm, true);
+                                            plan->num_sms, per_sm, true, 0,
+                                            plan->sched_permille, plan->sched_pages);
     L.blocks = gr.blocks;
 
     // Workspace: metadata, partial (m, l), partial value sums.
@@ -434,6 +424,7 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     a.q_start = q_start;
     a.nq = nq;
     a.num_q = T;
+    a.probe_wait = pa::wait_probe();
 
     if (plan->ev_start) cudaEventRecord(plan->ev_start, stream);
     cudaError_t e = pa::launch_split(L, plan->kmap, plan->vmap, a, stream);
@@ -557,6 +548,24 @@ pa_status pa_plan_set_path(pa_plan* plan, int path) {
     if (!plan) return PA_ERR_NULL;
     if (path < PA_PATH_AUTO || path > PA_PATH_MMA) return PA_ERR_SHAPE;
     plan->forced_path = path;
+    return PA_OK;
+}
+
+pa_status pa_debug_set_wait_probe(int enable) {
+    g_wait_probe.store(enable ? 1 : 0, std::memory_order_relaxed);
+    return PA_OK;
+}
+
+pa_status pa_plan_set_schedule(pa_plan* plan, int dyn_permille, int dyn_pages) {
+    if (!plan) return PA_ERR_NULL;
+    if (dyn_permille < 0) {
+        plan->sched_permille = -1;
+        plan->sched_pages = 0;
+        return PA_OK;
+    }
+    if (dyn_permille > 500 || dyn_pages < 1 || dyn_pages > 4096) return PA_ERR_SHAPE;
+    plan->sched_permille = dyn_permille;
+    plan->sched_pages = dyn_pages;
     return PA_OK;
 }
 

@@ -34,6 +34,7 @@ struct ScoreArgs {
     int* err;
     int B, Hkv, D, max_blocks, num_blocks, max_seq_len;
     int stages, stage_bytes, lens_bytes;
+    int probe_wait;    // 1: the first pipeline wait of each warp expires (a test hook)
 };
 
 // Dynamic tail of the score kernel: the last 15 % of the page list in pieces
@@ -96,6 +97,13 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 1) page_score_kernel(const S
     int* len = pre + (a.B + 1);
     const uint32_t ring0 = base + a.lens_bytes;
     const uint32_t bars0 = ring0 + kScoreWarps * a.stages * a.stage_bytes;
+    // After the barriers and page records: an mbarrier that nothing completes
+    // (the wait-expiry probe's first wait).
+    const uint32_t probe_bar = bars0 + kScoreWarps * a.stages * 12;
+    if (threadIdx.x == 0 && a.probe_wait) {
+        mbar_init(probe_bar, 1);
+        fence_barrier_init();
+    }
     const int limit = min(a.max_seq_len, a.max_blocks * BS);
     split::scan_lengths<BS>(a.seq_lens, a.B, limit, pre, len, a.err);
 
@@ -194,7 +202,9 @@ __global__ void __launch_bounds__(kScoreWarps * 32, 1) page_score_kernel(const S
         const int h = n_done % H;  // every page issues its H heads in a row
         const uint32_t bar = my_bars + 8 * s;
         const uint32_t stg = my_ring + s * a.stage_bytes;
-        const bool ready = mbar_wait_bounded(bar, (phase >> s) & 1u, kWaitLimitNs);
+        const bool ready = (a.probe_wait && n_done == 0)
+                               ? mbar_wait_bounded(probe_bar, 0, kProbeLimitNs)
+                               : mbar_wait_bounded(bar, (phase >> s) & 1u, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ready)) {
             if (lane == 0) report(a.err, kErrTimeout);
             for (int j = n_done; j < n_issued; ++j) {
@@ -301,7 +311,8 @@ cudaError_t launch_scores(ScoreArgs a, bool bf16, int num_sms, cudaStream_t stre
     a.lens_bytes = static_cast<int>((static_cast<size_t>(2 * a.B + 1) * 4 + 127) / 128 * 128);
     a.stages = std::max(1, std::min(8, (192 * 1024) / (kScoreWarps * a.stage_bytes)));
     const size_t smem = 128 + a.lens_bytes + static_cast<size_t>(kScoreWarps) * a.stages * a.stage_bytes +
-                        static_cast<size_t>(kScoreWarps) * a.stages * (8 + 4);
+                        static_cast<size_t>(kScoreWarps) * a.stages * (8 + 4) + 8;
+    a.probe_wait = wait_probe();
     auto kern = bf16 ? page_score_kernel<BS, uint16_t> : page_score_kernel<BS, float>;
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -354,7 +365,7 @@ extern "C" pa_status pa_page_scores(const void* k_pool, const void* v_pool,
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return PA_ERR_CUDA;
     pa::ScoreArgs a{k_pool, v_pool, block_tables, seq_lens, scores, victims, device_error,
-                    B, Hkv, D, max_blocks, num_blocks, max_seq_len, 0, 0, 0};
+                    B, Hkv, D, max_blocks, num_blocks, max_seq_len, 0, 0, 0, 0};
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const bool bf16 = kv_dtype == PA_BF16;
     const cudaError_t e = block_size == 16 ? pa::launch_scores<16>(a, bf16, sms, s)

@@ -25,6 +25,13 @@ constexpr int kErrCopy = 16;
 // Wall-clock limit of any single pipeline wait inside a kernel.
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
+// Wait-expiry probe (pa_debug_set_wait_probe): while it is on, kernels make
+// their first pipeline wait on an mbarrier that nothing completes, bounded by
+// this limit, so that the wait expires and the kernel takes its give-up path.
+constexpr uint64_t kProbeLimitNs = 20000;  // 20 us
+// 1 while the probe is on (read at launch time by every launch site).
+int wait_probe();
+
 enum SplitKind { kSplitFma = 0, kSplitMma = 1 };
 
 // Tokens per pipeline stage of the split kernels: two 16-token pages or one
@@ -63,6 +70,7 @@ struct SplitArgs {
     const int32_t* q_start;
     int nq;
     int num_q;                 // T: rows of q and out
+    int probe_wait;            // 1: the first pipeline wait of each warp expires (a test hook)
 };
 
 struct SplitLaunch {
@@ -95,11 +103,11 @@ struct SplitShape {
     size_t stage_bytes = 0, lens_bytes = 0, smem = 0;
 };
 // kind: kSplitFma (one query head per kv unit) or kSplitMma; nq > 0 selects
-// the multi-query tile (nq queries x g heads, tensor cores). tunable: honour
-// the PA_SPLIT_TUNING override of the block shape. Returns false when the
-// sizes do not fit (page count over 32 bits, shared memory over the limit).
+// the multi-query tile (nq queries x g heads, tensor cores). Returns false
+// when the sizes do not fit (page count over 32 bits, shared memory over the
+// limit).
 bool split_shape(int kind, int nq, int B, int Hq, int Hkv, int D, int block_size, int max_blocks,
-                 int max_seq_len, bool tunable, SplitShape* s);
+                 int max_seq_len, SplitShape* s);
 
 // Grid, dynamic tail and workspace carve-up at per_sm resident blocks.
 struct SplitGrid {
@@ -110,11 +118,13 @@ struct SplitGrid {
     size_t workspace_bytes() const { return meta_bytes + ml_bytes + acc_bytes; }
 };
 // rows: output rows the merge writes (B * Hq, or T * Hq with several queries
-// per sequence). tunable: honour the PA_SPLIT_DYNAMIC override of the dynamic
-// tail; dynamic = false plans static ranges only (the fewest partials);
-// max_blocks > 0 caps the grid (fewer warps, fewer partials).
+// per sequence). dynamic = false plans static ranges only (the fewest
+// partials); max_blocks > 0 caps the grid (fewer warps, fewer partials);
+// force_permille >= 0 (with force_pages >= 1) replaces the automatic choice
+// of the dynamic tail, for any tile (a test and benchmark hook).
 SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t rows, int num_sms,
-                     int per_sm, bool tunable, bool dynamic = true, int max_blocks = 0);
+                     int per_sm, bool dynamic = true, int max_blocks = 0,
+                     int force_permille = -1, int force_pages = 0);
 
 // Copies the planned fields (shape, grid, tail) into a.
 void set_split_plan(SplitArgs* a, const SplitShape& s, const SplitGrid& gr);

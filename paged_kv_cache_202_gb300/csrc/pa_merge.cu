@@ -8,8 +8,6 @@
 // too. Segments finished inside one range were already written by the split
 // kernel and are skipped. The merge also resets the split kernel's
 // dynamic-piece counter for the next call.
-#include <cstdlib>
-
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
 
@@ -219,14 +217,10 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
     const int rows = a.rows;
     if (rows == 0) return cudaSuccess;
-    // Warps per row when dynamic pieces cut long segments into many partials
-    // (tuning override PA_MERGE_WARPS = 2, 4 or 8); one warp per row otherwise.
-    static const int wide_warps = [] {
-        const char* e = std::getenv("PA_MERGE_WARPS");
-        const int w = e ? std::atoi(e) : 4;
-        return (w == 2 || w == 4 || w == 8) ? w : 4;
-    }();
-    const int wpr = a.wide ? wide_warps : 1;
+    // Four warps per row when dynamic pieces cut long segments into many
+    // partials (measured against 2 and 8 on the Llama-3-8B GQA step); one warp
+    // per row otherwise.
+    const int wpr = a.wide ? 4 : 1;
     const int rows_per_block = 8 / wpr;
     void (*fn)(MergeArgs) = nullptr;
     if (a.D == 128) {

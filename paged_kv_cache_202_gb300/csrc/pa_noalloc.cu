@@ -21,10 +21,15 @@
 // those do not fit either, on fewer blocks; only a call whose partials would
 // not fit for one block returns PA_ERR_WORKSPACE, before any launch.
 //
-// Set-up. The device address of the array is looked up once per device with
-// cudaGetSymbolAddress, on the first call made while that device is current;
-// host code never passes the array's host-side name to a kernel. That first
-// call should come before any stream capture.
+// Set-up. The device address of the array is looked up per device with
+// cudaGetSymbolAddress, on the first call made while that device is current,
+// and kept once the lookup succeeds (a failed lookup, say during a stream
+// capture or before the device has a context, is retried by the next call);
+// host code never passes the array's host-side name to a kernel. The array
+// itself is reserved on a device when the library's device code is loaded
+// there, which with lazy module loading (the CUDA default) can be that first
+// call: make one warm-up call at start-up, before sizing the KV pool from the
+// free memory and before any stream capture.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -48,24 +53,26 @@ static __device__ __align__(256) unsigned char g_decode_scratch[kNoAllocScratchB
 namespace {
 
 struct DeviceScratch {
-    std::once_flag once;
-    void* ptr = nullptr;
-    cudaError_t status = cudaSuccess;
+    std::mutex mu;
+    void* ptr = nullptr;  // set once a lookup has succeeded
 };
 DeviceScratch g_scratch[kMaxDevices];
 
 // Device address of the scratch array on device `dev` (the current device).
+// Only a successful lookup is kept; a failed one is retried by the next call.
 void* scratch_address(int dev, cudaError_t* status) {
     if (dev < 0 || dev >= kMaxDevices) {
         *status = cudaErrorInvalidDevice;
         return nullptr;
     }
     DeviceScratch& d = g_scratch[dev];
-    std::call_once(d.once, [&d] {
-        d.status = cudaGetSymbolAddress(&d.ptr, g_decode_scratch);
-        if (d.status != cudaSuccess) d.ptr = nullptr;
-    });
-    *status = d.status;
+    std::lock_guard<std::mutex> lk(d.mu);
+    *status = cudaSuccess;
+    if (!d.ptr) {
+        void* p = nullptr;
+        *status = cudaGetSymbolAddress(&p, g_decode_scratch);
+        if (*status == cudaSuccess) d.ptr = p;
+    }
     return d.ptr;
 }
 
@@ -125,7 +132,7 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     const int g = Hq / Hkv;
     pa::SplitShape sh;
     if (!pa::split_shape(pa::kSplitMma, 0, B, Hq, Hkv, D, block_size, max_blocks, max_seq_len,
-                         false, &sh))
+                         &sh))
         return PA_ERR_SHAPE;
 
     int dev = 0, num_sms = 0;
@@ -148,19 +155,20 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     auto fits = [&](const pa::SplitGrid& g) {
         return err_bytes + g.workspace_bytes() <= kNoAllocScratchBytes;
     };
-    pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size, out_rows, num_sms, per_sm, false);
-    if (!fits(gr)) gr = pa::split_grid(sh, B, D, block_size, out_rows, num_sms, per_sm, false, false);
+    pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size, out_rows, num_sms, per_sm);
+    if (!fits(gr)) gr = pa::split_grid(sh, B, D, block_size, out_rows, num_sms, per_sm, false);
     if (!fits(gr)) {
-        // Static ranges only: two partial slots of GS rows of (D sums + m, l)
-        // per warp, plus one spare range; 256 bytes of rounding per array.
-        const size_t per_warp = static_cast<size_t>(2) * sh.GS * (D + 2) * 4u;
-        const size_t head = err_bytes + gr.meta_bytes + 512;
-        const int64_t warps_fit =
-            head < kNoAllocScratchBytes ? static_cast<int64_t>((kNoAllocScratchBytes - head) / per_warp) - 1 : 0;
-        const int blocks_fit = static_cast<int>(std::min<int64_t>(warps_fit / sh.warps, INT32_MAX));
-        if (blocks_fit >= 1)
-            gr = pa::split_grid(sh, B, D, block_size, out_rows, num_sms, per_sm, false, false,
-                                blocks_fit);
+        // The largest grid whose static-range partials fit, found with the
+        // planner itself: the workspace grows with the block count.
+        int lo = 1, hi = gr.blocks;
+        while (lo < hi) {
+            const int mid = lo + (hi - lo + 1) / 2;
+            if (fits(pa::split_grid(sh, B, D, block_size, out_rows, num_sms, per_sm, false, mid)))
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        gr = pa::split_grid(sh, B, D, block_size, out_rows, num_sms, per_sm, false, lo);
     }
     if (!fits(gr)) return PA_ERR_WORKSPACE;
     L.blocks = gr.blocks;
@@ -200,6 +208,7 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     a.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     a.out_bf16 = out_dtype == PA_BF16;
     pa::set_split_plan(&a, sh, gr);
+    a.probe_wait = pa::wait_probe();
     if (pa::launch_split(L, kmap, vmap, a, stream) != cudaSuccess) return PA_ERR_CUDA;
     pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, sh.GS, sh.nslices, sh.U, D,
                     out_dtype == PA_BF16, gr.dyn_permille > 0, B * Hq, nullptr};

@@ -92,9 +92,11 @@ constexpr uint32_t kBarDrain = kBarO + 16;
 constexpr uint32_t kSlotTmem = kBarDrain + 8;
 constexpr uint32_t kSlotAbort = kSlotTmem + 4;
 constexpr uint32_t kSlotSeq = kSlotAbort + 4;
+constexpr uint32_t kBarProbe = kSlotSeq + 8;          // nothing completes it (wait-expiry probe)
 constexpr uint32_t kOffLens = kOffBar + 256;          // [kSortMax] lengths, for the ordering
 constexpr uint32_t kSmemBytes = 1024 + kOffLens + 4 * kSortMax;
-static_assert(kSlotSeq + 4 <= kOffLens - kOffBar, "barrier area overlaps the length array");
+static_assert(kBarProbe % 8 == 0 && kBarProbe + 8 <= kOffLens - kOffBar,
+              "barrier area overlaps the length array");
 static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzle atoms");
 static_assert(kSmemBytes <= 227 * 1024 && 2 * kSmemBytes > 228 * 1024,
               "one block per SM: it holds all 512 tensor-memory columns");
@@ -113,6 +115,7 @@ struct PrefillArgs {
     int max_blocks, num_blocks, max_seq_len;
     float scale_log2;
     int out_bf16;
+    int probe_wait;           // 1: the MMA thread's first wait expires (a test hook)
 };
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
@@ -244,6 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(bars + kBarO + 8 * u, 1);
         }
         mbar_init(bars + kBarDrain, 1);
+        mbar_init(bars + kBarProbe, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -296,12 +300,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 issued = c + 1;
             }
-            if (*abort_flag) {
-                // Copies still in flight land before the block leaves: the
-                // last chunk issued on each stage (its phase is then final).
-                for (int c = max(0, issued - nst); c < issued; ++c)
-                    mbar_wait_bounded(full + 8 * (c % nst), (c / nst) & 1, kWaitLimitNs);
-            }
+            // Copies still in flight land before the block leaves: the last
+            // chunk issued on each stage (its phase is then final; earlier
+            // chunks of a stage were consumed before it was reissued). Without
+            // an abort the consumers have waited for them already.
+            for (int c = max(0, issued - nst); c < issued; ++c)
+                mbar_wait_bounded(full + 8 * (c % nst), (c / nst) & 1, kWaitLimitNs);
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
@@ -331,7 +335,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc::mma_bf16_ts(tmem + col_o(u), tmem + col_s(u) + kk * 8, b0 + kk * (2048 >> 4), hi,
                                     kIdescO, c > 0 || kk > 0);
             };
-            bool ok = wait_role(bars + kBarKFull, 0, abort_flag, a.err);
+            bool ok;
+            if (a.probe_wait) {
+                // The wait-expiry probe: a bounded wait on a barrier nothing
+                // completes, then the abort every other role follows.
+                mbar_wait_bounded(bars + kBarProbe, 0, kProbeLimitNs);
+                *abort_flag = 1;
+                atomicOr(a.err, kErrTimeout);
+                ok = false;
+            } else {
+                ok = wait_role(bars + kBarKFull, 0, abort_flag, a.err);
+            }
             if (ok) {
                 tc::fence_after_sync();
                 issue_s(0, 0);
@@ -516,6 +530,7 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
     a.max_seq_len = max_seq_len;
     a.scale_log2 = scale_log2;
     a.out_bf16 = out_bf16;
+    a.probe_wait = wait_probe();
     if (B > 65535 || Hkv > 65535) return cudaErrorInvalidValue;
     dim3 grid((max_q + 2 * a.Qb - 1) / (2 * a.Qb), Hkv, B);
     auto kern = block_size == 16 ? prefill_kernel<16> : prefill_kernel<32>;

@@ -583,10 +583,16 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
     const uint32_t bars0 = ring0 + static_cast<uint32_t>(W * S * a.stage_bytes);
     // Per stage: range x0, x1, id (16-byte records, so 16-byte aligned).
     const uint32_t meta0 = bars0 + ((static_cast<uint32_t>(W * S * 8) + 15u) & ~15u);
+    // An mbarrier that nothing completes: the wait-expiry probe's first wait.
+    const uint32_t probe_bar = meta0 + static_cast<uint32_t>(W * S * 16);
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(kmap);
         prefetch_tensormap(vmap);
+        if (a.probe_wait) {
+            mbar_init(probe_bar, 1);
+            fence_barrier_init();
+        }
     }
     // Everything below may read what the previous kernel of the stream wrote.
     griddep_wait();
@@ -761,7 +767,9 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
     while (n_done < n_issued) {
         const uint32_t bar = my_bars + 8 * s;
         const uint32_t stg = my_ring + static_cast<uint32_t>(s * a.stage_bytes);
-        const bool ready = mbar_wait_bounded(bar, (phase >> s) & 1u, kWaitLimitNs);
+        const bool ready = (a.probe_wait && n_done == 0)
+                               ? mbar_wait_bounded(probe_bar, 0, kProbeLimitNs)
+                               : mbar_wait_bounded(bar, (phase >> s) & 1u, kWaitLimitNs);
         if (!__all_sync(0xffffffffu, ready)) {
             // Give up: report, wait (bounded) for this warp's copies in flight, return.
             if (lane == 0) atomicOr(a.err, kErrTimeout);

@@ -158,26 +158,6 @@ class Workload:
     def max_seq_len(self) -> int:
         return int(self.seq_lens.max()) if self.B else 1
 
-    def append_in_place(self) -> None:
-        """Write the step's new token into this workload's own pools (numpy index write)."""
-        bs = self.block_size
-        for b in range(self.B):
-            pos = int(self.cache_lens[b])
-            phys = int(self.block_tables[b, pos // bs])
-            self.k_pool[phys, :, pos % bs, :] = self.k_new[b]
-            self.v_pool[phys, :, pos % bs, :] = self.v_new[b]
-
-    def pools_after_append(self):
-        """Copies of the pools with the step's new token written in (numpy index write)."""
-        kp, vp = self.k_pool.copy(), self.v_pool.copy()
-        bs = self.block_size
-        for b in range(self.B):
-            pos = int(self.cache_lens[b])
-            phys = int(self.block_tables[b, pos // bs])
-            kp[phys, :, pos % bs, :] = self.k_new[b]
-            vp[phys, :, pos % bs, :] = self.v_new[b]
-        return kp, vp
-
 
 def _draw_lengths(spec, B: int, rng: np.random.Generator) -> np.ndarray:
     kind = spec[0]

@@ -70,18 +70,29 @@ def _decode(lib, **kw):
     (dict(q=ALIGNED + 8), pa.PA_ERR_ALIGN),
     (dict(out=ALIGNED + 2), pa.PA_ERR_ALIGN),
     (dict(v=ALIGNED + 4), pa.PA_ERR_ALIGN),
+    # float32 pools run on the unsplit kernel, bounded in length
+    (dict(kvdt=pa.PA_F32, odt=pa.PA_F32, maxlen=pa.PA_SIMPLE_MAX_SEQ_LEN + 1, mb=1024),
+     pa.PA_ERR_SHAPE),
+    (dict(kvdt=pa.PA_F32, odt=pa.PA_F32, maxlen=131072, mb=8192), pa.PA_ERR_SHAPE),
 ])
 def test_decode_rejects_bad_arguments_on_host(lib, kw, status):
     assert _decode(lib, **kw) == status
 
 
-def test_decode_late_shape_errors_create_no_plan(lib, monkeypatch):
+def test_decode_late_shape_errors_create_no_plan(lib):
     # Rejected from the sizes alone, before any CUDA call: the page count
-    # over all (sequence, kv head) units overflows 32 bits ...
+    # over all (sequence, kv head) units overflows 32 bits.
     assert _decode(lib, B=8192, Hq=64, Hkv=64, mb=65536, maxlen=1 << 20) == pa.PA_ERR_SHAPE
-    # ... or a forced block shape needs more shared memory than a block has.
-    monkeypatch.setenv("PA_SPLIT_TUNING", "8,16")
-    assert _decode(lib) == pa.PA_ERR_SHAPE
+
+
+def test_library_reads_no_environment_variables(lib):
+    # Launch shapes come from the arguments and explicit plan setters only:
+    # the library's code names no environment variable.
+    import glob
+    import os
+    for src in glob.glob(os.path.join(os.path.dirname(pa.__file__), "csrc", "*")):
+        with open(src) as f:
+            assert "getenv" not in f.read(), src
 
 
 def test_decode_empty_batch_is_a_no_op(lib):
@@ -152,6 +163,13 @@ def test_plan_calls_reject_null(lib):
     assert lib.pa_plan_set_path(None, 0) == pa.PA_ERR_NULL
     assert lib.pa_plan_info(None, None, None, None) == pa.PA_ERR_NULL
     assert lib.pa_plan_set_split_events(None, None, None) == pa.PA_ERR_NULL
+    assert lib.pa_plan_set_schedule(None, 150, 16) == pa.PA_ERR_NULL
+
+
+def test_wait_probe_switch_is_host_only(lib):
+    # Switching the test hook touches no device; it is read at launch time.
+    assert lib.pa_debug_set_wait_probe(1) == pa.PA_OK
+    assert lib.pa_debug_set_wait_probe(0) == pa.PA_OK
     assert lib.pa_last_device_error(None, None) == pa.PA_ERR_NULL
 
 

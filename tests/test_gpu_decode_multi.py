@@ -13,6 +13,7 @@ import torch
 import oracle
 import paged_kv_cache_202_gb300 as pa
 from paged_kv_cache_202_gb300.workloads import bf16_bits, make_workload
+from oracle_steps import append_in_place
 
 from gpu_helpers import BF16_TOL, DeviceStep, out_f64, to_dev
 
@@ -28,7 +29,7 @@ def _built():
 def _case(lens, ns, Hq=32, Hkv=8, bs=16, D=128, seed=0):
     wl = make_workload("llama3_8b_gqa", seed=seed, B=len(lens), Hq=Hq, Hkv=Hkv, D=D,
                        block_size=bs, lengths=("list", lens), max_len=max(lens) + bs)
-    wl.append_in_place()   # the drafted tokens are already in the pools
+    append_in_place(wl)   # the drafted tokens are already in the pools
     rng = np.random.default_rng(seed + 1)
     q = bf16_bits(rng.standard_normal((int(sum(ns)), Hq, D)).astype(np.float32))
     qs = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
@@ -67,16 +68,18 @@ def test_decode_multi_matches_oracle(Hq, Hkv, bs, D, lens, ns):
     assert e <= BF16_TOL, f"max abs error {e:.3e}"
 
 
-@pytest.mark.parametrize("tail", [None, "150,1"])
-def test_long_sequences_merge_many_partials(tail, monkeypatch):
+@pytest.mark.parametrize("tail", [None, (150, 1)])
+def test_long_sequences_merge_many_partials(tail):
     # Long rows are cut by many static ranges; with a forced dynamic tail of
-    # one-page pieces (the tuning override) they are also cut into many
+    # one-page pieces (pa_plan_set_schedule) they are also cut into many
     # pieces and merged four warps per row.
-    if tail:
-        monkeypatch.setenv("PA_SPLIT_DYNAMIC", tail)
     lens, ns = [20000, 17000, 300, 9000], [4, 2, 4, 1]
     wl, q, qs = _case(lens, ns, seed=3)
-    got, err = _run(wl, q, qs, 4)
+    with pa.Plan() as plan:
+        if tail:
+            _run(wl, q, qs, 4, plan)      # creates the plan
+            plan.set_schedule(*tail)
+        got, err = _run(wl, q, qs, 4, plan)
     assert err == 0
     ref = oracle.prefill(q, wl.k_pool, wl.v_pool, wl.block_tables, wl.seq_lens, qs, wl.scale)
     assert np.abs(got - ref).max() <= BF16_TOL
@@ -112,7 +115,7 @@ def test_invalid_query_count_gives_zero_rows_and_an_error():
 
 def test_speculative_workload_full_size_sampled_rows():
     wl = make_workload("spec_gqa")
-    wl.append_in_place()
+    append_in_place(wl)
     ns = np.minimum(wl.seq_lens, 4).astype(np.int64)
     qs = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
     T = int(qs[-1])
@@ -158,19 +161,15 @@ def test_one_plan_alternates_decode_and_multi():
             assert err == 0 and np.array_equal(got, want_multi)
 
 
-def test_launch_shape_and_clamped_override(monkeypatch):
+def test_launch_shape():
     # 16 columns (4 queries x 4 heads) run two blocks of five warps per SM,
-    # the kernel's launch bound; a tuning override asking for more warps per
-    # block is clamped to it rather than failing the launch.
+    # the kernel's launch bound.
     lens, ns = [700, 300, 2000], [4, 4, 3]
     wl, q, qs = _case(lens, ns, seed=12)
     ref = oracle.prefill(q, wl.k_pool, wl.v_pool, wl.block_tables, wl.seq_lens, qs, wl.scale)
-    for override in (None, "8,1"):
-        if override:
-            monkeypatch.setenv("PA_SPLIT_TUNING", override)
-        with pa.Plan() as plan:
-            got, err = _run(wl, q, qs, 4, plan)
-            path, blocks, warps = plan.info()
-        assert err == 0 and path == pa.PA_PATH_MMA
-        assert warps == 5 * blocks
-        assert np.abs(got - ref).max() <= BF16_TOL
+    with pa.Plan() as plan:
+        got, err = _run(wl, q, qs, 4, plan)
+        path, blocks, warps = plan.info()
+    assert err == 0 and path == pa.PA_PATH_MMA
+    assert warps == 5 * blocks
+    assert np.abs(got - ref).max() <= BF16_TOL

@@ -13,6 +13,7 @@ import torch
 import oracle
 import paged_kv_cache_202_gb300 as pa
 from paged_kv_cache_202_gb300.workloads import make_workload
+from oracle_steps import append_in_place
 
 from gpu_helpers import DeviceStep
 
@@ -66,7 +67,7 @@ def test_page_scores_match_oracle(name, extra):
     wl = make_workload(name, **extra)
     ds = DeviceStep(wl)
     ds.append()
-    wl.append_in_place()
+    append_in_place(wl)
     got_s, got_v, err = _run(ds, wl)
     assert err == 0
     ref_s, ref_v = oracle.page_scores(wl.k_pool, wl.v_pool, wl.block_tables, wl.seq_lens)
@@ -77,7 +78,7 @@ def test_page_scores_full_size():
     wl = make_workload("llama3_8b_gqa")
     ds = DeviceStep(wl)
     ds.append()
-    wl.append_in_place()
+    append_in_place(wl)
     got_s, got_v, err = _run(ds, wl)
     assert err == 0
     ref_s, ref_v = oracle.page_scores(wl.k_pool, wl.v_pool, wl.block_tables, wl.seq_lens)
@@ -88,7 +89,7 @@ def test_bad_table_entry_gives_nan_and_no_victim():
     wl = make_workload("llama3_8b_gqa", B=3, lengths=("list", [64, 64, 48]), max_len=64)
     ds = DeviceStep(wl)
     ds.append()
-    wl.append_in_place()
+    append_in_place(wl)
     t = ds.tables.clone()
     t[1, 2] = wl.num_blocks
     got_s, got_v, err = _run(ds, wl, tables=t)

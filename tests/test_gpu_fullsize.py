@@ -10,6 +10,7 @@ import torch
 import oracle
 import paged_kv_cache_202_gb300 as pa
 from paged_kv_cache_202_gb300.workloads import make_workload
+from oracle_steps import append_in_place
 
 from gpu_helpers import DeviceStep, bits, out_f64, tol
 
@@ -33,7 +34,7 @@ def test_full_size_sampled_rows(name, extra):
     wl = make_workload(name, **extra)
     ds = DeviceStep(wl)
     torch.cuda.synchronize()
-    wl.append_in_place()
+    append_in_place(wl)
     with pa.Plan() as plan:
         ds.append()
         out = ds.decode(plan)

@@ -13,6 +13,7 @@ import torch
 import oracle
 import paged_kv_cache_202_gb300 as pa
 from paged_kv_cache_202_gb300.workloads import make_workload
+from oracle_steps import pools_after_append
 
 from gpu_helpers import DeviceStep, bits, out_f64, to_dev, tol
 
@@ -45,7 +46,7 @@ def _built():
 
 
 def _reference(wl):
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     return oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale), kp, vp
 
 
@@ -126,7 +127,7 @@ def test_launch_shape(Hq, Hkv, warps_per_block):
 @pytest.mark.parametrize("key", ["gqa_small", "mha_small", "long_small"])
 def test_physical_permutation_gives_identical_bits(key):
     wl = _wl(key)
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     ds = DeviceStep(wl)
     ds.k_pool.copy_(to_dev(kp, wl.dtype))
     ds.v_pool.copy_(to_dev(vp, wl.dtype))
@@ -147,7 +148,7 @@ def test_physical_permutation_gives_identical_bits(key):
 
 def test_contiguous_layout_equals_paged_layout():
     wl = _wl("gqa_small")
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     ds = DeviceStep(wl)
     ds.k_pool.copy_(to_dev(kp, wl.dtype))
     ds.v_pool.copy_(to_dev(vp, wl.dtype))

@@ -11,6 +11,7 @@ import torch
 import oracle
 import paged_kv_cache_202_gb300 as pa
 from paged_kv_cache_202_gb300.workloads import bf16_bits, make_workload
+from oracle_steps import append_in_place
 
 from gpu_helpers import BF16_TOL, DeviceStep, out_f64, to_dev
 
@@ -31,7 +32,7 @@ _MANY_NS = [int(min(x, y)) for x, y in zip(_MANY_LENS, _rng.integers(1, 20, size
 def _case(lens, ns, Hq=32, Hkv=8, bs=16, seed=0):
     wl = make_workload("llama3_8b_gqa", seed=seed, B=len(lens), Hq=Hq, Hkv=Hkv, block_size=bs,
                        lengths=("list", lens), max_len=max(lens) + bs)
-    wl.append_in_place()   # every token of the chunk is already in the pools
+    append_in_place(wl)   # every token of the chunk is already in the pools
     rng = np.random.default_rng(seed + 1)
     T = int(sum(ns))
     q = bf16_bits(rng.standard_normal((T, Hq, wl.D)).astype(np.float32))
@@ -102,7 +103,7 @@ def test_prefill_full_size_sampled_rows(name):
     oracle on its own (query i of sequence b sees its first L - n + i + 1
     tokens), including the first and last query row of every sequence."""
     wl = make_workload(name)
-    wl.append_in_place()
+    append_in_place(wl)
     ns = np.minimum(wl.seq_lens, 256).astype(np.int64)
     qs = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
     T = int(qs[-1])

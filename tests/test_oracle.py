@@ -16,6 +16,7 @@ from scipy.special import softmax
 
 import oracle
 from paged_kv_cache_202_gb300.workloads import bf16_bits, bits_to_f32, make_workload
+from oracle_steps import pools_after_append
 
 
 def _golden(golden_dir, name):
@@ -189,7 +190,7 @@ def _small(key, seed=None):
 @pytest.mark.parametrize("key", sorted(SMALL))
 def test_oracle_matches_dense_softmax(key):
     wl = _small(key)
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     out = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale)
     assert np.isfinite(out).all()
     np.testing.assert_allclose(out, _dense_reference(wl, kp, vp), rtol=1e-12, atol=1e-13)
@@ -198,7 +199,7 @@ def test_oracle_matches_dense_softmax(key):
 @pytest.mark.parametrize("key", ["gqa_bf16", "bs32_bf16", "shared_bf16"])
 def test_physical_permutation_is_bitwise_invariant(key):
     wl = _small(key)
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     out = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale)
     perm = np.random.default_rng(5).permutation(wl.num_blocks)
     kp2 = np.empty_like(kp)
@@ -212,7 +213,7 @@ def test_physical_permutation_is_bitwise_invariant(key):
 
 def test_sampled_pairs_equal_full_rows():
     wl = _small("gqa_bf16")
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     full = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale)
     pairs = [(4, 31), (0, 0), (2, 17)]
     some = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale, pairs=pairs)
@@ -222,7 +223,7 @@ def test_sampled_pairs_equal_full_rows():
 
 def test_thread_count_does_not_change_bits():
     wl = _small("gqa_bf16")
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     a = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale, nthreads=1)
     b = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale, nthreads=5)
     assert np.array_equal(a, b)
@@ -232,7 +233,7 @@ def test_thread_count_does_not_change_bits():
 
 def test_weights_sum_to_one_and_match_softmax():
     wl = _small("gqa_bf16")
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     for b, h in [(0, 3), (3, 30), (4, 8)]:
         w = oracle.weights(wl.q, kp, wl.block_tables, wl.seq_lens, wl.scale, b, h)
         assert w.shape == (wl.seq_lens[b],)
@@ -243,7 +244,7 @@ def test_weights_sum_to_one_and_match_softmax():
 @pytest.mark.parametrize("seed", [0, 1, 2])
 def test_merge_of_random_splits_equals_one_pass(seed):
     wl = _small("bs32_bf16")
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     full = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale)
     rng = np.random.default_rng(seed)
     for b, h in [(0, 0), (1, 7), (1, 2)]:
@@ -262,7 +263,7 @@ def test_merge_with_leading_and_inner_empty_partials():
     # must merge to the one-pass result (an empty partial contributes
     # nothing, even before any non-empty one has been folded in).
     wl = _small("bs32_bf16")
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     full = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale)
     b, h = 1, 3
     L = int(wl.seq_lens[b])
@@ -432,12 +433,28 @@ def test_append_writes_one_slot_bit_exactly(golden_dir):
     assert np.array_equal(vp[4, 0, 11], v_new[0, 0])
 
 
-def test_append_bf16_and_generator_copy_agree():
+def test_append_puts_each_new_token_at_its_logical_position():
+    # After the append, gathering each sequence's blocks in table order and
+    # reading the flattened token axis gives the new K/V row at logical
+    # position cache_len ("The Cache Was Storing Nothing" §2.2: the table maps
+    # logical blocks to physical ones); no other slot of either pool changes.
     wl = _small("shared_bf16")
     kp, vp = wl.k_pool.copy(), wl.v_pool.copy()
     oracle.append(wl.k_new, wl.v_new, kp, vp, wl.block_tables, wl.cache_lens)
-    kr, vr = wl.pools_after_append()
-    assert np.array_equal(kp, kr) and np.array_equal(vp, vr)
+    bs = wl.block_size
+    for b in range(wl.B):
+        nb = -(-int(wl.seq_lens[b]) // bs)
+        blocks = wl.block_tables[b, :nb]
+        k_tokens = kp[blocks].transpose(1, 0, 2, 3).reshape(wl.Hkv, nb * bs, wl.D)
+        v_tokens = vp[blocks].transpose(1, 0, 2, 3).reshape(wl.Hkv, nb * bs, wl.D)
+        pos = int(wl.cache_lens[b])
+        assert np.array_equal(k_tokens[:, pos], wl.k_new[b])
+        assert np.array_equal(v_tokens[:, pos], wl.v_new[b])
+    # Exactly one (block, kv head, slot) row per (sequence, kv head) changes:
+    # the target slot held the NaN poison, the new row is finite.
+    for new, before in ((kp, wl.k_pool), (vp, wl.v_pool)):
+        rows = np.nonzero((new != before).any(axis=-1))
+        assert len(rows[0]) == wl.B * wl.Hkv
     # The shared prefix blocks are never the append target.
     for b in range(wl.B):
         phys = wl.block_tables[b, wl.cache_lens[b] // wl.block_size]

@@ -13,6 +13,7 @@ import pytest
 
 import oracle
 from paged_kv_cache_202_gb300.workloads import bf16_bits, make_workload
+from oracle_steps import pools_after_append
 
 
 def _pool(NB, Hkv, bs, D, seed=0):
@@ -66,7 +67,7 @@ def test_brute_force_tiny():
 
 def test_tail_slots_and_unused_blocks_are_not_read():
     wl = make_workload("llama3_8b_gqa", B=4, lengths=("list", [17, 32, 5, 48]), max_len=64)
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     s, victims = oracle.page_scores(kp, vp, wl.block_tables, wl.seq_lens)
     for b in range(wl.B):
         nb = -(-int(wl.seq_lens[b]) // 16)
@@ -78,7 +79,7 @@ def test_tail_slots_and_unused_blocks_are_not_read():
 def test_physical_permutation_invariance():
     wl = make_workload("mixed_shared", B=8, shared_prefix_blocks=2, max_len=128,
                        lengths=("geometric", 1 / 40, 1, 128))
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     s, vic = oracle.page_scores(kp, vp, wl.block_tables, wl.seq_lens)
     perm = np.random.default_rng(1).permutation(wl.num_blocks)
     kp2, vp2 = np.empty_like(kp), np.empty_like(vp)

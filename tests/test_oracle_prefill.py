@@ -13,6 +13,7 @@ from scipy.special import softmax
 
 import oracle
 from paged_kv_cache_202_gb300.workloads import bits_to_f32, make_workload
+from oracle_steps import pools_after_append
 
 
 def _wl(lens, **kw):
@@ -32,7 +33,7 @@ def _queries(wl, ns, seed=0):
 
 def test_single_query_equals_decode():
     wl = _wl([40, 17, 64, 1])
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     out = oracle.prefill(wl.q, kp, vp, wl.block_tables, wl.seq_lens, _qs([1, 1, 1, 1]), wl.scale)
     ref = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale)
     assert np.array_equal(out, ref)
@@ -41,7 +42,7 @@ def test_single_query_equals_decode():
 def test_matches_scipy_with_causal_mask():
     lens, ns = [70, 33, 128], [9, 33, 16]
     wl = _wl(lens)
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     q = _queries(wl, ns)
     out = oracle.prefill(q, kp, vp, wl.block_tables, wl.seq_lens, _qs(ns), wl.scale)
     g = wl.Hq // wl.Hkv
@@ -65,7 +66,7 @@ def test_matches_scipy_with_causal_mask():
 def test_future_tokens_are_not_read():
     lens, ns = [50], [20]
     wl = _wl(lens)
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     q = _queries(wl, ns)
     a = oracle.prefill(q, kp, vp, wl.block_tables, wl.seq_lens, _qs(ns), wl.scale)
     # Query 0 sits at position 30: poison tokens 31..49 and its row must not move.
@@ -102,6 +103,6 @@ def test_brute_force_tiny():
 
 def test_rejects_more_queries_than_tokens():
     wl = _wl([8])
-    kp, vp = wl.pools_after_append()
+    kp, vp = pools_after_append(wl)
     with pytest.raises(ValueError):
         oracle.prefill(_queries(wl, [9]), kp, vp, wl.block_tables, wl.seq_lens, _qs([9]), wl.scale)

@@ -59,5 +59,5 @@ def test_reference_arm_nonzero_rank_does_nothing(capsys):
     class Args:
         pass
 
-    assert bench.run_reference(Args(), 1) is None
+    assert bench.run_reference(Args(), 1, 2) is None
     assert capsys.readouterr().out == ""
