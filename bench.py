@@ -287,6 +287,16 @@ def cpu_baseline_leg(wl, out, args, bf: bool):
     return cpu, parity
 
 
+def configure_plan(plan, args):
+    """Explicit plan choices from the command line (merge mode, dynamic tail)."""
+    import paged_kv_cache_202_gb300 as pa
+    if args.merge != "auto":
+        plan.set_merge({"kernel": pa.PA_MERGE_KERNEL, "fused": pa.PA_MERGE_FUSED}[args.merge])
+    if args.schedule:
+        permille, pages = (int(x) for x in args.schedule.split(","))
+        plan.set_schedule(permille, pages)
+
+
 # Seconds the timed region spans at least: the K-step loop is repeated until
 # it does, so that the clock sampler (one sample per 100 ms) sees it.
 TIMED_SPAN_S = 2.0
@@ -331,6 +341,8 @@ def run_ours(args, rank, world, local_rank):
         pa.pa_append_kv(k_new, v_new, k_pool, v_pool, tables, cache_lens, stream)
         pa.pa_decode(q, k_pool, v_pool, tables, seq_lens, wl.scale, out, max_len, plan, stream)
 
+    step()                        # creates the plan
+    configure_plan(plan, args)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -510,14 +522,15 @@ def run_ours(args, rank, world, local_rank):
                     "how": "per step: the inputs from pinned host memory (one staging copy), "
                            "pa_append_kv, pa_decode, the output back, captured once in a CUDA "
                            "graph and replayed, then a wait for the result"},
-            "gpu_launches": 3 * args.steps * repeats,
+            "gpu_launches": (2 if args.merge == "fused" else 3) * args.steps * repeats,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "clocks_kernel_pass": clocks_kernel_pass,
             "parity": parity,
             "device_error": err,
             "kernel": {"path": {1: "simple", 2: "fma", 3: "mma"}.get(path, path),
-                       "blocks": blocks, "warps": warps},
+                       "blocks": blocks, "warps": warps, "merge": args.merge,
+                       "schedule": args.schedule or "auto"},
         }
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -759,6 +772,10 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
+    ap.add_argument("--merge", default="auto", choices=["auto", "kernel", "fused"],
+                    help="how the decode combines split partials (pa_plan_set_merge)")
+    ap.add_argument("--schedule", default=None,
+                    help="permille,pages: force the dynamic tail (pa_plan_set_schedule)")
     ap.add_argument("--row", default="decode",
                     choices=["decode", "copy_blocks", "page_scores", "prefill", "spec"])
     args = ap.parse_args()

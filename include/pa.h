@@ -190,6 +190,21 @@ pa_status pa_plan_set_path(pa_plan* plan, int path);
  * when a call launches its kernels). Nothing ever waits without a bound. */
 pa_status pa_debug_set_wait_probe(int enable);
 
+/* How pa_decode combines the partials of a sequence split across warps
+ * (pa_plan_set_merge). */
+enum {
+    PA_MERGE_AUTO = 0,   /* the measured best for the shape (a second kernel) */
+    PA_MERGE_KERNEL = 1, /* a second, small merge kernel over all split rows */
+    PA_MERGE_FUSED = 2   /* the warp that writes a segment's last partial folds them
+                            (atomic counter per segment, no waiting, no second kernel);
+                            one query per sequence, up to 8 query heads per kv head */
+};
+
+/* Choose the merge of later pa_decode calls on this plan (PA_MERGE_*). A
+ * call whose shape the fused merge does not serve returns PA_ERR_SHAPE while
+ * PA_MERGE_FUSED is set. A test and benchmark hook beside pa_plan_set_path. */
+pa_status pa_plan_set_merge(pa_plan* plan, int mode);
+
 /* Force the dynamic tail of later pa_decode / pa_decode_multi calls on this
  * plan: the last dyn_permille / 1000 of the page stream (0..500) is handed
  * out in pieces of dyn_pages pages (1..4096) to whichever warp is free, for

@@ -32,6 +32,7 @@ PA_F32, PA_BF16 = 0, 1
 PA_DEVERR_SEQ_LEN, PA_DEVERR_TABLE, PA_DEVERR_TIMEOUT, PA_DEVERR_CACHE_LEN = 1, 2, 4, 8
 PA_DEVERR_COPY = 16
 PA_PATH_AUTO, PA_PATH_SIMPLE, PA_PATH_FMA, PA_PATH_MMA = 0, 1, 2, 3
+PA_MERGE_AUTO, PA_MERGE_KERNEL, PA_MERGE_FUSED = 0, 1, 2
 PA_SIMPLE_MAX_SEQ_LEN = 8192   # longest max_seq_len of the unsplit kernel (float32 pools)
 
 _lib = None
@@ -68,6 +69,8 @@ def lib() -> ctypes.CDLL:
     L.pa_plan_set_path.restype = ci
     L.pa_debug_set_wait_probe.argtypes = [ci]
     L.pa_debug_set_wait_probe.restype = ci
+    L.pa_plan_set_merge.argtypes = [vp, ci]
+    L.pa_plan_set_merge.restype = ci
     L.pa_plan_set_schedule.argtypes = [vp, ci, ci]
     L.pa_plan_set_schedule.restype = ci
     L.pa_plan_info.argtypes = [vp, ctypes.POINTER(ci), ctypes.POINTER(ci), ctypes.POINTER(ci)]
@@ -189,6 +192,10 @@ class Plan:
 
     def set_path(self, path: int) -> None:
         _check(lib().pa_plan_set_path(self.handle, int(path)), "pa_plan_set_path")
+
+    def set_merge(self, mode: int) -> None:
+        """PA_MERGE_AUTO, PA_MERGE_KERNEL or PA_MERGE_FUSED for later decodes."""
+        _check(lib().pa_plan_set_merge(self.handle, int(mode)), "pa_plan_set_merge")
 
     def set_schedule(self, dyn_permille: int, dyn_pages: int = 1) -> None:
         """Force the dynamic tail (per mille of the page stream, pages per piece);

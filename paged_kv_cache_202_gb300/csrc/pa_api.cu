@@ -42,6 +42,7 @@ struct OccKey {
     size_t smem;
     int blocks_per_sm;
     int mq;
+    int fused;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -222,6 +223,9 @@ struct pa_plan {
     int* err = nullptr;
     int forced_path = PA_PATH_AUTO;
     int sched_permille = -1, sched_pages = 0;  // forced dynamic tail (pa_plan_set_schedule)
+    int merge_mode = PA_MERGE_AUTO;             // pa_plan_set_merge
+    int last_fused = 0;
+    size_t cnt_clean = 0;  // bytes at the end of the workspace known to be zero
     int last_path = 0, last_blocks = 0, last_warps = 0;
     cudaEvent_t ev_start = nullptr, ev_stop = nullptr;
     MapKey kkey, vkey;
@@ -352,22 +356,28 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     // Split paths (bf16 pools).
     SplitLaunch L{sh.kind, D, block_size, sh.NT, sh.warps, 0, sh.smem};
     L.mq = sh.mq;
+    // The fused merge serves one query per sequence on one n-tile.
+    const bool can_fuse = !q_start && sh.kind == pa::kSplitMma && sh.NT == 1 && sh.warps == 3;
+    L.fused = can_fuse && plan->merge_mode == PA_MERGE_FUSED ? 1 : 0;
+    if (plan->merge_mode == PA_MERGE_FUSED && !can_fuse) return PA_ERR_SHAPE;
     int per_sm = 0;
     for (const OccKey& o : plan->occ) {
         if (o.kind == L.kind && o.D == D && o.BS == block_size && o.NT == L.NT &&
-            o.warps == L.warps && o.smem == L.smem && o.mq == L.mq)
+            o.warps == L.warps && o.smem == L.smem && o.mq == L.mq && o.fused == L.fused)
             per_sm = o.blocks_per_sm;
     }
     if (per_sm == 0) {
         cudaError_t e;
         per_sm = pa::split_blocks_per_sm(L, &e);
         if (e != cudaSuccess || per_sm < 1) return PA_ERR_CUDA;
-        plan->occ.push_back(OccKey{L.kind, D, block_size, L.NT, L.warps, L.smem, per_sm, L.mq});
+        plan->occ.push_back(OccKey{L.kind, D, block_size, L.NT, L.warps, L.smem, per_sm, L.mq,
+                                   L.fused});
     }
-    const pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size,
-                                            static_cast<int64_t>(q_start ? T : B) * Hq,
-                                            plan->num_sms, per_sm, true, 0,
-                                            plan->sched_permille, plan->sched_pages);
+    pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size,
+                                      static_cast<int64_t>(q_start ? T : B) * Hq,
+                                      plan->num_sms, per_sm, true, 0,
+                                      plan->sched_permille, plan->sched_pages);
+    if (L.fused) gr.cnt_bytes = round_up(static_cast<size_t>(B) * sh.U * 4u, 256);
     L.blocks = gr.blocks;
 
     // Workspace: metadata, partial (m, l), partial value sums.
@@ -379,11 +389,27 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
         if (cudaMalloc(&plan->ws, need_ws) != cudaSuccess) return PA_ERR_CUDA;
         if (cudaMemset(plan->ws, 0, need_ws) != cudaSuccess) return PA_ERR_CUDA;  // piece counter = 0
         plan->ws_bytes = need_ws;
+        plan->cnt_clean = need_ws;
     }
     char* ws = static_cast<char*>(plan->ws);
     int* meta = reinterpret_cast<int*>(ws);
     float* ml = reinterpret_cast<float*>(ws + gr.meta_bytes);
     float* acc = reinterpret_cast<float*>(ws + gr.meta_bytes + gr.ml_bytes);
+    // The segment counters of the fused merge sit at the end of the
+    // workspace. A fused call leaves them zero; the plan tracks how many bytes
+    // at the end are known to be zero (all of a fresh workspace, less what
+    // any call's partials have overwritten) and clears the counters when a
+    // call needs more than that.
+    int* cnt = nullptr;
+    if (L.fused) {
+        cnt = reinterpret_cast<int*>(ws + plan->ws_bytes - gr.cnt_bytes);
+        if (plan->cnt_clean < gr.cnt_bytes) {
+            if (cudaMemsetAsync(cnt, 0, gr.cnt_bytes, stream) != cudaSuccess) return PA_ERR_CUDA;
+            plan->cnt_clean = gr.cnt_bytes;
+        }
+    }
+    plan->cnt_clean = std::min(plan->cnt_clean,
+                               plan->ws_bytes - (gr.meta_bytes + gr.ml_bytes + gr.acc_bytes));
 
     const int rows = num_blocks * Hkv;
     MapKey kk{k_pool, rows, D, block_size}, vk{v_pool, rows, D, block_size};
@@ -425,14 +451,19 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     a.nq = nq;
     a.num_q = T;
     a.probe_wait = pa::wait_probe();
+    a.ws_cnt = cnt;
 
     if (plan->ev_start) cudaEventRecord(plan->ev_start, stream);
     cudaError_t e = pa::launch_split(L, plan->kmap, plan->vmap, a, stream);
     if (plan->ev_stop) cudaEventRecord(plan->ev_stop, stream);
     if (e != cudaSuccess) return PA_ERR_CUDA;
-    pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, sh.GS, sh.nslices, sh.U, D,
-                    out_dtype == PA_BF16, gr.dyn_permille > 0, (q_start ? T : B) * Hq, q_start};
-    e = pa::launch_merge(m, stream);
+    plan->last_fused = L.fused;
+    if (!L.fused) {
+        pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, sh.GS, sh.nslices, sh.U, D,
+                        out_dtype == PA_BF16, gr.dyn_permille > 0, (q_start ? T : B) * Hq,
+                        q_start};
+        e = pa::launch_merge(m, stream);
+    }
     plan->last_path = path;
     plan->last_blocks = L.blocks;
     plan->last_warps = gr.NW;
@@ -548,6 +579,13 @@ pa_status pa_plan_set_path(pa_plan* plan, int path) {
     if (!plan) return PA_ERR_NULL;
     if (path < PA_PATH_AUTO || path > PA_PATH_MMA) return PA_ERR_SHAPE;
     plan->forced_path = path;
+    return PA_OK;
+}
+
+pa_status pa_plan_set_merge(pa_plan* plan, int mode) {
+    if (!plan) return PA_ERR_NULL;
+    if (mode < PA_MERGE_AUTO || mode > PA_MERGE_FUSED) return PA_ERR_SHAPE;
+    plan->merge_mode = mode;
     return PA_OK;
 }
 

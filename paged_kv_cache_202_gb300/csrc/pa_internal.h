@@ -9,11 +9,14 @@ namespace pa {
 
 // Workspace metadata written by block 0 of the split kernel and read by the
 // merge kernel: [0] total pages P, [1] pages per static range, [2] warps NW,
-// [3] dynamic-piece counter (zero between calls; the merge kernel resets it),
-// [4] end A of the static part of the page stream, [5] pages per dynamic
-// piece, [6] dynamic pieces, [7] unused, then the page prefix sums pre[0..B]
-// (pre[b] = pages of sequences < b).
-constexpr int kMetaHeader = 8;
+// [3] dynamic-piece counter (zero between calls; the merge kernel resets it,
+// or with the fused merge the last warp to leave the split kernel), [4] end A
+// of the static part of the page stream, [5] pages per dynamic piece, [6]
+// dynamic pieces, [7] warps that have left the split kernel (fused merge;
+// zero between calls), [8] set when a warp gave up (fused merge: the last
+// warp to leave then clears the segment counters), [9] unused, then the page
+// prefix sums pre[0..B] (pre[b] = pages of sequences < b).
+constexpr int kMetaHeader = 10;
 
 // Bits of the device error word (mirrors PA_DEVERR_* in pa.h).
 constexpr int kErrSeqLen = 1;
@@ -71,6 +74,10 @@ struct SplitArgs {
     int nq;
     int num_q;                 // T: rows of q and out
     int probe_wait;            // 1: the first pipeline wait of each warp expires (a test hook)
+    // Fused merge (one query per sequence, one n-tile): ws_cnt[b * U + u]
+    // counts the partials of segment (b, u) written so far (zero between
+    // calls); the warp that writes the last one folds them into the output.
+    int* ws_cnt;
 };
 
 struct SplitLaunch {
@@ -80,6 +87,7 @@ struct SplitLaunch {
     int blocks;    // grid size
     size_t smem;   // dynamic shared memory bytes
     int mq = 0;    // 1: several queries per sequence (tensor-core path only)
+    int fused = 0; // 1: the split kernel merges its own partials (no merge kernel)
 };
 
 // Returns the resident blocks per SM of a split-kernel variant at the given
@@ -115,7 +123,8 @@ struct SplitGrid {
     int dyn_permille = 0, dyn_pages = 0;
     int64_t ranges = 0;            // partial records: static ranges + dynamic pieces
     size_t meta_bytes = 0, ml_bytes = 0, acc_bytes = 0;
-    size_t workspace_bytes() const { return meta_bytes + ml_bytes + acc_bytes; }
+    size_t cnt_bytes = 0;          // segment counters of the fused merge (0 without it)
+    size_t workspace_bytes() const { return meta_bytes + ml_bytes + acc_bytes + cnt_bytes; }
 };
 // rows: output rows the merge writes (B * Hq, or T * Hq with several queries
 // per sequence). dynamic = false plans static ranges only (the fewest

@@ -566,9 +566,110 @@ __device__ __forceinline__ int4 lds_v4i(uint32_t addr) {
     return v;
 }
 
-template <int D, int BS, typename State, bool MQ = false>
+// Number of ranges that hold part of pages [x0, x1) of the stream: static
+// ranges of `per` pages up to A, then dynamic pieces of qd pages. Each writes
+// one partial of a segment that occupies those pages.
+__device__ __forceinline__ int ranges_over(int x0, int x1, int per, int A, int qd) {
+    int n = 0;
+    if (x0 < A) n += (min(x1, A) - 1) / per - x0 / per + 1;
+    if (x1 > A) n += (x1 - 1 - A) / qd - (max(x0, A) - A) / qd + 1;
+    return n;
+}
+
+// Fused merge: fold the partials of the segment on pages [x0, x1) for its nh
+// query-head columns and write the normalised rows row0 .. row0 + nh - 1 --
+// the two-partial rule of "39 · PagedAttention" §3 applied to batches of
+// partials against a running maximum (log2 domain), as the merge kernel does.
+// Run by the warp that wrote the segment's last partial; the partials of
+// other warps are read from L2 (ld.global.cg), past the fence that published
+// them.
+template <int D>
+__device__ __forceinline__ void fold_segment(const SplitArgs& a, int x0, int x1, int per, int A,
+                                          int NW, int qd, size_t row0, int nh, int lane) {
+    constexpr int DPL = D / 32;
+    constexpr int kBatch = 8;
+    auto range_of = [&](int x) { return x < A ? x / per : NW + (x - A) / qd; };
+    auto holds = [&](int r) { return r >= NW || static_cast<long long>(r) * per < A; };
+    const int rf = range_of(x0), rl = range_of(x1 - 1);
+    const int d0 = lane * DPL;
+    for (int j = 0; j < nh; ++j) {
+        float m = -INFINITY, l = 0.f, acc[DPL];
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] = 0.f;
+        bool poison = false;
+        for (int r0 = rf; r0 <= rl; r0 += kBatch) {
+            float mi[kBatch], li[kBatch], v[kBatch][DPL];
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const int r = r0 + k;
+                mi[k] = -INFINITY;
+                li[k] = 0.f;
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) v[k][i] = 0.f;
+                if (r <= rl && holds(r)) {
+                    const size_t base = static_cast<size_t>(r == rf ? 2 * r + 1 : 2 * r) * a.GS + j;
+                    const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.ws_ml) + base);
+                    mi[k] = ml.x;
+                    li[k] = ml.y;
+                    const float* src = a.ws_acc + base * D + d0;
+                    if constexpr (DPL == 4) {
+                        const float4 t = __ldcg(reinterpret_cast<const float4*>(src));
+                        v[k][0] = t.x; v[k][1] = t.y; v[k][2] = t.z; v[k][3] = t.w;
+                    } else {
+                        const float2 t = __ldcg(reinterpret_cast<const float2*>(src));
+                        v[k][0] = t.x; v[k][1] = t.y;
+                    }
+                }
+            }
+            float mb = m;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                poison |= mi[k] != mi[k];   // the poison marker of a bad table entry
+                mb = fmaxf(mb, mi[k]);      // fmaxf passes over NaN
+            }
+            if (mb == -INFINITY) continue;
+            const float fo = fast_exp2(m - mb);
+            l *= fo;
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) acc[i] *= fo;
+#pragma unroll
+            for (int k = 0; k < kBatch; ++k) {
+                const float f = fast_exp2(mi[k] - mb);
+                l = fmaf(li[k], f, l);
+#pragma unroll
+                for (int i = 0; i < DPL; ++i) acc[i] = fmaf(v[k][i], f, acc[i]);
+            }
+            m = mb;
+        }
+        // A poisoned partial (bad table entry) makes the sums NaN: the row is
+        // written as zeros, not scaled by zero.
+        const bool zero = poison || !(l > 0.f);
+        const float inv = zero ? 0.f : 1.f / l;
+#pragma unroll
+        for (int i = 0; i < DPL; ++i) acc[i] = zero ? 0.f : acc[i];
+        const size_t o = (row0 + j) * D + d0;
+        if (a.out_bf16) {
+            uint16_t* dst = static_cast<uint16_t*>(a.out) + o;
+            if constexpr (DPL == 4) {
+                uint2 w;
+                w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+                w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+                *reinterpret_cast<uint2*>(dst) = w;
+            } else {
+                *reinterpret_cast<uint32_t*>(dst) = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+            }
+        } else {
+            float* dst = static_cast<float*>(a.out) + o;
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) dst[i] = acc[i] * inv;
+        }
+    }
+}
+
+template <int D, int BS, typename State, bool MQ = false, bool FUSED = false>
 __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtensorMap* vmap,
                                            const SplitArgs& a) {
+    static_assert(!(MQ && FUSED), "the fused merge serves one query per sequence");
     static_assert(!MQ || State::kQS, "the multi-query tile reads its query rows from the stage");
     constexpr int CT = kChunkTokens;
     constexpr int CP = CT / BS;  // pages per chunk
@@ -625,6 +726,43 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
         }
     }
     const int gw = blockIdx.x * W + warp;
+    if constexpr (FUSED) {
+        // No merge kernel follows: rows of invalid sequences get zeros here.
+        for (int b = gw; b < a.B; b += NW) {
+            if (len[b] != 0) continue;
+            const size_t row0 = static_cast<size_t>(b) * a.Hq * D;
+            for (int i = lane; i < a.Hq * D; i += 32) {
+                if (a.out_bf16) static_cast<uint16_t*>(a.out)[row0 + i] = 0;
+                else static_cast<float*>(a.out)[row0 + i] = 0.f;
+            }
+        }
+    }
+    // Every warp calls this once, as it leaves (warp-collective). With the
+    // fused merge the last warp of the grid to leave resets the dynamic-piece
+    // counter for the next call and, if any warp gave up, the segment
+    // counters (whose partials may never have arrived).
+    auto leave = [&](bool gave_up) {
+        if constexpr (FUSED) {
+            int done = 0;
+            if (lane == 0) {
+                if (gave_up) atomicExch(a.ws_meta + 8, 1);
+                __threadfence();
+                done = atomicAdd(a.ws_meta + 7, 1);
+            }
+            done = __shfl_sync(0xffffffffu, done, 0);
+            if (done == NW - 1) {
+                __threadfence();
+                const bool clear = *reinterpret_cast<volatile int*>(a.ws_meta + 8) != 0;
+                if (clear)
+                    for (int i = lane; i < a.B * a.U; i += 32) a.ws_cnt[i] = 0;
+                if (lane == 0) {
+                    a.ws_meta[3] = 0;
+                    a.ws_meta[7] = 0;
+                    a.ws_meta[8] = 0;
+                }
+            }
+        }
+    };
     const uint32_t my_bars = bars0 + warp * S * 8;
     const uint32_t my_meta = meta0 + warp * S * 16;
     const uint32_t my_ring = ring0 + static_cast<uint32_t>(warp * S * a.stage_bytes);
@@ -654,7 +792,10 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
 
     Range ri{gw * per, min(gw * per + per, A), gw};
     if (ri.x0 >= ri.x1) ri = claim();
-    if (ri.id < 0) return;
+    if (ri.id < 0) {
+        leave(false);
+        return;
+    }
     Cursor ci = locate(ri.x0);
     int xi = ri.x0;
     bool issue_done = false;
@@ -777,6 +918,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
                 const int sj = j % S;
                 mbar_wait_bounded(my_bars + 8 * sj, (phase >> sj) & 1u, kWaitLimitNs);
             }
+            leave(true);
             return;
         }
         phase ^= 1u << s;
@@ -830,12 +972,32 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
                 st.template finish<true>(a, cc.b, hq0, nh, full, poison, slot, lane, qrow0);
             else
                 st.finish(a, cc.b, hq0, nh, full, poison, slot, lane);
+            if constexpr (FUSED) {
+                if (!full) {
+                    // Publish this partial, count it; the warp that writes the
+                    // segment's last partial folds them all.
+                    __threadfence();
+                    __syncwarp();
+                    const int x0 = a.U * pre[cc.b] + cc.u * cc.nb;
+                    const int parts = ranges_over(x0, x0 + cc.nb, per, A, qd);
+                    int prev = 0;
+                    if (lane == 0) prev = atomicAdd(a.ws_cnt + cc.b * a.U + cc.u, 1);
+                    prev = __shfl_sync(0xffffffffu, prev, 0);
+                    if (prev == parts - 1) {
+                        __threadfence();
+                        fold_segment<D>(a, x0, x0 + cc.nb, per, A, NW, qd,
+                                        static_cast<size_t>(cc.b) * a.Hq + hq0, nh, lane);
+                        if (lane == 0) a.ws_cnt[cc.b * a.U + cc.u] = 0;
+                    }
+                }
+            }
         }
         for (int j = 0; j < n; ++j) advance(cc, pre, a.U, a.B);
         xc += n;
         ++n_done;
         if (++s == S) s = 0;
     }
+    leave(false);
 }
 
 }  // namespace split

@@ -164,6 +164,7 @@ def test_plan_calls_reject_null(lib):
     assert lib.pa_plan_info(None, None, None, None) == pa.PA_ERR_NULL
     assert lib.pa_plan_set_split_events(None, None, None) == pa.PA_ERR_NULL
     assert lib.pa_plan_set_schedule(None, 150, 16) == pa.PA_ERR_NULL
+    assert lib.pa_plan_set_merge(None, pa.PA_MERGE_FUSED) == pa.PA_ERR_NULL
 
 
 def test_wait_probe_switch_is_host_only(lib):

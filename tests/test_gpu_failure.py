@@ -161,3 +161,25 @@ def test_page_scores_give_up_report_and_recover(probe):
     for b in range(B):
         nb = -(-int(wl.seq_lens[b]) // wl.block_size)
         np.testing.assert_allclose(got[b, :nb], ref_s[b, :nb], rtol=1e-4)
+
+
+def test_fused_merge_gives_up_reports_and_recovers(probe):
+    # With the fused merge a warp that gave up leaves its segments' counters
+    # short; the last warp to leave clears them, so the next call is exact.
+    wl = _gqa(36)
+    ds = DeviceStep(wl)
+    ds.append()
+    kp, vp = pools_after_append(wl)
+    ref = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale)
+    with pa.Plan() as plan:
+        ds.decode(plan)
+        plan.set_merge(pa.PA_MERGE_FUSED)
+        plan.set_schedule(150, 1)
+        with probe:
+            ds.decode(plan)
+            err = plan.last_device_error()
+        assert err & pa.PA_DEVERR_TIMEOUT
+        for _ in range(2):
+            out = ds.decode(plan)
+            assert plan.last_device_error() == 0
+            assert np.abs(out_f64(out) - ref).max() <= BF16_TOL

@@ -326,3 +326,92 @@ def test_python_binding_raises_on_bad_arguments():
             pa.pa_decode(ds.q, ds.k_pool, ds.v_pool, ds.tables, ds.seq_lens, wl.scale, ds.out, 0,
                          plan)
         assert ei.value.status == pa.PA_ERR_SHAPE
+
+
+# ---------------------------------------------------------------- fused merge
+
+@pytest.mark.parametrize("key", ["gqa_small", "mha_small", "long_small", "mixed_small"])
+def test_fused_merge_matches_oracle(key):
+    # The warp that writes a segment's last partial folds them: no merge
+    # kernel. Two calls in a row (the segment counters must come back to
+    # zero), with the automatic tail and with a forced tail of one-page
+    # pieces (many partials per segment).
+    wl = _wl(key)
+    ref, _, _ = _reference(wl)
+    ds = DeviceStep(wl)
+    ds.append()
+    with pa.Plan() as plan:
+        ds.decode(plan)
+        plan.set_merge(pa.PA_MERGE_FUSED)
+        for tail in (None, (150, 1), (0, 1)):
+            if tail:
+                plan.set_schedule(*tail)
+            for _ in range(2):
+                out = ds.decode(plan)
+                torch.cuda.synchronize()
+                assert plan.last_device_error() == 0
+                err = np.abs(out_f64(out) - ref).max()
+                assert err <= tol(wl), f"{key}/{tail}: max abs error {err:.3e}"
+
+
+def test_fused_merge_after_other_calls_on_the_same_plan():
+    # A workspace whose end held another call's partials: the fused call must
+    # clear its counters first. Shapes alternate between a long batch (large
+    # workspace) and a short one, with and without the fused merge.
+    big, small = _wl("long_small"), _wl("gqa_small")
+    refs = {id(w): _reference(w)[0] for w in (big, small)}
+    steps = {id(w): DeviceStep(w) for w in (big, small)}
+    for ds in steps.values():
+        ds.append()
+    with pa.Plan() as plan:
+        for wl, mode in ((big, pa.PA_MERGE_KERNEL), (small, pa.PA_MERGE_FUSED),
+                         (big, pa.PA_MERGE_KERNEL), (big, pa.PA_MERGE_FUSED),
+                         (small, pa.PA_MERGE_KERNEL), (small, pa.PA_MERGE_FUSED)):
+            ds = steps[id(wl)]
+            ds.decode(plan)
+            plan.set_merge(mode)
+            plan.set_schedule(150, 1)
+            out = ds.decode(plan)
+            torch.cuda.synchronize()
+            assert plan.last_device_error() == 0
+            assert np.abs(out_f64(out) - refs[id(wl)]).max() <= tol(wl)
+
+
+def test_fused_merge_bad_inputs_give_zero_rows():
+    wl = _wl("gqa_small")
+    ref, _, _ = _reference(wl)
+    ds = DeviceStep(wl)
+    ds.append()
+    bad_b = int(np.argmax(wl.seq_lens))
+    t = ds.tables.clone()
+    t[bad_b, 1] = wl.num_blocks + 5
+    sl = ds.seq_lens.clone()
+    sl[0 if bad_b else 1] = 0
+    zero_b = 0 if bad_b else 1
+    ds.tables, ds.seq_lens = t, sl
+    with pa.Plan() as plan:
+        ds.decode(plan)
+        plan.set_merge(pa.PA_MERGE_FUSED)
+        plan.set_schedule(150, 1)
+        plan.last_device_error()
+        for _ in range(2):
+            out = ds.decode(plan)
+            err = plan.last_device_error()
+            assert err & pa.PA_DEVERR_TABLE and err & pa.PA_DEVERR_SEQ_LEN
+            got = out_f64(out)
+            assert (got[bad_b] == 0).all() and (got[zero_b] == 0).all()
+            keep = [b for b in range(wl.B) if b not in (bad_b, zero_b)]
+            assert np.abs(got[keep] - ref[keep]).max() <= tol(wl)
+
+
+def test_fused_merge_refuses_shapes_it_does_not_serve():
+    # 16 query heads per kv head run two n-tiles: no fused merge.
+    wl = _exact(32, 2, 128, 16, [100, 300], seed=78)
+    ds = DeviceStep(wl)
+    ds.append()
+    with pa.Plan() as plan:
+        ds.decode(plan)
+        plan.set_merge(pa.PA_MERGE_FUSED)
+        with pytest.raises(pa.PagedAttentionError) as ei:
+            ds.decode(plan)
+        assert ei.value.status == pa.PA_ERR_SHAPE
