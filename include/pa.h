@@ -235,9 +235,11 @@ pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
  * diagnosis"; each row is exactly the decode attention over its prefix). The
  * K/V of the new tokens must already be in the pools.
  *
- *   q         device bf16 [q_start[B]][Hq][D], rows of sequence b at
+ *   q         device bf16 [num_queries][Hq][D], rows of sequence b at
  *             q_start[b] .. q_start[b+1]-1
  *   q_start   device int32 [B + 1], nondecreasing, q_start[0] = 0
+ *   num_queries  host: rows of q and out (q_start[B]); a sequence whose rows
+ *             fall outside them is refused on the device
  *   max_q     host bound on every n_b (sizes the launch)
  *   out       device [q_start[B]][Hq][D] out_dtype
  *   device_error  device int or NULL (NULL = the library-wide word read by
@@ -246,11 +248,13 @@ pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
  * Supported: bf16 pools, D = 128, block_size 16 or 32, Hq / Hkv dividing 128,
  * max_blocks <= 16384. Built for many queries per sequence (chunked prefill);
  * with a few (max_q * Hq / Hkv <= 16, e.g. speculative verification)
- * pa_decode_multi computes the same rows at the decode's bandwidth. n_b < 1, n_b > L_b or L_b out of range raise
- * PA_DEVERR_SEQ_LEN and leave that sequence's rows untouched; a table entry
- * outside the pool raises PA_DEVERR_TABLE and zeroes the affected rows.
+ * pa_decode_multi computes the same rows at the decode's bandwidth. n_b < 1, n_b > L_b,
+ * L_b out of range or rows outside [0, num_queries) raise PA_DEVERR_SEQ_LEN
+ * and leave that sequence's rows untouched; a table entry outside the pool
+ * raises PA_DEVERR_TABLE and zeroes the affected rows.
  */
-pa_status pa_prefill(const void* q, const int32_t* q_start, const void* k_pool, const void* v_pool,
+pa_status pa_prefill(const void* q, const int32_t* q_start, int num_queries, const void* k_pool,
+                     const void* v_pool,
                      const int32_t* block_tables, int max_blocks, const int32_t* seq_lens, int B,
                      int Hq, int Hkv, int D, int block_size, int num_blocks, int max_q,
                      int max_seq_len, float scale, pa_dtype kv_dtype, void* out, pa_dtype out_dtype,

@@ -92,8 +92,8 @@ def lib() -> ctypes.CDLL:
     L.pa_bm_num_free.argtypes = [vp, ctypes.POINTER(ci)]
     L.pa_bm_prepare_append.argtypes = [vp, i32p, ci, ci, i32p, ci, i32p, i32p,
                                        ctypes.POINTER(ci)]
-    L.pa_prefill.argtypes = [vp, vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf, ci, vp,
-                             ci, vp, vp]
+    L.pa_prefill.argtypes = [vp, vp, ci, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, ci, ci, cf, ci,
+                             vp, ci, vp, vp]
     L.pa_prefill.restype = ci
     L.pa_decode_multi.argtypes = [vp, vp, ci, ci, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, ci, cf,
                                   ci, vp, ci, ctypes.POINTER(vp), vp]
@@ -341,7 +341,7 @@ def pa_prefill(q: torch.Tensor, q_start: torch.Tensor, k_pool: torch.Tensor,
     _on_one_device(q, q_start, device_error)
     _expect(q_start, "q_start", (B + 1,), torch.int32)
     err = _error_word(device_error)
-    st = lib().pa_prefill(_ptr(q), _ptr(q_start), _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
+    st = lib().pa_prefill(_ptr(q), _ptr(q_start), T, _ptr(k_pool), _ptr(v_pool), _ptr(block_tables),
                           MB, _ptr(seq_lens), B, Hq, Hkv, D, bs, NB, int(max_q),
                           int(max_seq_len), float(scale), _dtype(k_pool), _ptr(out), _dtype(out),
                           err, _stream(stream))

@@ -511,7 +511,7 @@ pa_status pa_copy_blocks(void* k_pool, void* v_pool, const int32_t* copy_src,
                : PA_ERR_CUDA;
 }
 
-pa_status pa_prefill(const void* q, const int32_t* q_start, const void* k_pool,
+pa_status pa_prefill(const void* q, const int32_t* q_start, int num_queries, const void* k_pool,
                      const void* v_pool, const int32_t* block_tables, int max_blocks,
                      const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
                      int num_blocks, int max_q, int max_seq_len, float scale, pa_dtype kv_dtype,
@@ -523,7 +523,7 @@ pa_status pa_prefill(const void* q, const int32_t* q_start, const void* k_pool,
     if (block_size != 16 && block_size != 32) return PA_ERR_BLOCK_SIZE;
     if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D != 128 || num_blocks < 1 ||
         max_blocks < 1 || max_blocks > 16384 || max_q < 1 || max_seq_len < 1 ||
-        !std::isfinite(scale))
+        !std::isfinite(scale) || num_queries < 0)
         return PA_ERR_SHAPE;
     const int g = Hq / Hkv;
     if (g > 128 || 128 % g != 0) return PA_ERR_SHAPE;  // a block holds 128 / g whole queries
@@ -532,7 +532,7 @@ pa_status pa_prefill(const void* q, const int32_t* q_start, const void* k_pool,
         return PA_ERR_SHAPE;
     if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
         return PA_ERR_ALIGN;
-    if (B == 0) return PA_OK;
+    if (B == 0 || num_queries == 0) return PA_OK;
     CUtensorMap kmap, vmap;
     if (!pa::encode_pool_map(&kmap, k_pool, num_blocks * Hkv, D, block_size) ||
         !pa::encode_pool_map(&vmap, v_pool, num_blocks * Hkv, D, block_size))
@@ -540,8 +540,8 @@ pa_status pa_prefill(const void* q, const int32_t* q_start, const void* k_pool,
     int* err = device_error;
     if (!err && pa::append_error_address(&err) != cudaSuccess) return PA_ERR_CUDA;
     const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    return pa::launch_prefill(kmap, vmap, q, q_start, block_tables, seq_lens, out, err, B, Hq, Hkv,
-                              max_blocks, num_blocks, max_seq_len, max_q, scale_log2,
+    return pa::launch_prefill(kmap, vmap, q, num_queries, q_start, block_tables, seq_lens, out,
+                              err, B, Hq, Hkv, max_blocks, num_blocks, max_seq_len, max_q, scale_log2,
                               out_dtype == PA_BF16, block_size,
                               reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? PA_OK

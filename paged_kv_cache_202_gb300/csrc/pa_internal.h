@@ -195,9 +195,9 @@ cudaError_t read_append_error(int* err);
 cudaError_t append_error_address(int** p);
 
 cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, const void* q,
-                           const int32_t* q_start, const int32_t* tables, const int32_t* seq_lens,
-                           void* out, int* err, int B, int Hq, int Hkv, int max_blocks,
-                           int num_blocks, int max_seq_len, int max_q, float scale_log2,
-                           int out_bf16, int block_size, cudaStream_t stream);
+                           int num_q, const int32_t* q_start, const int32_t* tables,
+                           const int32_t* seq_lens, void* out, int* err, int B, int Hq, int Hkv,
+                           int max_blocks, int num_blocks, int max_seq_len, int max_q,
+                           float scale_log2, int out_bf16, int block_size, cudaStream_t stream);
 
 }  // namespace pa

@@ -11,21 +11,23 @@
 //
 // One block = two query tiles of the same (sequence, kv head) that share the
 // K/V stream, with specialised warps:
-//   * warps 8 and 10 (producers): tiled bulk tensor copies of 128-token K
+//   * warps 16 and 18 (producers): tiled bulk tensor copies of 128-token K
 //     and V chunks (whole pages, through the block table) into a 2-stage K
 //     ring and a 3-stage V ring, each stream on its own warp so that a wait
 //     for a free V stage never holds back the next K;
-//   * warp 9 (MMA): one thread issues S_t = Q_t K^T (M=128, N=128, K=128,
+//   * warp 17 (MMA): one thread issues S_t = Q_t K^T (M=128, N=128, K=128,
 //     both operands in shared memory) into tensor memory and
 //     O_t += P_t V (M=128, N=128, K=128) with P_t read from tensor memory and
 //     V read MN-major straight from the page layout, for both tiles t, and
 //     signals completion through tcgen05.commit on mbarriers;
-//   * warps 0-3 / 4-7 (softmax, one warpgroup per tile, one thread per row):
-//     load the row's 128 scores from tensor memory, scale (log2 domain), mask
-//     causally by predicate, run the online softmax and store the bf16
-//     probabilities P_t over the first 64 columns of the same scores (the
-//     A operand of the PV product); at the end, read the row of O_t,
-//     normalise and store it.
+//   * warps 0-7 / 8-15 (softmax, two warpgroups per tile, two threads per
+//     row, each on 64 of the row's 128 scores, tensor memory read in the
+//     16-lane 16x32bx2 shape so that the partner threads sit in one warp):
+//     load the scores from tensor memory, scale (log2 domain), mask causally
+//     by predicate, join the row maximum with the partner (one shuffle), run
+//     the online softmax and store the bf16 probabilities P_t over the first
+//     64 columns of the same scores (the A operand of the PV product); at the
+//     end, read the row of O_t, normalise and store it.
 // The MMA thread issues PV_0(c), S_0(c+1), PV_1(c), S_1(c+1), ...: one
 // thread's products run in issue order, so S_t(c+1) overwrites P_t(c) only
 // after PV_t(c) has read it, and its completion (one commit covers every
@@ -60,10 +62,11 @@ constexpr int kChunk = 128;     // tokens per K/V chunk
 constexpr int kD = 128;         // head dimension
 constexpr int kStagesK = 2;     // K ring depth
 constexpr int kStagesV = 3;     // V ring depth (PV waits on V last)
-constexpr int kSoftmaxThreads = 2 * kRows;
-constexpr int kWarpLoad = kSoftmaxThreads / 32;  // warp 8: K copies
-constexpr int kWarpMma = kWarpLoad + 1;          // warp 9
-constexpr int kWarpLoadV = kWarpMma + 1;         // warp 10: V copies
+constexpr int kTileThreads = 2 * kRows;            // softmax threads of a tile: two per row
+constexpr int kSoftmaxThreads = 2 * kTileThreads;   // two tiles
+constexpr int kWarpLoad = kSoftmaxThreads / 32;     // warp 16: K copies
+constexpr int kWarpMma = kWarpLoad + 1;             // warp 17
+constexpr int kWarpLoadV = kWarpMma + 1;            // warp 18: V copies
 constexpr int kThreads = kSoftmaxThreads + 96;
 constexpr int kSortMax = 256;   // sequences ordered by length up to this batch size
 constexpr uint32_t kTmemCols = 512;
@@ -112,6 +115,7 @@ struct PrefillArgs {
     void* out;                // [T][Hq][D]
     int* err;
     int B, Hq, Hkv, g, Qb;    // Qb = queries per tile = 128 / g
+    int num_q;                // rows of q and out
     int max_blocks, num_blocks, max_seq_len;
     float scale_log2;
     int out_bf16;
@@ -124,11 +128,13 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
-__device__ __forceinline__ void write_row(const PrefillArgs& a, size_t row, const float* v, float inv,
-                                          int d0, int nd) {
+template <int ND>
+__device__ __forceinline__ void write_row(const PrefillArgs& a, size_t row, const float (&v)[ND],
+                                          float inv, int d0) {
     if (a.out_bf16) {
         uint16_t* o = static_cast<uint16_t*>(a.out) + row * kD + d0;
-        for (int i = 0; i < nd; i += 8) {
+#pragma unroll
+        for (int i = 0; i < ND; i += 8) {
             uint4 w;
             w.x = pack_bf16x2(v[i] * inv, v[i + 1] * inv);
             w.y = pack_bf16x2(v[i + 2] * inv, v[i + 3] * inv);
@@ -138,7 +144,8 @@ __device__ __forceinline__ void write_row(const PrefillArgs& a, size_t row, cons
         }
     } else {
         float* o = static_cast<float*>(a.out) + row * kD + d0;
-        for (int i = 0; i < nd; i += 4)
+#pragma unroll
+        for (int i = 0; i < ND; i += 4)
             *reinterpret_cast<float4*>(o + i) =
                 make_float4(v[i] * inv, v[i + 1] * inv, v[i + 2] * inv, v[i + 3] * inv);
     }
@@ -197,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n = a.q_start[b + 1] - qs;
     const int L = a.seq_lens[b];
     const int limit = min(a.max_seq_len, a.max_blocks * BS);
-    if (n < 1 || L < n || L > limit) {
+    if (n < 1 || L < n || L > limit || qs < 0 || qs + n > a.num_q) {
         if (blockIdx.x == 0 && h == 0 && tid == 0) atomicOr(a.err, kErrSeqLen);
         return;  // rows of an invalid sequence are left untouched
     }
@@ -211,8 +218,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nb = (ntok + BS - 1) / BS;
     const int32_t* table = a.tables + static_cast<size_t>(b) * a.max_blocks;
 
-    // This thread's query row (softmax warps): tile t, row r of the tile.
-    const int t = tid >> 7, row = tid & (kRows - 1);
+    // This thread's query row (softmax warps): tile t, row r of the tile, and
+    // which half of the row's 128 columns it holds. The 8 warps of a tile
+    // cover the tile's 128 tensor-memory lanes in 16-lane groups, each warp
+    // within its lane quarter (32 * (warp % 4) + 0 or 16); threads i and
+    // i + 16 of a warp share a row.
+    const int t = tid / kTileThreads;
+    const int quarter = warp & 3, sub16 = (warp >> 2) & 1, half = lane >> 4;
+    const int row = 32 * quarter + 16 * sub16 + (lane & 15);
     const bool softmax = tid < kSoftmaxThreads;
     const int qi = row / a.g, qj = row - qi * a.g;
     const bool row_valid = softmax && qi < (t == 0 ? nq0 : nq1);
@@ -227,8 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (__syncthreads_or(bad)) {
         if (tid == 0) atomicOr(a.err, kErrTable);
         if (row_valid) {
-            float z[kD] = {};
-            write_row(a, out_row, z, 0.f, 0, kD);
+            float z[kD / 2] = {};
+            write_row<kD / 2>(a, out_row, z, 0.f, 64 * half);
         }
         return;
     }
@@ -243,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int u = 0; u < 2; ++u) {
             mbar_init(bars + kBarS + 8 * u, 1);
-            mbar_init(bars + kBarP + 8 * u, kRows);
+            mbar_init(bars + kBarP + 8 * u, kTileThreads);
             mbar_init(bars + kBarO + 8 * u, 1);
         }
         mbar_init(bars + kBarDrain, 1);
@@ -255,16 +268,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::alloc(bars + kSlotTmem, kTmemCols);
         tc::relinquish();
     }
-    // Query rows -> swizzled K-major tiles (two 64-column halves each).
+    // Query rows -> swizzled K-major tiles (two 64-column halves each); each
+    // thread moves its half of the row.
     if (softmax) {
-        const uint16_t* src = a.q + out_row * kD;
-        const uint32_t qt = base + kOffQ + t * kTileQ;
+        const uint16_t* src = a.q + out_row * kD + 64 * half;
+        const uint32_t qt = base + kOffQ + t * kTileQ + half * 16384 + row * 128;
 #pragma unroll
-        for (int c = 0; c < 16; ++c) {
-            const uint4 w = row_valid ? *reinterpret_cast<const uint4*>(src + c * 8)
+        for (int cc = 0; cc < 8; ++cc) {
+            const uint4 w = row_valid ? *reinterpret_cast<const uint4*>(src + cc * 8)
                                       : make_uint4(0, 0, 0, 0);
-            const int half = c >> 3, cc = c & 7;
-            st_shared_v4(qt + half * 16384 + row * 128 + ((cc ^ (row & 7)) << 4), w);
+            st_shared_v4(qt + ((cc ^ (row & 7)) << 4), w);
         }
     }
     fence_proxy_async_smem();
@@ -392,7 +405,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
     } else if (t == 0 || two) {
         // ------------------------------------------------------------ softmax (tile t)
-        const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+        // Two threads per row: thread half h holds the row's scores of tokens
+        // 64h .. 64h + 63 of each chunk and writes their probabilities to P
+        // columns 32h .. 32h + 31; the row maximum and, at the end, the row
+        // sum are joined with the partner thread (lane ^ 16).
+        const uint32_t lane_base = static_cast<uint32_t>(32 * quarter + 16 * sub16) << 16;
         const uint32_t s_addr = tmem + lane_base + col_s(t);
         const uint32_t o_addr = tmem + lane_base + col_o(t);
         const int pos_r = L - n + q0 + t * a.Qb + qi;  // last token this row sees
@@ -403,24 +420,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, wait_role(bars + kBarS + 8 * t, c & 1, abort_flag, a.err));
             if (!ok) break;
             tc::fence_after_sync();
-            float sv[kChunk];
-#pragma unroll
-            for (int i = 0; i < kChunk / 32; ++i)
-                tc::ld32(s_addr + 32 * i, *reinterpret_cast<float(*)[32]>(sv + 32 * i));
+            float sv[kChunk / 2];
+            tc::ld16x2_32<64>(s_addr, *reinterpret_cast<float(*)[32]>(sv));
+            tc::ld16x2_32<64>(s_addr + 32, *reinterpret_cast<float(*)[32]>(sv + 32));
             tc::wait_ld();
             // Causal mask by predicate; the warp skips it when no row needs it.
-            const int tok0 = c * kChunk;
-            if (!__all_sync(0xffffffffu, row_valid && tok0 + kChunk - 1 <= pos_r)) {
+            const int tok0 = c * kChunk + 64 * half;
+            if (!__all_sync(0xffffffffu, row_valid && c * kChunk + kChunk - 1 <= pos_r)) {
 #pragma unroll
-                for (int i = 0; i < kChunk; ++i)
+                for (int i = 0; i < kChunk / 2; ++i)
                     sv[i] = (row_valid && tok0 + i <= pos_r) ? sv[i] : -INFINITY;
             }
-            // Row max: three-input max over pairs, four short chains.
+            // Row max: three-input max over pairs, four short chains, then the
+            // partner's half.
             float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-            for (int i = 0; i < kChunk / 2; ++i) mq[i & 3] = max3(mq[i & 3], sv[2 * i], sv[2 * i + 1]);
-            // scale > 0, so this is the max of the scaled scores
-            const float mx = max3(mq[0], mq[1], fmaxf(mq[2], mq[3])) * a.scale_log2;
+            for (int i = 0; i < kChunk / 4; ++i) mq[i & 3] = max3(mq[i & 3], sv[2 * i], sv[2 * i + 1]);
+            float mx = max3(mq[0], mq[1], fmaxf(mq[2], mq[3]));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            mx *= a.scale_log2;  // scale > 0, so this is the max of the scaled scores
             // Raise the reference max only when the chunk exceeds it by > 2^8.
             float alpha = 1.f;
             if (mx > m + kRescaleLog2) {
@@ -429,52 +447,52 @@ __global__ void __launch_bounds__(kThreads, 1)
                 l *= alpha;
             }
             const float m_use = m == -INFINITY ? 0.f : m;
-            // P = 2^(s * scale - m) (bf16 pairs) over the first 64 columns of
-            // this row's scores; the arguments and the row sum two at a time.
+            // P = 2^(s * scale - m) (bf16 pairs) over P columns 32h .. 32h + 31
+            // of this row; the arguments and the partial row sum two at a time.
             const uint64_t sc2 = f32x2(a.scale_log2, a.scale_log2), nm2 = f32x2(-m_use, -m_use);
             uint64_t ps2[2] = {f32x2(0.f, 0.f), f32x2(0.f, 0.f)};
 #pragma unroll
-            for (int h2 = 0; h2 < kChunk / 64; ++h2) {
-                uint32_t pw[32];
+            for (int h2 = 0; h2 < 2; ++h2) {
+                uint32_t pw[16];
 #pragma unroll
-                for (int i = 0; i < 32; ++i) {
+                for (int i = 0; i < 16; ++i) {
                     const float2 x = f32x2_split(
-                        fma_f32x2(f32x2(sv[64 * h2 + 2 * i], sv[64 * h2 + 2 * i + 1]), sc2, nm2));
+                        fma_f32x2(f32x2(sv[32 * h2 + 2 * i], sv[32 * h2 + 2 * i + 1]), sc2, nm2));
                     const float p0 = fast_exp2(x.x), p1 = fast_exp2(x.y);
                     ps2[i & 1] = add_f32x2(ps2[i & 1], f32x2(p0, p1));
                     pw[i] = pack_bf16x2(p0, p1);
                 }
-                tc::st32u(s_addr + 32 * h2, pw);
+                tc::st16x2_16u<32>(s_addr + 16 * h2, pw);
             }
             {
                 const float2 s0 = f32x2_split(ps2[0]), s1 = f32x2_split(ps2[1]);
                 l += (s0.x + s0.y) + (s1.x + s1.y);
             }
-            // Rescale this row of O_t if the reference max moved (PV_t(c-1) is done).
+            // Rescale this row's half of O_t if the reference max moved (PV_t(c-1) is done).
             if (c > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
 #pragma unroll
-                for (int piece = 0; piece < kD / 32; ++piece) {
+                for (int piece = 0; piece < 2; ++piece) {
                     float o[32];
-                    tc::ld32(o_addr + piece * 32, o);
+                    tc::ld16x2_32<64>(o_addr + 32 * piece, o);
                     tc::wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] *= alpha;
-                    tc::st32(o_addr + piece * 32, o);
+                    tc::st16x2_32<64>(o_addr + 32 * piece, o);
                 }
             }
             // Final chunk: tile 0 zeroes the V rows past the last token (both
             // tiles' products run after tile 0 has published its P).
             if (t == 0 && c == nc - 1) {
-                const int valid = ntok - tok0;
+                const int valid = ntok - c * kChunk;
                 // V of this chunk arrives on its own barrier.
                 ok = __all_sync(0xffffffffu, wait_role(bars + kBarVFull + 8 * (c % kStagesV),
                                                        (c / kStagesV) & 1, abort_flag, a.err));
                 if (!ok) break;
                 if (valid < kChunk) {
                     const uint32_t vst = base + kOffV + (c % kStagesV) * kStageKV;
-                    for (int idx = tid; idx < (kChunk - valid) * 16; idx += kRows) {
-                        const int r = valid + (idx >> 4), half = (idx >> 3) & 1, ch = idx & 7;
-                        st_shared_v4(vst + half * kHalfKV + r * 128 + ch * 16, make_uint4(0, 0, 0, 0));
+                    for (int idx = tid; idx < (kChunk - valid) * 16; idx += kTileThreads) {
+                        const int r = valid + (idx >> 4), hf = (idx >> 3) & 1, ch = idx & 7;
+                        st_shared_v4(vst + hf * kHalfKV + r * 128 + ch * 16, make_uint4(0, 0, 0, 0));
                     }
                 }
                 fence_proxy_async_smem();
@@ -487,13 +505,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, wait_role(bars + kBarO + 8 * t, 0, abort_flag, a.err));
             if (ok) {
                 tc::fence_after_sync();
-                const float inv = (row_valid && l > 0.f) ? 1.f / l : 0.f;
+                const float lt = l + __shfl_xor_sync(0xffffffffu, l, 16);
+                const float inv = (row_valid && lt > 0.f) ? 1.f / lt : 0.f;
 #pragma unroll
-                for (int piece = 0; piece < kD / 32; ++piece) {
+                for (int piece = 0; piece < 2; ++piece) {
                     float o[32];
-                    tc::ld32(o_addr + piece * 32, o);
+                    tc::ld16x2_32<64>(o_addr + 32 * piece, o);
                     tc::wait_ld();
-                    if (row_valid) write_row(a, out_row, o, inv, piece * 32, 32);
+                    if (row_valid) write_row<32>(a, out_row, o, inv, 64 * half + 32 * piece);
                 }
             }
         }
@@ -509,10 +528,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, const void* q,
-                           const int32_t* q_start, const int32_t* tables, const int32_t* seq_lens,
-                           void* out, int* err, int B, int Hq, int Hkv, int max_blocks,
-                           int num_blocks, int max_seq_len, int max_q, float scale_log2,
-                           int out_bf16, int block_size, cudaStream_t stream) {
+                           int num_q, const int32_t* q_start, const int32_t* tables,
+                           const int32_t* seq_lens, void* out, int* err, int B, int Hq, int Hkv,
+                           int max_blocks, int num_blocks, int max_seq_len, int max_q,
+                           float scale_log2, int out_bf16, int block_size, cudaStream_t stream) {
     PrefillArgs a{};
     a.q = static_cast<const uint16_t*>(q);
     a.q_start = q_start;
@@ -525,6 +544,7 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
     a.Hkv = Hkv;
     a.g = Hq / Hkv;
     a.Qb = kRows / a.g;
+    a.num_q = num_q;
     a.max_blocks = max_blocks;
     a.num_blocks = num_blocks;
     a.max_seq_len = max_seq_len;

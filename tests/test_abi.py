@@ -229,12 +229,13 @@ def test_binding_rejects_host_tensors():
 # CUDA call, so these run without a GPU.
 
 def _prefill(lib, **kw):
-    args = dict(q=ALIGNED, qs=ALIGNED, k=ALIGNED, v=ALIGNED, bt=ALIGNED, mb=4, sl=ALIGNED, B=2,
-                Hq=8, Hkv=2, D=128, bs=16, NB=64, maxq=4, maxlen=64, scale=0.1, kvdt=pa.PA_BF16,
-                out=ALIGNED, odt=pa.PA_BF16)
+    args = dict(q=ALIGNED, qs=ALIGNED, T=8, k=ALIGNED, v=ALIGNED, bt=ALIGNED, mb=4, sl=ALIGNED,
+                B=2, Hq=8, Hkv=2, D=128, bs=16, NB=64, maxq=4, maxlen=64, scale=0.1,
+                kvdt=pa.PA_BF16, out=ALIGNED, odt=pa.PA_BF16)
     args.update(kw)
-    return lib.pa_prefill(args["q"], args["qs"], args["k"], args["v"], args["bt"], args["mb"],
-                          args["sl"], args["B"], args["Hq"], args["Hkv"], args["D"], args["bs"],
+    return lib.pa_prefill(args["q"], args["qs"], args["T"], args["k"], args["v"], args["bt"],
+                          args["mb"], args["sl"], args["B"], args["Hq"], args["Hkv"], args["D"],
+                          args["bs"],
                           args["NB"], args["maxq"], args["maxlen"], args["scale"], args["kvdt"],
                           args["out"], args["odt"], None, None)
 
@@ -247,6 +248,7 @@ def _prefill(lib, **kw):
     (dict(D=64), pa.PA_ERR_SHAPE),                # the tcgen05 tiles are built for D = 128
     (dict(Hq=24, Hkv=8), pa.PA_ERR_SHAPE),        # g = 3 does not divide the 128-row tile
     (dict(maxq=0), pa.PA_ERR_SHAPE),
+    (dict(T=-1), pa.PA_ERR_SHAPE),
     (dict(scale=float("inf")), pa.PA_ERR_SHAPE),
     (dict(k=ALIGNED + 4), pa.PA_ERR_ALIGN),
 ])
@@ -256,6 +258,7 @@ def test_prefill_rejects_bad_arguments_on_host(lib, kw, status):
 
 def test_prefill_empty_batch_is_a_no_op(lib):
     assert _prefill(lib, B=0) == pa.PA_OK
+    assert _prefill(lib, T=0) == pa.PA_OK
 
 
 def _scores(lib, **kw):

@@ -96,6 +96,26 @@ def test_prefill_bad_lengths_and_table():
     assert np.abs(got[:10] - ref).max() <= BF16_TOL
 
 
+def test_prefill_rows_past_the_query_array_are_refused():
+    # q_start says 20 rows, but q and out hold 15: the second sequence's rows
+    # would fall outside them, so it is refused (PA_DEVERR_SEQ_LEN, rows
+    # untouched) and nothing is read or written past the arrays.
+    wl, q, qs = _case([100, 50], [10, 10])
+    ds = DeviceStep(wl)
+    qd = to_dev(q[:15], "bf16")
+    out = torch.full((15, wl.Hq, wl.D), 7.0, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_prefill(qd, torch.from_numpy(qs).cuda(), ds.k_pool, ds.v_pool, ds.tables, ds.seq_lens,
+                  wl.scale, out, 10, wl.max_seq_len, device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.PA_DEVERR_SEQ_LEN
+    got = out_f64(out)
+    assert (got[10:] == 7.0).all()
+    ref = oracle.prefill(q[:10], wl.k_pool, wl.v_pool, wl.block_tables[:1], wl.seq_lens[:1],
+                         qs[:2], wl.scale)
+    assert np.abs(got[:10] - ref).max() <= BF16_TOL
+
+
 @pytest.mark.parametrize("name", ["prefill_gqa", "llama3_8b_gqa"])
 def test_prefill_full_size_sampled_rows(name):
     """The benchmark's workloads at full size (the newest 256 tokens of every
