@@ -37,8 +37,8 @@ L2_BYTES = 126 * 2**20
 # DRAM traffic of the split-attention kernel from an ncu capture (per launch,
 # scaled to the full workload), valid only for the kernel sources it was
 # measured on (sha256 of the split kernel's source files).
-TRAFFIC = {"source_sha": "3a8bec0b37495f3882534aff9dbd3d0fe60e4223f68b0f1ff843af5e6fa792ee",
-           "workload": "llama3_8b_gqa", "bytes_per_launch": 2205654272 + 5797888}
+TRAFFIC = {"source_sha": "deaf1e3f7c1a96631784a68e6003b4384edca453f4f56b0e7356700c6509a914",
+           "workload": "llama3_8b_gqa", "bytes_per_launch": 2205606912 + 5019520}
 
 
 def split_source_sha() -> str:
@@ -297,8 +297,9 @@ def configure_plan(plan, args):
         plan.set_schedule(permille, pages)
 
 
-# Seconds the timed region spans at least: the K-step loop is repeated until
-# it does, so that the clock sampler (one sample per 100 ms) sees it.
+# Seconds the timed region spans at least (--span): the K-step loop is
+# repeated until it does, so that the clock sampler (one sample per 100 ms)
+# sees it.
 TIMED_SPAN_S = 2.0
 
 
@@ -362,7 +363,7 @@ def run_ours(args, rank, world, local_rank):
     e_b.record(stream)
     torch.cuda.synchronize()
     probe_ms, _ = aggregate_over_ranks(world, e_a.elapsed_time(e_b), 0, dev)
-    repeats = max(1, min(100000, math.ceil(TIMED_SPAN_S * 1e3 / max(probe_ms, 1e-3))))
+    repeats = max(1, min(100000, math.ceil(args.span * 1e3 / max(probe_ms, 1e-3))))
 
     # Timed region: R repeats of exactly K steps, each bracketed by a barrier
     # and a synchronize, issued exactly as a caller issues them. The split
@@ -447,7 +448,7 @@ def run_ours(args, rank, world, local_rank):
     h_out = torch.empty_like(out, device="cpu").pin_memory()
     h2d = total
     d2h = h_out.numel() * h_out.element_size()
-    e2e_steps = max(args.steps, min(2000, math.ceil(TIMED_SPAN_S * 1e3 / max(ms_step, 1e-3))))
+    e2e_steps = max(args.steps, min(2000, math.ceil(args.span * 1e3 / max(ms_step, 1e-3))))
 
     def e2e_calls(s):
         d_in.copy_(h_in, non_blocking=True)
@@ -772,6 +773,9 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
+    ap.add_argument("--span", type=float, default=TIMED_SPAN_S,
+                    help="seconds the timed region spans at least (0: exactly K steps, "
+                         "e.g. under a profiler)")
     ap.add_argument("--merge", default="auto", choices=["auto", "kernel", "fused"],
                     help="how the decode combines split partials (pa_plan_set_merge)")
     ap.add_argument("--schedule", default=None,
