@@ -79,7 +79,8 @@ enum {
     PA_PATH_SIMPLE = 1,  /* one warp per (sequence, q head), plain loads, no split;
                             max_seq_len <= PA_SIMPLE_MAX_SEQ_LEN */
     PA_PATH_FMA = 2,     /* bf16 only: bulk-staged pages, CUDA-core dot products */
-    PA_PATH_MMA = 3      /* bf16 only: bulk-staged pages, a kv head's query heads (any g) through bf16 mma tiles */
+    PA_PATH_MMA = 3,     /* bf16 only: bulk-staged pages, a kv head's query heads (any g) through bf16 mma tiles */
+    PA_PATH_PREFILL = 4  /* reported by pa_plan_info only: pa_decode_multi ran the prefill kernel */
 };
 
 /* Longest max_seq_len the unsplit kernel (float32 pools, or PA_PATH_SIMPLE)
@@ -274,13 +275,19 @@ pa_status pa_prefill(const void* q, const int32_t* q_start, int num_queries, con
  * across the split are combined as in pa_decode ("39 · PagedAttention" §3).
  *
  *   q, q_start, out   as for pa_prefill; num_queries = q_start[B] (host)
- *   max_q     host bound on every n_b; max_q * (Hq / Hkv) <= 16
- *   plan_inout  as for pa_decode (the plan's forced path does not apply:
- *             this call always uses the tensor-core tiles)
+ *   max_q     host bound on every n_b
+ *   plan_inout  as for pa_decode (the plan's forced path does not apply)
  *   other arguments   as for pa_decode
  *
- * Supported: bf16 pools (PA_ERR_DTYPE otherwise), D in {64, 128}, block_size
- * 16 or 32. max_q * (Hq / Hkv) > 16 returns PA_ERR_SHAPE (use pa_prefill).
+ * The call picks the kernel from the shape: with max_q * (Hq / Hkv) <= 16
+ * (query, head) columns per kv head it runs the split decode's tiles above;
+ * with more it runs pa_prefill's tcgen05 kernel on the same arguments
+ * (pa_plan_info then reports PA_PATH_PREFILL), whose 128-row query tiles
+ * need D = 128, Hq / Hkv dividing 128 and max_blocks <= 16384 (PA_ERR_SHAPE
+ * otherwise); its device errors then go to the plan's error word.
+ *
+ * Supported: bf16 pools (PA_ERR_DTYPE otherwise), D in {64, 128} (128 above
+ * 16 columns), block_size 16 or 32.
  * A sequence with n_b < 1, n_b > max_q, n_b > L_b, rows outside
  * [0, num_queries) or L_b out of range raises PA_DEVERR_SEQ_LEN in the plan's
  * error word and gets zero rows (q_start must still be nondecreasing); a table

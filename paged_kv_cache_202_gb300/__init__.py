@@ -31,7 +31,7 @@ PA_ERR_WORKSPACE, PA_ERR_CUDA, PA_ERR_BOUNDS, PA_ERR_ALIGN, PA_ERR_NO_BLOCKS = 5
 PA_F32, PA_BF16 = 0, 1
 PA_DEVERR_SEQ_LEN, PA_DEVERR_TABLE, PA_DEVERR_TIMEOUT, PA_DEVERR_CACHE_LEN = 1, 2, 4, 8
 PA_DEVERR_COPY = 16
-PA_PATH_AUTO, PA_PATH_SIMPLE, PA_PATH_FMA, PA_PATH_MMA = 0, 1, 2, 3
+PA_PATH_AUTO, PA_PATH_SIMPLE, PA_PATH_FMA, PA_PATH_MMA, PA_PATH_PREFILL = 0, 1, 2, 3, 4
 PA_MERGE_AUTO, PA_MERGE_KERNEL, PA_MERGE_FUSED = 0, 1, 2
 PA_SIMPLE_MAX_SEQ_LEN = 8192   # longest max_seq_len of the unsplit kernel (float32 pools)
 

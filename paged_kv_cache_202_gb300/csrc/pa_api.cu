@@ -294,11 +294,19 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
         return PA_ERR_SHAPE;
     if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
         return PA_ERR_ALIGN;
+    // Several queries per sequence: up to 16 (query, head) columns per kv
+    // head run on the split decode's tensor-core tiles (the pages streamed
+    // once for all of them); more run on the prefill kernel's tcgen05 tiles
+    // (128-row query tiles, D = 128, Hq / Hkv dividing 128). bf16 pools.
+    bool via_prefill = false;
     if (q_start) {
-        // Several queries per sequence run on the tensor-core tiles only: up to
-        // 16 (query, head) columns per kv head, bf16 pools.
         if (kv_dtype != PA_BF16) return PA_ERR_DTYPE;
-        if (T < 0 || nq < 1 || nq * (Hq / Hkv) > 16) return PA_ERR_SHAPE;
+        if (T < 0 || nq < 1) return PA_ERR_SHAPE;
+        if (nq * (Hq / Hkv) > 16) {
+            const int gq = Hq / Hkv;
+            if (D != 128 || gq > 128 || 128 % gq != 0 || max_blocks > 16384) return PA_ERR_SHAPE;
+            via_prefill = true;
+        }
         if (T == 0) return PA_OK;
     }
     if (B == 0) return PA_OK;
@@ -317,7 +325,7 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     if (path == PA_PATH_SIMPLE && max_seq_len > PA_SIMPLE_MAX_SEQ_LEN) return PA_ERR_SHAPE;
     const float scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     pa::SplitShape sh;
-    if (path != PA_PATH_SIMPLE &&
+    if (path != PA_PATH_SIMPLE && !via_prefill &&
         !pa::split_shape(path == PA_PATH_FMA ? pa::kSplitFma : pa::kSplitMma, q_start ? nq : 0, B,
                          Hq, Hkv, D, block_size, max_blocks, max_seq_len, &sh))
         return PA_ERR_SHAPE;
@@ -339,6 +347,23 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
         *plan_inout = plan;
     }
     if (plan->device != dev) return PA_ERR_CUDA;  // a plan belongs to one device
+
+    if (via_prefill) {
+        CUtensorMap kmap, vmap;
+        if (!pa::encode_pool_map(&kmap, k_pool, num_blocks * Hkv, D, block_size) ||
+            !pa::encode_pool_map(&vmap, v_pool, num_blocks * Hkv, D, block_size))
+            return PA_ERR_CUDA;
+        if (plan->ev_start) cudaEventRecord(plan->ev_start, stream);
+        const cudaError_t e = pa::launch_prefill(kmap, vmap, q, T, q_start, block_tables, seq_lens,
+                                                 out, plan->err, B, Hq, Hkv, max_blocks,
+                                                 num_blocks, max_seq_len, nq, scale_log2,
+                                                 out_dtype == PA_BF16, block_size, stream);
+        if (plan->ev_stop) cudaEventRecord(plan->ev_stop, stream);
+        plan->last_path = PA_PATH_PREFILL;
+        plan->last_blocks = 0;
+        plan->last_warps = 0;
+        return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+    }
 
     if (path == PA_PATH_SIMPLE) {
         pa::SimpleArgs a{q, k_pool, v_pool, block_tables, seq_lens, out, plan->err,

@@ -117,7 +117,11 @@ def _decode_multi(lib, **kw):
     (dict(qs=None), pa.PA_ERR_NULL),
     (dict(q=None), pa.PA_ERR_NULL),
     (dict(kvdt=pa.PA_F32), pa.PA_ERR_DTYPE),       # tensor-core tiles take bf16 pools
-    (dict(maxq=5), pa.PA_ERR_SHAPE),                # 5 queries x 4 heads > 16 columns
+    # More than 16 (query, head) columns run on the prefill kernel's 128-row
+    # tiles, which need D = 128 and a group size dividing 128.
+    (dict(maxq=5, D=64), pa.PA_ERR_SHAPE),
+    (dict(maxq=6, Hq=24, Hkv=8), pa.PA_ERR_SHAPE),     # 18 columns, g = 3
+    (dict(maxq=5, mb=16385), pa.PA_ERR_SHAPE),
     (dict(maxq=0), pa.PA_ERR_SHAPE),
     (dict(T=-1), pa.PA_ERR_SHAPE),
     (dict(q=ALIGNED + 8), pa.PA_ERR_ALIGN),

@@ -173,3 +173,20 @@ def test_launch_shape():
     assert err == 0 and path == pa.PA_PATH_MMA
     assert warps == 5 * blocks
     assert np.abs(got - ref).max() <= BF16_TOL
+
+
+@pytest.mark.parametrize("Hq,Hkv,lens,ns", [
+    (32, 8, [700, 300, 2000], [64, 17, 5]),      # 64 queries x 4 heads: the prefill kernel's tiles
+    (8, 8, [129, 40], [20, 3]),                  # g = 1, 20 queries: 20 columns
+])
+def test_many_queries_route_to_the_prefill_kernel(Hq, Hkv, lens, ns):
+    # Above 16 (query, head) columns per kv head the call runs the tcgen05
+    # prefill kernel on the same arguments and reports it; the rows are the
+    # same causal attention.
+    wl, q, qs = _case(lens, ns, Hq=Hq, Hkv=Hkv, seed=40)
+    with pa.Plan() as plan:
+        got, err = _run(wl, q, qs, max(ns), plan)
+        assert plan.info()[0] == pa.PA_PATH_PREFILL
+    assert err == 0
+    ref = oracle.prefill(q, wl.k_pool, wl.v_pool, wl.block_tables, wl.seq_lens, qs, wl.scale)
+    assert np.abs(got - ref).max() <= BF16_TOL
