@@ -761,6 +761,48 @@ def run_row(args, local_rank):
     }), flush=True)
 
 
+def run_read_ceiling(args) -> None:
+    """Read-only HBM ceiling beside the copy peak (`bench_read_ceiling.cu`).
+
+    The decode step only reads its pools; the copy peak moves half its bytes
+    as writes. A standalone CUDA program times a device-to-device copy, a
+    streaming 16-byte read and a read of 4 KB pages in random order over the
+    decode's 2.2 GB, and this leg prints its figures as one JSON line.
+    """
+    from paged_kv_cache_202_gb300 import _build
+    src = os.path.join(ROOT, "bench_read_ceiling.cu")
+    exe = os.path.join(ROOT, "_build", "read_ceiling")
+    if not os.path.exists(exe) or os.path.getmtime(exe) < os.path.getmtime(src):
+        os.makedirs(os.path.dirname(exe), exist_ok=True)
+        r = subprocess.run([_build._nvcc(), *_build.ARCH, "-O3", "-std=c++17", src, "-o", exe],
+                           capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed for bench_read_ceiling.cu:\n{r.stderr}")
+    r = subprocess.run([exe, "538112", str(max(args.steps, 3))], capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"read_ceiling exited {r.returncode}: {r.stderr.strip()}")
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    res = {x["name"]: x for x in d["results"]}
+    stream = max((x for x in d["results"] if x["name"].startswith("stream_")),
+                 key=lambda x: x["median_gbs"])
+    pages = max((x for x in d["results"] if x["name"].startswith("pages_")),
+                key=lambda x: x["median_gbs"])
+    peak, kind = measured_peak_gbs()
+    print(json.dumps({
+        "row": "read_ceiling", "metric": "read-only HBM GB/s (streaming, 16-byte loads)",
+        "value": stream["median_gbs"], "unit": "GB/s", "n_gpus": 1, "steps": d["reps"],
+        "higher_is_better": True, "dtype": "u8", "data": "synthetic",
+        "config": {"workload": "read_ceiling", "bytes": d["bytes"],
+                   "l2": "buffer 17x larger than L2, no flush"},
+        "pages_4k_random_gbs": pages["median_gbs"], "copy_d2d_gbs": res["copy_d2d"]["median_gbs"],
+        "copy_peak": {"value": peak, "kind": kind},
+        "stream_over_copy_peak": stream["median_gbs"] / peak,
+        "pages_over_copy_peak": pages["median_gbs"] / peak,
+        "results": d["results"], "gpu_launches": (len(d["results"]) - 1) * (d["reps"] + 3),
+        "timing": "each launch timed alone by CUDA events; median of `steps` launches after 3 warm-up",
+    }))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -781,7 +823,8 @@ def main():
     ap.add_argument("--schedule", default=None,
                     help="permille,pages: force the dynamic tail (pa_plan_set_schedule)")
     ap.add_argument("--row", default="decode",
-                    choices=["decode", "copy_blocks", "page_scores", "prefill", "spec"])
+                    choices=["decode", "copy_blocks", "page_scores", "prefill", "spec",
+                             "read_ceiling"])
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -790,6 +833,8 @@ def main():
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.row == "read_ceiling":
+        run_read_ceiling(args)
     elif args.row != "decode":
         run_row(args, local_rank)
     else:
