@@ -769,6 +769,7 @@ def run_read_ceiling(args) -> None:
     streaming 16-byte read and a read of 4 KB pages in random order over the
     decode's 2.2 GB, and this leg prints its figures as one JSON line.
     """
+    import paged_kv_cache_202_gb300 as pa
     from paged_kv_cache_202_gb300 import _build
     src = os.path.join(ROOT, "bench_read_ceiling.cu")
     exe = os.path.join(ROOT, "_build", "read_ceiling")
@@ -778,7 +779,13 @@ def run_read_ceiling(args) -> None:
                            capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"nvcc failed for bench_read_ceiling.cu:\n{r.stderr}")
-    r = subprocess.run([exe, "538112", str(max(args.steps, 3))], capture_output=True, text=True)
+    from paged_kv_cache_202_gb300.workloads import CONFIGS, workload_lengths
+    cfg = CONFIGS[args.workload]
+    eb = 2 if cfg["dtype"] == "bf16" else 4
+    dec_bytes = pa.decode_bytes(workload_lengths(args.workload, args.seed), cfg["Hq"], cfg["Hkv"],
+                                cfg["D"], cfg["block_size"], eb, eb)
+    pages = -(-dec_bytes // 4096)
+    r = subprocess.run([exe, str(pages), str(max(args.steps, 3))], capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"read_ceiling exited {r.returncode}: {r.stderr.strip()}")
     d = json.loads(r.stdout.strip().splitlines()[-1])
@@ -793,7 +800,8 @@ def run_read_ceiling(args) -> None:
         "value": stream["median_gbs"], "unit": "GB/s", "n_gpus": 1, "steps": d["reps"],
         "higher_is_better": True, "dtype": "u8", "data": "synthetic",
         "config": {"workload": "read_ceiling", "bytes": d["bytes"],
-                   "l2": "buffer 17x larger than L2, no flush"},
+                   "sized_as": f"one decode of {args.workload} ({dec_bytes} bytes), in 4 KB pages",
+                   "l2": f"buffer {d['bytes'] / L2_BYTES:.1f}x the L2, no flush"},
         "pages_4k_random_gbs": pages["median_gbs"], "copy_d2d_gbs": res["copy_d2d"]["median_gbs"],
         "copy_peak": {"value": peak, "kind": kind},
         "stream_over_copy_peak": stream["median_gbs"] / peak,

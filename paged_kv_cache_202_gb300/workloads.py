@@ -209,6 +209,29 @@ def _normal(seq: np.random.SeedSequence, shape, dtype: str) -> np.ndarray:
     return out.reshape(shape)
 
 
+def _lengths(cfg: dict, rng: np.random.Generator) -> np.ndarray:
+    """Sequence lengths of a recipe: the first draw from the workload's generator."""
+    B, bs = cfg["B"], cfg["block_size"]
+    shared = int(cfg.get("shared_prefix_blocks", 0))
+    L = _draw_lengths(cfg["lengths"], B, rng) if B else np.zeros(0, dtype=np.int64)
+    if shared and cfg.get("clip_shared", True):
+        # Sharing sequences (even b) keep their append position past the shared
+        # prefix so that the shared blocks are never written. With
+        # clip_shared=False a sharing sequence may append inside the prefix;
+        # its step then needs copy on write first.
+        L[0::2] = np.clip(L[0::2], shared * bs + 1, cfg["max_len"])
+    return L
+
+
+def workload_lengths(name: str, seed: int | None = None, **overrides) -> np.ndarray:
+    """The sequence lengths `make_workload` draws for the same arguments, without the pools."""
+    cfg = dict(CONFIGS[name])
+    cfg.update(overrides)
+    if seed is None:
+        seed = 1000 + _ORDINAL[name]
+    return _lengths(cfg, np.random.default_rng(seed))
+
+
 def make_workload(name: str, seed: int | None = None, **overrides) -> Workload:
     """Build one seeded decode-step workload.
 
@@ -229,13 +252,7 @@ def make_workload(name: str, seed: int | None = None, **overrides) -> Workload:
     dtype = cfg["dtype"]
     shared = int(cfg.get("shared_prefix_blocks", 0))
 
-    L = _draw_lengths(cfg["lengths"], B, rng) if B else np.zeros(0, dtype=np.int64)
-    if shared and cfg.get("clip_shared", True):
-        # Sharing sequences (even b) keep their append position past the shared
-        # prefix so that the shared blocks are never written. With
-        # clip_shared=False a sharing sequence may append inside the prefix;
-        # its step then needs copy on write first.
-        L[0::2] = np.clip(L[0::2], shared * bs + 1, cfg["max_len"])
+    L = _lengths(cfg, rng)
     nblk = (L + bs - 1) // bs
     max_blocks = int(cfg.get("max_blocks", -(-cfg["max_len"] // bs)))
     if B and int(nblk.max()) > max_blocks:

@@ -3,6 +3,7 @@ and rejects bad arguments on the host before touching a GPU (no GPU needed)."""
 
 import ctypes
 
+import numpy as np
 import pytest
 
 import paged_kv_cache_202_gb300 as pa
@@ -342,3 +343,17 @@ def test_noalloc_rejects_bad_arguments_on_host(lib, kw, status):
 
 def test_noalloc_empty_batch_is_a_no_op(lib):
     assert _noalloc(lib, B=0) == pa.PA_OK
+
+
+@pytest.mark.parametrize("name", ["llama7b_mha", "llama3_8b_gqa", "mixed_shared", "spec_gqa",
+                                  "llama3_405b_gqa", "prefill_gqa"])
+def test_workload_lengths_are_the_lengths_make_workload_draws(name):
+    # The read-ceiling row sizes its buffer from these lengths without the pools.
+    from paged_kv_cache_202_gb300.workloads import make_workload, workload_lengths
+    wl = make_workload(name, B=6, max_len=4096, lengths=("uniform", 100, 4000))
+    np.testing.assert_array_equal(
+        workload_lengths(name, B=6, max_len=4096, lengths=("uniform", 100, 4000)), wl.seq_lens)
+    wl = make_workload(name, seed=5, B=3, max_len=2048, lengths=("loguniform", 20, 2000))
+    np.testing.assert_array_equal(
+        workload_lengths(name, seed=5, B=3, max_len=2048, lengths=("loguniform", 20, 2000)),
+        wl.seq_lens)
