@@ -34,8 +34,9 @@
  * that pa_last_device_error reads back.
  *
  * Supported shapes: kv_dtype PA_BF16 or PA_F32, D in {64, 128}, block_size in
- * {16, 32}, Hq a multiple of Hkv. Pools, q, k_new, v_new and out must be
- * 16-byte aligned.
+ * {16, 32}, Hq a multiple of Hkv, at most 2^30 output rows (B * Hq, or
+ * num_queries * Hq for the multi-query calls). Pools, q, k_new, v_new and out
+ * must be 16-byte aligned.
  */
 #ifndef PA_H
 #define PA_H
@@ -247,7 +248,9 @@ pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
  *             pa_last_device_error(NULL, ...)): PA_DEVERR_* bits
  *
  * Supported: bf16 pools, D = 128, block_size 16 or 32, Hq / Hkv dividing 128,
- * max_blocks <= 16384. Built for many queries per sequence (chunked prefill);
+ * max_blocks <= 16384, B and Hkv at most 65535 (PA_ERR_SHAPE otherwise).
+ * The launch is sized by min(max_q, num_queries). Built for many queries per
+ * sequence (chunked prefill);
  * with a few (max_q * Hq / Hkv <= 16, e.g. speculative verification)
  * pa_decode_multi computes the same rows at the decode's bandwidth. n_b < 1, n_b > L_b,
  * L_b out of range or rows outside [0, num_queries) raise PA_DEVERR_SEQ_LEN
@@ -283,8 +286,9 @@ pa_status pa_prefill(const void* q, const int32_t* q_start, int num_queries, con
  * (query, head) columns per kv head it runs the split decode's tiles above;
  * with more it runs pa_prefill's tcgen05 kernel on the same arguments
  * (pa_plan_info then reports PA_PATH_PREFILL), whose 128-row query tiles
- * need D = 128, Hq / Hkv dividing 128 and max_blocks <= 16384 (PA_ERR_SHAPE
- * otherwise); its device errors then go to the plan's error word.
+ * need D = 128, Hq / Hkv dividing 128, max_blocks <= 16384 and Hkv <= 65535
+ * (PA_ERR_SHAPE otherwise); its device errors then go to the plan's error
+ * word.
  *
  * Supported: bf16 pools (PA_ERR_DTYPE otherwise), D in {64, 128} (128 above
  * 16 columns), block_size 16 or 32.

@@ -302,13 +302,16 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     if (q_start) {
         if (kv_dtype != PA_BF16) return PA_ERR_DTYPE;
         if (T < 0 || nq < 1) return PA_ERR_SHAPE;
-        if (nq * (Hq / Hkv) > 16) {
+        if (static_cast<int64_t>(nq) * (Hq / Hkv) > 16) {
             const int gq = Hq / Hkv;
-            if (D != 128 || gq > 128 || 128 % gq != 0 || max_blocks > 16384) return PA_ERR_SHAPE;
+            if (D != 128 || gq > 128 || 128 % gq != 0 || max_blocks > 16384 ||
+                Hkv > pa::kMaxGridYZ)
+                return PA_ERR_SHAPE;
             via_prefill = true;
         }
-        if (T == 0) return PA_OK;
     }
+    if (static_cast<int64_t>(q_start ? T : B) * Hq > pa::kMaxRows) return PA_ERR_SHAPE;
+    if (q_start && T == 0) return PA_OK;
     if (B == 0) return PA_OK;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
 
@@ -548,7 +551,7 @@ pa_status pa_prefill(const void* q, const int32_t* q_start, int num_queries, con
     if (block_size != 16 && block_size != 32) return PA_ERR_BLOCK_SIZE;
     if (B < 0 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || D != 128 || num_blocks < 1 ||
         max_blocks < 1 || max_blocks > 16384 || max_q < 1 || max_seq_len < 1 ||
-        !std::isfinite(scale) || num_queries < 0)
+        !std::isfinite(scale) || num_queries < 0 || B > pa::kMaxGridYZ || Hkv > pa::kMaxGridYZ)
         return PA_ERR_SHAPE;
     const int g = Hq / Hkv;
     if (g > 128 || 128 % g != 0) return PA_ERR_SHAPE;  // a block holds 128 / g whole queries

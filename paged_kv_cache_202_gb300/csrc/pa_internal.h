@@ -100,6 +100,8 @@ cudaError_t launch_split(const SplitLaunch& L, const CUtensorMap& kmap, const CU
 // pa_decode_multi and pa_decode_noalloc.
 constexpr size_t kSmemLimit = 232448;  // opt-in dynamic shared memory per block on sm_10x
 constexpr int kMaxBatch = 8192;        // per-sequence arrays live in shared memory
+constexpr int64_t kMaxRows = int64_t(1) << 30;  // output rows (rows x heads), counted in int
+constexpr int kMaxGridYZ = 65535;      // grid.y / grid.z limit of the prefill launch
 
 // Kv units, tile width and block shape, from the sizes alone.
 struct SplitShape {

@@ -120,7 +120,8 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
         max_blocks < 1 || max_seq_len < 1 || !std::isfinite(scale) || B > pa::kMaxBatch)
         return PA_ERR_SHAPE;
     if (static_cast<int64_t>(num_blocks) * Hkv > INT32_MAX ||
-        static_cast<int64_t>(max_blocks) * block_size > INT32_MAX)
+        static_cast<int64_t>(max_blocks) * block_size > INT32_MAX ||
+        static_cast<int64_t>(B) * Hq > pa::kMaxRows)
         return PA_ERR_SHAPE;
     if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out))
         return PA_ERR_ALIGN;

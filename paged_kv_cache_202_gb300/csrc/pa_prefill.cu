@@ -49,6 +49,8 @@
 // the MMA thread for its products, and the block frees its tensor memory.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "pa.h"
 #include "pa_internal.h"
 #include "pa_ptx.cuh"
@@ -551,8 +553,10 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
     a.scale_log2 = scale_log2;
     a.out_bf16 = out_bf16;
     a.probe_wait = wait_probe();
-    if (B > 65535 || Hkv > 65535) return cudaErrorInvalidValue;
-    dim3 grid((max_q + 2 * a.Qb - 1) / (2 * a.Qb), Hkv, B);
+    if (B > kMaxGridYZ || Hkv > kMaxGridYZ) return cudaErrorInvalidValue;  // checked by the callers
+    // No sequence has more queries than the call has rows.
+    const int64_t nq = std::min<int64_t>(max_q, num_q);
+    dim3 grid(static_cast<unsigned>((nq + 2 * a.Qb - 1) / (2 * a.Qb)), Hkv, B);
     auto kern = block_size == 16 ? prefill_kernel<16> : prefill_kernel<32>;
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,

@@ -68,6 +68,7 @@ def _decode(lib, **kw):
     (dict(maxlen=0), pa.PA_ERR_SHAPE),
     (dict(scale=float("nan")), pa.PA_ERR_SHAPE),
     (dict(B=100000), pa.PA_ERR_SHAPE),
+    (dict(B=8192, Hq=131080, Hkv=8), pa.PA_ERR_SHAPE),   # more than 2^30 output rows
     (dict(q=ALIGNED + 8), pa.PA_ERR_ALIGN),
     (dict(out=ALIGNED + 2), pa.PA_ERR_ALIGN),
     (dict(v=ALIGNED + 4), pa.PA_ERR_ALIGN),
@@ -123,6 +124,8 @@ def _decode_multi(lib, **kw):
     (dict(maxq=5, D=64), pa.PA_ERR_SHAPE),
     (dict(maxq=6, Hq=24, Hkv=8), pa.PA_ERR_SHAPE),     # 18 columns, g = 3
     (dict(maxq=5, mb=16385), pa.PA_ERR_SHAPE),
+    (dict(maxq=20, Hq=70000, Hkv=70000), pa.PA_ERR_SHAPE),   # kv heads past the grid limit
+    (dict(T=1 << 25, Hq=64, Hkv=8), pa.PA_ERR_SHAPE),        # more than 2^30 output rows
     (dict(maxq=0), pa.PA_ERR_SHAPE),
     (dict(T=-1), pa.PA_ERR_SHAPE),
     (dict(q=ALIGNED + 8), pa.PA_ERR_ALIGN),
@@ -255,6 +258,8 @@ def _prefill(lib, **kw):
     (dict(maxq=0), pa.PA_ERR_SHAPE),
     (dict(T=-1), pa.PA_ERR_SHAPE),
     (dict(scale=float("inf")), pa.PA_ERR_SHAPE),
+    (dict(B=70000), pa.PA_ERR_SHAPE),             # sequences past the grid limit
+    (dict(Hq=70000, Hkv=70000), pa.PA_ERR_SHAPE), # kv heads past the grid limit
     (dict(k=ALIGNED + 4), pa.PA_ERR_ALIGN),
 ])
 def test_prefill_rejects_bad_arguments_on_host(lib, kw, status):
@@ -335,6 +340,7 @@ def _noalloc(lib, **kw):
     (dict(Hq=6, Hkv=4), pa.PA_ERR_SHAPE),
     (dict(B=8193), pa.PA_ERR_SHAPE),
     (dict(B=8192, Hq=64, Hkv=64, mb=65536, maxlen=1 << 20), pa.PA_ERR_SHAPE),  # pages over 32 bits
+    (dict(B=8192, Hq=131080, Hkv=8), pa.PA_ERR_SHAPE),   # more than 2^30 output rows
     (dict(out=ALIGNED + 2), pa.PA_ERR_ALIGN),
 ])
 def test_noalloc_rejects_bad_arguments_on_host(lib, kw, status):
