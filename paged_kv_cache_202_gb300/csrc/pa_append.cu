@@ -16,8 +16,11 @@ __device__ int g_append_error;  // library-wide word of append and block copies 
 // sequence's new K and V rows (blockIdx.y picks the group of 256 vectors).
 // The vector's load does not depend on where it goes, so it is issued first
 // and its latency overlaps the two dependent index loads (cache length, then
-// table entry).
+// table entry). Launched as a programmatic dependent of whatever the stream
+// ran before (the previous step's merge, typically): its launch overlaps that
+// kernel's run, and it waits for its completion before touching memory.
 __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
+    griddep_wait();               // the stream's previous kernel has completed
     griddep_launch_dependents();  // a following decode may start launching
     const int b = blockIdx.x;
     const int row_bytes = a.D * a.elem_bytes;
@@ -97,8 +100,16 @@ cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream) {
     const int threads = per_seq >= 256 ? 256 : ((per_seq + 31) / 32) * 32;
     const int groups = (per_seq + threads - 1) / threads;
     if (groups > 65535) return cudaErrorInvalidValue;
-    append_kernel<<<dim3(a.B, groups), threads, 0, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.B, groups);
+    cfg.blockDim = dim3(threads);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, append_kernel, a);
 }
 
 cudaError_t read_append_error(int* err) {
