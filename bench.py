@@ -220,9 +220,14 @@ def aggregate_over_ranks(world: int, seconds: float, units: float, device) -> tu
     return float(t.item()), float(u.item())
 
 
-def decode_config(wl, world: int) -> dict:
+LAYOUTS = {"paged": "each sequence's blocks shuffled over the pool",
+           "contiguous": "each sequence's blocks consecutive in the pool (same bits, renumbered)"}
+
+
+def decode_config(wl, world: int, layout: str = "paged") -> dict:
     """The ``config`` of a decode-step line, the same for both arms."""
-    return {"workload": wl.name, "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
+    return {"workload": wl.name, "layout": LAYOUTS[layout],
+            "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
             "block_size": wl.block_size, "num_blocks": wl.num_blocks,
             "tokens": int(wl.seq_lens.sum()), "kv_dtype": wl.dtype,
             "l2": f"inputs larger than L2 ({2 * wl.k_pool.nbytes / 2**30:.2f} GiB of pools vs "
@@ -233,8 +238,11 @@ def decode_config(wl, world: int) -> dict:
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    from paged_kv_cache_202_gb300.workloads import make_workload
-    wl = oracle_step_state(make_workload(args.workload))
+    from paged_kv_cache_202_gb300.workloads import contiguous_layout, make_workload
+    wl = make_workload(args.workload)
+    if getattr(args, "layout", "paged") == "contiguous":
+        wl = contiguous_layout(wl)
+    wl = oracle_step_state(wl)
     total = args.steps + args.warmup
     per_step = max(0.05, min(20.0, 120.0 / max(total, 1)))
     vals = []
@@ -253,7 +261,7 @@ def run_reference(args, rank, world):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * t_all / max(len(vals), 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": decode_config(wl, world),
+        "config": decode_config(wl, world, args.layout),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"{pairs_all} random (sequence, q-head) rows over "
                                    f"{len(vals)} steps, ~{per_step:.2f} s each"},
@@ -306,7 +314,7 @@ TIMED_SPAN_S = 2.0
 def run_ours(args, rank, world, local_rank):
     import __graft_entry__
     import paged_kv_cache_202_gb300 as pa
-    from paged_kv_cache_202_gb300.workloads import make_workload
+    from paged_kv_cache_202_gb300.workloads import contiguous_layout, make_workload
 
     __graft_entry__.build()
     torch.cuda.set_device(local_rank)
@@ -320,6 +328,8 @@ def run_ours(args, rank, world, local_rank):
             torch.distributed.barrier()
 
     wl = make_workload(args.workload, seed=args.seed + rank if args.seed is not None else None)
+    if args.layout == "contiguous":
+        wl = contiguous_layout(wl)
     bf = wl.dtype == "bf16"
 
     def to_dev(a):
@@ -505,7 +515,7 @@ def run_ours(args, rank, world, local_rank):
                       f"stream), {1e-3 * sum(rep_ms) * args.steps:.2f} s timed in all",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
             if bf else "f32", "data": "synthetic",
-            "config": decode_config(wl, world),
+            "config": decode_config(wl, world, args.layout),
             "pct_of_peak": 100.0 * value / world / peak,
             "qheads_per_s": job_qheads / (ms_step * 1e-3),
             "parts_ms": {"append": append_ms, "decode": decode_ms, "split_kernel": split_ms,
@@ -830,6 +840,9 @@ def main():
                     help="how the decode combines split partials (pa_plan_set_merge)")
     ap.add_argument("--schedule", default=None,
                     help="permille,pages: force the dynamic tail (pa_plan_set_schedule)")
+    ap.add_argument("--layout", default="paged", choices=sorted(LAYOUTS),
+                    help="decode row: the pool layout (contiguous = every sequence's blocks "
+                         "consecutive, the unpaged baseline of the paging cost)")
     ap.add_argument("--row", default="decode",
                     choices=["decode", "copy_blocks", "page_scores", "prefill", "spec",
                              "read_ceiling"])

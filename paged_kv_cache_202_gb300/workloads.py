@@ -332,3 +332,36 @@ def _scale_stored(x: np.ndarray, factor: float, dtype: str) -> np.ndarray:
     if dtype == "f32":
         return (x * np.float32(factor)).astype(np.float32)
     return bf16_bits(bits_to_f32(x) * np.float32(factor))
+
+
+def contiguous_layout(wl: Workload) -> Workload:
+    """The same step with every sequence's blocks renumbered to lie consecutively.
+
+    Physical ids are handed out in order of first appearance, sequence by
+    sequence and logical block by logical block (a block two tables share
+    keeps the place of its first use); blocks no table names come last. The
+    pools are permuted to match, so every gathered page holds the same bits
+    and only the addresses change: the layout of an unpaged cache, for
+    comparing a paged read against a contiguous one on the same data.
+    """
+    NB, bs = wl.num_blocks, wl.block_size
+    new_id = np.full(NB, -1, dtype=np.int64)
+    nxt = 0
+    for b in range(wl.B):
+        nb = -(-int(wl.seq_lens[b]) // bs)
+        for p in wl.block_tables[b, :nb]:
+            if new_id[p] < 0:
+                new_id[p] = nxt
+                nxt += 1
+    rest = np.nonzero(new_id < 0)[0]
+    new_id[rest] = np.arange(nxt, nxt + len(rest))
+    k_pool = np.empty_like(wl.k_pool)
+    v_pool = np.empty_like(wl.v_pool)
+    k_pool[new_id] = wl.k_pool
+    v_pool[new_id] = wl.v_pool
+    tables = np.where(wl.block_tables >= 0, new_id[np.maximum(wl.block_tables, 0)],
+                      -1).astype(np.int32)
+    refcount = np.empty_like(wl.refcount)
+    refcount[new_id] = wl.refcount
+    return dataclasses.replace(wl, block_tables=tables, k_pool=k_pool, v_pool=v_pool,
+                               refcount=refcount)
