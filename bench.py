@@ -37,8 +37,8 @@ L2_BYTES = 126 * 2**20
 # DRAM traffic of the split-attention kernel from an ncu capture (per launch,
 # scaled to the full workload), valid only for the kernel sources it was
 # measured on (sha256 of the split kernel's source files).
-TRAFFIC = {"source_sha": "deaf1e3f7c1a96631784a68e6003b4384edca453f4f56b0e7356700c6509a914",
-           "workload": "llama3_8b_gqa", "bytes_per_launch": 2205606912 + 5019520}
+TRAFFIC = {"source_sha": "34b19d5e2ad95951e9dfe4531882438c806a5069e9286538bcee284c0a277f09",
+           "workload": "llama3_8b_gqa", "bytes_per_launch": 2205581056 + 5087872}
 
 
 def split_source_sha() -> str:
@@ -224,7 +224,11 @@ LAYOUTS = {"paged": "each sequence's blocks shuffled over the pool",
            "contiguous": "each sequence's blocks consecutive in the pool (same bits, renumbered)"}
 
 
-def decode_config(wl, world: int, layout: str = "paged") -> dict:
+STEPS = {"separate": "pa_append_kv + pa_decode",
+         "fused": "pa_append_decode (the append inside the decode's split kernel)"}
+
+
+def decode_config(wl, world: int, layout: str = "paged", step: str = "separate") -> dict:
     """The ``config`` of a decode-step line, the same for both arms."""
     return {"workload": wl.name, "layout": LAYOUTS[layout],
             "B": wl.B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
@@ -232,7 +236,7 @@ def decode_config(wl, world: int, layout: str = "paged") -> dict:
             "tokens": int(wl.seq_lens.sum()), "kv_dtype": wl.dtype,
             "l2": f"inputs larger than L2 ({2 * wl.k_pool.nbytes / 2**30:.2f} GiB of pools vs "
                   f"{L2_BYTES / 2**20:.0f} MiB L2), no flush",
-            "step": "pa_append_kv + pa_decode", "parallelism": f"replicas x{world}"}
+            "step": STEPS[step], "parallelism": f"replicas x{world}"}
 
 
 def run_reference(args, rank, world):
@@ -261,7 +265,7 @@ def run_reference(args, rank, world):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * t_all / max(len(vals), 1), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": decode_config(wl, world, args.layout),
+        "config": decode_config(wl, world, args.layout, args.step),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": threads, "kind": "oracle",
                          "sample": f"{pairs_all} random (sequence, q-head) rows over "
                                    f"{len(vals)} steps, ~{per_step:.2f} s each"},
@@ -348,9 +352,26 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     max_len = wl.max_seq_len
 
+    def calls(kn, vn, qq, bt, sl, cl, s, ev=None):
+        """One step's calls: the append then the decode, or the fused call;
+        ev = three events around (append, decode) for the kernel pass."""
+        if ev:
+            ev[0].record(s)
+        if args.step == "fused":
+            if ev:
+                ev[1].record(s)
+            pa.pa_append_decode(qq, kn, vn, k_pool, v_pool, bt, sl, wl.scale, out, max_len, plan,
+                                s)
+        else:
+            pa.pa_append_kv(kn, vn, k_pool, v_pool, bt, cl, s)
+            if ev:
+                ev[1].record(s)
+            pa.pa_decode(qq, k_pool, v_pool, bt, sl, wl.scale, out, max_len, plan, s)
+        if ev:
+            ev[2].record(s)
+
     def step():
-        pa.pa_append_kv(k_new, v_new, k_pool, v_pool, tables, cache_lens, stream)
-        pa.pa_decode(q, k_pool, v_pool, tables, seq_lens, wl.scale, out, max_len, plan, stream)
+        calls(k_new, v_new, q, tables, seq_lens, cache_lens, stream)
 
     step()                        # creates the plan
     configure_plan(plan, args)
@@ -415,11 +436,7 @@ def run_ours(args, rank, world, local_rank):
     w2 = time.time()
     for i in range(k_steps):
         plan.set_split_events(*ev_split[i])
-        ev_parts[i][0].record(stream)
-        pa.pa_append_kv(k_new, v_new, k_pool, v_pool, tables, cache_lens, stream)
-        ev_parts[i][1].record(stream)
-        pa.pa_decode(q, k_pool, v_pool, tables, seq_lens, wl.scale, out, max_len, plan, stream)
-        ev_parts[i][2].record(stream)
+        calls(k_new, v_new, q, tables, seq_lens, cache_lens, stream, ev=ev_parts[i])
     torch.cuda.synchronize()
     w3 = time.time()
     plan.set_split_events(None, None)
@@ -462,8 +479,7 @@ def run_ours(args, rank, world, local_rank):
 
     def e2e_calls(s):
         d_in.copy_(h_in, non_blocking=True)
-        pa.pa_append_kv(e_kn, e_vn, k_pool, v_pool, e_bt, e_cl, s)
-        pa.pa_decode(e_q, k_pool, v_pool, e_bt, e_sl, wl.scale, out, max_len, plan, s)
+        calls(e_kn, e_vn, e_q, e_bt, e_sl, e_cl, s)
         h_out.copy_(out, non_blocking=True)
 
     # The step's calls, warmed up once, then captured in a CUDA graph: every
@@ -515,10 +531,11 @@ def run_ours(args, rank, world, local_rank):
                       f"stream), {1e-3 * sum(rep_ms) * args.steps:.2f} s timed in all",
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16"
             if bf else "f32", "data": "synthetic",
-            "config": decode_config(wl, world, args.layout),
+            "config": decode_config(wl, world, args.layout, args.step),
             "pct_of_peak": 100.0 * value / world / peak,
             "qheads_per_s": job_qheads / (ms_step * 1e-3),
-            "parts_ms": {"append": append_ms, "decode": decode_ms, "split_kernel": split_ms,
+            "parts_ms": {"append": append_ms if args.step != "fused" else None,
+                         "decode": decode_ms, "split_kernel": split_ms,
                          "timing": "CUDA events around each call in the kernel pass (events "
                                    "between calls, so no launch overlap); rank 0"},
             "roofline": {"bound": "hbm", "kernel": "split attention", "achieved": achieved,
@@ -533,7 +550,8 @@ def run_ours(args, rank, world, local_rank):
                     "how": "per step: the inputs from pinned host memory (one staging copy), "
                            "pa_append_kv, pa_decode, the output back, captured once in a CUDA "
                            "graph and replayed, then a wait for the result"},
-            "gpu_launches": (2 if args.merge == "fused" else 3) * args.steps * repeats,
+            "gpu_launches": (2 if args.merge == "fused" or args.step == "fused" else 3)
+            * args.steps * repeats,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "clocks_kernel_pass": clocks_kernel_pass,
@@ -771,6 +789,73 @@ def run_row(args, local_rank):
     }), flush=True)
 
 
+def run_latency(args, local_rank) -> None:
+    """Step latency against sequence length at a fixed batch (context row).
+
+    One append + decode step of the workload's head shape, every sequence of
+    the same length, for lengths 128 .. 32768: where the step is bound by
+    launch and latency and where by bandwidth. Plain calls on one stream,
+    CUDA events around `steps` steps after `warmup`.
+    """
+    import __graft_entry__
+    import paged_kv_cache_202_gb300 as pa
+    from paged_kv_cache_202_gb300.workloads import make_workload
+    __graft_entry__.build()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    B = args.batch
+    lengths = [128 << k for k in range(9)]
+    rows = []
+    for L in lengths:
+        wl = make_workload(args.workload, B=B, lengths=("fixed", L), max_len=L,
+                           pool=("factor", 1.0))
+
+        def to_dev(a):
+            return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+        q, kn, vn = to_dev(wl.q), to_dev(wl.k_new), to_dev(wl.v_new)
+        kp, vp = to_dev(wl.k_pool), to_dev(wl.v_pool)
+        bt = torch.from_numpy(wl.block_tables).to(dev)
+        sl = torch.from_numpy(wl.seq_lens).to(dev)
+        cl = torch.from_numpy(wl.cache_lens).to(dev)
+        out = torch.empty(wl.B, wl.Hq, wl.D, dtype=torch.bfloat16, device=dev)
+        stream = torch.cuda.current_stream()
+        with pa.Plan() as plan:
+            def step():
+                if args.step == "fused":
+                    pa.pa_append_decode(q, kn, vn, kp, vp, bt, sl, wl.scale, out, L, plan, stream)
+                else:
+                    pa.pa_append_kv(kn, vn, kp, vp, bt, cl, stream)
+                    pa.pa_decode(q, kp, vp, bt, sl, wl.scale, out, L, plan, stream)
+            for _ in range(args.warmup):
+                step()
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(args.steps):
+                step()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us = e0.elapsed_time(e1) * 1e3 / args.steps
+            assert pa.pa_last_device_error(plan) == 0
+        eb = wl.elem_bytes
+        nbytes = pa.decode_bytes(wl.seq_lens, wl.Hq, wl.Hkv, wl.D, wl.block_size, eb, eb) + \
+            pa.append_bytes(wl.B, wl.Hkv, wl.D, eb)
+        rows.append({"seq_len": L, "us_per_step": round(us, 2), "gbs": round(nbytes / us / 1e3, 1)})
+        del kp, vp
+        torch.cuda.empty_cache()
+    by = {r["seq_len"]: r["us_per_step"] for r in rows}
+    print(json.dumps({
+        "row": "latency", "metric": "decode step latency vs sequence length", "unit": "us",
+        "value": by[2048], "higher_is_better": False, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "B": B, "Hq": wl.Hq, "Hkv": wl.Hkv, "D": wl.D,
+                   "block_size": wl.block_size, "step": STEPS[args.step]},
+        "steps": args.steps, "warmup": args.warmup, "lengths": rows,
+        "growth_128_to_2048": round(by[2048] / by[128], 3),
+        "gpu_launches": (2 if args.step == "fused" else 3) * (args.steps + args.warmup) * len(lengths),
+        "timing": "CUDA events around `steps` back-to-back steps per length",
+    }))
+
+
 def run_read_ceiling(args) -> None:
     """Read-only HBM ceiling beside the copy peak (`bench_read_ceiling.cu`).
 
@@ -840,22 +925,29 @@ def main():
                     help="how the decode combines split partials (pa_plan_set_merge)")
     ap.add_argument("--schedule", default=None,
                     help="permille,pages: force the dynamic tail (pa_plan_set_schedule)")
+    ap.add_argument("--step", default="separate", choices=sorted(STEPS),
+                    help="decode row: the step's calls (fused = pa_append_decode)")
     ap.add_argument("--layout", default="paged", choices=sorted(LAYOUTS),
                     help="decode row: the pool layout (contiguous = every sequence's blocks "
                          "consecutive, the unpaged baseline of the paging cost)")
     ap.add_argument("--row", default="decode",
                     choices=["decode", "copy_blocks", "page_scores", "prefill", "spec",
-                             "read_ceiling"])
+                             "read_ceiling", "latency"])
+    ap.add_argument("--batch", type=int, default=1,
+                    help="latency row: sequences per step (all of one length)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.workload is None:
-        args.workload = {"prefill": "prefill_gqa", "spec": "spec_gqa"}.get(args.row, "llama3_8b_gqa")
+        args.workload = {"prefill": "prefill_gqa", "spec": "spec_gqa",
+                         "latency": "llama7b_mha"}.get(args.row, "llama3_8b_gqa")
     rank, world, local_rank = dist_env()
     if args.impl == "reference":
         run_reference(args, rank, world)
     elif args.row == "read_ceiling":
         run_read_ceiling(args)
+    elif args.row == "latency":
+        run_latency(args, local_rank)
     elif args.row != "decode":
         run_row(args, local_rank)
     else:

@@ -160,6 +160,37 @@ pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
                     float scale, pa_dtype kv_dtype, void* out, pa_dtype out_dtype,
                     pa_plan** plan_inout, struct CUstream_st* stream);
 
+/*
+ * pa_append_decode -- one decode step in one call: pa_append_kv of the step's
+ * new token at position seq_lens[b] - 1, then pa_decode over seq_lens[b]
+ * tokens (the cache grows by the token the step attends with, "PagedAttention:
+ * The Cache Was Storing Nothing" §1-§2.2; attention as in pa_decode).
+ *
+ *   k_new, v_new  device, [B][Hkv][D] kv_dtype, read only, 16-byte aligned
+ *   k_pool/v_pool device, written in place at the new token's slot
+ *   other arguments as for pa_decode
+ *
+ * Results and pool contents equal pa_append_kv (with cache_lens = seq_lens - 1)
+ * followed by pa_decode, bit for bit. On bf16 pools with the tensor-core
+ * path and the merge kernel (the automatic choices), the append runs inside
+ * the decode kernel: the warp that reads a sequence's last page writes the
+ * new row into its staged copy and into the pool, which saves the append's
+ * launch and its round trips. Otherwise (float32 pools, a forced CUDA-core
+ * path, the fused merge) the append runs as its own kernel first, and its
+ * PA_DEVERR_* bits go to the library-wide append word as for pa_append_kv.
+ * Precondition as for pa_append_kv: the written block is private to its
+ * sequence. A sequence whose length is out of range gets no append and zero
+ * rows (PA_DEVERR_SEQ_LEN); a table entry outside the pool skips the append
+ * and zeroes the affected rows (PA_DEVERR_TABLE). NULL k_new or v_new returns
+ * PA_ERR_NULL.
+ */
+pa_status pa_append_decode(const void* q, const void* k_new, const void* v_new, void* k_pool,
+                           void* v_pool, const int32_t* block_tables, int max_blocks,
+                           const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
+                           int num_blocks, int max_seq_len, float scale, pa_dtype kv_dtype,
+                           void* out, pa_dtype out_dtype, pa_plan** plan_inout,
+                           struct CUstream_st* stream);
+
 /* Release a plan and its device workspace. NULL is a no-op. The caller must
  * make sure no work using the plan is still running (e.g. sync its stream). */
 pa_status pa_free(pa_plan* plan);

@@ -59,6 +59,9 @@ def lib() -> ctypes.CDLL:
     L.pa_decode.argtypes = [vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, ci, cf, ci, vp, ci,
                             ctypes.POINTER(vp), vp]
     L.pa_decode.restype = ci
+    L.pa_append_decode.argtypes = [vp, vp, vp, vp, vp, vp, ci, vp, ci, ci, ci, ci, ci, ci, ci, cf,
+                                   ci, vp, ci, ctypes.POINTER(vp), vp]
+    L.pa_append_decode.restype = ci
     L.pa_free.argtypes = [vp]
     L.pa_free.restype = ci
     L.pa_status_str.argtypes = [ci]
@@ -266,6 +269,26 @@ def pa_decode(q: torch.Tensor, k_pool: torch.Tensor, v_pool: torch.Tensor,
                          int(max_seq_len), float(scale), _dtype(k_pool), _ptr(out), _dtype(out),
                          ctypes.byref(plan.handle), _stream(stream))
     _check(st, "pa_decode")
+    return out
+
+
+def pa_append_decode(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                     k_pool: torch.Tensor, v_pool: torch.Tensor, block_tables: torch.Tensor,
+                     seq_lens: torch.Tensor, scale: float, out: torch.Tensor, max_seq_len: int,
+                     plan: Plan, stream=None) -> torch.Tensor:
+    """One decode step in one call: append the new K/V token of every sequence
+    at position ``seq_lens[b] - 1`` (in place), then decode into ``out``."""
+    B, Hq, D = q.shape
+    NB, Hkv, bs, _ = _pools(k_pool, v_pool)
+    _check_decode(q, k_pool, v_pool, block_tables, seq_lens, out, B)
+    _on_one_device(q, k_new, v_new)
+    _expect(k_new, "k_new", (B, Hkv, D), k_pool.dtype)
+    _expect(v_new, "v_new", (B, Hkv, D), k_pool.dtype)
+    st = lib().pa_append_decode(_ptr(q), _ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool),
+                                _ptr(block_tables), block_tables.shape[1], _ptr(seq_lens), B, Hq,
+                                Hkv, D, bs, NB, int(max_seq_len), float(scale), _dtype(k_pool),
+                                _ptr(out), _dtype(out), ctypes.byref(plan.handle), _stream(stream))
+    _check(st, "pa_append_decode")
     return out
 
 

@@ -43,6 +43,7 @@ struct OccKey {
     int blocks_per_sm;
     int mq;
     int fused;
+    int append;
 };
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -274,15 +275,18 @@ pa_status pa_append_kv(const void* k_new, const void* v_new, void* k_pool, void*
 
 namespace {
 
-// The decode of pa_decode and, with q_start != null (T query rows, at most
-// nq per sequence), of pa_decode_multi.
+// The decode of pa_decode, with q_start != null (T query rows, at most nq per
+// sequence) of pa_decode_multi, and with k_new != null of pa_append_decode
+// (the step's new rows appended at position seq_lens[b] - 1 first).
 pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, const void* k_pool,
                       const void* v_pool, const int32_t* block_tables, int max_blocks,
                       const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
                       int num_blocks, int max_seq_len, float scale, pa_dtype kv_dtype, void* out,
-                      pa_dtype out_dtype, pa_plan** plan_inout, struct CUstream_st* stream_) {
+                      pa_dtype out_dtype, pa_plan** plan_inout, struct CUstream_st* stream_,
+                      const void* k_new = nullptr, const void* v_new = nullptr) {
     if (!q || !k_pool || !v_pool || !block_tables || !seq_lens || !out || !plan_inout)
         return PA_ERR_NULL;
+    if (k_new && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_ALIGN;
     if ((kv_dtype != PA_F32 && kv_dtype != PA_BF16) || (out_dtype != PA_F32 && out_dtype != PA_BF16))
         return PA_ERR_DTYPE;
     if (block_size != 16 && block_size != 32) return PA_ERR_BLOCK_SIZE;
@@ -368,7 +372,18 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
         return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
     }
 
+    // The append as its own kernel, for the paths that do not fuse it: the
+    // step's rows at position seq_lens[b] - 1, before the decode reads them.
+    auto append_first = [&]() -> cudaError_t {
+        pa::AppendArgs ap{k_new, v_new, const_cast<void*>(k_pool), const_cast<void*>(v_pool),
+                          block_tables, seq_lens, B, Hkv, D, block_size, max_blocks, num_blocks,
+                          kv_dtype == PA_F32 ? 4 : 2};
+        ap.pos_offset = 1;
+        return pa::launch_append(ap, stream);
+    };
+
     if (path == PA_PATH_SIMPLE) {
+        if (k_new && append_first() != cudaSuccess) return PA_ERR_CUDA;
         pa::SimpleArgs a{q, k_pool, v_pool, block_tables, seq_lens, out, plan->err,
                          B, Hq, Hkv, D, block_size, max_blocks, num_blocks, max_seq_len,
                          scale_log2, kv_dtype == PA_BF16, out_dtype == PA_BF16};
@@ -388,10 +403,14 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     const bool can_fuse = !q_start && sh.kind == pa::kSplitMma && sh.NT == 1 && sh.warps == 3;
     L.fused = can_fuse && plan->merge_mode == PA_MERGE_FUSED ? 1 : 0;
     if (plan->merge_mode == PA_MERGE_FUSED && !can_fuse) return PA_ERR_SHAPE;
+    // The append rides in the split kernel on the tensor-core tiles with one
+    // stage per warp and the merge kernel; elsewhere it runs first on its own.
+    L.append = k_new && !q_start && !L.fused && sh.kind == pa::kSplitMma && sh.stages == 1 ? 1 : 0;
     int per_sm = 0;
     for (const OccKey& o : plan->occ) {
         if (o.kind == L.kind && o.D == D && o.BS == block_size && o.NT == L.NT &&
-            o.warps == L.warps && o.smem == L.smem && o.mq == L.mq && o.fused == L.fused)
+            o.warps == L.warps && o.smem == L.smem && o.mq == L.mq && o.fused == L.fused &&
+            o.append == L.append)
             per_sm = o.blocks_per_sm;
     }
     if (per_sm == 0) {
@@ -399,7 +418,7 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
         per_sm = pa::split_blocks_per_sm(L, &e);
         if (e != cudaSuccess || per_sm < 1) return PA_ERR_CUDA;
         plan->occ.push_back(OccKey{L.kind, D, block_size, L.NT, L.warps, L.smem, per_sm, L.mq,
-                                   L.fused});
+                                   L.fused, L.append});
     }
     pa::SplitGrid gr = pa::split_grid(sh, B, D, block_size,
                                       static_cast<int64_t>(q_start ? T : B) * Hq,
@@ -480,6 +499,14 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     a.num_q = T;
     a.probe_wait = pa::wait_probe();
     a.ws_cnt = cnt;
+    if (L.append) {
+        a.k_new = static_cast<const uint16_t*>(k_new);
+        a.v_new = static_cast<const uint16_t*>(v_new);
+        a.kpool_w = static_cast<uint16_t*>(const_cast<void*>(k_pool));
+        a.vpool_w = static_cast<uint16_t*>(const_cast<void*>(v_pool));
+    } else if (k_new && append_first() != cudaSuccess) {
+        return PA_ERR_CUDA;
+    }
 
     if (plan->ev_start) cudaEventRecord(plan->ev_start, stream);
     cudaError_t e = pa::launch_split(L, plan->kmap, plan->vmap, a, stream);
@@ -508,6 +535,18 @@ pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
     return decode_impl(q, nullptr, B, 1, k_pool, v_pool, block_tables, max_blocks, seq_lens, B,
                        Hq, Hkv, D, block_size, num_blocks, max_seq_len, scale, kv_dtype, out,
                        out_dtype, plan_inout, stream);
+}
+
+pa_status pa_append_decode(const void* q, const void* k_new, const void* v_new, void* k_pool,
+                           void* v_pool, const int32_t* block_tables, int max_blocks,
+                           const int32_t* seq_lens, int B, int Hq, int Hkv, int D, int block_size,
+                           int num_blocks, int max_seq_len, float scale, pa_dtype kv_dtype,
+                           void* out, pa_dtype out_dtype, pa_plan** plan_inout,
+                           struct CUstream_st* stream) {
+    if (!k_new || !v_new) return PA_ERR_NULL;
+    return decode_impl(q, nullptr, B, 1, k_pool, v_pool, block_tables, max_blocks, seq_lens, B,
+                       Hq, Hkv, D, block_size, num_blocks, max_seq_len, scale, kv_dtype, out,
+                       out_dtype, plan_inout, stream, k_new, v_new);
 }
 
 pa_status pa_decode_multi(const void* q, const int32_t* q_start, int num_queries, int max_q,

@@ -37,7 +37,7 @@ __global__ void __launch_bounds__(256) append_kernel(const AppendArgs a) {
                           (static_cast<size_t>(b) * a.Hkv + h) * row_bytes + c * 16;
         w = *reinterpret_cast<const uint4*>(src);
     }
-    const int pos = a.cache_lens[b];
+    const int pos = a.cache_lens[b] - a.pos_offset;
     if (pos < 0 || pos >= a.max_blocks * a.BS) {
         if (threadIdx.x == 0) atomicOr(&g_append_error, kErrCacheLen);
         return;

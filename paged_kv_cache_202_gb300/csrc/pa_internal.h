@@ -78,6 +78,12 @@ struct SplitArgs {
     // counts the partials of segment (b, u) written so far (zero between
     // calls); the warp that writes the last one folds them into the output.
     int* ws_cnt;
+    // Fused append (pa_append_decode): the step's new rows [B][Hkv][D] go to
+    // position seq_lens[b] - 1 of the pools (bf16 bits), written in place.
+    const uint16_t* k_new;
+    const uint16_t* v_new;
+    uint16_t* kpool_w;
+    uint16_t* vpool_w;
 };
 
 struct SplitLaunch {
@@ -88,6 +94,7 @@ struct SplitLaunch {
     size_t smem;   // dynamic shared memory bytes
     int mq = 0;    // 1: several queries per sequence (tensor-core path only)
     int fused = 0; // 1: the split kernel merges its own partials (no merge kernel)
+    int append = 0; // 1: the split kernel also appends the step's new K/V rows
 };
 
 // Returns the resident blocks per SM of a split-kernel variant at the given
@@ -179,6 +186,7 @@ struct AppendArgs {
     const int32_t* tables;
     const int32_t* cache_lens;
     int B, Hkv, D, BS, max_blocks, num_blocks, elem_bytes;
+    int pos_offset = 0;  // position = cache_lens[b] - pos_offset (1 when given seq_lens)
 };
 cudaError_t launch_append(const AppendArgs& a, cudaStream_t stream);
 

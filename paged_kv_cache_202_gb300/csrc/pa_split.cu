@@ -21,6 +21,14 @@ __global__ void __launch_bounds__(NT == 2 ? 160 : 256, NT == 2 ? 2 : 1)
     split_body<D, BS, MmaState<D, kChunkTokens, NT, NT == 2>>(&kmap, &vmap, a);
 }
 
+// The same kernels with the step's append fused in (pa_append_decode).
+template <int D, int BS, int NT>
+__global__ void __launch_bounds__(NT == 2 ? 160 : 256, NT == 2 ? 2 : 1)
+    mma_append_kernel(const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap, const SplitArgs a) {
+    split_body<D, BS, MmaState<D, kChunkTokens, NT, NT == 2>, false, false, true>(&kmap, &vmap, a);
+}
+
 // One n-tile with the fused merge: the warp that writes a segment's last
 // partial folds them, so no merge kernel follows. Three warps a block and
 // four blocks an SM, as the plain kernel runs: at most 170 registers a thread.
@@ -54,6 +62,11 @@ KernelFn select(const SplitLaunch& L) {
         if (L.fused) {                                                          \
             if (L.kind == kSplitMma && L.NT == 1 && L.warps == 3)              \
                 return mma_fused_kernel<D_, BS_>;                               \
+            return nullptr;                                                     \
+        }                                                                       \
+        if (L.append) {                                                         \
+            if (L.kind == kSplitMma && L.NT == 1) return mma_append_kernel<D_, BS_, 1>; \
+            if (L.kind == kSplitMma && L.NT == 2) return mma_append_kernel<D_, BS_, 2>; \
             return nullptr;                                                     \
         }                                                                       \
         if (L.kind == kSplitFma) return fma_kernel<D_, BS_>;                    \

@@ -558,6 +558,12 @@ __device__ __forceinline__ void sts_v4i(uint32_t addr, int a0, int a1, int a2) {
                  : "memory");
 }
 
+__device__ __forceinline__ void sts_u128(uint32_t addr, uint4 v) {
+    asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ int4 lds_v4i(uint32_t addr) {
     int4 v;
     asm volatile("ld.shared.v4.s32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
@@ -666,10 +672,18 @@ __device__ __forceinline__ void fold_segment(const SplitArgs& a, int x0, int x1,
     }
 }
 
-template <int D, int BS, typename State, bool MQ = false, bool FUSED = false>
+// APPEND: the step's new K/V rows are appended by this kernel (one stage per
+// warp). The warp whose chunk holds a segment's last page loads the rows
+// before it waits for the stage, writes them into the staged page at
+// position seq_len - 1 once the copy has landed, and (first slice of the kv
+// head) into the pools. No other warp reads that slot in this call: every
+// page belongs to one range, and the other slices of a kv head patch their
+// own staged copies.
+template <int D, int BS, typename State, bool MQ = false, bool FUSED = false, bool APPEND = false>
 __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtensorMap* vmap,
                                            const SplitArgs& a) {
     static_assert(!(MQ && FUSED), "the fused merge serves one query per sequence");
+    static_assert(!(APPEND && (MQ || FUSED)), "the fused append serves the plain decode");
     static_assert(!MQ || State::kQS, "the multi-query tile reads its query rows from the stage");
     constexpr int CT = kChunkTokens;
     constexpr int CP = CT / BS;  // pages per chunk
@@ -908,6 +922,30 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
     while (n_done < n_issued) {
         const uint32_t bar = my_bars + 8 * s;
         const uint32_t stg = my_ring + static_cast<uint32_t>(s * a.stage_bytes);
+        // Fused append: does this stage hold a segment's last page? The range
+        // record is this warp's own earlier write, readable before the wait.
+        constexpr int RV = D / 8;  // 16-byte vectors of one K or V row
+        int ap_row = -1, ap_kvh = 0, ap_slice = 0, ap_phys = 0, ap_slot = 0;
+        uint4 ap_w = make_uint4(0, 0, 0, 0);
+        if constexpr (APPEND) {
+            const int4 p4 = lds_v4i(my_meta + 16 * s);
+            const bool fresh = p4.z != rc.id;
+            const Cursor pc = fresh ? locate(p4.x) : cc;
+            const int pn = min(min(CP, pc.nb - pc.p), fresh ? p4.y - p4.x : rc.x1 - xc);
+            if (pc.p + pn == pc.nb && !((badmask >> s) & 1u)) {
+                ap_kvh = pc.u / a.nslices;
+                ap_slice = pc.u - ap_kvh * a.nslices;
+                ap_slot = (len[pc.b] - 1) % BS;
+                ap_row = (pc.nb - 1 - pc.p) * BS + ap_slot;
+                ap_phys = table_entry(pc.b, pc.nb - 1, pc.nb);
+                if (lane < 2 * RV) {
+                    const uint16_t* src = (lane < RV ? a.k_new : a.v_new) +
+                                          (static_cast<size_t>(pc.b) * a.Hkv + ap_kvh) * D +
+                                          (lane % RV) * 8;
+                    ap_w = *reinterpret_cast<const uint4*>(src);
+                }
+            }
+        }
         const bool ready = (a.probe_wait && n_done == 0)
                                ? mbar_wait_bounded(probe_bar, 0, kProbeLimitNs)
                                : mbar_wait_bounded(bar, (phase >> s) & 1u, kWaitLimitNs);
@@ -943,6 +981,21 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
             st.start(stg + 2 * CT * D * 2, nh, lane);
             p_first = cc.p;
             poison = false;
+        }
+        if constexpr (APPEND) {
+            if (ap_row >= 0) {
+                if (lane < 2 * RV) {
+                    const uint32_t region = stg + (lane < RV ? 0u : static_cast<uint32_t>(CT * D * 2));
+                    sts_u128(swz(region, lane % RV, ap_row, CT), ap_w);
+                    if (ap_slice == 0) {
+                        uint16_t* pool = lane < RV ? a.kpool_w : a.vpool_w;
+                        const size_t off =
+                            ((static_cast<size_t>(ap_phys) * a.Hkv + ap_kvh) * BS + ap_slot) * D;
+                        *reinterpret_cast<uint4*>(pool + off + (lane % RV) * 8) = ap_w;
+                    }
+                }
+                __syncwarp();
+            }
         }
         if ((badmask >> s) & 1u) {
             poison = true;

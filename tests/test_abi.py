@@ -87,6 +87,42 @@ def test_decode_late_shape_errors_create_no_plan(lib):
     assert _decode(lib, B=8192, Hq=64, Hkv=64, mb=65536, maxlen=1 << 20) == pa.PA_ERR_SHAPE
 
 
+def _append_decode(lib, **kw):
+    args = dict(q=ALIGNED, kn=ALIGNED, vn=ALIGNED, k=ALIGNED, v=ALIGNED, bt=ALIGNED, mb=4,
+                sl=ALIGNED, B=2, Hq=8, Hkv=2, D=128, bs=16, NB=64, maxlen=64, scale=0.1,
+                kvdt=pa.PA_BF16, out=ALIGNED, odt=pa.PA_BF16)
+    args.update(kw)
+    plan = ctypes.c_void_p(None)
+    st = lib.pa_append_decode(args["q"], args["kn"], args["vn"], args["k"], args["v"], args["bt"],
+                              args["mb"], args["sl"], args["B"], args["Hq"], args["Hkv"],
+                              args["D"], args["bs"], args["NB"], args["maxlen"], args["scale"],
+                              args["kvdt"], args["out"], args["odt"], ctypes.byref(plan), None)
+    assert plan.value is None, "an argument error must not create a plan"
+    return st
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(kn=None), pa.PA_ERR_NULL),
+    (dict(vn=None), pa.PA_ERR_NULL),
+    (dict(q=None), pa.PA_ERR_NULL),
+    (dict(kn=ALIGNED + 8), pa.PA_ERR_ALIGN),
+    (dict(vn=ALIGNED + 4), pa.PA_ERR_ALIGN),
+    (dict(D=96), pa.PA_ERR_SHAPE),
+    (dict(bs=8), pa.PA_ERR_BLOCK_SIZE),
+    (dict(kvdt=7), pa.PA_ERR_DTYPE),
+    (dict(kvdt=pa.PA_F32, odt=pa.PA_F32, maxlen=pa.PA_SIMPLE_MAX_SEQ_LEN + 1, mb=1024),
+     pa.PA_ERR_SHAPE),
+])
+def test_append_decode_rejects_bad_arguments_on_host(lib, kw, status):
+    # Every argument error returns before anything launches: the append is
+    # never run ahead of a decode that would be refused.
+    assert _append_decode(lib, **kw) == status
+
+
+def test_append_decode_empty_batch_is_a_no_op(lib):
+    assert _append_decode(lib, B=0) == pa.PA_OK
+
+
 def test_library_reads_no_environment_variables(lib):
     # Launch shapes come from the arguments and explicit plan setters only:
     # the library's code names no environment variable.

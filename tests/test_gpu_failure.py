@@ -183,3 +183,26 @@ def test_fused_merge_gives_up_reports_and_recovers(probe):
             out = ds.decode(plan)
             assert plan.last_device_error() == 0
             assert np.abs(out_f64(out) - ref).max() <= BF16_TOL
+
+
+def test_fused_append_decode_gives_up_reports_and_recovers(probe):
+    # A warp that gives up may have appended some rows already; the next
+    # call writes the same rows to the same slots, so it is exact.
+    wl = _gqa(37)
+    ds = DeviceStep(wl)
+    kp, vp = pools_after_append(wl)
+    ref = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale)
+
+    def call(plan):
+        pa.pa_append_decode(ds.q, ds.k_new, ds.v_new, ds.k_pool, ds.v_pool, ds.tables,
+                            ds.seq_lens, wl.scale, ds.out, wl.max_seq_len, plan)
+        return plan.last_device_error()
+
+    with pa.Plan() as plan:
+        call(plan)
+        with probe:
+            err = call(plan)
+        assert err & pa.PA_DEVERR_TIMEOUT
+        assert call(plan) == 0
+    assert np.abs(out_f64(ds.out) - ref).max() <= BF16_TOL
+    assert np.array_equal(ds.k_pool.view(torch.int16).cpu().numpy().view(np.uint16), kp)

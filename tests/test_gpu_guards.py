@@ -125,6 +125,29 @@ def test_append_and_decode_write_only_their_arrays(case):
     assert np.abs(out_f64(gs.out.t) - ref).max() <= tol
 
 
+@pytest.mark.parametrize("case", range(len(SHAPES)))
+def test_fused_append_decode_writes_only_its_arrays(case):
+    # The fused call writes the pools (one slot per sequence and kv head) and
+    # the output; every guard byte and every input must survive.
+    name, extra = SHAPES[case]
+    wl = make_workload(name, seed=900 + case, **extra)
+    gs = GuardedStep(wl, seed=case * 10 + 5)
+    with pa.Plan() as plan:
+        pa.pa_append_decode(gs.q.t, gs.k_new.t, gs.v_new.t, gs.k_pool.t, gs.v_pool.t,
+                            gs.tables.t, gs.seq_lens.t, wl.scale, gs.out.t, wl.max_seq_len, plan)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == 0
+    assert pa.pa_last_device_error(None) == 0
+    assert gs.all_guards_intact()
+    assert gs.inputs_unchanged()
+    kp, vp = pools_after_append(wl)
+    assert np.array_equal(bits(gs.k_pool.t), kp.view(bits(gs.k_pool.t).dtype))
+    assert np.array_equal(bits(gs.v_pool.t), vp.view(bits(gs.v_pool.t).dtype))
+    ref = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale)
+    tol = BF16_TOL if wl.dtype == "bf16" else 2e-3
+    assert np.abs(out_f64(gs.out.t) - ref).max() <= tol
+
+
 @pytest.mark.parametrize("case", [0, 1, 2])
 def test_noalloc_decode_writes_only_its_output(case):
     name, extra = SHAPES[case]
