@@ -1,5 +1,6 @@
 /*
- * The C boundary used from C: one decode step (pa_append_kv, then pa_decode)
+ * The C boundary used from C: one decode step (pa_append_kv, then pa_decode;
+ * and the same step as one pa_append_decode call on a copy of the pools)
  * and a verification step for the newest two tokens of every sequence
  * (pa_decode_multi) on device memory from cudaMalloc, with no Python or
  * PyTorch involved, checked against the fp64 oracle (linked from oracle/ as
@@ -126,6 +127,14 @@ int main(void) {
     CHECK_CUDA(cudaMemcpy(dsl, seq_lens, sizeof seq_lens, cudaMemcpyHostToDevice));
     CHECK_CUDA(cudaMemcpy(dcl, cache_lens, sizeof cache_lens, cudaMemcpyHostToDevice));
 
+    /* A second copy of the pools for the same step in one call. */
+    void *dk2, *dv2, *dout3;
+    CHECK_CUDA(cudaMalloc(&dk2, pool_elems * 2));
+    CHECK_CUDA(cudaMalloc(&dv2, pool_elems * 2));
+    CHECK_CUDA(cudaMalloc(&dout3, (size_t)B * HQ * D * 2));
+    CHECK_CUDA(cudaMemcpy(dk2, kpool, pool_elems * 2, cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemcpy(dv2, vpool, pool_elems * 2, cudaMemcpyHostToDevice));
+
     const float scale = 1.0f / sqrtf((float)D);
     pa_plan* plan = NULL;
     CHECK_PA(pa_append_kv(dkn, dvn, dk, dv, dtab, MAXB, dcl, B, HKV, D, BS, NB, PA_BF16, NULL));
@@ -142,6 +151,24 @@ int main(void) {
     CHECK_CUDA(cudaMemcpy(kgot, dk, pool_elems * 2, cudaMemcpyDeviceToHost));
     CHECK_CUDA(cudaMemcpy(vgot, dv, pool_elems * 2, cudaMemcpyDeviceToHost));
     CHECK_CUDA(cudaMemcpy(out, dout, sizeof out, cudaMemcpyDeviceToHost));
+
+    /* The same step as one call: the append at seq_lens - 1 inside the decode. */
+    pa_plan* plan3 = NULL;
+    CHECK_PA(pa_append_decode(dq, dkn, dvn, dk2, dv2, dtab, MAXB, dsl, B, HQ, HKV, D, BS, NB,
+                              MAXB * BS, scale, PA_BF16, dout3, PA_BF16, &plan3, NULL));
+    CHECK_CUDA(cudaDeviceSynchronize());
+    int ferr = -1;
+    CHECK_PA(pa_last_device_error(plan3, &ferr));
+    CHECK_PA(pa_free(plan3));
+    uint16_t* k3 = malloc(pool_elems * 2);
+    uint16_t* v3 = malloc(pool_elems * 2);
+    uint16_t out3[B * HQ * D];
+    CHECK_CUDA(cudaMemcpy(k3, dk2, pool_elems * 2, cudaMemcpyDeviceToHost));
+    CHECK_CUDA(cudaMemcpy(v3, dv2, pool_elems * 2, cudaMemcpyDeviceToHost));
+    CHECK_CUDA(cudaMemcpy(out3, dout3, sizeof out3, cudaMemcpyDeviceToHost));
+    const int fused_same = memcmp(k3, kgot, pool_elems * 2) == 0 &&
+                           memcmp(v3, vgot, pool_elems * 2) == 0 &&
+                           memcmp(out3, out, sizeof out) == 0;
 
     /* Verification step: the newest min(2, L_b) tokens of each sequence. */
     int32_t q_start[B + 1];
@@ -194,10 +221,11 @@ int main(void) {
         const double e = fabs(g - ref2[i]);
         if (e > worst2) worst2 = e;
     }
-    printf("device errors %d/%d/%d, pools equal %d, finite %d, max abs error %.3e / %.3e\n", derr,
-           aerr, merr, pools_equal, finite, worst, worst2);
-    return (derr == 0 && aerr == 0 && merr == 0 && pools_equal && finite && worst <= 1.5e-2 &&
-            worst2 <= 1.5e-2)
+    printf("device errors %d/%d/%d/%d, pools equal %d, one-call step identical %d, finite %d, "
+           "max abs error %.3e / %.3e\n", derr, aerr, merr, ferr, pools_equal, fused_same, finite,
+           worst, worst2);
+    return (derr == 0 && aerr == 0 && merr == 0 && ferr == 0 && pools_equal && fused_same &&
+            finite && worst <= 1.5e-2 && worst2 <= 1.5e-2)
                ? 0
                : 1;
 }
