@@ -679,7 +679,7 @@ def run_row(args, local_rank):
                         torch.from_numpy(wl.cache_lens).to(dev))
         torch.cuda.synchronize()
     if args.row in ("prefill", "spec"):
-        n_new = int(CONFIGS_NEW_TOKENS(args.workload))
+        n_new = int(args.new_tokens or CONFIGS_NEW_TOKENS(args.workload))
         ns = np.minimum(wl.seq_lens, n_new).astype(np.int64)
         qs = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
         T = int(qs[-1])
@@ -705,6 +705,8 @@ def run_row(args, local_rank):
             def call():
                 pa.pa_decode_multi(q, q_start, k_pool, v_pool, tables, seq_lens, wl.scale, out,
                                    int(ns.max()), wl.max_seq_len, plan)
+            call()                       # creates the plan
+            configure_plan(plan, args)   # --schedule / --merge, for same-box comparisons
         what = f"{T} query rows ({n_new} newest tokens per sequence), causal"
     elif args.row == "copy_blocks":
         n = min(8192, wl.num_blocks // 2)
@@ -763,7 +765,7 @@ def run_row(args, local_rank):
                {"metric": "speculative verification (pa_decode_multi): achieved HBM GB/s",
                 "value": gbs, "unit": "GB/s"}), "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, "what": what},
+            "config": {"workload": wl.name, "what": what, "queries_per_sequence": n_new},
             "roofline": ({"bound": "hbm", "achieved": gbs, "peak": peak, "peak_kind": peak_kind,
                           "unit": "GB/s", "frac": gbs / peak, "algorithmic_bytes": nbytes,
                           "tflops": tfs} if hbm_bound else
@@ -925,6 +927,8 @@ def main():
                     help="how the decode combines split partials (pa_plan_set_merge)")
     ap.add_argument("--schedule", default=None,
                     help="permille,pages: force the dynamic tail (pa_plan_set_schedule)")
+    ap.add_argument("--new-tokens", type=int, default=None,
+                    help="prefill / spec rows: queries per sequence (default: the workload's)")
     ap.add_argument("--step", default="separate", choices=sorted(STEPS),
                     help="decode row: the step's calls (fused = pa_append_decode)")
     ap.add_argument("--layout", default="paged", choices=sorted(LAYOUTS),
