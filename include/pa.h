@@ -207,14 +207,15 @@ const char* pa_status_str(pa_status status);
  */
 pa_status pa_last_device_error(pa_plan* plan, int* err);
 
-/* Force a kernel path for later pa_decode calls on this plan (PA_PATH_*).
- * A forced path that does not support a call's shape makes that call return
- * PA_ERR_DTYPE. */
+/* Force a kernel path for later pa_decode and pa_append_decode calls on this
+ * plan (PA_PATH_*; pa_append_decode then appends with its own kernel first on
+ * any path but PA_PATH_MMA). A forced path that does not support a call's
+ * shape makes that call return PA_ERR_DTYPE. */
 pa_status pa_plan_set_path(pa_plan* plan, int path);
 
 /* Test hook for the failure handling. While enable != 0, every kernel this
- * library launches (decode, multi-query decode, no-alloc decode, prefill,
- * page scores) makes its first pipeline wait on an mbarrier that nothing
+ * library launches (decode, one-call append and decode, multi-query decode,
+ * no-alloc decode, prefill, page scores) makes its first pipeline wait on an mbarrier that nothing
  * completes, bounded by 20 us, so that the wait expires: the kernel raises
  * PA_DEVERR_TIMEOUT, waits (bounded) for its own copies and tensor-core
  * products in flight, frees its tensor memory and returns. The outputs of
@@ -233,7 +234,9 @@ enum {
                             one query per sequence, up to 8 query heads per kv head */
 };
 
-/* Choose the merge of later pa_decode calls on this plan (PA_MERGE_*). A
+/* Choose the merge of later pa_decode and pa_append_decode calls on this plan
+ * (PA_MERGE_*; with PA_MERGE_FUSED, pa_append_decode appends with its own
+ * kernel first). A
  * call whose shape the fused merge does not serve returns PA_ERR_SHAPE while
  * PA_MERGE_FUSED is set. A test and benchmark hook beside pa_plan_set_path. */
 pa_status pa_plan_set_merge(pa_plan* plan, int mode);
