@@ -513,8 +513,11 @@ def run_ours(args, rank, world, local_rank):
     peak, peak_kind = measured_peak_gbs()
     achieved = dec_bytes / (split_ms * 1e-3) / 1e9
     sha = split_source_sha()
+    # The recorded counters are the plain split kernel's: none for the fused
+    # append's kernel or another layout.
     traffic = TRAFFIC["bytes_per_launch"] if TRAFFIC["source_sha"] == sha and \
-        TRAFFIC["workload"] == wl.name else None
+        TRAFFIC["workload"] == wl.name and args.step == "separate" and \
+        args.layout == "paged" else None
     value = job_bytes / (ms_step * 1e-3) / 1e9
     clocks = sampler.summary(w0, w1)
     clocks_kernel_pass = sampler.summary(w2, w3)
