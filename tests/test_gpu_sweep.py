@@ -5,7 +5,8 @@ Each case draws a head dimension (64 or 128), a block size (16 or 32), a kv
 head count and a group size (1 to 16 query heads per kv head, including ones
 that do not divide 128), a batch of 1 to 24 sequences and their lengths: some
 on the edges of a page (1, bs - 1, bs, bs + 1, 2 bs), the rest log-uniform up
-to a few thousand tokens. It then runs one append + decode step, a
+to a few thousand tokens. It then runs one append + decode step (as two
+calls and as one pa_append_decode call), a
 multi-query decode with 1 to 6 queries per sequence (on the split tiles up to
 16 (query, head) columns per kv head, on the prefill kernel above, or refused
 where that kernel does not serve the shape), and, where the shape allows, a
@@ -85,6 +86,28 @@ def test_decode_step_matches_oracle(i):
 
 
 @pytest.mark.parametrize("i", range(N_CASES))
+def test_one_call_step_matches_oracle(i):
+    # pa_append_decode on the same shapes: the pools equal oracle.append bit
+    # for bit and the output matches the oracle.
+    _, c = _draw(i)
+    wl = _workload(i, c)
+    kp, vp = pools_after_append(wl)
+    ref = oracle.decode(wl.q, kp, vp, wl.block_tables, wl.seq_lens, wl.scale)
+    ds = DeviceStep(wl)
+    with pa.Plan() as plan:
+        pa.pa_append_decode(ds.q, ds.k_new, ds.v_new, ds.k_pool, ds.v_pool, ds.tables,
+                            ds.seq_lens, wl.scale, ds.out, wl.max_seq_len, plan)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == 0
+    got = out_f64(ds.out)
+    assert np.isfinite(got).all()
+    e = np.abs(got - ref).max()
+    assert e <= BF16_TOL, f"{c}: max abs error {e:.3e}"
+    assert np.array_equal(ds.k_pool.view(torch.int16).cpu().numpy().view(np.uint16), kp)
+    assert np.array_equal(ds.v_pool.view(torch.int16).cpu().numpy().view(np.uint16), vp)
+
+
+@pytest.mark.parametrize("i", range(N_CASES))
 def test_multi_query_decode_matches_oracle(i):
     rng, c = _draw(i)
     wl = _workload(i, c)
@@ -159,6 +182,16 @@ def test_long_sequences_with_the_dynamic_tail_match_oracle(i):
     assert np.isfinite(got).all()
     e = np.abs(got - ref).max()
     assert e <= BF16_TOL, f"D {D} g {g} Hkv {Hkv} lens {lens}: max abs error {e:.3e}"
+    # The same step as one call, on fresh pools: the dynamic tail's pieces
+    # carry the appended slots too.
+    ds1 = DeviceStep(wl)
+    with pa.Plan() as plan:
+        pa.pa_append_decode(ds1.q, ds1.k_new, ds1.v_new, ds1.k_pool, ds1.v_pool, ds1.tables,
+                            ds1.seq_lens, wl.scale, ds1.out, wl.max_seq_len, plan)
+        torch.cuda.synchronize()
+        assert plan.last_device_error() == 0
+    assert torch.equal(ds1.out.view(torch.int16), ds.out.view(torch.int16))
+    assert torch.equal(ds1.k_pool.view(torch.int16), ds.k_pool.view(torch.int16))
 
     append_in_place(wl)
     ns, qs, q = _queries(rng, wl, max(1, 16 // g))
