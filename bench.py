@@ -37,8 +37,8 @@ L2_BYTES = 126 * 2**20
 # DRAM traffic of the split-attention kernel from an ncu capture (per launch,
 # scaled to the full workload), valid only for the kernel sources it was
 # measured on (sha256 of the split kernel's source files).
-TRAFFIC = {"source_sha": "34b19d5e2ad95951e9dfe4531882438c806a5069e9286538bcee284c0a277f09",
-           "workload": "llama3_8b_gqa", "bytes_per_launch": 2205581056 + 5087872}
+TRAFFIC = {"source_sha": "dada515cdcaf5f7fe87024fae57afc2148cf5706c625c1a023417ca97de38170",
+           "workload": "llama3_8b_gqa", "bytes_per_launch": 2205629824 + 5011456}
 
 
 def split_source_sha() -> str:

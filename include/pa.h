@@ -172,12 +172,13 @@ pa_status pa_decode(const void* q, const void* k_pool, const void* v_pool,
  *
  * Results and pool contents equal pa_append_kv (with cache_lens = seq_lens - 1)
  * followed by pa_decode, bit for bit. On bf16 pools with the tensor-core
- * path and the merge kernel (the automatic choices), the append runs inside
- * the decode kernel: the warp that reads a sequence's last page writes the
- * new row into its staged copy and into the pool, which saves the append's
- * launch and its round trips. Otherwise (float32 pools, a forced CUDA-core
- * path, the fused merge) the append runs as its own kernel first, and its
- * PA_DEVERR_* bits go to the library-wide append word as for pa_append_kv.
+ * path, up to 8 query heads per kv head and the merge kernel (the automatic
+ * choices), the append runs inside the decode kernel: the warp that reads a
+ * sequence's last page writes the new row into its staged copy and into the
+ * pool, which saves the append's launch and its round trips. Otherwise
+ * (float32 pools, a forced CUDA-core path, 9-16 query heads per kv head, the
+ * fused merge) the append runs as its own kernel first, and its PA_DEVERR_*
+ * bits go to the library-wide append word as for pa_append_kv.
  * Precondition as for pa_append_kv: the written block is private to its
  * sequence. A sequence whose length is out of range gets no append and zero
  * rows (PA_DEVERR_SEQ_LEN); a table entry outside the pool skips the append

@@ -19,7 +19,7 @@ namespace {
 using pa::SplitLaunch;
 
 constexpr int kDefaultWarps = 3;           // warps per block of the split kernels
-constexpr int kMultiWarps = 5;             // ... with several queries per sequence
+constexpr int kMqWarps = 5;                // ... with 9-16 multi-query columns (two blocks per SM)
 constexpr int kDefaultStages = 1;          // pipeline stages per warp
 constexpr int kDynPermille = 150;          // share of the page stream scheduled dynamically
 constexpr int kDynMinPages = 1024;         // ... when a sequence may have this many pages
@@ -121,29 +121,52 @@ bool split_shape(int kind, int nq, int B, int Hq, int Hkv, int D, int block_size
     s.P_max = static_cast<int64_t>(B) * s.U * s.max_pages;
     if (s.P_max > INT32_MAX) return false;
 
-    // K and V of a chunk, then the query rows (padded rows for the tiles that
-    // reread them at every chunk: several queries per sequence, or two
-    // n-tiles).
-    const bool qs = s.mq || s.NT == 2;
-    const size_t q_row = qs ? static_cast<size_t>(mq_q_pitch(D)) : static_cast<size_t>(D) * 2u;
-    s.stage_bytes = round_up(2u * kChunkTokens * D * 2u + static_cast<size_t>(s.GS) * q_row, 1024);
     s.lens_bytes = round_up(static_cast<size_t>(2 * B + 1) * 4u, 1024);
     // Many warps with one stage each: a warp waits for its chunk while the other
-    // warps of the SM compute, so bytes in flight scale with the warp count
-    // (3 warps per block, up to 4 blocks per SM at 32-token stages).
-    // With 9-16 (query, head) columns the 21.5 KB stages allow ten warps per
-    // SM: two blocks of five (about 168 registers a thread).
-    s.warps = s.NT == 2 ? kMultiWarps : kDefaultWarps;
+    // warps of the SM compute, so bytes in flight scale with the warp count.
     s.stages = kDefaultStages;
-    if (qs) {
-        s.stages = 1;  // the query rows stay in the stage for the whole segment
-        s.warps = std::min(s.warps, kMultiWarps);  // the kernels' launch bound: 5 warps
+    if (s.mq) {
+        // Several queries per sequence: the query rows at a padded pitch in
+        // the stage after K and V (reread at every chunk; one stage per warp
+        // keeps a segment's rows in place), two blocks of five warps per SM
+        // at 16 columns, three warps a block below. The per-warp row region
+        // of the two-n-tile decode below measured slower for this kernel
+        // (its launch bound then caps registers at 170 instead of 204).
+        s.stages = 1;
+        s.stage_bytes = round_up(2u * kChunkTokens * D * 2u +
+                                     static_cast<size_t>(s.GS) * mq_q_pitch(D), 1024);
+        s.q_bytes = 0;
+        s.warps = s.NT == 2 ? kMqWarps : kDefaultWarps;
+    } else if (s.NT == 2) {
+        // One query, two n-tiles (9-16 query heads per kv head): the query
+        // rows are reread at every chunk from a region of their own per warp
+        // at a padded pitch, so that a stage is just a chunk's K and V and
+        // wastes nothing to the 1 KiB rounding. One stage per warp: a
+        // segment's rows stay in place until it ends. As many warps as the
+        // shared memory holds, in one block per SM: 11 at D = 128 (20.3 KB a
+        // warp), 12 at D = 64.
+        s.stages = 1;
+        s.stage_bytes = round_up(2u * kChunkTokens * D * 2u, 1024);
+        s.q_bytes = round_up(static_cast<size_t>(s.GS) * mq_q_pitch(D), 16);
+        const size_t per_warp = s.stage_bytes + s.q_bytes + 8 + 16;  // ring, rows, barrier, record
+        const size_t fixed = 1024 + s.lens_bytes + 16 + 16;         // alignment, arrays, padding, probe
+        if (fixed >= kSmemLimit) return false;
+        s.warps = static_cast<int>(std::min<size_t>(kQsMaxWarps, (kSmemLimit - fixed) / per_warp));
+        if (s.warps < 1) return false;
+    } else {
+        // K and V of a chunk, then the segment's query rows (read once per
+        // segment): 3 warps per block, up to 4 blocks per SM.
+        s.stage_bytes = round_up(2u * kChunkTokens * D * 2u + static_cast<size_t>(s.GS) * D * 2u,
+                                 1024);
+        s.q_bytes = 0;
+        s.warps = kDefaultWarps;
     }
     // ring, mbarriers (8 B each, padded to 16 B), per-stage range records (16 B
-    // each), the wait-probe mbarrier (16 B)
+    // each), the wait-probe mbarrier (16 B), the query-row regions
     s.smem = 1024 + s.lens_bytes + static_cast<size_t>(s.warps) * s.stages * s.stage_bytes +
              round_up(static_cast<size_t>(s.warps) * s.stages * 8, 16) +
-             static_cast<size_t>(s.warps) * s.stages * 16 + 16;
+             static_cast<size_t>(s.warps) * s.stages * 16 + 16 +
+             static_cast<size_t>(s.warps) * s.q_bytes;
     if (s.smem > kSmemLimit) return false;
     *out = s;
     return true;
@@ -210,6 +233,7 @@ void set_split_plan(SplitArgs* a, const SplitShape& s, const SplitGrid& gr) {
     a->stages = s.stages;
     a->stage_bytes = static_cast<int>(s.stage_bytes);
     a->lens_bytes = static_cast<int>(s.lens_bytes);
+    a->q_bytes = static_cast<int>(s.q_bytes);
     a->dyn_permille = gr.dyn_permille;
     a->dyn_pages = gr.dyn_pages;
 }
@@ -403,9 +427,14 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     const bool can_fuse = !q_start && sh.kind == pa::kSplitMma && sh.NT == 1 && sh.warps == 3;
     L.fused = can_fuse && plan->merge_mode == PA_MERGE_FUSED ? 1 : 0;
     if (plan->merge_mode == PA_MERGE_FUSED && !can_fuse) return PA_ERR_SHAPE;
-    // The append rides in the split kernel on the tensor-core tiles with one
-    // stage per warp and the merge kernel; elsewhere it runs first on its own.
-    L.append = k_new && !q_start && !L.fused && sh.kind == pa::kSplitMma && sh.stages == 1 ? 1 : 0;
+    // The append rides in the split kernel on the one-n-tile tensor-core
+    // tiles (up to 8 query heads per kv head) with one stage per warp and the
+    // merge kernel; elsewhere it runs first on its own. With two n-tiles the
+    // fused kernel measured slower than the two launches (Llama-3-405B
+    // grouping: step 283.5 vs 280.2 us), so those shapes take the append
+    // kernel.
+    L.append = k_new && !q_start && !L.fused && sh.kind == pa::kSplitMma && sh.NT == 1 &&
+                       sh.stages == 1 ? 1 : 0;
     int per_sm = 0;
     for (const OccKey& o : plan->occ) {
         if (o.kind == L.kind && o.D == D && o.BS == block_size && o.NT == L.NT &&

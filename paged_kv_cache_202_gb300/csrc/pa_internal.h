@@ -65,6 +65,7 @@ struct SplitArgs {
     int stages;                // pipeline stages per warp
     int stage_bytes;           // bytes per stage (multiple of 1024)
     int lens_bytes;            // bytes of the per-sequence arrays at the front of shared memory
+    int q_bytes;               // per warp: query-row region after the rings (0: rows in the stage)
     int dyn_permille;          // fraction of the page stream handed out dynamically (1/1000)
     int dyn_pages;             // pages per dynamic piece
     // Several queries per sequence (speculative verification): q and out are
@@ -118,7 +119,12 @@ struct SplitShape {
     int64_t max_pages = 0;         // pages of the longest possible sequence
     int64_t P_max = 0;             // pages over all (sequence, kv unit) segments, at most
     size_t stage_bytes = 0, lens_bytes = 0, smem = 0;
+    size_t q_bytes = 0;            // per warp: query rows outside the ring (tiles that reread them)
 };
+// Warps per block of the tiles that reread their query rows (several queries
+// per sequence, or two n-tiles): as many as the shared memory holds, at most
+// 12 (three warps per SM sub-partition at up to 170 registers a thread).
+constexpr int kQsMaxWarps = 12;
 // kind: kSplitFma (one query head per kv unit) or kSplitMma; nq > 0 selects
 // the multi-query tile (nq queries x g heads, tensor cores). Returns false
 // when the sizes do not fit (page count over 32 bits, shared memory over the

@@ -13,20 +13,20 @@ __global__ void __launch_bounds__(256, 1)
 
 // Two n-tiles (9-16 query heads per kv head) read their query fragments
 // from shared memory at every chunk, as the multi-query kernel does, and run
-// two blocks of five warps per SM.
+// one block of up to twelve warps per SM (as many as the shared memory holds).
 template <int D, int BS, int NT>
-__global__ void __launch_bounds__(NT == 2 ? 160 : 256, NT == 2 ? 2 : 1)
+__global__ void __launch_bounds__(NT == 2 ? 32 * kQsMaxWarps : 256, 1)
     mma_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                const SplitArgs a) {
     split_body<D, BS, MmaState<D, kChunkTokens, NT, NT == 2>>(&kmap, &vmap, a);
 }
 
-// The same kernels with the step's append fused in (pa_append_decode).
-template <int D, int BS, int NT>
-__global__ void __launch_bounds__(NT == 2 ? 160 : 256, NT == 2 ? 2 : 1)
+// The one-n-tile kernel with the step's append fused in (pa_append_decode).
+template <int D, int BS>
+__global__ void __launch_bounds__(256, 1)
     mma_append_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const SplitArgs a) {
-    split_body<D, BS, MmaState<D, kChunkTokens, NT, NT == 2>, false, false, true>(&kmap, &vmap, a);
+    split_body<D, BS, MmaState<D, kChunkTokens, 1, false>, false, false, true>(&kmap, &vmap, a);
 }
 
 // One n-tile with the fused merge: the warp that writes a segment's last
@@ -40,8 +40,8 @@ __global__ void __launch_bounds__(96, 4)
 }
 
 // Several queries per sequence (speculative verification) on the same tiles,
-// query fragments read from shared memory at every chunk; at most 204
-// registers a thread, so that two blocks of five warps fit an SM.
+// query fragments read from the stage's query rows at every chunk; at most
+// 204 registers a thread, so that two blocks of five warps fit an SM.
 template <int D, int BS, int NT>
 __global__ void __launch_bounds__(160, 2)
     mma_mq_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -65,8 +65,7 @@ KernelFn select(const SplitLaunch& L) {
             return nullptr;                                                     \
         }                                                                       \
         if (L.append) {                                                         \
-            if (L.kind == kSplitMma && L.NT == 1) return mma_append_kernel<D_, BS_, 1>; \
-            if (L.kind == kSplitMma && L.NT == 2) return mma_append_kernel<D_, BS_, 2>; \
+            if (L.kind == kSplitMma && L.NT == 1) return mma_append_kernel<D_, BS_>; \
             return nullptr;                                                     \
         }                                                                       \
         if (L.kind == kSplitFma) return fma_kernel<D_, BS_>;                    \

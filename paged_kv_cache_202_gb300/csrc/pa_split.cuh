@@ -700,6 +700,11 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
     const uint32_t meta0 = bars0 + ((static_cast<uint32_t>(W * S * 8) + 15u) & ~15u);
     // An mbarrier that nothing completes: the wait-expiry probe's first wait.
     const uint32_t probe_bar = meta0 + static_cast<uint32_t>(W * S * 16);
+    // The two-n-tile decode keeps its query rows per warp after the rest
+    // (one stage per warp); the other kernels carry them in the stage after
+    // K and V.
+    constexpr bool kQRegion = State::kQS && !MQ;
+    const uint32_t q_region0 = probe_bar + 16;
 
     if (threadIdx.x == 0) {
         prefetch_tensormap(kmap);
@@ -780,6 +785,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
     const uint32_t my_bars = bars0 + warp * S * 8;
     const uint32_t my_meta = meta0 + warp * S * 16;
     const uint32_t my_ring = ring0 + static_cast<uint32_t>(warp * S * a.stage_bytes);
+    const uint32_t my_q = q_region0 + static_cast<uint32_t>(warp * a.q_bytes);
     if (lane == 0) {
         for (int s = 0; s < S; ++s) mbar_init(my_bars + 8 * s, 1);
         fence_barrier_init();
@@ -887,7 +893,8 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
                         } else {
                             row = static_cast<size_t>(ci.b) * a.Hq + kvh * a.g + slice * a.GS + c;
                         }
-                        bulk_load(stg + 2 * CT * D * 2 + c * mq_q_pitch(D), a.q + row * D, D * 2, bar);
+                        bulk_load((kQRegion ? my_q : stg + 2 * CT * D * 2) + c * mq_q_pitch(D),
+                                  a.q + row * D, D * 2, bar);
                     }
                 } else {
                     const uint16_t* src =
@@ -978,7 +985,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
                 nh = min(a.GS, a.g - slice * a.GS);
                 hq0 = kvh * a.g + slice * a.GS;
             }
-            st.start(stg + 2 * CT * D * 2, nh, lane);
+            st.start(kQRegion ? my_q : stg + 2 * CT * D * 2, nh, lane);
             p_first = cc.p;
             poison = false;
         }
@@ -1006,8 +1013,7 @@ __device__ __forceinline__ void split_body(const CUtensorMap* kmap, const CUtens
                 st.template page<true>(stg, stg + CT * D * 2, nv, a.scale_log2, lane, rem, nqb, a.g,
                                        stg + 2 * CT * D * 2, nh);
             else if constexpr (State::kQS)
-                st.page(stg, stg + CT * D * 2, nv, a.scale_log2, lane, 0, 0, 1,
-                        stg + 2 * CT * D * 2, nh);
+                st.page(stg, stg + CT * D * 2, nv, a.scale_log2, lane, 0, 0, 1, my_q, nh);
             else
                 st.page(stg, stg + CT * D * 2, nv, a.scale_log2, lane);
         }

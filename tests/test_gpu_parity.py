@@ -106,10 +106,11 @@ def test_auto_path_choice():
             assert plan.info()[0] == want
 
 
-@pytest.mark.parametrize("Hq,Hkv,warps_per_block", [(32, 8, 3), (64, 4, 5), (128, 8, 5), (8, 8, 3)])
+@pytest.mark.parametrize("Hq,Hkv,warps_per_block", [(32, 8, 3), (64, 4, 11), (128, 8, 11), (8, 8, 3)])
 def test_launch_shape(Hq, Hkv, warps_per_block):
     # Up to 8 query heads per kv head: blocks of three warps; 9-16 (two
-    # n-tiles, query fragments reread from shared memory): blocks of five.
+    # n-tiles, query fragments reread from a per-warp region of shared
+    # memory): one block of eleven warps per SM at D = 128.
     wl = _exact(Hq, Hkv, 128, 16, [300, 1200], seed=77)
     ref, _, _ = _reference(wl)
     ds = DeviceStep(wl)
