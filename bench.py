@@ -73,6 +73,16 @@ def measured_peak_tflops():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
+def measured_peak_tflops_sustained():
+    """The bf16 GEMM rate held back to back for seconds (clocks under the power cap), or None."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            v = json.load(f).get("bf16_tflops_sustained")
+        return float(v) if v is not None else None
+    except (OSError, ValueError, TypeError):
+        return None
+
+
 def measured_peak_gbs():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -774,7 +784,13 @@ def run_row(args, local_rank):
                           "tflops": tfs} if hbm_bound else
                          {"bound": "tensor", "achieved": tfs, "peak": tpeak, "peak_kind": tkind,
                           "unit": "TFLOP/s", "frac": tfs / tpeak, "algorithmic_flops": flops,
-                          "hbm_gbs": gbs}),
+                          "hbm_gbs": gbs,
+                          # the same rate against the GEMM held for seconds, the fairer
+                          # denominator when this loop runs long enough to meet the power cap
+                          "peak_sustained": measured_peak_tflops_sustained(),
+                          "frac_sustained": (tfs / measured_peak_tflops_sustained()
+                                             if measured_peak_tflops_sustained() else None),
+                          "timed_s": ms * args.steps * 1e-3}),
             "parity": parity, "gpu_launches": (2 if args.row == "spec" else 1) * args.steps,
             "cpu_baseline": cpu,
         }), flush=True)

@@ -97,6 +97,22 @@ bool encode_pool_map(CUtensorMap* map, const void* pool, int rows, int D, int BS
     return r == CUDA_SUCCESS;
 }
 
+bool encode_query_map(CUtensorMap* map, const void* q, int T, int Hq, int g, int Qb) {
+    // q [T][Hq][D = 128] bf16 as (D, Hq, T); one box = one 64-column half of a
+    // query tile: Qb queries x the g heads of a kv head, rows in (query, head)
+    // order, 128-byte swizzle (the K-major layout of the tile's MMA operand).
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(Hq), static_cast<cuuint64_t>(T)};
+    cuuint64_t strides[2] = {128 * 2, static_cast<cuuint64_t>(Hq) * 128 * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g), static_cast<cuuint32_t>(Qb)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
+                    box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 bool split_shape(int kind, int nq, int B, int Hq, int Hkv, int D, int block_size, int max_blocks,
                  int max_seq_len, SplitShape* out) {
     SplitShape s;

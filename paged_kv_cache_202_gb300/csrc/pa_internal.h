@@ -210,6 +210,10 @@ cudaError_t read_append_error(int* err);
 // Device address of that word on the current device.
 cudaError_t append_error_address(int** p);
 
+// Tensor map of the prefill's query rows q [T][Hq][128] bf16: one box is one
+// 64-column half of a query tile (Qb queries x g heads, 128-byte swizzle).
+bool encode_query_map(CUtensorMap* map, const void* q, int T, int Hq, int g, int Qb);
+
 cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, const void* q,
                            int num_q, const int32_t* q_start, const int32_t* tables,
                            const int32_t* seq_lens, void* out, int* err, int B, int Hq, int Hkv,

@@ -14,7 +14,12 @@
 //   * warps 16 and 18 (producers): tiled bulk tensor copies of 128-token K
 //     and V chunks (whole pages, through the block table) into a 2-stage K
 //     ring and a 3-stage V ring, each stream on its own warp so that a wait
-//     for a free V stage never holds back the next K;
+//     for a free V stage never holds back the next K; the K warp first
+//     copies the block's query tiles (a tensor map over q whose box is one
+//     64-column half of a tile, rows in (query, head) order, landing in the
+//     swizzled K-major layout the score products read), so that the
+//     prologue holds no query rows in registers and the first chunk is on
+//     its way as soon as the table check has passed;
 //   * warp 17 (MMA): one thread issues S_t = Q_t K^T (M=128, N=128, K=128,
 //     both operands in shared memory) into tensor memory and
 //     O_t += P_t V (M=128, N=128, K=128) with P_t read from tensor memory and
@@ -98,9 +103,10 @@ constexpr uint32_t kSlotTmem = kBarDrain + 8;
 constexpr uint32_t kSlotAbort = kSlotTmem + 4;
 constexpr uint32_t kSlotSeq = kSlotAbort + 4;
 constexpr uint32_t kBarProbe = kSlotSeq + 8;          // nothing completes it (wait-expiry probe)
+constexpr uint32_t kBarQ = kBarProbe + 8;             // the block's query tiles have landed
 constexpr uint32_t kOffLens = kOffBar + 256;          // [kSortMax] lengths, for the ordering
 constexpr uint32_t kSmemBytes = 1024 + kOffLens + 4 * kSortMax;
-static_assert(kBarProbe % 8 == 0 && kBarProbe + 8 <= kOffLens - kOffBar,
+static_assert(kBarQ % 8 == 0 && kBarQ + 8 <= kOffLens - kOffBar,
               "barrier area overlaps the length array");
 static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0, "swizzle atoms");
 static_assert(kSmemBytes <= 227 * 1024 && 2 * kSmemBytes > 228 * 1024,
@@ -172,7 +178,7 @@ __device__ __forceinline__ bool wait_role(uint32_t bar, uint32_t parity, volatil
 template <int BS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                   const PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap qmap, const PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t raw = smem_addr(smem_raw);
@@ -233,20 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const bool row_valid = softmax && qi < (t == 0 ? nq0 : nq1);
     const size_t out_row = (static_cast<size_t>(qs) + q0 + t * a.Qb + qi) * a.Hq + h * a.g + qj;
 
-    // The table entries this block reads, validated once.
-    bool bad = false;
-    for (int i = tid; i < nb; i += kThreads) {
-        const int p = table[i];
-        bad |= p < 0 || p >= a.num_blocks;
-    }
-    if (__syncthreads_or(bad)) {
-        if (tid == 0) atomicOr(a.err, kErrTable);
-        if (row_valid) {
-            float z[kD / 2] = {};
-            write_row<kD / 2>(a, out_row, z, 0.f, 64 * half);
-        }
-        return;
-    }
+    // The block's barriers, set up before the table check so that the copy
+    // warps can start as soon as it has passed.
     if (tid == 0) {
         for (int s = 0; s < kStagesK; ++s) {
             mbar_init(bars + kBarKFull + 8 * s, 1);
@@ -263,30 +257,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(bars + kBarDrain, 1);
         mbar_init(bars + kBarProbe, 1);
+        mbar_init(bars + kBarQ, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == kWarpMma) {
-        tc::alloc(bars + kSlotTmem, kTmemCols);
-        tc::relinquish();
+    // The table entries this block reads, validated once.
+    bool bad = false;
+    for (int i = tid; i < nb; i += kThreads) {
+        const int p = table[i];
+        bad |= p < 0 || p >= a.num_blocks;
     }
-    // Query rows -> swizzled K-major tiles (two 64-column halves each); each
-    // thread moves its half of the row.
-    if (softmax) {
-        const uint16_t* src = a.q + out_row * kD + 64 * half;
-        const uint32_t qt = base + kOffQ + t * kTileQ + half * 16384 + row * 128;
-#pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-            const uint4 w = row_valid ? *reinterpret_cast<const uint4*>(src + cc * 8)
-                                      : make_uint4(0, 0, 0, 0);
-            st_shared_v4(qt + ((cc ^ (row & 7)) << 4), w);
+    if (__syncthreads_or(bad)) {
+        if (tid == 0) atomicOr(a.err, kErrTable);
+        if (row_valid) {
+            float z[kD / 2] = {};
+            write_row<kD / 2>(a, out_row, z, 0.f, 64 * half);
         }
+        return;
     }
-    fence_proxy_async_smem();
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(gbase + kOffBar + kSlotTmem);
+    // The copy warps go straight to work (the query tiles arrive by tiled
+    // bulk copies with the first chunk, see below). The softmax warps and the
+    // MMA warp meet on a named barrier of their own once the tensor memory
+    // is allocated.
+    uint32_t tmem = 0;
+    if (warp != kWarpLoad && warp != kWarpLoadV) {
+        if (warp == kWarpMma) {
+            tc::alloc(bars + kSlotTmem, kTmemCols);
+            tc::relinquish();
+        }
+        tc::fence_before_sync();
+        asm volatile("bar.sync 1, %0;" ::"n"(kSoftmaxThreads + 32) : "memory");
+        tc::fence_after_sync();
+        tmem = *reinterpret_cast<volatile uint32_t*>(gbase + kOffBar + kSlotTmem);
+    }
 
     if (warp == kWarpLoad || warp == kWarpLoadV) {
         // ------------------------------------------------------------ producers (K, V)
@@ -298,6 +301,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t ring = base + (is_k ? kOffK : kOffV);
             const CUtensorMap* map = is_k ? &kmap : &vmap;
             const uint64_t policy = policy_evict_first();
+            if (is_k) {
+                // The query tiles, in the swizzled K-major layout of the score
+                // products' A operand: one box per 64-column half, rows in
+                // (query, head) order. Rows past the tile's queries hold other
+                // rows of q or zeros; the softmax masks them by predicate.
+                mbar_arrive_expect_tx(bars + kBarQ, (two ? 2u : 1u) * kTileQ);
+                for (int u = 0; u < (two ? 2 : 1); ++u)
+#pragma unroll
+                    for (int hf = 0; hf < 2; ++hf)
+                        tma_load_3d(base + kOffQ + u * kTileQ + hf * 16384, &qmap, hf * 64, h * a.g,
+                                    qs + q0 + u * a.Qb, bars + kBarQ, policy);
+            }
             int issued = 0;
             for (int c = 0; c < nc; ++c) {
                 const int s = c % nst;
@@ -321,6 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // an abort the consumers have waited for them already.
             for (int c = max(0, issued - nst); c < issued; ++c)
                 mbar_wait_bounded(full + 8 * (c % nst), (c / nst) & 1, kWaitLimitNs);
+            if (is_k) mbar_wait_bounded(bars + kBarQ, 0, kWaitLimitNs);  // the query tiles too
         }
         __syncwarp();
     } else if (warp == kWarpMma) {
@@ -359,7 +375,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 atomicOr(a.err, kErrTimeout);
                 ok = false;
             } else {
-                ok = wait_role(bars + kBarKFull, 0, abort_flag, a.err);
+                ok = wait_role(bars + kBarQ, 0, abort_flag, a.err) &&
+                     wait_role(bars + kBarKFull, 0, abort_flag, a.err);
             }
             if (ok) {
                 tc::fence_after_sync();
@@ -557,12 +574,14 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
     // No sequence has more queries than the call has rows.
     const int64_t nq = std::min<int64_t>(max_q, num_q);
     dim3 grid(static_cast<unsigned>((nq + 2 * a.Qb - 1) / (2 * a.Qb)), Hkv, B);
+    CUtensorMap qmap;
+    if (!encode_query_map(&qmap, q, num_q, Hq, a.g, a.Qb)) return cudaErrorInvalidValue;
     auto kern = block_size == 16 ? prefill_kernel<16> : prefill_kernel<32>;
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(kmap, vmap, a);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(kmap, vmap, qmap, a);
     return cudaGetLastError();
 }
 
