@@ -313,22 +313,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                         tma_load_3d(base + kOffQ + u * kTileQ + hf * 16384, &qmap, hf * 64, h * a.g,
                                     qs + q0 + u * a.Qb, bars + kBarQ, policy);
             }
+            // The table entries of a chunk are loaded one chunk ahead, so
+            // that their latency overlaps the wait for a free stage instead
+            // of preceding every page's copy.
+            constexpr int kPages = kChunk / BS;
+            int pg[kPages];
+            auto load_pages = [&](int c) {
+#pragma unroll
+                for (int j = 0; j < kPages; ++j) {
+                    const int p = c * kPages + j;
+                    pg[j] = p < nb ? table[p] : 0;
+                }
+            };
+            load_pages(0);
             int issued = 0;
             for (int c = 0; c < nc; ++c) {
                 const int s = c % nst;
                 if (c >= nst && !wait_role(empty + 8 * s, ((c / nst) - 1) & 1, abort_flag, a.err)) break;
                 // One chunk (its pages, both 64-column halves) into the stage.
-                const int p0 = c * (kChunk / BS);
-                const int np = min(kChunk / BS, nb - p0);
+                const int np = min(kPages, nb - c * kPages);
                 const uint32_t bar = full + 8 * s, stage = ring + s * kStageKV;
                 mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np) * BS * kD * 2);
-                for (int j = 0; j < np; ++j) {
-                    const int r = table[p0 + j] * a.Hkv + h;
 #pragma unroll
-                    for (int half = 0; half < 2; ++half)
-                        tma_load_3d(stage + half * kHalfKV + j * BS * 128, map, half * 64, 0, r, bar, policy);
+                for (int j = 0; j < kPages; ++j) {
+                    if (j < np) {
+                        const int r = pg[j] * a.Hkv + h;
+#pragma unroll
+                        for (int hf = 0; hf < 2; ++hf)
+                            tma_load_3d(stage + hf * kHalfKV + j * BS * 128, map, hf * 64, 0, r, bar, policy);
+                    }
                 }
                 issued = c + 1;
+                load_pages(c + 1);
             }
             // Copies still in flight land before the block leaves: the last
             // chunk issued on each stage (its phase is then final; earlier
