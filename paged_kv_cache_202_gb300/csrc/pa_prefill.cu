@@ -32,7 +32,10 @@
 //     by predicate, join the row maximum with the partner (one shuffle), run
 //     the online softmax and store the bf16 probabilities P_t over the first
 //     64 columns of the same scores (the A operand of the PV product); at the
-//     end, read the row of O_t, normalise and store it.
+//     end, read the row of O_t and normalise it. A full tile with bf16
+//     output is staged in the tile's query buffer (the same swizzled box
+//     layout the query copy used) and leaves by two tiled bulk tensor
+//     stores; a partial tile or float output is stored by the threads.
 // The MMA thread issues PV_0(c), S_0(c+1), PV_1(c), S_1(c+1), ...: one
 // thread's products run in issue order, so S_t(c+1) overwrites P_t(c) only
 // after PV_t(c) has read it, and its completion (one commit covers every
@@ -136,6 +139,34 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
                  : "memory");
 }
 
+// Named barrier over `count` threads that also returns the AND of `pred`
+// over them.
+__device__ __forceinline__ bool bar_red_and(int id, int count, bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+// Tiled tensor copy shared -> global (3-D box), tracked as a bulk async group.
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%1, %2, %3}], [%4];"
+                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(src)
+                 : "memory");
+}
+
+// Close the bulk group and wait until its copies have read shared memory.
+__device__ __forceinline__ void bulk_commit_and_wait_read() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 template <int ND>
 __device__ __forceinline__ void write_row(const PrefillArgs& a, size_t row, const float (&v)[ND],
                                           float inv, int d0) {
@@ -178,7 +209,8 @@ __device__ __forceinline__ bool wait_role(uint32_t bar, uint32_t parity, volatil
 template <int BS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                   const __grid_constant__ CUtensorMap qmap, const PrefillArgs a) {
+                   const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap omap,
+                   const PrefillArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t raw = smem_addr(smem_raw);
@@ -536,19 +568,50 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_before_sync();
             mbar_arrive(bars + kBarP + 8 * t);
         }
-        if (ok) {
-            ok = __all_sync(0xffffffffu, wait_role(bars + kBarO + 8 * t, 0, abort_flag, a.err));
-            if (ok) {
-                tc::fence_after_sync();
-                const float lt = l + __shfl_xor_sync(0xffffffffu, l, 16);
-                const float inv = (row_valid && lt > 0.f) ? 1.f / lt : 0.f;
+        // Epilogue. A full tile with bf16 output goes out by tiled bulk
+        // tensor copies: each thread normalises its half row of O_t into the
+        // tile's query buffer (free once every product is done; a half row
+        // is one 128-byte row of a 64-column box, 16-byte chunk c at
+        // c ^ (row % 8)), then one thread stores both boxes. A partial tile
+        // (a box would cover rows of the next sequence) or float output is
+        // written by the threads directly.
+        const bool tma_out = a.out_bf16 && (t == 0 ? nq0 : nq1) == a.Qb;
+        const uint32_t qbuf = base + kOffQ + t * kTileQ;
+        bool fine = ok && __all_sync(0xffffffffu, wait_role(bars + kBarO + 8 * t, 0, abort_flag, a.err));
+        if (fine) {
+            tc::fence_after_sync();
+            if (tma_out) fence_proxy_async_smem();  // the buffer was last used by the copies and products
+            const float lt = l + __shfl_xor_sync(0xffffffffu, l, 16);
+            const float inv = (row_valid && lt > 0.f) ? 1.f / lt : 0.f;
+            const uint32_t srow = qbuf + half * 16384 + row * 128;
 #pragma unroll
-                for (int piece = 0; piece < 2; ++piece) {
-                    float o[32];
-                    tc::ld16x2_32<64>(o_addr + 32 * piece, o);
-                    tc::wait_ld();
-                    if (row_valid) write_row<32>(a, out_row, o, inv, 64 * half + 32 * piece);
+            for (int piece = 0; piece < 2; ++piece) {
+                float o[32];
+                tc::ld16x2_32<64>(o_addr + 32 * piece, o);
+                tc::wait_ld();
+                if (tma_out) {
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const uint4 w = make_uint4(pack_bf16x2(o[8 * k] * inv, o[8 * k + 1] * inv),
+                                                   pack_bf16x2(o[8 * k + 2] * inv, o[8 * k + 3] * inv),
+                                                   pack_bf16x2(o[8 * k + 4] * inv, o[8 * k + 5] * inv),
+                                                   pack_bf16x2(o[8 * k + 6] * inv, o[8 * k + 7] * inv));
+                        st_shared_v4(srow + (((4 * piece + k) ^ (row & 7)) << 4), w);
+                    }
+                } else if (row_valid) {
+                    write_row<32>(a, out_row, o, inv, 64 * half + 32 * piece);
                 }
+            }
+        }
+        if (tma_out) {
+            fence_proxy_async_smem();  // this thread's rows, visible to the tensor copy
+            // Every thread of the tile meets here; the copy runs only if all
+            // of them staged their rows.
+            if (bar_red_and(2 + t, kTileThreads, fine) && tid == t * kTileThreads) {
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf)
+                    tma_store_3d(&omap, qbuf + hf * 16384, hf * 64, h * a.g, qs + q0 + t * a.Qb);
+                bulk_commit_and_wait_read();
             }
         }
     }
@@ -590,14 +653,20 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
     // No sequence has more queries than the call has rows.
     const int64_t nq = std::min<int64_t>(max_q, num_q);
     dim3 grid(static_cast<unsigned>((nq + 2 * a.Qb - 1) / (2 * a.Qb)), Hkv, B);
-    CUtensorMap qmap;
+    CUtensorMap qmap, omap;
     if (!encode_query_map(&qmap, q, num_q, Hq, a.g, a.Qb)) return cudaErrorInvalidValue;
+    // bf16 output has q's shape, so the same box describes the output tiles.
+    if (out_bf16) {
+        if (!encode_query_map(&omap, out, num_q, Hq, a.g, a.Qb)) return cudaErrorInvalidValue;
+    } else {
+        omap = qmap;  // not used: float output is written by the threads
+    }
     auto kern = block_size == 16 ? prefill_kernel<16> : prefill_kernel<32>;
     cudaError_t e = cudaFuncSetAttribute(reinterpret_cast<const void*>(kern),
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kSmemBytes, stream>>>(kmap, vmap, qmap, a);
+    kern<<<grid, kThreads, kSmemBytes, stream>>>(kmap, vmap, qmap, omap, a);
     return cudaGetLastError();
 }
 

@@ -70,6 +70,33 @@ def test_prefill_matches_oracle(Hq, Hkv, bs, lens, ns):
     assert e <= BF16_TOL, f"max abs error {e:.3e}"
 
 
+@pytest.mark.parametrize("lens,ns", [
+    ([200, 64, 1000], [37, 64, 130]),   # full and partial query tiles
+    ([300, 500], [64, 128]),            # full tiles only
+])
+def test_float_output_rounds_to_the_bf16_output(lens, ns):
+    # bf16 output of full tiles leaves through tiled tensor stores, float
+    # output and partial tiles through the threads' own stores; the same
+    # normalised values rounded to nearest even must agree bit for bit.
+    wl, q, qs = _case(lens, ns)
+    ds = DeviceStep(wl)
+    qd = to_dev(q, "bf16")
+    outs = {}
+    for dt in (torch.bfloat16, torch.float32):
+        out = torch.full((q.shape[0], wl.Hq, wl.D), float("nan"), dtype=dt, device="cuda")
+        err = torch.zeros(1, dtype=torch.int32, device="cuda")
+        pa.pa_prefill(qd, torch.from_numpy(qs).cuda(), ds.k_pool, ds.v_pool, ds.tables, ds.seq_lens,
+                      wl.scale, out, max(ns), wl.max_seq_len, device_error=err)
+        torch.cuda.synchronize()
+        assert int(err.item()) == 0
+        outs[dt] = out
+    f32 = outs[torch.float32]
+    assert torch.isfinite(f32).all()
+    assert torch.equal(f32.to(torch.bfloat16).view(torch.int16), outs[torch.bfloat16].view(torch.int16))
+    ref = oracle.prefill(q, wl.k_pool, wl.v_pool, wl.block_tables, wl.seq_lens, qs, wl.scale)
+    assert np.abs(f32.double().cpu().numpy() - ref).max() <= BF16_TOL
+
+
 def test_single_query_prefill_matches_decode():
     wl, q, qs = _case([77, 300, 16], [1, 1, 1])
     got, err = _run(wl, q, qs, [1, 1, 1])
