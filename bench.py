@@ -55,6 +55,7 @@ def CONFIGS_NEW_TOKENS(name):
 
 
 FALLBACK_BF16_TFLOPS = 1900.0
+LATENCY_GRAPH_STEPS = 20  # steps per CUDA graph in the latency row
 
 
 def measured_peak_tflops():
@@ -839,8 +840,9 @@ def run_latency(args, local_rank) -> None:
         sl = torch.from_numpy(wl.seq_lens).to(dev)
         cl = torch.from_numpy(wl.cache_lens).to(dev)
         out = torch.empty(wl.B, wl.Hq, wl.D, dtype=torch.bfloat16, device=dev)
-        stream = torch.cuda.current_stream()
-        with pa.Plan() as plan:
+        torch.cuda.synchronize()
+        stream = torch.cuda.Stream(device=dev)  # graphs are captured on a stream of their own
+        with torch.cuda.stream(stream), pa.Plan() as plan:
             def step():
                 if args.step == "fused":
                     pa.pa_append_decode(q, kn, vn, kp, vp, bt, sl, wl.scale, out, L, plan, stream)
@@ -857,11 +859,30 @@ def run_latency(args, local_rank) -> None:
             e1.record(stream)
             torch.cuda.synchronize()
             us = e0.elapsed_time(e1) * 1e3 / args.steps
+            # The same steps replayed from a CUDA graph: the device's own step
+            # time, without the host's per-call cost (which bounds a loop of
+            # eager calls from Python at short lengths).
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=stream):
+                for _ in range(LATENCY_GRAPH_STEPS):
+                    step()
+            reps = max(1, args.steps // LATENCY_GRAPH_STEPS)
+            for _ in range(3):
+                graph.replay()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            for _ in range(reps):
+                graph.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            us_graph = e0.elapsed_time(e1) * 1e3 / (reps * LATENCY_GRAPH_STEPS)
+            del graph
             assert pa.pa_last_device_error(plan) == 0
         eb = wl.elem_bytes
         nbytes = pa.decode_bytes(wl.seq_lens, wl.Hq, wl.Hkv, wl.D, wl.block_size, eb, eb) + \
             pa.append_bytes(wl.B, wl.Hkv, wl.D, eb)
-        rows.append({"seq_len": L, "us_per_step": round(us, 2), "gbs": round(nbytes / us / 1e3, 1)})
+        rows.append({"seq_len": L, "us_per_step": round(us, 2), "us_per_step_graph": round(us_graph, 2),
+                     "gbs": round(nbytes / us / 1e3, 1), "gbs_graph": round(nbytes / us_graph / 1e3, 1)})
         del kp, vp
         torch.cuda.empty_cache()
     by = {r["seq_len"]: r["us_per_step"] for r in rows}
@@ -872,8 +893,11 @@ def run_latency(args, local_rank) -> None:
                    "block_size": wl.block_size, "step": STEPS[args.step]},
         "steps": args.steps, "warmup": args.warmup, "lengths": rows,
         "growth_128_to_2048": round(by[2048] / by[128], 3),
-        "gpu_launches": (2 if args.step == "fused" else 3) * (args.steps + args.warmup) * len(lengths),
-        "timing": "CUDA events around `steps` back-to-back steps per length",
+        "value_graph": {r["seq_len"]: r["us_per_step_graph"] for r in rows}[2048],
+        "gpu_launches": (2 if args.step == "fused" else 3) * len(lengths) * (
+            args.steps + args.warmup + (3 + max(1, args.steps // LATENCY_GRAPH_STEPS)) * LATENCY_GRAPH_STEPS),
+        "timing": "CUDA events around `steps` back-to-back eager steps per length (us_per_step), "
+                  "and around replays of a CUDA graph of %d steps (us_per_step_graph)" % LATENCY_GRAPH_STEPS,
     }))
 
 
