@@ -24,7 +24,7 @@ constexpr int kDefaultStages = 1;          // pipeline stages per warp
 constexpr int kDynPermille = 150;          // share of the page stream scheduled dynamically
 constexpr int kDynMinPages = 1024;         // ... when a sequence may have this many pages
 constexpr int kDynPiecePages = 16;         // ... in pieces of this many pages
-constexpr int kDynShortPermille = 500;     // ... on the one-head path with shorter sequences
+constexpr int kDynShortPermille = 250;     // ... on the one-head path with shorter sequences
 constexpr int kMergeRowsPerSm = 16;        // rows one SM merges at once with 4 warps per row
 constexpr int kMinPagesPerWarp = 4;
 constexpr int kHeadSlice = 16;             // query heads per kv unit on the tensor-core path
@@ -207,11 +207,13 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t 
     //    long sequences ran 2-5 % faster with it (DRAM-saturating kernels
     //    finish unevenly without it). 16 pages beat 8 and 32 on both the GQA
     //    batch (block size 16) and the 128k-token one (block size 32).
-    //  * one query head per kv unit with shorter sequences: half the stream
-    //    in 64-token pieces (one-head partials stay cheap), while the merge of
-    //    all rows fits in one wave; Llama-7B MHA (1024 rows) step 102.0 vs
-    //    104.8 us. Wider partials with shorter sequences gain nothing (mixed
-    //    shared prefix, 4 heads: 142 vs 141 us split, and a slower merge).
+    //  * one query head per kv unit with shorter sequences: a quarter of the
+    //    stream in 64-token pieces (one-head partials stay cheap), while the
+    //    merge of all rows fits in one wave; Llama-7B MHA (1024 rows) step
+    //    97.4-97.5 us against 98.4-98.5 with half and 101.8 with none (same
+    //    box; 15 % and 35 % 97.7-97.9). Wider partials with shorter sequences
+    //    gain nothing (mixed shared prefix, 4 heads: 142 vs 141 us split, and
+    //    a slower merge).
     //  * tiles of two n-tiles (9-16 columns), several queries per sequence
     //    included: none. Those kernels (ten warps per SM, DRAM about 84 %)
     //    finish evenly without it, and it only adds partials: four queries
