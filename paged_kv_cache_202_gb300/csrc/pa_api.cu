@@ -238,6 +238,20 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t 
     }
     const int64_t max_pieces = s.P_max * gr.dyn_permille / 1000 / gr.dyn_pages + 1;
     gr.ranges = static_cast<int64_t>(gr.NW) + max_pieces;
+    // Warps per output row in the merge kernel, from the partials per kv unit
+    // (static ranges + dynamic pieces, on average). Eight when the kv units
+    // have ~16 partials or more and eight warps per row still fit in one wave
+    // (at most 8 rows per SM), so that a warp folds its share in one batch of
+    // loads instead of several in turn; four with a dynamic tail or ~8
+    // partials or more (the Llama-3-8B GQA step measured 4 against 2 and 8);
+    // one otherwise. Against one warp per row without a tail, decode device
+    // time (graph replay, us): one GQA sequence of 2,048 / 8,192 tokens 9.8 /
+    // 12.9 vs 15.4 / 32.7, 8 sequences 17.2 / 49.4 vs 22.4 / 56.1, 16
+    // sequences 31.8 / 89.0 vs 34.5 / 92.5; 128k-token context 615.8 vs 621.0.
+    const int64_t units = static_cast<int64_t>(B) * s.U;
+    if (rows <= 8LL * num_sms && gr.ranges >= 16 * units) gr.merge_wpr = 8;
+    else if (gr.dyn_permille > 0 || gr.ranges >= 8 * units) gr.merge_wpr = 4;
+    else gr.merge_wpr = 1;
     gr.meta_bytes = round_up(static_cast<size_t>(kMetaHeader + B + 1) * 4u, 256);
     gr.ml_bytes = round_up(static_cast<size_t>(2) * gr.ranges * s.GS * 2 * 4u, 256);
     gr.acc_bytes = round_up(static_cast<size_t>(2) * gr.ranges * s.GS * D * 4u, 256);
@@ -562,7 +576,7 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
     plan->last_fused = L.fused;
     if (!L.fused) {
         pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, sh.GS, sh.nslices, sh.U, D,
-                        out_dtype == PA_BF16, gr.dyn_permille > 0, (q_start ? T : B) * Hq,
+                        out_dtype == PA_BF16, gr.merge_wpr, (q_start ? T : B) * Hq,
                         q_start};
         e = pa::launch_merge(m, stream);
     }

@@ -219,10 +219,9 @@ __global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
     const int rows = a.rows;
     if (rows == 0) return cudaSuccess;
-    // Four warps per row when dynamic pieces cut long segments into many
-    // partials (measured against 2 and 8 on the Llama-3-8B GQA step); one warp
-    // per row otherwise.
-    const int wpr = a.wide ? 4 : 1;
+    // The plan chooses the warps per row from the partials per row.
+    const int wpr = a.wpr;
+    if (wpr != 1 && wpr != 2 && wpr != 4 && wpr != 8) return cudaErrorInvalidValue;
     const int rows_per_block = 8 / wpr;
     void (*fn)(MergeArgs) = nullptr;
     if (a.D == 128) {

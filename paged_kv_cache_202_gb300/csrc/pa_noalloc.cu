@@ -212,6 +212,6 @@ extern "C" pa_status pa_decode_noalloc(const void* q, const void* k_pool, const 
     a.probe_wait = pa::wait_probe();
     if (pa::launch_split(L, kmap, vmap, a, stream) != cudaSuccess) return PA_ERR_CUDA;
     pa::MergeArgs m{meta, acc, ml, out, B, Hq, g, sh.GS, sh.nslices, sh.U, D,
-                    out_dtype == PA_BF16, gr.dyn_permille > 0, B * Hq, nullptr};
+                    out_dtype == PA_BF16, gr.merge_wpr, B * Hq, nullptr};
     return pa::launch_merge(m, stream) == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
