@@ -25,6 +25,9 @@ constexpr int kDynPermille = 150;          // share of the page stream scheduled
 constexpr int kDynMinPages = 1024;         // ... when a sequence may have this many pages
 constexpr int kDynPiecePages = 16;         // ... in pieces of this many pages
 constexpr int kDynShortPermille = 250;     // ... on the one-head path with shorter sequences
+constexpr int kDynMidPages = 256;          // multi-head units, sequences of 256 .. 1023 pages:
+constexpr int kDynMidPiecePages = 8;       // ... the same share in pieces of this many pages
+constexpr int kDynMidMaxRows = 2048;       // ... while the merge has at most this many rows
 constexpr int kMergeRowsPerSm = 16;        // rows one SM merges at once with 4 warps per row
 constexpr int kMinPagesPerWarp = 4;
 constexpr int kHeadSlice = 16;             // query heads per kv unit on the tensor-core path
@@ -207,6 +210,14 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t 
     //    long sequences ran 2-5 % faster with it (DRAM-saturating kernels
     //    finish unevenly without it). 16 pages beat 8 and 32 on both the GQA
     //    batch (block size 16) and the 128k-token one (block size 32).
+    //  * several query heads per kv unit, sequences of 256 .. 1023 pages, at
+    //    most 2048 merge rows: 15 % in 8-page pieces (the kernel still drops
+    //    the tail when the batch has fewer than 8 pieces per warp). Uniform
+    //    GQA batches, decode device time (graph replay, us): 32 x 8192 tokens
+    //    159.7-159.9 vs 166.3-167.0 without, 64 x 4096 159.3-159.4 vs
+    //    163.3-163.5, 32 x 4096 87.4-87.8 vs 90.0 (with the merge widths
+    //    below), 8-16 sequences 0.6-2 % faster. The mixed shared-prefix batch
+    //    (8192 rows) stays without a tail.
     //  * one query head per kv unit with shorter sequences: a quarter of the
     //    stream in 64-token pieces (one-head partials stay cheap), while the
     //    merge of all rows fits in one wave; Llama-7B MHA (1024 rows) step
@@ -227,6 +238,9 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t 
     if (dynamic && !s.mq && s.NT <= 1) {
         if (s.max_pages >= kDynMinPages) {
             gr.dyn_permille = kDynPermille;
+        } else if (s.GS > 1 && s.max_pages >= kDynMidPages && rows <= kDynMidMaxRows) {
+            gr.dyn_permille = kDynPermille;
+            gr.dyn_pages = kDynMidPiecePages;
         } else if (s.GS == 1 && merge_fits) {
             gr.dyn_permille = kDynShortPermille;
             gr.dyn_pages = 64 / block_size;
@@ -242,7 +256,7 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t 
     // (static ranges + dynamic pieces, on average). Eight when the kv units
     // have ~16 partials or more and eight warps per row still fit in one wave
     // (at most 8 rows per SM), so that a warp folds its share in one batch of
-    // loads instead of several in turn; four with a dynamic tail or ~8
+    // loads instead of several in turn; four with a dynamic tail or ~4
     // partials or more (the Llama-3-8B GQA step measured 4 against 2 and 8);
     // one otherwise. Against one warp per row without a tail, decode device
     // time (graph replay, us): one GQA sequence of 2,048 / 8,192 tokens 9.8 /
@@ -250,7 +264,7 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t 
     // sequences 31.8 / 89.0 vs 34.5 / 92.5; 128k-token context 615.8 vs 621.0.
     const int64_t units = static_cast<int64_t>(B) * s.U;
     if (rows <= 8LL * num_sms && gr.ranges >= 16 * units) gr.merge_wpr = 8;
-    else if (gr.dyn_permille > 0 || gr.ranges >= 8 * units) gr.merge_wpr = 4;
+    else if (gr.dyn_permille > 0 || gr.ranges >= 4 * units) gr.merge_wpr = 4;
     else gr.merge_wpr = 1;
     gr.meta_bytes = round_up(static_cast<size_t>(kMetaHeader + B + 1) * 4u, 256);
     gr.ml_bytes = round_up(static_cast<size_t>(2) * gr.ranges * s.GS * 2 * 4u, 256);
