@@ -326,6 +326,53 @@ def configure_plan(plan, args):
 TIMED_SPAN_S = 2.0
 
 
+# The other configurations, measured by the default run as well: each is
+# this script run in a child process with its own flags (so that a failure
+# there cannot touch the headline line), summarised under "extras".
+EXTRA_RUNS = [
+    ["--workload", "llama7b_mha", "--steps", "100", "--warmup", "10"],
+    ["--workload", "mixed_shared", "--steps", "100", "--warmup", "10"],
+    ["--workload", "long_splitk", "--steps", "20", "--warmup", "3"],
+    ["--workload", "llama3_405b_gqa", "--steps", "50", "--warmup", "5"],
+    ["--row", "spec", "--steps", "50", "--warmup", "5"],
+    ["--row", "prefill", "--steps", "40", "--warmup", "5"],
+]
+EXTRA_TIMEOUT_S = 300
+
+
+def run_extras() -> list:
+    out = []
+    for extra in EXTRA_RUNS:
+        cmd = [sys.executable, os.path.join(ROOT, "bench.py"), *extra, "--span", "0.5",
+               "--cpu-seconds", "2", "--no-extras"]
+        t0 = time.time()
+        entry = {"args": " ".join(extra)}
+        try:
+            r = subprocess.run(cmd, capture_output=True, text=True, timeout=EXTRA_TIMEOUT_S)
+            lines = [x for x in r.stdout.strip().splitlines() if x.startswith("{")]
+            if r.returncode != 0 or not lines:
+                entry["error"] = (r.stderr.strip().splitlines() or ["exit %d" % r.returncode])[-1][:300]
+            else:
+                d = json.loads(lines[-1])
+                roof = d.get("roofline") or {}
+                entry.update({
+                    "row": d.get("row", "decode"), "workload": d["config"].get("workload"),
+                    "metric": d.get("metric"), "value": d.get("value"), "unit": d.get("unit"),
+                    "ms_per_step": d.get("ms_per_step"),
+                    "kernel_ms": roof.get("ms_per_launch"), "frac": roof.get("frac"),
+                    "peak": roof.get("peak"), "e2e": (d.get("e2e") or {}).get("value"),
+                    "parity": d.get("parity"), "device_error": d.get("device_error"),
+                    "clocks": {k: (d.get("clocks") or {}).get(k) for k in ("sm_mhz", "reasons")},
+                })
+        except subprocess.TimeoutExpired:
+            entry["error"] = f"timed out after {EXTRA_TIMEOUT_S} s"
+        except Exception as e:  # a malformed line: recorded, never fatal to the headline
+            entry["error"] = repr(e)[:300]
+        entry["wall_s"] = round(time.time() - t0, 1)
+        out.append(entry)
+    return out
+
+
 def run_ours(args, rank, world, local_rank):
     import __graft_entry__
     import paged_kv_cache_202_gb300 as pa
@@ -575,6 +622,9 @@ def run_ours(args, rank, world, local_rank):
                        "blocks": blocks, "warps": warps, "merge": args.merge,
                        "schedule": args.schedule or "auto"},
         }
+        if world == 1 and not args.no_extras and args.layout == "paged" and args.step == "separate" \
+                and args.workload == "llama3_8b_gqa" and args.merge == "auto" and args.schedule is None:
+            line["extras"] = run_extras()
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -963,6 +1013,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-parity", action="store_true")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the other configurations the default run also measures")
     ap.add_argument("--span", type=float, default=TIMED_SPAN_S,
                     help="seconds the timed region spans at least (0: exactly K steps, "
                          "e.g. under a profiler)")
