@@ -389,7 +389,9 @@ def run_ours(args, rank, world, local_rank):
         if world > 1:
             torch.distributed.barrier()
 
-    wl = make_workload(args.workload, seed=args.seed + rank if args.seed is not None else None)
+    overrides = {"B": args.sequences} if args.sequences else {}
+    wl = make_workload(args.workload, seed=args.seed + rank if args.seed is not None else None,
+                       **overrides)
     if args.layout == "contiguous":
         wl = contiguous_layout(wl)
     bf = wl.dtype == "bf16"
@@ -623,7 +625,8 @@ def run_ours(args, rank, world, local_rank):
                        "schedule": args.schedule or "auto"},
         }
         if world == 1 and not args.no_extras and args.layout == "paged" and args.step == "separate" \
-                and args.workload == "llama3_8b_gqa" and args.merge == "auto" and args.schedule is None:
+                and args.workload == "llama3_8b_gqa" and args.merge == "auto" and args.schedule is None \
+                and args.sequences is None:
             line["extras"] = run_extras()
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -1034,6 +1037,9 @@ def main():
                              "read_ceiling", "latency"])
     ap.add_argument("--batch", type=int, default=1,
                     help="latency row: sequences per step (all of one length)")
+    ap.add_argument("--sequences", type=int, default=None,
+                    help="decode row: N sequences drawn by the workload's recipe (a smaller "
+                         "case of the same workload, e.g. for a multi-pass profiler capture)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
