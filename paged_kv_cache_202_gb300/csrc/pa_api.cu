@@ -262,8 +262,13 @@ SplitGrid split_grid(const SplitShape& s, int B, int D, int block_size, int64_t 
     // time (graph replay, us): one GQA sequence of 2,048 / 8,192 tokens 9.8 /
     // 12.9 vs 15.4 / 32.7, 8 sequences 17.2 / 49.4 vs 22.4 / 56.1, 16
     // sequences 31.8 / 89.0 vs 34.5 / 92.5; 128k-token context 615.8 vs 621.0.
+    // Rows of 64 or 128 partials or more (one or two very long sequences)
+    // take 16 or 32 warps while the rows still fit one wave at 64 warps per
+    // SM.
     const int64_t units = static_cast<int64_t>(B) * s.U;
-    if (rows <= 8LL * num_sms && gr.ranges >= 16 * units) gr.merge_wpr = 8;
+    if (rows * 32 <= 64LL * num_sms && gr.ranges >= 128 * units) gr.merge_wpr = 32;
+    else if (rows * 16 <= 64LL * num_sms && gr.ranges >= 64 * units) gr.merge_wpr = 16;
+    else if (rows <= 8LL * num_sms && gr.ranges >= 16 * units) gr.merge_wpr = 8;
     else if (gr.dyn_permille > 0 || gr.ranges >= 4 * units) gr.merge_wpr = 4;
     else gr.merge_wpr = 1;
     gr.meta_bytes = round_up(static_cast<size_t>(kMetaHeader + B + 1) * 4u, 256);

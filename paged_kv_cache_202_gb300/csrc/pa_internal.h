@@ -137,7 +137,7 @@ struct SplitGrid {
     int blocks = 0, NW = 0;        // grid size, warps in the grid
     int dyn_permille = 0, dyn_pages = 0;
     int64_t ranges = 0;            // partial records: static ranges + dynamic pieces
-    int merge_wpr = 1;             // warps per output row in the merge kernel (1, 4 or 8)
+    int merge_wpr = 1;             // warps per output row in the merge kernel (1 .. 32)
     size_t meta_bytes = 0, ml_bytes = 0, acc_bytes = 0;
     size_t cnt_bytes = 0;          // segment counters of the fused merge (0 without it)
     size_t workspace_bytes() const { return meta_bytes + ml_bytes + acc_bytes + cnt_bytes; }
@@ -165,7 +165,7 @@ struct MergeArgs {
     void* out;
     int B, Hq, g, GS, nslices, U, D;
     int out_bf16;
-    int wpr;   // warps per output row: 1, 2, 4 or 8 (more for more partials per row)
+    int wpr;   // warps per output row: 1, 2, 4, 8, 16 or 32 (more for more partials per row)
     int rows;  // output rows: B * Hq, or T * Hq with several queries per sequence
     const int32_t* q_start;  // several queries per sequence (see SplitArgs), else null
 };

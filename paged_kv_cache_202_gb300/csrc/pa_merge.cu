@@ -14,8 +14,8 @@
 namespace pa {
 namespace {
 
-// WPR warps per (sequence, query head) row, 8 / WPR rows per block of 8
-// warps. Warp w of a row folds partials rf + w, rf + w + WPR, ... in batches
+// WPR warps per (sequence, query head) row; a block has max(8, WPR) warps
+// and max(8, WPR) / WPR rows. Warp w of a row folds partials rf + w, rf + w + WPR, ... in batches
 // of kBatch: the loads of a whole batch are issued before any is used, then
 // the batch is folded into the warp's running (m, l, acc) with one rescale.
 // The warps of a row then combine their results through shared memory, on a
@@ -26,13 +26,14 @@ namespace {
 // Batches of 4 keep the kernel at 55 registers, four blocks per SM (8 took 73
 // registers and three blocks; the Llama-3-8B GQA step was 1 us longer).
 template <int D, int WPR>
-__global__ void __launch_bounds__(256) merge_kernel(const MergeArgs a) {
+__global__ void __launch_bounds__(32 * (WPR > 8 ? WPR : 8)) merge_kernel(const MergeArgs a) {
     constexpr int DPL = D / 32;
     constexpr int kBatch = 4;
-    constexpr int kRowsPerBlock = 8 / WPR;
-    __shared__ float sm_m[8], sm_l[8];
-    __shared__ int sm_poison[8];
-    __shared__ float sm_acc[WPR > 1 ? 8 : 1][D];
+    constexpr int kWarps = WPR > 8 ? WPR : 8;
+    constexpr int kRowsPerBlock = kWarps / WPR;
+    __shared__ float sm_m[kWarps], sm_l[kWarps];
+    __shared__ int sm_poison[kWarps];
+    __shared__ float sm_acc[WPR > 1 ? kWarps : 1][D];
     const int lane = threadIdx.x & 31;
     const int gwarp = threadIdx.x >> 5;
     const int warp = gwarp % WPR;            // warp within the row
@@ -221,20 +222,24 @@ cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
     if (rows == 0) return cudaSuccess;
     // The plan chooses the warps per row from the partials per row.
     const int wpr = a.wpr;
-    if (wpr != 1 && wpr != 2 && wpr != 4 && wpr != 8) return cudaErrorInvalidValue;
-    const int rows_per_block = 8 / wpr;
+    if (wpr != 1 && wpr != 2 && wpr != 4 && wpr != 8 && wpr != 16 && wpr != 32)
+        return cudaErrorInvalidValue;
+    const int warps = wpr > 8 ? wpr : 8;
+    const int rows_per_block = warps / wpr;
     void (*fn)(MergeArgs) = nullptr;
     if (a.D == 128) {
         fn = wpr == 1 ? merge_kernel<128, 1> : wpr == 2 ? merge_kernel<128, 2>
-           : wpr == 4 ? merge_kernel<128, 4> : merge_kernel<128, 8>;
+           : wpr == 4 ? merge_kernel<128, 4> : wpr == 8 ? merge_kernel<128, 8>
+           : wpr == 16 ? merge_kernel<128, 16> : merge_kernel<128, 32>;
     } else if (a.D == 64) {
         fn = wpr == 1 ? merge_kernel<64, 1> : wpr == 2 ? merge_kernel<64, 2>
-           : wpr == 4 ? merge_kernel<64, 4> : merge_kernel<64, 8>;
+           : wpr == 4 ? merge_kernel<64, 4> : wpr == 8 ? merge_kernel<64, 8>
+           : wpr == 16 ? merge_kernel<64, 16> : merge_kernel<64, 32>;
     }
     if (!fn) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((rows + rows_per_block - 1) / rows_per_block);
-    cfg.blockDim = dim3(256);
+    cfg.blockDim = dim3(32 * warps);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
