@@ -284,10 +284,13 @@ pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
  *
  * Supported: bf16 pools, D = 128, block_size 16 or 32, Hq / Hkv dividing 128,
  * max_blocks <= 16384, B and Hkv at most 65535 (PA_ERR_SHAPE otherwise).
- * The launch is sized by min(max_q, num_queries). Built for many queries per
- * sequence (chunked prefill);
- * with a few (max_q * Hq / Hkv <= 16, e.g. speculative verification)
- * pa_decode_multi computes the same rows at the decode's bandwidth. n_b < 1, n_b > L_b,
+ * The launch is sized by min(max_q, num_queries). A query tile holds 128 /
+ * (Hq / Hkv) queries of one sequence; when every sequence fits one tile the
+ * call runs a one-tile kernel that overlaps a tile's softmax with its own
+ * next score products, otherwise a kernel that alternates two tiles per
+ * block. With a few queries (max_q * Hq / Hkv <= 16, e.g. speculative
+ * verification) pa_decode_multi computes the same rows at the decode's
+ * bandwidth. n_b < 1, n_b > L_b,
  * L_b out of range or rows outside [0, num_queries) raise PA_DEVERR_SEQ_LEN
  * and leave that sequence's rows untouched; a table entry outside the pool
  * raises PA_DEVERR_TABLE and zeroes the affected rows.
@@ -319,7 +322,7 @@ pa_status pa_prefill(const void* q, const int32_t* q_start, int num_queries, con
  *
  * The call picks the kernel from the shape: with max_q * (Hq / Hkv) <= 16
  * (query, head) columns per kv head it runs the split decode's tiles above;
- * with more it runs pa_prefill's tcgen05 kernel on the same arguments
+ * with more it runs pa_prefill's tcgen05 kernels on the same arguments
  * (pa_plan_info then reports PA_PATH_PREFILL), whose 128-row query tiles
  * need D = 128, Hq / Hkv dividing 128, max_blocks <= 16384 and Hkv <= 65535
  * (PA_ERR_SHAPE otherwise); its device errors then go to the plan's error

@@ -215,10 +215,19 @@ cudaError_t append_error_address(int** p);
 // 64-column half of a query tile (Qb queries x g heads, 128-byte swizzle).
 bool encode_query_map(CUtensorMap* map, const void* q, int T, int Hq, int g, int Qb);
 
+// Causal paged multi-query attention on the tensor cores. Calls whose
+// sequences all fit one query tile (min(max_q, num_q) <= 128 / g) run the
+// one-tile kernel (pa_prefill_1t.cu), the others the two-tile kernel.
 cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, const void* q,
                            int num_q, const int32_t* q_start, const int32_t* tables,
                            const int32_t* seq_lens, void* out, int* err, int B, int Hq, int Hkv,
                            int max_blocks, int num_blocks, int max_seq_len, int max_q,
                            float scale_log2, int out_bf16, int block_size, cudaStream_t stream);
+cudaError_t launch_prefill_one_tile(const CUtensorMap& kmap, const CUtensorMap& vmap, const void* q,
+                                    int num_q, const int32_t* q_start, const int32_t* tables,
+                                    const int32_t* seq_lens, void* out, int* err, int B, int Hq,
+                                    int Hkv, int max_blocks, int num_blocks, int max_seq_len,
+                                    int max_q, float scale_log2, int out_bf16, int block_size,
+                                    cudaStream_t stream);
 
 }  // namespace pa

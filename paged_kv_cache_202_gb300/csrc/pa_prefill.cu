@@ -630,6 +630,13 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
                            const int32_t* seq_lens, void* out, int* err, int B, int Hq, int Hkv,
                            int max_blocks, int num_blocks, int max_seq_len, int max_q,
                            float scale_log2, int out_bf16, int block_size, cudaStream_t stream) {
+    // Every sequence fits one query tile: this kernel's second tile would be
+    // empty, and the one-tile kernel overlaps a tile's softmax with its own
+    // next score products instead.
+    if (std::min<int64_t>(max_q, num_q) <= kRows / (Hq / Hkv))
+        return launch_prefill_one_tile(kmap, vmap, q, num_q, q_start, tables, seq_lens, out, err, B,
+                                       Hq, Hkv, max_blocks, num_blocks, max_seq_len, max_q,
+                                       scale_log2, out_bf16, block_size, stream);
     PrefillArgs a{};
     a.q = static_cast<const uint16_t*>(q);
     a.q_start = q_start;
