@@ -285,10 +285,11 @@ pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
  * Supported: bf16 pools, D = 128, block_size 16 or 32, Hq / Hkv dividing 128,
  * max_blocks <= 16384, B and Hkv at most 65535 (PA_ERR_SHAPE otherwise).
  * The launch is sized by min(max_q, num_queries). A query tile holds 128 /
- * (Hq / Hkv) queries of one sequence; when every sequence fits one tile the
- * call runs a one-tile kernel that overlaps a tile's softmax with its own
- * next score products, otherwise a kernel that alternates two tiles per
- * block. With a few queries (max_q * Hq / Hkv <= 16, e.g. speculative
+ * (Hq / Hkv) queries of one sequence. When every sequence fits one tile, or
+ * the call has at most three waves of tiles (tiles x Hkv x B <= 3 x SMs),
+ * it runs a one-tile kernel that overlaps a tile's softmax with its own
+ * next score products; otherwise a kernel that alternates two tiles per
+ * block (half the K/V intake per row). With a few queries (max_q * Hq / Hkv <= 16, e.g. speculative
  * verification) pa_decode_multi computes the same rows at the decode's
  * bandwidth. n_b < 1, n_b > L_b,
  * L_b out of range or rows outside [0, num_queries) raise PA_DEVERR_SEQ_LEN

@@ -630,13 +630,29 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
                            const int32_t* seq_lens, void* out, int* err, int B, int Hq, int Hkv,
                            int max_blocks, int num_blocks, int max_seq_len, int max_q,
                            float scale_log2, int out_bf16, int block_size, cudaStream_t stream) {
-    // Every sequence fits one query tile: this kernel's second tile would be
-    // empty, and the one-tile kernel overlaps a tile's softmax with its own
-    // next score products instead.
-    if (std::min<int64_t>(max_q, num_q) <= kRows / (Hq / Hkv))
-        return launch_prefill_one_tile(kmap, vmap, q, num_q, q_start, tables, seq_lens, out, err, B,
-                                       Hq, Hkv, max_blocks, num_blocks, max_seq_len, max_q,
-                                       scale_log2, out_bf16, block_size, stream);
+    // The one-tile kernel overlaps a tile's softmax with its own next score
+    // products (~2,100 cycles per 128-token chunk and tile); this kernel
+    // alternates two tiles (~3,100 cycles per chunk for both), which halves
+    // the K/V bytes each SM takes in per row. The one-tile kernel runs when
+    // every sequence fits one tile (this kernel's second tile would be
+    // empty) or when its grid is at most three waves of blocks, where a
+    // block's chunk time, not the SMs' intake, sets the call's time. Prefill
+    // workload (16 sequences), us: 33 / 48 / 64 / 96 queries per sequence
+    // 117 / 116 / 106 / 131 against 197 / 192 / 150 / 148; 128 queries (four
+    // waves) 170 against 150 on this kernel, which then stays.
+    {
+        const int64_t nq = std::min<int64_t>(max_q, num_q);
+        const int qb = kRows / (Hq / Hkv);
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return cudaErrorInvalidValue;
+        const int64_t blocks1 = (nq + qb - 1) / qb * static_cast<int64_t>(Hkv) * B;
+        if (nq <= qb || blocks1 <= 3LL * sms)
+            return launch_prefill_one_tile(kmap, vmap, q, num_q, q_start, tables, seq_lens, out, err,
+                                           B, Hq, Hkv, max_blocks, num_blocks, max_seq_len, max_q,
+                                           scale_log2, out_bf16, block_size, stream);
+    }
     PrefillArgs a{};
     a.q = static_cast<const uint16_t*>(q);
     a.q_start = q_start;
