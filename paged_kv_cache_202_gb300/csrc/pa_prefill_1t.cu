@@ -507,6 +507,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // O holds the products of chunks < c in units of 2^mprev: rescale
             // this row's half once PV(c - 1) is done (PV(c) waits for this P).
+            // The parity wait is unambiguous: the barrier of buffer (c-1) % 3
+            // last completed for PV(c - 4), which was done before S(c - 1)
+            // (issued after it) was, and this group has seen chunk c - 1's max.
             if (c > 0 && __any_sync(0xffffffffu, mc != mprev)) {
                 const int jp = (c - 1) % kSbuf;
                 ok = __all_sync(0xffffffffu, wait_role(bars + kBarPV + 8 * jp, ((c - 1) / kSbuf) & 1,
@@ -525,7 +528,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // Final chunk: zero the V rows past the last token before its
-            // value product.
+            // value product. The stage's previous chunk (c - 3) was consumed by
+            // PV(c - 3), issued before S(c), so this parity wait is unambiguous.
             if (c == nc - 1) {
                 const int valid = ntok - c * kChunk;
                 ok = __all_sync(0xffffffffu, wait_role(bars + kBarVFull + 8 * (c % kStagesV),
