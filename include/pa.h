@@ -324,7 +324,11 @@ pa_status pa_prefill(const void* q, const int32_t* q_start, int num_queries, con
  * The call picks the kernel from the shape: with max_q * (Hq / Hkv) <= 16
  * (query, head) columns per kv head it runs the split decode's tiles above;
  * with more it runs pa_prefill's tcgen05 kernels on the same arguments
- * (pa_plan_info then reports PA_PATH_PREFILL), whose 128-row query tiles
+ * (pa_plan_info then reports PA_PATH_PREFILL). On a small call (fewer
+ * one-tile blocks than SMs) the one-tile kernel then splits every tile's key
+ * range over several blocks, whose partials go to the plan's workspace
+ * (grown on demand, like the split decode's) and are merged by a second
+ * kernel. Those 128-row query tiles
  * need D = 128, Hq / Hkv dividing 128, max_blocks <= 16384 and Hkv <= 65535
  * (PA_ERR_SHAPE otherwise); its device errors then go to the plan's error
  * word.

@@ -435,11 +435,33 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
         if (!pa::encode_pool_map(&kmap, k_pool, num_blocks * Hkv, D, block_size) ||
             !pa::encode_pool_map(&vmap, v_pool, num_blocks * Hkv, D, block_size))
             return PA_ERR_CUDA;
+        // A small call (fewer one-tile blocks than SMs) splits every tile's
+        // key range over several blocks; their partials live in the plan's
+        // workspace after its first 64 bytes, which hold the split decode's
+        // counters (zero between calls, left untouched here).
+        const int64_t nqq = std::min<int64_t>(nq, T);
+        const int splits = pa::prefill_split_count(B, Hq, Hkv, nqq, max_seq_len, plan->num_sms);
+        float* part = nullptr;
+        if (splits > 1) {
+            const size_t need = 64 + pa::prefill_split_bytes(B, Hq, Hkv, nqq, splits);
+            if (plan->ws_bytes < need) {
+                if (plan->ws) cudaFree(plan->ws);
+                plan->ws = nullptr;
+                plan->ws_bytes = 0;
+                if (cudaMalloc(&plan->ws, need) != cudaSuccess) return PA_ERR_CUDA;
+                if (cudaMemset(plan->ws, 0, need) != cudaSuccess) return PA_ERR_CUDA;
+                plan->ws_bytes = need;
+                plan->cnt_clean = need;
+            }
+            part = reinterpret_cast<float*>(static_cast<char*>(plan->ws) + 64);
+            plan->cnt_clean = std::min(plan->cnt_clean, plan->ws_bytes - need);
+        }
         if (plan->ev_start) cudaEventRecord(plan->ev_start, stream);
         const cudaError_t e = pa::launch_prefill(kmap, vmap, q, T, q_start, block_tables, seq_lens,
                                                  out, plan->err, B, Hq, Hkv, max_blocks,
                                                  num_blocks, max_seq_len, nq, scale_log2,
-                                                 out_dtype == PA_BF16, block_size, stream);
+                                                 out_dtype == PA_BF16, block_size, stream, part,
+                                                 splits);
         if (plan->ev_stop) cudaEventRecord(plan->ev_stop, stream);
         plan->last_path = PA_PATH_PREFILL;
         plan->last_blocks = 0;

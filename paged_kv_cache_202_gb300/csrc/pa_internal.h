@@ -216,18 +216,26 @@ cudaError_t append_error_address(int** p);
 bool encode_query_map(CUtensorMap* map, const void* q, int T, int Hq, int g, int Qb);
 
 // Causal paged multi-query attention on the tensor cores. Calls whose
-// sequences all fit one query tile (min(max_q, num_q) <= 128 / g) run the
-// one-tile kernel (pa_prefill_1t.cu), the others the two-tile kernel.
+// sequences all fit one query tile, or with at most three waves of tiles,
+// run the one-tile kernel (pa_prefill_1t.cu), the others the two-tile
+// kernel. splits > 1 (one-tile kernel only) cuts every tile's key range into
+// that many blocks whose partials go to part (prefill_split_bytes) and are
+// merged by a second kernel.
 cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, const void* q,
                            int num_q, const int32_t* q_start, const int32_t* tables,
                            const int32_t* seq_lens, void* out, int* err, int B, int Hq, int Hkv,
                            int max_blocks, int num_blocks, int max_seq_len, int max_q,
-                           float scale_log2, int out_bf16, int block_size, cudaStream_t stream);
+                           float scale_log2, int out_bf16, int block_size, cudaStream_t stream,
+                           float* part = nullptr, int splits = 1);
 cudaError_t launch_prefill_one_tile(const CUtensorMap& kmap, const CUtensorMap& vmap, const void* q,
                                     int num_q, const int32_t* q_start, const int32_t* tables,
                                     const int32_t* seq_lens, void* out, int* err, int B, int Hq,
                                     int Hkv, int max_blocks, int num_blocks, int max_seq_len,
                                     int max_q, float scale_log2, int out_bf16, int block_size,
-                                    cudaStream_t stream);
+                                    cudaStream_t stream, float* part, int splits);
+// Key splits for a one-tile call (1: none) and the partial bytes they need;
+// nq = min(max_q, num_queries).
+int prefill_split_count(int B, int Hq, int Hkv, int64_t nq, int max_seq_len, int num_sms);
+size_t prefill_split_bytes(int B, int Hq, int Hkv, int64_t nq, int splits);
 
 }  // namespace pa

@@ -629,7 +629,8 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
                            int num_q, const int32_t* q_start, const int32_t* tables,
                            const int32_t* seq_lens, void* out, int* err, int B, int Hq, int Hkv,
                            int max_blocks, int num_blocks, int max_seq_len, int max_q,
-                           float scale_log2, int out_bf16, int block_size, cudaStream_t stream) {
+                           float scale_log2, int out_bf16, int block_size, cudaStream_t stream,
+                           float* part, int splits) {
     // The one-tile kernel overlaps a tile's softmax with its own next score
     // products (~2,100 cycles per 128-token chunk and tile); this kernel
     // alternates two tiles (~3,100 cycles per chunk for both), which halves
@@ -651,7 +652,8 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
         if (nq <= qb || blocks1 <= 3LL * sms)
             return launch_prefill_one_tile(kmap, vmap, q, num_q, q_start, tables, seq_lens, out, err,
                                            B, Hq, Hkv, max_blocks, num_blocks, max_seq_len, max_q,
-                                           scale_log2, out_bf16, block_size, stream);
+                                           scale_log2, out_bf16, block_size, stream, part,
+                                           splits);
     }
     PrefillArgs a{};
     a.q = static_cast<const uint16_t*>(q);

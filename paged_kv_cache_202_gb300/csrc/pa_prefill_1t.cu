@@ -123,6 +123,14 @@ struct PrefillArgs {
     float scale_log2;
     int out_bf16;
     int probe_wait;           // 1: the MMA thread's first wait expires (a test hook)
+    // Key split: grid.x = tiles x splits, block x takes split x % splits of
+    // tile x / splits. With splits > 1 every block writes a partial instead
+    // of output rows: O unnormalised [num_parts][kRows][kD] at part, then
+    // (reference max, row sum) [num_parts][kRows][2]; the merge kernel below
+    // combines them.
+    int splits, tiles;
+    int num_parts;            // B * Hkv * tiles * splits
+    float* part;
 };
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
@@ -211,13 +219,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (blockIdx.x == 0 && h == 0 && tid == 0) atomicOr(a.err, kErrSeqLen);
         return;  // rows of an invalid sequence are left untouched
     }
-    const int q0 = blockIdx.x * a.Qb;
+    const int split = blockIdx.x % a.splits, tile = blockIdx.x / a.splits;
+    const int q0 = tile * a.Qb;
     if (q0 >= n) return;
     const int nq = min(a.Qb, n - q0);
     const int ntok = L - n + q0 + nq;  // tokens the tile's last row sees
     const int nc = (ntok + kChunk - 1) / kChunk;
     const int nb = (ntok + BS - 1) / BS;
     const int32_t* table = a.tables + static_cast<size_t>(b) * a.max_blocks;
+    // This block's chunks: c_beg .. c_beg + nk - 1, its split of the key range.
+    // Pipeline stages, score buffers, barrier phases and the softmax groups
+    // count k = c - c_beg; pages and the causal mask use the chunk index c.
+    const int per = (nc + a.splits - 1) / a.splits;
+    const int c_beg = min(nc, split * per);
+    const int nk = min(nc, c_beg + per) - c_beg;
+    const bool partial = a.splits > 1;
+    const size_t pidx = ((static_cast<size_t>(b) * a.Hkv + h) * a.tiles + tile) * a.splits + split;
+    float* part_o = partial ? a.part + pidx * kRows * kD : nullptr;
+    float* part_ml = partial ? a.part + static_cast<size_t>(a.num_parts) * kRows * kD + pidx * kRows * 2
+                             : nullptr;
+    if (nk == 0) {  // a split past a short sequence's end: an empty partial
+        if (tid < kRows) {
+            part_ml[2 * tid] = -INFINITY;
+            part_ml[2 * tid + 1] = 0.f;
+        }
+        return;
+    }
 
     // This thread's query row (softmax warps): group G (warps 0-7 take the
     // even chunks, warps 8-15 the odd ones), row r of the tile, and which
@@ -269,6 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             float z[kD / 2] = {};
             write_row<kD / 2>(a, out_row, z, 0.f, 64 * half);
         }
+        if (partial && tid < kRows) part_ml[2 * tid] = NAN;  // the merge writes zeros too
         return;
     }
     // The copy warps go straight to work. The softmax warps and the MMA warp
@@ -319,11 +347,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     pg[j] = p < nb ? table[p] : 0;
                 }
             };
-            load_pages(0);
+            load_pages(c_beg);
             int issued = 0;
-            for (int c = 0; c < nc; ++c) {
-                const int s = c % nst;
-                if (c >= nst && !wait_role(empty + 8 * s, ((c / nst) - 1) & 1, abort_flag, a.err)) break;
+            for (int k = 0; k < nk; ++k) {
+                const int c = c_beg + k;
+                const int s = k % nst;
+                if (k >= nst && !wait_role(empty + 8 * s, ((k / nst) - 1) & 1, abort_flag, a.err)) break;
                 // One chunk (its pages, both 64-column halves) into the stage.
                 const int np = min(kPages, nb - c * kPages);
                 const uint32_t bar = full + 8 * s, stage = ring + s * kStageKV;
@@ -337,15 +366,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             tma_load_3d(stage + hf * kHalfKV + j * BS * 128, map, hf * 64, 0, r, bar, policy);
                     }
                 }
-                issued = c + 1;
+                issued = k + 1;
                 load_pages(c + 1);
             }
             // Copies still in flight land before the block leaves: the last
             // chunk issued on each stage (its phase is then final; earlier
             // chunks of a stage were consumed before it was reissued). Without
             // an abort the consumers have waited for them already.
-            for (int c = max(0, issued - nst); c < issued; ++c)
-                mbar_wait_bounded(full + 8 * (c % nst), (c / nst) & 1, kWaitLimitNs);
+            for (int k = max(0, issued - nst); k < issued; ++k)
+                mbar_wait_bounded(full + 8 * (k % nst), (k / nst) & 1, kWaitLimitNs);
             if (is_k) mbar_wait_bounded(bars + kBarQ, 0, kWaitLimitNs);  // the query tile too
         }
         __syncwarp();
@@ -358,6 +387,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t lo_q = tc::desc_lo(base + kOffQ, 16);
             const uint32_t lo_k = tc::desc_lo(base + kOffK, 16);
             const uint32_t lo_v = tc::desc_lo(base + kOffV, kHalfKV);
+            // (The MMA thread counts the block's own chunks, 0 .. nk - 1.)
             // S(c) = Q K(c)^T into score buffer c % kSbuf; its completion frees
             // the K stage.
             auto issue_s = [&](int c) {
@@ -396,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = wait_role(bars + kBarQ, 0, abort_flag, a.err);
             }
             // The first score products, as their K chunks land.
-            for (int c = 0; c < min(kSbuf, nc) && ok; ++c) {
+            for (int c = 0; c < min(kSbuf, nk) && ok; ++c) {
                 ok = wait_role(bars + kBarKFull + 8 * (c % kStagesK), (c / kStagesK) & 1, abort_flag, a.err);
                 if (!ok) break;
                 tc::fence_after_sync();
@@ -406,14 +436,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             // score product kSbuf chunks ahead into the buffer P(c) leaves.
             // One thread's products run in issue order, so S(c + kSbuf)
             // overwrites P(c) only after PV(c) has read it.
-            for (int c = 0; c < nc && ok; ++c) {
+            for (int c = 0; c < nk && ok; ++c) {
                 ok = wait_role(bars + kBarP + 8 * (c % kSbuf), (c / kSbuf) & 1, abort_flag, a.err) &&
                      wait_role(bars + kBarVFull + 8 * (c % kStagesV), (c / kStagesV) & 1, abort_flag, a.err);
                 if (!ok) break;
                 tc::fence_after_sync();
                 issue_pv(c);
                 const int c3 = c + kSbuf;
-                if (c3 < nc) {
+                if (c3 < nk) {
                     ok = wait_role(bars + kBarKFull + 8 * (c3 % kStagesK), (c3 / kStagesK) & 1, abort_flag,
                                    a.err);
                     if (!ok) break;
@@ -442,10 +472,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float* mpub = reinterpret_cast<float*>(gbase + kOffM);
         float m_l = -INFINITY, l = 0.f;  // this thread's part of the row sum, in units of 2^m_l
         bool ok = true;
-        for (int c = grp; c < nc; c += 2) {
-            const int j = c % kSbuf;
+        for (int k = grp; k < nk; k += 2) {
+            const int c = c_beg + k;  // the chunk of the sequence (k: of this block)
+            const int j = k % kSbuf;
             const uint32_t s_addr = tmem + lane_base + col_s(j);
-            ok = __all_sync(0xffffffffu, wait_role(bars + kBarS + 8 * j, (c / kSbuf) & 1, abort_flag, a.err));
+            ok = __all_sync(0xffffffffu, wait_role(bars + kBarS + 8 * j, (k / kSbuf) & 1, abort_flag, a.err));
             if (!ok) break;
             tc::fence_after_sync();
             float sv[kChunk / 2];
@@ -470,15 +501,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The reference max of chunk c - 1, from the other group; raise it
             // only when this chunk exceeds it by > 2^8.
             float mprev = -INFINITY;
-            if (c > 0) {
-                ok = __all_sync(0xffffffffu, wait_role(bars + kBarM + 8 * ((c - 1) & 1), ((c - 1) >> 1) & 1,
+            if (k > 0) {
+                ok = __all_sync(0xffffffffu, wait_role(bars + kBarM + 8 * ((k - 1) & 1), ((k - 1) >> 1) & 1,
                                                        abort_flag, a.err));
                 if (!ok) break;
-                mprev = mpub[((c - 1) & 1) * kRows + row];
+                mprev = mpub[((k - 1) & 1) * kRows + row];
             }
             const float mc = mx > mprev + kRescaleLog2 ? mx : mprev;
-            if (half == 0) mpub[(c & 1) * kRows + row] = mc;
-            mbar_arrive(bars + kBarM + 8 * (c & 1));
+            if (half == 0) mpub[(k & 1) * kRows + row] = mc;
+            mbar_arrive(bars + kBarM + 8 * (k & 1));
             if (mc != m_l) {
                 l = l > 0.f ? l * fast_exp2(m_l - mc) : 0.f;
                 m_l = mc;
@@ -510,9 +541,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             // The parity wait is unambiguous: the barrier of buffer (c-1) % 3
             // last completed for PV(c - 4), which was done before S(c - 1)
             // (issued after it) was, and this group has seen chunk c - 1's max.
-            if (c > 0 && __any_sync(0xffffffffu, mc != mprev)) {
-                const int jp = (c - 1) % kSbuf;
-                ok = __all_sync(0xffffffffu, wait_role(bars + kBarPV + 8 * jp, ((c - 1) / kSbuf) & 1,
+            if (k > 0 && __any_sync(0xffffffffu, mc != mprev)) {
+                const int jp = (k - 1) % kSbuf;
+                ok = __all_sync(0xffffffffu, wait_role(bars + kBarPV + 8 * jp, ((k - 1) / kSbuf) & 1,
                                                        abort_flag, a.err));
                 if (!ok) break;
                 tc::fence_after_sync();
@@ -532,11 +563,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // PV(c - 3), issued before S(c), so this parity wait is unambiguous.
             if (c == nc - 1) {
                 const int valid = ntok - c * kChunk;
-                ok = __all_sync(0xffffffffu, wait_role(bars + kBarVFull + 8 * (c % kStagesV),
-                                                       (c / kStagesV) & 1, abort_flag, a.err));
+                ok = __all_sync(0xffffffffu, wait_role(bars + kBarVFull + 8 * (k % kStagesV),
+                                                       (k / kStagesV) & 1, abort_flag, a.err));
                 if (!ok) break;
                 if (valid < kChunk) {
-                    const uint32_t vst = base + kOffV + (c % kStagesV) * kStageKV;
+                    const uint32_t vst = base + kOffV + (k % kStagesV) * kStageKV;
                     for (int idx = tid % kGroupThreads; idx < (kChunk - valid) * 16; idx += kGroupThreads) {
                         const int r = valid + (idx >> 4), hf = (idx >> 3) & 1, ch = idx & 7;
                         st_shared_v4(vst + hf * kHalfKV + r * 128 + ch * 16, make_uint4(0, 0, 0, 0));
@@ -548,12 +579,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc::fence_before_sync();
             mbar_arrive(bars + kBarP + 8 * j);
         }
-        // Epilogue. The final reference max is chunk nc - 1's; both groups
-        // bring their row sums to it and add them through shared memory (the
-        // area of the published max, reused after a barrier of both groups).
-        bool fine = ok && __all_sync(0xffffffffu, wait_role(bars + kBarM + 8 * ((nc - 1) & 1),
-                                                             ((nc - 1) >> 1) & 1, abort_flag, a.err));
-        const float mfin = fine ? mpub[((nc - 1) & 1) * kRows + row] : 0.f;
+        // Epilogue. The final reference max is the block's last chunk's; both
+        // groups bring their row sums to it and add them through shared memory
+        // (the area of the published max, reused after a barrier of both
+        // groups).
+        bool fine = ok && __all_sync(0xffffffffu, wait_role(bars + kBarM + 8 * ((nk - 1) & 1),
+                                                             ((nk - 1) >> 1) & 1, abort_flag, a.err));
+        const float mfin = fine ? mpub[((nk - 1) & 1) * kRows + row] : 0.f;
         if (fine && mfin != m_l) l = l > 0.f ? l * fast_exp2(m_l - mfin) : 0.f;
         l += __shfl_xor_sync(0xffffffffu, l, 16);
         asm volatile("bar.sync 2, %0;" ::"n"(kSoftmaxThreads) : "memory");
@@ -565,14 +597,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (fine) {
             fine = __all_sync(0xffffffffu, wait_role(bars + kBarO, 0, abort_flag, a.err));
             if (fine) {
-                // Each group normalises and writes 32 of the row's 64 columns per
-                // thread half: columns 64hf + 32grp .. + 31.
+                // Each group takes 32 of the row's 64 columns per thread half:
+                // columns 64hf + 32grp .. + 31. Without a split it normalises
+                // and writes them; with one it stores them unnormalised in the
+                // block's partial, with the row's (reference max, row sum).
                 tc::fence_after_sync();
-                const float inv = (row_valid && lt > 0.f) ? 1.f / lt : 0.f;
                 float o[32];
                 tc::ld16x2_32<64>(o_addr + 32 * grp, o);
                 tc::wait_ld();
-                if (row_valid) write_row<32>(a, out_row, o, inv, 64 * half + 32 * grp);
+                if (!partial) {
+                    const float inv = (row_valid && lt > 0.f) ? 1.f / lt : 0.f;
+                    if (row_valid) write_row<32>(a, out_row, o, inv, 64 * half + 32 * grp);
+                } else if (row_valid) {
+                    float* dst = part_o + static_cast<size_t>(row) * kD + 64 * half + 32 * grp;
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4)
+                        *reinterpret_cast<float4*>(dst + i) = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+                    if (grp == 0 && half == 0) {
+                        part_ml[2 * row] = mfin;
+                        part_ml[2 * row + 1] = lt;
+                    }
+                }
             }
         }
     }
@@ -584,14 +629,103 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Combines the partials of a split call: one warp per output row (query,
+// head), lane l on columns 4l .. 4l + 3. The two-partial rule of
+// "39 · PagedAttention" §3 over the splits: m = max_s m_s, l = sum_s l_s
+// 2^(m_s - m), o = sum_s O_s 2^(m_s - m) / l (maxima in the log2 domain); a
+// split with m_s = -inf saw no token of the row and is skipped, a NaN m_s
+// (a bad table entry) makes the row zeros. Rows of invalid sequences are
+// left untouched, as the unsplit kernel leaves them.
+struct SplitMergeArgs {
+    const float* part;
+    int num_parts;
+    const int32_t* q_start;
+    const int32_t* seq_lens;
+    void* out;
+    int out_bf16;
+    int B, Hq, Hkv, g, Qb, tiles, splits, num_q, limit;
+};
+
+__global__ void __launch_bounds__(256) prefill_split_merge_kernel(const SplitMergeArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t R = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
+    if (R >= static_cast<int64_t>(a.num_q) * a.Hq) return;
+    const int t = static_cast<int>(R / a.Hq), hq = static_cast<int>(R - static_cast<int64_t>(t) * a.Hq);
+    int lo = 0, hi = a.B - 1;  // the sequence whose query rows hold t
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.q_start[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    const int b = lo;
+    const int qs = a.q_start[b], n = a.q_start[b + 1] - qs, L = a.seq_lens[b];
+    if (n < 1 || L < n || L > a.limit || qs < 0 || qs + n > a.num_q || t < qs || t >= qs + n) return;
+    const int i = t - qs, tile = i / a.Qb;
+    const int h = hq / a.g, r = (i - tile * a.Qb) * a.g + (hq - h * a.g);
+    const size_t p0 = ((static_cast<size_t>(b) * a.Hkv + h) * a.tiles + tile) * a.splits;
+    const float* ml = a.part + static_cast<size_t>(a.num_parts) * kRows * kD;
+    float M = -INFINITY;
+    bool poison = false;
+    for (int sp = 0; sp < a.splits; ++sp) {
+        const float m = ml[((p0 + sp) * kRows + r) * 2];
+        poison |= m != m;
+        M = fmaxf(M, m);
+    }
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    float lsum = 0.f;
+    if (!poison && M != -INFINITY) {
+        for (int sp = 0; sp < a.splits; ++sp) {
+            const size_t pr = (p0 + sp) * kRows + r;
+            const float m = ml[pr * 2];
+            if (m == -INFINITY) continue;
+            const float w = fast_exp2(m - M);
+            lsum = fmaf(ml[pr * 2 + 1], w, lsum);
+            const float4 o = *reinterpret_cast<const float4*>(a.part + pr * kD + 4 * lane);
+            acc[0] = fmaf(o.x, w, acc[0]);
+            acc[1] = fmaf(o.y, w, acc[1]);
+            acc[2] = fmaf(o.z, w, acc[2]);
+            acc[3] = fmaf(o.w, w, acc[3]);
+        }
+    }
+    const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+    const size_t o0 = static_cast<size_t>(R) * kD + 4 * lane;
+    if (a.out_bf16) {
+        uint2 w;
+        w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
+        w.y = pack_bf16x2(acc[2] * inv, acc[3] * inv);
+        *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + o0) = w;
+    } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o0) =
+            make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
+    }
+}
+
 }  // namespace
+
+int prefill_split_count(int B, int Hq, int Hkv, int64_t nq, int max_seq_len, int num_sms) {
+    // A small call (fewer tile blocks than SMs) splits every tile's key range
+    // into as many pieces as fill the SMs once, each of at least two chunks.
+    const int qb = kRows / (Hq / Hkv);
+    const int64_t tiles = (nq + qb - 1) / qb;
+    const int64_t blocks = tiles * Hkv * B;
+    if (blocks <= 0 || blocks >= num_sms) return 1;
+    const int64_t chunks = (static_cast<int64_t>(max_seq_len) + kChunk - 1) / kChunk;
+    const int64_t s = std::min<int64_t>({num_sms / blocks, chunks / 2, 32});
+    return static_cast<int>(std::max<int64_t>(1, s));
+}
+
+size_t prefill_split_bytes(int B, int Hq, int Hkv, int64_t nq, int splits) {
+    const int qb = kRows / (Hq / Hkv);
+    const int64_t tiles = (nq + qb - 1) / qb;
+    const size_t parts = static_cast<size_t>(tiles) * Hkv * B * splits;
+    return parts * kRows * (kD + 2) * sizeof(float);
+}
 
 cudaError_t launch_prefill_one_tile(const CUtensorMap& kmap, const CUtensorMap& vmap, const void* q,
                                     int num_q, const int32_t* q_start, const int32_t* tables,
                                     const int32_t* seq_lens, void* out, int* err, int B, int Hq,
                                     int Hkv, int max_blocks, int num_blocks, int max_seq_len,
                                     int max_q, float scale_log2, int out_bf16, int block_size,
-                                    cudaStream_t stream) {
+                                    cudaStream_t stream, float* part, int splits) {
     PrefillArgs a{};
     a.q = static_cast<const uint16_t*>(q);
     a.q_start = q_start;
@@ -614,7 +748,13 @@ cudaError_t launch_prefill_one_tile(const CUtensorMap& kmap, const CUtensorMap& 
     if (B > kMaxGridYZ || Hkv > kMaxGridYZ) return cudaErrorInvalidValue;  // checked by the callers
     // No sequence has more queries than the call has rows.
     const int64_t nq = std::min<int64_t>(max_q, num_q);
-    dim3 grid(static_cast<unsigned>((nq + a.Qb - 1) / a.Qb), Hkv, B);
+    if (splits < 1 || (splits > 1 && !part)) return cudaErrorInvalidValue;
+    const int64_t tiles = (nq + a.Qb - 1) / a.Qb;
+    a.splits = splits;
+    a.tiles = static_cast<int>(tiles);
+    a.num_parts = static_cast<int>(tiles * Hkv * B * splits);
+    a.part = splits > 1 ? part : nullptr;
+    dim3 grid(static_cast<unsigned>(tiles * splits), Hkv, B);
     CUtensorMap qmap;
     if (!encode_query_map(&qmap, q, num_q, Hq, a.g, a.Qb)) return cudaErrorInvalidValue;
     auto kern = block_size == 16 ? prefill_one_tile_kernel<16> : prefill_one_tile_kernel<32>;
@@ -623,6 +763,12 @@ cudaError_t launch_prefill_one_tile(const CUtensorMap& kmap, const CUtensorMap& 
                                          static_cast<int>(kSmemBytes));
     if (e != cudaSuccess) return e;
     kern<<<grid, kThreads, kSmemBytes, stream>>>(kmap, vmap, qmap, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || splits == 1) return e;
+    SplitMergeArgs m{part, a.num_parts, q_start, seq_lens, out, out_bf16, B, Hq, Hkv, a.g, a.Qb,
+                     a.tiles, splits, num_q, std::min(max_seq_len, max_blocks * block_size)};
+    const int64_t rows = static_cast<int64_t>(num_q) * Hq;
+    prefill_split_merge_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(m);
     return cudaGetLastError();
 }
 
