@@ -34,6 +34,13 @@
 // V rows past the last token of the final chunk are zeroed before its value
 // product. Blocks are ordered longest sequence first.
 //
+// Key split (a small call with a workspace, from pa_decode_multi): grid.x
+// holds tiles x splits blocks, and split s of a tile takes its chunks
+// s * ceil(nc / splits) onward. The pipeline counts the block's own chunks;
+// pages and the causal mask use the sequence's. Each block writes its O
+// unnormalised with every row's reference max and row sum, and
+// prefill_split_merge_kernel combines the splits of each row.
+//
 // Every mbarrier wait is bounded. A role that gives up raises a shared abort
 // flag (and PA_DEVERR_TIMEOUT); the others see it in their own waits. Before
 // the block leaves, each producer waits (bounded) for its copies in flight,
