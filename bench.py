@@ -728,7 +728,11 @@ def run_row(args, local_rank):
     __graft_entry__.build()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    wl = make_workload(args.workload)
+    overrides = {"B": args.sequences} if args.sequences else {}
+    if args.seq_len:
+        overrides.update(lengths=("fixed", args.seq_len), max_len=args.seq_len,
+                         pool=("factor", 1.0))
+    wl = make_workload(args.workload, **overrides)
     bf = wl.dtype == "bf16"
 
     def to_dev(a):
@@ -816,6 +820,29 @@ def run_row(args, local_rank):
     ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in ev)
     peak, peak_kind = measured_peak_gbs()
     gbs = nbytes / (ms * 1e-3) / 1e9
+    ms_graph = None
+    if args.row in ("prefill", "spec"):
+        # The same calls replayed from a CUDA graph: the device's own time per
+        # call, without the host's per-call cost (which the events above
+        # include when a call is shorter than its launch from Python).
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(LATENCY_GRAPH_STEPS):
+                    call()
+            reps = max(1, args.steps // LATENCY_GRAPH_STEPS)
+            for _ in range(2):
+                graph.replay()
+            side.synchronize()
+            t0.record(side)
+            for _ in range(reps):
+                graph.replay()
+            t1.record(side)
+            side.synchronize()
+            ms_graph = t0.elapsed_time(t1) / (reps * LATENCY_GRAPH_STEPS)
+            del graph
     if args.row in ("prefill", "spec"):
         tpeak, tkind = measured_peak_tflops()
         tfs = flops / (ms * 1e-3) / 1e12
@@ -831,8 +858,12 @@ def run_row(args, local_rank):
                if args.row == "prefill" else
                {"metric": "speculative verification (pa_decode_multi): achieved HBM GB/s",
                 "value": gbs, "unit": "GB/s"}), "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": ms, "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": wl.name, "what": what, "queries_per_sequence": n_new},
+            "ms_per_step": ms, "ms_per_step_graph": ms_graph,
+            "value_graph": (flops / (ms_graph * 1e-3) / 1e12 if args.row == "prefill" else
+                            nbytes / (ms_graph * 1e-3) / 1e9),
+            "higher_is_better": True, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": wl.name, "what": what, "queries_per_sequence": n_new,
+                       "B": wl.B, "seq_len": args.seq_len or "the workload's"},
             "roofline": ({"bound": "hbm", "achieved": gbs, "peak": peak, "peak_kind": peak_kind,
                           "unit": "GB/s", "frac": gbs / peak, "algorithmic_bytes": nbytes,
                           "tflops": tfs} if hbm_bound else
@@ -845,7 +876,9 @@ def run_row(args, local_rank):
                           "frac_sustained": (tfs / measured_peak_tflops_sustained()
                                              if measured_peak_tflops_sustained() else None),
                           "timed_s": ms * args.steps * 1e-3}),
-            "parity": parity, "gpu_launches": (2 if args.row == "spec" else 1) * args.steps,
+            "parity": parity,
+            "gpu_launches": (2 if args.row == "spec" else 1) * (
+                args.steps + args.warmup + LATENCY_GRAPH_STEPS * (2 + max(1, args.steps // LATENCY_GRAPH_STEPS))),
             "cpu_baseline": cpu,
         }), flush=True)
         return
@@ -1038,8 +1071,11 @@ def main():
     ap.add_argument("--batch", type=int, default=1,
                     help="latency row: sequences per step (all of one length)")
     ap.add_argument("--sequences", type=int, default=None,
-                    help="decode row: N sequences drawn by the workload's recipe (a smaller "
-                         "case of the same workload, e.g. for a multi-pass profiler capture)")
+                    help="decode and other rows: N sequences drawn by the workload's recipe (a "
+                         "smaller case of the same workload, e.g. for a profiler capture or a "
+                         "small batch)")
+    ap.add_argument("--seq-len", type=int, default=None,
+                    help="rows other than decode: every sequence of this many tokens")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
