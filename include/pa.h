@@ -289,7 +289,11 @@ pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
  * the call has at most three waves of tiles (tiles x Hkv x B <= 3 x SMs),
  * it runs a one-tile kernel that overlaps a tile's softmax with its own
  * next score products; otherwise a kernel that alternates two tiles per
- * block (half the K/V intake per row). With a few queries (max_q * Hq / Hkv <= 16, e.g. speculative
+ * block (half the K/V intake per row). pa_prefill holds no workspace, so a
+ * call with fewer one-tile blocks than SMs (a few sequences) streams each
+ * sequence's whole key range in one block; pa_decode_multi computes the
+ * same rows with a plan whose workspace lets such calls split the key range
+ * over several blocks. With a few queries (max_q * Hq / Hkv <= 16, e.g. speculative
  * verification) pa_decode_multi computes the same rows at the decode's
  * bandwidth. n_b < 1, n_b > L_b,
  * L_b out of range or rows outside [0, num_queries) raise PA_DEVERR_SEQ_LEN
