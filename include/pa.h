@@ -225,6 +225,16 @@ pa_status pa_plan_set_path(pa_plan* plan, int path);
  * when a call launches its kernels). Nothing ever waits without a bound. */
 pa_status pa_debug_set_wait_probe(int enable);
 
+/* Test hook: which tensor-core kernel pa_prefill (and pa_decode_multi above
+ * 16 columns) runs. PA_PREFILL_AUTO (the default) chooses from the shape, as
+ * described at pa_prefill; PA_PREFILL_ONE_TILE and PA_PREFILL_TWO_TILE pin
+ * one kernel for every call, so that tests can check both on any shape (the
+ * key split of small pa_decode_multi calls belongs to the one-tile kernel
+ * and is skipped under PA_PREFILL_TWO_TILE). Process-wide, read when a call
+ * launches; PA_ERR_SHAPE for any other value. */
+enum { PA_PREFILL_AUTO = 0, PA_PREFILL_ONE_TILE = 1, PA_PREFILL_TWO_TILE = 2 };
+pa_status pa_debug_set_prefill_kernel(int which);
+
 /* How pa_decode combines the partials of a sequence split across warps
  * (pa_plan_set_merge). */
 enum {

@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
     L.pa_plan_set_path.restype = ci
     L.pa_debug_set_wait_probe.argtypes = [ci]
     L.pa_debug_set_wait_probe.restype = ci
+    L.pa_debug_set_prefill_kernel.argtypes = [ci]
+    L.pa_debug_set_prefill_kernel.restype = ci
     L.pa_plan_set_merge.argtypes = [vp, ci]
     L.pa_plan_set_merge.restype = ci
     L.pa_plan_set_schedule.argtypes = [vp, ci, ci]
@@ -467,6 +469,15 @@ def pa_debug_set_wait_probe(enable: bool) -> None:
     """Test hook: while on, each kernel's first pipeline wait expires (bounded),
     so the kernel reports PA_DEVERR_TIMEOUT and takes its give-up path."""
     _check(lib().pa_debug_set_wait_probe(1 if enable else 0), "pa_debug_set_wait_probe")
+
+
+PA_PREFILL_AUTO, PA_PREFILL_ONE_TILE, PA_PREFILL_TWO_TILE = 0, 1, 2
+
+
+def pa_debug_set_prefill_kernel(which: int) -> None:
+    """Test hook: pin the prefill kernel (PA_PREFILL_ONE_TILE / _TWO_TILE) or
+    restore the shape-based choice (PA_PREFILL_AUTO)."""
+    _check(lib().pa_debug_set_prefill_kernel(int(which)), "pa_debug_set_prefill_kernel")
 
 
 def pa_free(plan: Plan) -> None:

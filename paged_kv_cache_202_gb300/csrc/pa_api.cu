@@ -68,6 +68,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 std::atomic<int> g_wait_probe{0};
+std::atomic<int> g_prefill_kernel{PA_PREFILL_AUTO};
 
 struct DeviceGuard {
     int prev = -1;
@@ -85,6 +86,7 @@ struct DeviceGuard {
 namespace pa {
 
 int wait_probe() { return g_wait_probe.load(std::memory_order_relaxed); }
+int prefill_kernel_choice() { return g_prefill_kernel.load(std::memory_order_relaxed); }
 
 bool encode_pool_map(CUtensorMap* map, const void* pool, int rows, int D, int BS) {
     auto fn = encode_fn();
@@ -760,6 +762,13 @@ pa_status pa_plan_set_merge(pa_plan* plan, int mode) {
 
 pa_status pa_debug_set_wait_probe(int enable) {
     g_wait_probe.store(enable ? 1 : 0, std::memory_order_relaxed);
+    return PA_OK;
+}
+
+pa_status pa_debug_set_prefill_kernel(int which) {
+    if (which != PA_PREFILL_AUTO && which != PA_PREFILL_ONE_TILE && which != PA_PREFILL_TWO_TILE)
+        return PA_ERR_SHAPE;
+    g_prefill_kernel.store(which, std::memory_order_relaxed);
     return PA_OK;
 }
 

@@ -34,6 +34,8 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 constexpr uint64_t kProbeLimitNs = 20000;  // 20 us
 // 1 while the probe is on (read at launch time by every launch site).
 int wait_probe();
+// The prefill kernel a test has forced (PA_PREFILL_*; PA_PREFILL_AUTO: none).
+int prefill_kernel_choice();
 
 enum SplitKind { kSplitFma = 0, kSplitMma = 1 };
 

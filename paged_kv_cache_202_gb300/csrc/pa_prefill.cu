@@ -649,7 +649,9 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return cudaErrorInvalidValue;
         const int64_t blocks1 = (nq + qb - 1) / qb * static_cast<int64_t>(Hkv) * B;
-        if (nq <= qb || blocks1 <= 3LL * sms)
+        const int force = prefill_kernel_choice();  // a test may pin either kernel
+        if (force == PA_PREFILL_ONE_TILE ||
+            (force == PA_PREFILL_AUTO && (nq <= qb || blocks1 <= 3LL * sms)))
             return launch_prefill_one_tile(kmap, vmap, q, num_q, q_start, tables, seq_lens, out, err,
                                            B, Hq, Hkv, max_blocks, num_blocks, max_seq_len, max_q,
                                            scale_log2, out_bf16, block_size, stream, part,

@@ -109,8 +109,20 @@ def test_noalloc_decode_gives_up_reports_and_recovers(probe):
     assert np.abs(out_f64(ds.out) - ref).max() <= BF16_TOL
 
 
+@pytest.fixture(params=[1, 2], ids=["one_tile", "two_tile"])
+def prefill_kernel(request):
+    """Pins the prefill call to one of the two tensor-core kernels."""
+    which = {1: pa.PA_PREFILL_ONE_TILE, 2: pa.PA_PREFILL_TWO_TILE}[request.param]
+    pa.pa_debug_set_prefill_kernel(which)
+    try:
+        yield which
+    finally:
+        pa.pa_debug_set_prefill_kernel(pa.PA_PREFILL_AUTO)
+
+
 @pytest.mark.parametrize("lens,ns", [([700, 300, 2000], [200, 64, 256]), ([90], [1])])
-def test_prefill_gives_up_reports_frees_tensor_memory_and_recovers(probe, lens, ns):
+def test_prefill_gives_up_reports_frees_tensor_memory_and_recovers(probe, prefill_kernel,
+                                                                    lens, ns):
     wl = make_workload("llama3_8b_gqa", seed=34, B=len(lens), lengths=("list", lens),
                        max_len=max(lens) + 16)
     append_in_place(wl)

@@ -29,6 +29,20 @@ _MANY_LENS = [int(x) for x in _rng.integers(1, 80, size=300)]
 _MANY_NS = [int(min(x, y)) for x, y in zip(_MANY_LENS, _rng.integers(1, 20, size=300))]
 
 
+# Small calls choose the one-tile kernel by themselves; the tests below run
+# each case on both kernels, pinned through the test hook.
+KERNELS = [pa.PA_PREFILL_ONE_TILE, pa.PA_PREFILL_TWO_TILE]
+
+
+@pytest.fixture(params=KERNELS, ids=["one_tile", "two_tile"])
+def kernel(request):
+    pa.pa_debug_set_prefill_kernel(request.param)
+    try:
+        yield request.param
+    finally:
+        pa.pa_debug_set_prefill_kernel(pa.PA_PREFILL_AUTO)
+
+
 def _case(lens, ns, Hq=32, Hkv=8, bs=16, seed=0):
     wl = make_workload("llama3_8b_gqa", seed=seed, B=len(lens), Hq=Hq, Hkv=Hkv, block_size=bs,
                        lengths=("list", lens), max_len=max(lens) + bs)
@@ -60,7 +74,7 @@ def _run(wl, q, qs, ns):
     (32, 8, 16, [50] * 20 + [120] * 20, [10] * 40),     # equal lengths: the longest-first order breaks ties
     (32, 8, 16, _MANY_LENS, _MANY_NS),                  # more sequences than are ordered by length
 ])
-def test_prefill_matches_oracle(Hq, Hkv, bs, lens, ns):
+def test_prefill_matches_oracle(Hq, Hkv, bs, lens, ns, kernel):
     wl, q, qs = _case(lens, ns, Hq=Hq, Hkv=Hkv, bs=bs)
     got, err = _run(wl, q, qs, ns)
     assert err == 0
@@ -74,7 +88,7 @@ def test_prefill_matches_oracle(Hq, Hkv, bs, lens, ns):
     ([200, 64, 1000], [37, 64, 130]),   # full and partial query tiles
     ([300, 500], [64, 128]),            # full tiles only
 ])
-def test_float_output_rounds_to_the_bf16_output(lens, ns):
+def test_float_output_rounds_to_the_bf16_output(lens, ns, kernel):
     # bf16 output of full tiles leaves through tiled tensor stores, float
     # output and partial tiles through the threads' own stores; the same
     # normalised values rounded to nearest even must agree bit for bit.
@@ -97,14 +111,14 @@ def test_float_output_rounds_to_the_bf16_output(lens, ns):
     assert np.abs(f32.double().cpu().numpy() - ref).max() <= BF16_TOL
 
 
-def test_single_query_prefill_matches_decode():
+def test_single_query_prefill_matches_decode(kernel):
     wl, q, qs = _case([77, 300, 16], [1, 1, 1])
     got, err = _run(wl, q, qs, [1, 1, 1])
     ref = oracle.prefill(q, wl.k_pool, wl.v_pool, wl.block_tables, wl.seq_lens, qs, wl.scale)
     assert err == 0 and np.abs(got - ref).max() <= BF16_TOL
 
 
-def test_prefill_bad_lengths_and_table():
+def test_prefill_bad_lengths_and_table(kernel):
     wl, q, qs = _case([100, 50], [10, 10])
     ds = DeviceStep(wl)
     qd = to_dev(q, "bf16")
@@ -123,7 +137,7 @@ def test_prefill_bad_lengths_and_table():
     assert np.abs(got[:10] - ref).max() <= BF16_TOL
 
 
-def test_prefill_rows_past_the_query_array_are_refused():
+def test_prefill_rows_past_the_query_array_are_refused(kernel):
     # q_start says 20 rows, but q and out hold 15: the second sequence's rows
     # would fall outside them, so it is refused (PA_DEVERR_SEQ_LEN, rows
     # untouched) and nothing is read or written past the arrays.
