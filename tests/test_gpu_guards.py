@@ -175,6 +175,35 @@ def test_noalloc_decode_writes_only_its_output(case):
     (16, 1, 16, [130, 17], [1, 1]),
 ])
 def test_multi_query_calls_write_only_their_output(multi, Hq, Hkv, bs, lens, ns):
+    _multi_query_guarded(multi, Hq, Hkv, bs, lens, ns)
+
+
+# Both tensor-core prefill kernels, pinned through the test hook: whole query
+# tiles (the output leaves by tiled bulk tensor stores) and ragged tiles.
+@pytest.mark.parametrize("kernel", [1, 2], ids=["one_tile", "two_tile"])
+@pytest.mark.parametrize("lens,ns", [
+    ([700, 2000], [64, 128]),      # whole tiles of 32 queries x 4 heads
+    ([900, 1500, 260], [40, 77, 5]),   # ragged tiles
+    ([6000], [32]),                # one whole tile over a long key range
+])
+def test_tensor_core_prefill_writes_only_its_output(kernel, lens, ns):
+    which = {1: pa.PA_PREFILL_ONE_TILE, 2: pa.PA_PREFILL_TWO_TILE}[kernel]
+    pa.pa_debug_set_prefill_kernel(which)
+    try:
+        _multi_query_guarded(False, 32, 8, 16, lens, ns)
+    finally:
+        pa.pa_debug_set_prefill_kernel(pa.PA_PREFILL_AUTO)
+
+
+@pytest.mark.parametrize("lens,ns", [([12000], [8]), ([5000, 300], [12, 9])])
+def test_split_verification_writes_only_its_output(lens, ns):
+    # More than 16 (query, head) columns per kv head on a small batch: the
+    # key split's partials go to the plan's workspace and a merge kernel
+    # writes the output.
+    _multi_query_guarded(True, 32, 8, 16, lens, ns)
+
+
+def _multi_query_guarded(multi, Hq, Hkv, bs, lens, ns):
     wl = make_workload("llama3_8b_gqa", seed=sum(lens), B=len(lens), Hq=Hq, Hkv=Hkv,
                        block_size=bs, lengths=("list", lens), max_len=max(lens) + bs)
     kp, vp = pools_after_append(wl)
