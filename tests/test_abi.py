@@ -218,6 +218,18 @@ def test_wait_probe_switch_is_host_only(lib):
     assert lib.pa_last_device_error(None, None) == pa.PA_ERR_NULL
 
 
+def test_prefill_kernel_pin_is_host_only_and_checked(lib):
+    # The prefill-kernel pin is a host setting read at launch time; values
+    # other than the three named ones are refused and leave it unchanged.
+    for which in (pa.PA_PREFILL_ONE_TILE, pa.PA_PREFILL_TWO_TILE, pa.PA_PREFILL_AUTO):
+        assert lib.pa_debug_set_prefill_kernel(which) == pa.PA_OK
+    for bad in (-1, 3, 1 << 20):
+        assert lib.pa_debug_set_prefill_kernel(bad) == pa.PA_ERR_SHAPE
+    with pytest.raises(RuntimeError):
+        pa.pa_debug_set_prefill_kernel(7)
+    assert lib.pa_debug_set_prefill_kernel(pa.PA_PREFILL_AUTO) == pa.PA_OK
+
+
 def test_binding_byte_counter_matches_oracle():
     import numpy as np
     import oracle
