@@ -305,7 +305,7 @@ pa_status pa_plan_set_split_events(pa_plan* plan, struct CUevent_st* start,
  * same rows with a plan whose workspace lets such calls split the key range
  * over several blocks. With a few queries (max_q * Hq / Hkv <= 16, e.g. speculative
  * verification) pa_decode_multi computes the same rows at the decode's
- * bandwidth. n_b < 1, n_b > L_b,
+ * bandwidth. n_b < 1, n_b > max_q, n_b > L_b,
  * L_b out of range or rows outside [0, num_queries) raise PA_DEVERR_SEQ_LEN
  * and leave that sequence's rows untouched; a table entry outside the pool
  * raises PA_DEVERR_TABLE and zeroes the affected rows.

@@ -463,7 +463,7 @@ pa_status decode_impl(const void* q, const int32_t* q_start, int T, int nq, cons
                                                  out, plan->err, B, Hq, Hkv, max_blocks,
                                                  num_blocks, max_seq_len, nq, scale_log2,
                                                  out_dtype == PA_BF16, block_size, stream, part,
-                                                 splits);
+                                                 splits, /*zero_invalid=*/1);
         if (plan->ev_stop) cudaEventRecord(plan->ev_stop, stream);
         plan->last_path = PA_PATH_PREFILL;
         plan->last_blocks = 0;

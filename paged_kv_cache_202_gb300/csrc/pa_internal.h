@@ -228,13 +228,14 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
                            const int32_t* seq_lens, void* out, int* err, int B, int Hq, int Hkv,
                            int max_blocks, int num_blocks, int max_seq_len, int max_q,
                            float scale_log2, int out_bf16, int block_size, cudaStream_t stream,
-                           float* part = nullptr, int splits = 1);
+                           float* part = nullptr, int splits = 1, int zero_invalid = 0);
 cudaError_t launch_prefill_one_tile(const CUtensorMap& kmap, const CUtensorMap& vmap, const void* q,
                                     int num_q, const int32_t* q_start, const int32_t* tables,
                                     const int32_t* seq_lens, void* out, int* err, int B, int Hq,
                                     int Hkv, int max_blocks, int num_blocks, int max_seq_len,
                                     int max_q, float scale_log2, int out_bf16, int block_size,
-                                    cudaStream_t stream, float* part, int splits);
+                                    cudaStream_t stream, float* part, int splits,
+                                    int zero_invalid);
 // Key splits for a one-tile call (1: none) and the partial bytes they need;
 // nq = min(max_q, num_queries).
 int prefill_split_count(int B, int Hq, int Hkv, int64_t nq, int max_seq_len, int num_sms);

@@ -131,6 +131,8 @@ struct PrefillArgs {
     float scale_log2;
     int out_bf16;
     int probe_wait;           // 1: the MMA thread's first wait expires (a test hook)
+    int max_q;                // bound on every sequence's query count
+    int zero_invalid;         // 1: an invalid sequence's rows get zeros (multi-query calls)
 };
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint4 v) {
@@ -190,6 +192,19 @@ __device__ __forceinline__ void write_row(const PrefillArgs& a, size_t row, cons
     }
 }
 
+// Zeroes output rows [r0, r1) x query heads [h0, h0 + g) (an invalid
+// sequence of a multi-query call), the block's threads in turn.
+__device__ void zero_rows(const PrefillArgs& a, int64_t r0, int64_t r1, int h0, int tid) {
+    const int64_t per_row = static_cast<int64_t>(a.g) * kD;
+    const int64_t total = (r1 - r0) * per_row;
+    for (int64_t i = tid; i < total; i += kThreads) {
+        const int64_t r = r0 + i / per_row, e = i - (i / per_row) * per_row;
+        const size_t idx = (static_cast<size_t>(r) * a.Hq + h0) * kD + static_cast<size_t>(e);
+        if (a.out_bf16) static_cast<uint16_t*>(a.out)[idx] = 0;
+        else static_cast<float*>(a.out)[idx] = 0.f;
+    }
+}
+
 // Bounded wait that also gives up when another role raised the abort flag.
 __device__ __forceinline__ bool wait_role(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                           int* err) {
@@ -240,14 +255,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         b = *seq_slot;
     }
     const int h = blockIdx.y;
-    const int qs = a.q_start[b];
-    const int n = a.q_start[b + 1] - qs;
     const int L = a.seq_lens[b];
     const int limit = min(a.max_seq_len, a.max_blocks * BS);
-    if (n < 1 || L < n || L > limit || qs < 0 || qs + n > a.num_q) {
-        if (blockIdx.x == 0 && h == 0 && tid == 0) atomicOr(a.err, kErrSeqLen);
-        return;  // rows of an invalid sequence are left untouched
+    {
+        const int64_t qs64 = a.q_start[b], n64 = static_cast<int64_t>(a.q_start[b + 1]) - qs64;
+        if (n64 < 1 || n64 > a.max_q || L < n64 || L > limit || qs64 < 0 || qs64 + n64 > a.num_q) {
+            if (blockIdx.x == 0 && h == 0 && tid == 0) atomicOr(a.err, kErrSeqLen);
+            // The rows inside the arrays get zeros in a multi-query call and
+            // are left untouched otherwise.
+            if (a.zero_invalid && blockIdx.x == 0)
+                zero_rows(a, qs64 > 0 ? qs64 : 0,
+                          n64 > 0 ? (qs64 + n64 < a.num_q ? qs64 + n64 : a.num_q) : 0, h * a.g, tid);
+            return;
+        }
     }
+    const int qs = a.q_start[b];
+    const int n = a.q_start[b + 1] - qs;
     const int q0 = blockIdx.x * 2 * a.Qb;
     if (q0 >= n) return;
     const int nq0 = min(a.Qb, n - q0);
@@ -630,7 +653,7 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
                            const int32_t* seq_lens, void* out, int* err, int B, int Hq, int Hkv,
                            int max_blocks, int num_blocks, int max_seq_len, int max_q,
                            float scale_log2, int out_bf16, int block_size, cudaStream_t stream,
-                           float* part, int splits) {
+                           float* part, int splits, int zero_invalid) {
     // The one-tile kernel overlaps a tile's softmax with its own next score
     // products (~2,100 cycles per 128-token chunk and tile); this kernel
     // alternates two tiles (~3,100 cycles per chunk for both), which halves
@@ -655,7 +678,7 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
             return launch_prefill_one_tile(kmap, vmap, q, num_q, q_start, tables, seq_lens, out, err,
                                            B, Hq, Hkv, max_blocks, num_blocks, max_seq_len, max_q,
                                            scale_log2, out_bf16, block_size, stream, part,
-                                           splits);
+                                           splits, zero_invalid);
     }
     PrefillArgs a{};
     a.q = static_cast<const uint16_t*>(q);
@@ -676,6 +699,8 @@ cudaError_t launch_prefill(const CUtensorMap& kmap, const CUtensorMap& vmap, con
     a.scale_log2 = scale_log2;
     a.out_bf16 = out_bf16;
     a.probe_wait = wait_probe();
+    a.max_q = max_q;
+    a.zero_invalid = zero_invalid;
     if (B > kMaxGridYZ || Hkv > kMaxGridYZ) return cudaErrorInvalidValue;  // checked by the callers
     // No sequence has more queries than the call has rows.
     const int64_t nq = std::min<int64_t>(max_q, num_q);

@@ -130,6 +130,8 @@ struct PrefillArgs {
     float scale_log2;
     int out_bf16;
     int probe_wait;           // 1: the MMA thread's first wait expires (a test hook)
+    int max_q;                // bound on every sequence's query count
+    int zero_invalid;         // 1: an invalid sequence's rows get zeros (multi-query calls)
     // Key split: grid.x = tiles x splits, block x takes split x % splits of
     // tile x / splits. With splits > 1 every block writes a partial instead
     // of output rows: O unnormalised [num_parts][kRows][kD] at part, then
@@ -185,6 +187,19 @@ __device__ __forceinline__ bool wait_role(uint32_t bar, uint32_t parity, volatil
     }
 }
 
+// Zeroes output rows [r0, r1) x query heads [h0, h0 + g) (an invalid
+// sequence of a multi-query call), the block's threads in turn.
+__device__ void zero_rows(const PrefillArgs& a, int64_t r0, int64_t r1, int h0, int tid) {
+    const int64_t per_row = static_cast<int64_t>(a.g) * kD;
+    const int64_t total = (r1 - r0) * per_row;
+    for (int64_t i = tid; i < total; i += kThreads) {
+        const int64_t r = r0 + i / per_row, e = i - (i / per_row) * per_row;
+        const size_t idx = (static_cast<size_t>(r) * a.Hq + h0) * kD + static_cast<size_t>(e);
+        if (a.out_bf16) static_cast<uint16_t*>(a.out)[idx] = 0;
+        else static_cast<float*>(a.out)[idx] = 0.f;
+    }
+}
+
 template <int BS>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_one_tile_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
@@ -218,14 +233,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         b = *seq_slot;
     }
     const int h = blockIdx.y;
-    const int qs = a.q_start[b];
-    const int n = a.q_start[b + 1] - qs;
     const int L = a.seq_lens[b];
     const int limit = min(a.max_seq_len, a.max_blocks * BS);
-    if (n < 1 || L < n || L > limit || qs < 0 || qs + n > a.num_q) {
-        if (blockIdx.x == 0 && h == 0 && tid == 0) atomicOr(a.err, kErrSeqLen);
-        return;  // rows of an invalid sequence are left untouched
+    {
+        const int64_t qs64 = a.q_start[b], n64 = static_cast<int64_t>(a.q_start[b + 1]) - qs64;
+        if (n64 < 1 || n64 > a.max_q || L < n64 || L > limit || qs64 < 0 || qs64 + n64 > a.num_q) {
+            if (blockIdx.x == 0 && h == 0 && tid == 0) atomicOr(a.err, kErrSeqLen);
+            // The rows inside the arrays get zeros in a multi-query call and
+            // are left untouched otherwise.
+            if (a.zero_invalid && blockIdx.x == 0)
+                zero_rows(a, qs64 > 0 ? qs64 : 0,
+                          n64 > 0 ? (qs64 + n64 < a.num_q ? qs64 + n64 : a.num_q) : 0, h * a.g, tid);
+            return;
+        }
     }
+    const int qs = a.q_start[b];
+    const int n = a.q_start[b + 1] - qs;
     const int split = blockIdx.x % a.splits, tile = blockIdx.x / a.splits;
     const int q0 = tile * a.Qb;
     if (q0 >= n) return;
@@ -641,8 +664,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 // "39 · PagedAttention" §3 over the splits: m = max_s m_s, l = sum_s l_s
 // 2^(m_s - m), o = sum_s O_s 2^(m_s - m) / l (maxima in the log2 domain); a
 // split with m_s = -inf saw no token of the row and is skipped, a NaN m_s
-// (a bad table entry) makes the row zeros. Rows of invalid sequences are
-// left untouched, as the unsplit kernel leaves them.
+// (a bad table entry) makes the row zeros. Rows of invalid sequences get
+// zeros (only multi-query calls split).
 struct SplitMergeArgs {
     const float* part;
     int num_parts;
@@ -650,7 +673,7 @@ struct SplitMergeArgs {
     const int32_t* seq_lens;
     void* out;
     int out_bf16;
-    int B, Hq, Hkv, g, Qb, tiles, splits, num_q, limit;
+    int B, Hq, Hkv, g, Qb, tiles, splits, num_q, limit, max_q;
 };
 
 __global__ void __launch_bounds__(256) prefill_split_merge_kernel(const SplitMergeArgs a) {
@@ -664,9 +687,18 @@ __global__ void __launch_bounds__(256) prefill_split_merge_kernel(const SplitMer
         if (a.q_start[mid] <= t) lo = mid; else hi = mid - 1;
     }
     const int b = lo;
-    const int qs = a.q_start[b], n = a.q_start[b + 1] - qs, L = a.seq_lens[b];
-    if (n < 1 || L < n || L > a.limit || qs < 0 || qs + n > a.num_q || t < qs || t >= qs + n) return;
-    const int i = t - qs, tile = i / a.Qb;
+    const size_t o0 = static_cast<size_t>(R) * kD + 4 * lane;
+    const int64_t qs64 = a.q_start[b], n64 = static_cast<int64_t>(a.q_start[b + 1]) - qs64;
+    const int L = a.seq_lens[b];
+    if (n64 < 1 || n64 > a.max_q || L < n64 || L > a.limit || qs64 < 0 || qs64 + n64 > a.num_q ||
+        t < qs64 || t >= qs64 + n64) {
+        // An invalid sequence (the split blocks wrote no partial for it): zeros.
+        if (a.out_bf16) *reinterpret_cast<uint2*>(static_cast<uint16_t*>(a.out) + o0) = make_uint2(0, 0);
+        else *reinterpret_cast<float4*>(static_cast<float*>(a.out) + o0) = make_float4(0.f, 0.f, 0.f, 0.f);
+        return;
+    }
+    const int qs = static_cast<int>(qs64);
+    const int i = t - qs, tile = i / a.Qb;  // i < min(max_q, num_q): tile < tiles
     const int h = hq / a.g, r = (i - tile * a.Qb) * a.g + (hq - h * a.g);
     const size_t p0 = ((static_cast<size_t>(b) * a.Hkv + h) * a.tiles + tile) * a.splits;
     const float* ml = a.part + static_cast<size_t>(a.num_parts) * kRows * kD;
@@ -694,7 +726,6 @@ __global__ void __launch_bounds__(256) prefill_split_merge_kernel(const SplitMer
         }
     }
     const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-    const size_t o0 = static_cast<size_t>(R) * kD + 4 * lane;
     if (a.out_bf16) {
         uint2 w;
         w.x = pack_bf16x2(acc[0] * inv, acc[1] * inv);
@@ -732,7 +763,8 @@ cudaError_t launch_prefill_one_tile(const CUtensorMap& kmap, const CUtensorMap& 
                                     const int32_t* seq_lens, void* out, int* err, int B, int Hq,
                                     int Hkv, int max_blocks, int num_blocks, int max_seq_len,
                                     int max_q, float scale_log2, int out_bf16, int block_size,
-                                    cudaStream_t stream, float* part, int splits) {
+                                    cudaStream_t stream, float* part, int splits,
+                                    int zero_invalid) {
     PrefillArgs a{};
     a.q = static_cast<const uint16_t*>(q);
     a.q_start = q_start;
@@ -752,6 +784,8 @@ cudaError_t launch_prefill_one_tile(const CUtensorMap& kmap, const CUtensorMap& 
     a.scale_log2 = scale_log2;
     a.out_bf16 = out_bf16;
     a.probe_wait = wait_probe();
+    a.max_q = max_q;
+    a.zero_invalid = zero_invalid;
     if (B > kMaxGridYZ || Hkv > kMaxGridYZ) return cudaErrorInvalidValue;  // checked by the callers
     // No sequence has more queries than the call has rows.
     const int64_t nq = std::min<int64_t>(max_q, num_q);
@@ -773,7 +807,7 @@ cudaError_t launch_prefill_one_tile(const CUtensorMap& kmap, const CUtensorMap& 
     e = cudaGetLastError();
     if (e != cudaSuccess || splits == 1) return e;
     SplitMergeArgs m{part, a.num_parts, q_start, seq_lens, out, out_bf16, B, Hq, Hkv, a.g, a.Qb,
-                     a.tiles, splits, num_q, std::min(max_seq_len, max_blocks * block_size)};
+                     a.tiles, splits, num_q, std::min(max_seq_len, max_blocks * block_size), max_q};
     const int64_t rows = static_cast<int64_t>(num_q) * Hq;
     prefill_split_merge_kernel<<<static_cast<unsigned>((rows + 7) / 8), 256, 0, stream>>>(m);
     return cudaGetLastError();

@@ -6,9 +6,11 @@ range over several blocks and a second kernel merges their partials.
 Against the fp64 oracle's causal multi-query attention: one to three
 sequences of up to ~20k tokens with 5 to 32 queries each (one and several
 splits, splits past a short sequence's end), both block sizes, float
-output; a bad table entry (the poisoned partials give zero rows); a plain
-decode on the same plan afterwards (the split decode's counters in the
-workspace are left intact), and a second call giving the same bits.
+output; a bad table entry (the poisoned partials give zero rows); a
+sequence with more queries than max_q or than tokens (an error and zero
+rows, on split and unsplit calls of both prefill kernels); a plain decode
+on the same plan afterwards (the split decode's counters in the workspace
+are left intact), and a second call giving the same bits.
 """
 
 import numpy as np
@@ -119,3 +121,31 @@ def test_decode_on_the_same_plan_after_a_split_call():
             torch.cuda.synchronize()
             assert plan.last_device_error() == 0
             assert np.abs(out_f64(dout) - dref).max() <= tol(dwl)
+
+
+@pytest.mark.parametrize("lens,ns,max_q,bad", [
+    ([9000, 6000], [8, 20], 8, 1),     # more queries than max_q (split call)
+    ([9000, 10], [8, 12], 12, 1),      # more queries than tokens (split call)
+    ([3000] * 39 + [20], [24] * 39 + [30], 24, 39),   # one-tile kernel, no split; n > max_q
+    ([3000] * 39 + [2000], [64] * 39 + [70], 64, 39),  # two-tile kernel; n > max_q
+])
+def test_invalid_sequence_gets_zero_rows_and_an_error(lens, ns, max_q, bad):
+    # Above 16 columns pa_decode_multi runs the prefill kernels; an invalid
+    # sequence raises PA_DEVERR_SEQ_LEN and gets zero rows, as on the split
+    # decode's tiles, and the split merge reads no partial for it.
+    wl, q, qs = _case(lens, [min(n, l) for n, l in zip(ns, lens)])
+    qs = np.concatenate([[0], np.cumsum(ns)]).astype(np.int32)
+    rng = np.random.default_rng(7)
+    q = bf16_bits(rng.standard_normal((int(qs[-1]), wl.Hq, wl.D)).astype(np.float32))
+    ds = DeviceStep(wl)
+    with pa.Plan() as plan:
+        out = _call(ds, wl, q, qs, max_q, plan)
+        assert plan.last_device_error() & pa.PA_DEVERR_SEQ_LEN
+        assert plan.info()[0] == pa.PA_PATH_PREFILL
+    got = out_f64(out)
+    assert (got[qs[bad]:qs[bad + 1]] == 0).all()
+    good = [b for b in range(len(lens)) if b != bad][:3]
+    for b in good:
+        ref = oracle.prefill(q[qs[b]:qs[b + 1]], wl.k_pool, wl.v_pool, wl.block_tables[b:b + 1],
+                             wl.seq_lens[b:b + 1], np.array([0, ns[b]], np.int32), wl.scale)
+        assert np.abs(got[qs[b]:qs[b + 1]] - ref).max() <= BF16_TOL

@@ -157,6 +157,24 @@ def test_prefill_rows_past_the_query_array_are_refused(kernel):
     assert np.abs(got[:10] - ref).max() <= BF16_TOL
 
 
+def test_prefill_more_queries_than_max_q_are_refused(kernel):
+    # The second sequence has 70 queries against max_q = 64: refused
+    # (PA_DEVERR_SEQ_LEN, its rows untouched); the first is computed.
+    wl, q, qs = _case([900, 1500], [64, 70])
+    ds = DeviceStep(wl)
+    out = torch.full((q.shape[0], wl.Hq, wl.D), 7.0, dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pa.pa_prefill(to_dev(q, "bf16"), torch.from_numpy(qs).cuda(), ds.k_pool, ds.v_pool, ds.tables,
+                  ds.seq_lens, wl.scale, out, 64, wl.max_seq_len, device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pa.PA_DEVERR_SEQ_LEN
+    got = out_f64(out)
+    assert (got[qs[1]:] == 7.0).all()
+    ref = oracle.prefill(q[:64], wl.k_pool, wl.v_pool, wl.block_tables[:1], wl.seq_lens[:1],
+                         qs[:2], wl.scale)
+    assert np.abs(got[:64] - ref).max() <= BF16_TOL
+
+
 @pytest.mark.parametrize("name", ["prefill_gqa", "llama3_8b_gqa"])
 def test_prefill_full_size_sampled_rows(name):
     """The benchmark's workloads at full size (the newest 256 tokens of every
