@@ -27,7 +27,7 @@ from gpu_helpers import BF16_TOL, DeviceStep, out_f64, to_dev
 
 pytestmark = pytest.mark.gpu
 
-N_CASES = 64
+N_CASES = 160
 
 
 @pytest.fixture(scope="module", autouse=True)
