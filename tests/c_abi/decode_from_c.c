@@ -3,14 +3,17 @@
  * and the same step as one pa_append_decode call on a copy of the pools)
  * and a verification step for the newest two tokens of every sequence
  * (pa_decode_multi, then the same rows through pa_prefill's tensor-core
- * kernel) on device memory from cudaMalloc, with no Python or
+ * kernel), the PagedEviction page scores of the appended pools
+ * (pa_page_scores) and two copy-on-write block copies (pa_copy_blocks) on
+ * device memory from cudaMalloc, with no Python or
  * PyTorch involved, checked against the fp64 oracle (linked from oracle/ as
  * test infrastructure). Inputs are deterministic (an integer hash), the pools hold
  * NaN in every slot past each sequence, and the tables name a shuffled set of
  * physical blocks with -1 past each sequence.
  *
- * Exit status 0 when the appended pools match the oracle's bit for bit and
- * every attention output is within the bf16 tolerance (1.5e-2 absolute).
+ * Exit status 0 when the appended and the copied pools match the oracle's bit
+ * for bit, every attention output is within the bf16 tolerance (1.5e-2
+ * absolute), the page scores within 1e-4 relative and the victims equal.
  */
 #include <cuda_runtime.h>
 #include <math.h>
@@ -33,6 +36,11 @@ int oracle_prefill(const void* q, const void* kpool, const void* vpool, const in
                    int max_blocks, const int32_t* seq_lens, const int32_t* q_start, int B, int Hq,
                    int Hkv, int D, int bs, int num_blocks, float scale, int dtype, double* out,
                    int nthreads);
+int oracle_page_scores(const void* kpool, const void* vpool, const int32_t* table, int max_blocks,
+                       const int32_t* seq_lens, int B, int Hkv, int D, int bs, int num_blocks,
+                       int dtype, double* scores, int32_t* victims);
+int oracle_copy_blocks(void* kpool, void* vpool, const int32_t* src, const int32_t* dst, int n,
+                       int num_blocks, int64_t block_bytes);
 
 enum { B = 3, HQ = 8, HKV = 2, D = 128, BS = 16, MAXB = 20, SPARE = 5 };
 static const int kLens[B] = {1, 37, 300}; /* tokens after the append */
@@ -205,6 +213,25 @@ int main(void) {
     uint16_t out4[2 * B * HQ * D];
     CHECK_CUDA(cudaMemcpy(out4, dout4, (size_t)T * HQ * D * 2, cudaMemcpyDeviceToHost));
 
+    /* PagedEviction page scores over the appended pools. */
+    float* dsc;
+    int32_t* dvi;
+    int* dserr;
+    CHECK_CUDA(cudaMalloc((void**)&dsc, sizeof(float) * B * MAXB));
+    CHECK_CUDA(cudaMalloc((void**)&dvi, sizeof(int32_t) * B));
+    CHECK_CUDA(cudaMalloc((void**)&dserr, sizeof(int)));
+    CHECK_CUDA(cudaMemset(dsc, 0, sizeof(float) * B * MAXB));
+    CHECK_CUDA(cudaMemset(dserr, 0, sizeof(int)));
+    CHECK_PA(pa_page_scores(dk, dv, dtab, MAXB, dsl, B, HKV, D, BS, NB, MAXB * BS, PA_BF16, dsc, dvi,
+                            dserr, NULL));
+    CHECK_CUDA(cudaDeviceSynchronize());
+    float sc[B * MAXB];
+    int32_t vi[B];
+    int serr = -1;
+    CHECK_CUDA(cudaMemcpy(sc, dsc, sizeof sc, cudaMemcpyDeviceToHost));
+    CHECK_CUDA(cudaMemcpy(vi, dvi, sizeof vi, cudaMemcpyDeviceToHost));
+    CHECK_CUDA(cudaMemcpy(&serr, dserr, sizeof serr, cudaMemcpyDeviceToHost));
+
     /* The oracle: append on the host pools, then fp64 attention. */
     if (oracle_append(k_new, v_new, kpool, vpool, table, MAXB, cache_lens, B, HKV, D, BS, NB, 2) != 0)
         return 4;
@@ -218,6 +245,38 @@ int main(void) {
         return 4;
     const int pools_equal = memcmp(kgot, kpool, pool_elems * 2) == 0 &&
                             memcmp(vgot, vpool, pool_elems * 2) == 0;
+    double rsc[B * MAXB];
+    int32_t rvi[B];
+    if (oracle_page_scores(kpool, vpool, table, MAXB, seq_lens, B, HKV, D, BS, NB, 1, rsc, rvi) != 0)
+        return 4;
+    double worst_sc = 0.0; /* relative */
+    int victims_equal = 1, scores_ok = 1;
+    for (int b = 0; b < B; ++b) {
+        victims_equal &= vi[b] == rvi[b];
+        for (int p = 0; p < (kLens[b] + BS - 1) / BS; ++p) {
+            const double r = rsc[b * MAXB + p], e = fabs((double)sc[b * MAXB + p] - r) / fabs(r);
+            scores_ok &= e <= 1e-4; /* false for NaN */
+            if (e > worst_sc) worst_sc = e;
+        }
+    }
+
+    /* Copy on write: two blocks of sequence 2 into two free blocks. */
+    int32_t csrc[2] = {table[2 * MAXB], table[2 * MAXB + 1]};
+    int32_t cdst[2] = {perm[used], perm[used + 1]};
+    int32_t *dcs, *dcd;
+    CHECK_CUDA(cudaMalloc((void**)&dcs, sizeof csrc));
+    CHECK_CUDA(cudaMalloc((void**)&dcd, sizeof cdst));
+    CHECK_CUDA(cudaMemcpy(dcs, csrc, sizeof csrc, cudaMemcpyHostToDevice));
+    CHECK_CUDA(cudaMemcpy(dcd, cdst, sizeof cdst, cudaMemcpyHostToDevice));
+    CHECK_PA(pa_copy_blocks(dk, dv, dcs, dcd, 2, HKV, D, BS, NB, PA_BF16, NULL));
+    CHECK_CUDA(cudaDeviceSynchronize());
+    int cerr = -1;
+    CHECK_PA(pa_last_device_error(NULL, &cerr));
+    CHECK_CUDA(cudaMemcpy(kgot, dk, pool_elems * 2, cudaMemcpyDeviceToHost));
+    CHECK_CUDA(cudaMemcpy(vgot, dv, pool_elems * 2, cudaMemcpyDeviceToHost));
+    if (oracle_copy_blocks(kpool, vpool, csrc, cdst, 2, NB, (int64_t)HKV * BS * D * 2) != 0) return 4;
+    const int copies_equal = memcmp(kgot, kpool, pool_elems * 2) == 0 &&
+                             memcmp(vgot, vpool, pool_elems * 2) == 0;
     double worst = 0.0;
     int finite = 1;
     for (int i = 0; i < B * HQ * D; ++i) {
@@ -234,11 +293,14 @@ int main(void) {
         if (e > worst2) worst2 = e;
         if (e4 > worst3) worst3 = e4;
     }
-    printf("device errors %d/%d/%d/%d/%d, pools equal %d, one-call step identical %d, finite %d, "
-           "max abs error %.3e / %.3e / %.3e\n", derr, aerr, merr, ferr, perr, pools_equal,
-           fused_same, finite, worst, worst2, worst3);
-    return (derr == 0 && aerr == 0 && merr == 0 && ferr == 0 && perr == 0 && pools_equal &&
-            fused_same && finite && worst <= 1.5e-2 && worst2 <= 1.5e-2 && worst3 <= 1.5e-2)
+    printf("device errors %d/%d/%d/%d/%d/%d/%d, pools equal %d, one-call step identical %d, "
+           "finite %d, max abs error %.3e / %.3e / %.3e, page scores rel %.3e, victims equal %d, "
+           "copies equal %d\n", derr, aerr, merr, ferr, perr, serr, cerr, pools_equal, fused_same,
+           finite, worst, worst2, worst3, worst_sc, victims_equal, copies_equal);
+    return (derr == 0 && aerr == 0 && merr == 0 && ferr == 0 && perr == 0 && serr == 0 &&
+            cerr == 0 && pools_equal && fused_same && finite && worst <= 1.5e-2 &&
+            worst2 <= 1.5e-2 && worst3 <= 1.5e-2 && scores_ok && victims_equal &&
+            copies_equal)
                ? 0
                : 1;
 }

@@ -1,7 +1,8 @@
 """GPU: the C boundary called from a C program (no Python, no PyTorch on the
-path): one append + decode step, one few-queries verification step and the
-same rows through pa_prefill on cudaMalloc'd memory, checked against the
-oracle inside the program (tests/c_abi/decode_from_c.c)."""
+path): one append + decode step, one few-queries verification step, the
+same rows through pa_prefill, the page scores and two block copies on
+cudaMalloc'd memory, checked against the oracle inside the program
+(tests/c_abi/decode_from_c.c)."""
 
 import os
 import shutil
