@@ -113,6 +113,18 @@ def test_invalid_query_count_gives_zero_rows_and_an_error():
     assert np.abs(got[qs[2]:qs[3]] - ref2).max() <= BF16_TOL
 
 
+def test_more_queries_than_max_q_give_zero_rows_and_an_error():
+    lens, ns = [100, 50, 70], [2, 5, 2]   # sequence 1 has more queries than max_q = 2
+    wl, q, qs = _case(lens, ns, seed=6)
+    got, err = _run(wl, q, qs, 2)
+    assert err & pa.PA_DEVERR_SEQ_LEN
+    assert (got[qs[1]:qs[2]] == 0).all()
+    for b in (0, 2):
+        ref = oracle.prefill(q[qs[b]:qs[b + 1]], wl.k_pool, wl.v_pool, wl.block_tables[b:b + 1],
+                             wl.seq_lens[b:b + 1], [0, ns[b]], wl.scale)
+        assert np.abs(got[qs[b]:qs[b + 1]] - ref).max() <= BF16_TOL
+
+
 def test_speculative_workload_full_size_sampled_rows():
     wl = make_workload("spec_gqa")
     append_in_place(wl)
